@@ -1,0 +1,377 @@
+"""CPU oracle for the self-speculative verification step (test infrastructure).
+
+This module is TEST INFRASTRUCTURE.  Only the test suite, the package smoke
+check and the CPU-baseline leg of the benchmark may import or run it; the
+product path never does.  It shares no code with the CUDA path.
+
+It is a plain, slow, obviously-correct restatement, in float64 numpy, of
+what one verification step computes:
+
+  1. ``mask_build``       visibility of the speculative block's rows
+  2. ``verify_attention`` masked softmax attention over
+                          (committed prefix || soft prompt || block)
+  3. ``vocab_reduce``     per judged row: argmax, log-sum-exp, proposal logit
+  4. ``accept``           threshold longest prefix, or greedy tree walk
+  5. ``kv_commit``        append the accepted rows' K/V to the cache
+
+Sources (page title, section / equation):
+
+* "Lookahead Attention: Self-Speculative Verification via Parallel Token
+  Proposals" (LA): sec. 2.1 diagram, sec. 2.2-2.4, sec. 3.1 mask M_LA,
+  sec. 3.2 (lookahead KV discarded), sec. 3.3 (padding to one length).
+* "ConFu: Contemplate the Future for Better Speculative Sampling" notes:
+  key design 1 (soft prompt seen only by contemplate tokens, one contemplate
+  token per draft node, 2T tokens verified in one pass).
+* "Speculative Streaming: Fast LLM Inference without Auxiliary Models":
+  Eq. 1 (main-stream MHA, softmax(QK^T/sqrt(d))V), Eq. 2 (stream j sees the
+  main stream <= t and streams <= j at the same t), Eq. 4 and the text after
+  it (tree nodes see their ancestors), the verification step (hard matching,
+  beta accepted + 1 correction token).
+
+Readings where the pages are garbled or silent (each is listed with its
+reason in the design notes):
+
+* LA prints M_LA with rows = keys and columns = queries; the masks here are
+  query-major.  The diagram's top-left block is printed as the identity; the
+  formula's M_causal (standard causal) is used.
+* A lookahead row sees itself (diagonal) and no other lookahead row.
+* The LA proposal of row i is judged by row i's own distribution, with
+  p_i >= tau accepted ("exceeds" read as >=; tau = 0.3).
+* SS Eq. 4 read together with the sentence after it: a node sees all of its
+  ancestors and itself (not only its immediate parent).
+* A stream row sees itself (Eq. 2, S_{t(<=j)} includes j).
+* A ConFu contemplate token sees the prefix, its node's ancestors, its node,
+  itself and the soft prompt; draft nodes never see the soft prompt.
+* Tree root = node 0, always accepted; its K/V is committed first.
+* Padding rows (vparent = -2) see nothing: O = 0, LSE = -inf.
+* Paged cache: requests in ascending order take pages from the free list in
+  order, after filling their partly used tail page.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+VP_ROOT = -1
+VP_PAD = -2
+
+MODE_THRESH_CHAIN = 0
+MODE_GREEDY_TREE = 1
+
+
+# --------------------------------------------------------------------------
+# 1. mask
+# --------------------------------------------------------------------------
+
+def la_prefill_mask(n: int, k: int) -> np.ndarray:
+    """Full LA mask M_LA for n original and k lookahead positions.
+
+    LA sec. 3.1, written query-major (row = query, column = key): original
+    queries are causal over originals and never see lookahead keys; a
+    lookahead query sees every original key and itself only.
+    """
+    L = n + k
+    m = np.zeros((L, L), dtype=bool)
+    for i in range(n):
+        for j in range(i + 1):
+            m[i, j] = True
+    for i in range(n, L):
+        for j in range(n):
+            m[i, j] = True
+        m[i, i] = True
+    return m
+
+
+def mask_build(vparent: np.ndarray, soft_flags=None):
+    """Visibility of the speculative block, per request.
+
+    ``vparent[b][r]``: -1 -> row r sees only the prefix and itself (LA
+    lookahead row, tree root); -2 -> padding row; p >= 0 -> row r sees what
+    row p sees plus itself (tree ancestor closure, SS Eq. 2/4, ConFu).
+
+    Returns (vis [B][R][R] bool: row r sees block column c,
+             valid [B][R] bool, sees_soft [B][R] bool).
+    Raises ValueError for a parent that is not an earlier valid row.
+    """
+    vparent = np.asarray(vparent)
+    B, R = vparent.shape
+    vis = np.zeros((B, R, R), dtype=bool)
+    valid = np.zeros((B, R), dtype=bool)
+    for b in range(B):
+        for r in range(R):
+            p = int(vparent[b, r])
+            if p == VP_PAD:
+                continue
+            if p == VP_ROOT:
+                pass
+            elif p < 0 or p >= r or not valid[b, p]:
+                raise ValueError(f"bad parent {p} for row {r} of request {b}")
+            valid[b, r] = True
+            # walk the parent chain: r, parent(r), parent(parent(r)), ...
+            c = r
+            while c >= 0:
+                vis[b, r, c] = True
+                c = int(vparent[b, c])
+    if soft_flags is None:
+        sees_soft = np.zeros((B, R), dtype=bool)
+    else:
+        sees_soft = (np.asarray(soft_flags) != 0) & valid
+    return vis, valid, sees_soft
+
+
+# --------------------------------------------------------------------------
+# 2. attention
+# --------------------------------------------------------------------------
+
+def verify_attention(q, prefix_k, prefix_v, k_block, v_block, vis, valid,
+                     sees_soft, soft_k=None, soft_v=None, scale=None,
+                     requests=None, heads=None):
+    """Masked attention of the speculative rows, in float64.
+
+    q        [B][R][Hq][d]
+    prefix_k list over requests of [Hkv][S_b][d] (committed prefix, logical
+             order); prefix_v likewise
+    k_block  [B][Hkv][R][d]  the block's own keys (v_block: values)
+    soft_k   [Hkv][n_soft][d] or None
+    vis, valid, sees_soft  from ``mask_build``
+
+    For query head h the key/value head is h // (Hq / Hkv).  The columns of
+    row r are [prefix 0..S_b) || [soft 0..n_soft) || [block 0..R), with the
+    explicit additive mask 0 (visible) / -inf (hidden): every valid row sees
+    the whole prefix, the soft columns iff sees_soft, block column c iff
+    vis[r][c].  Scores s = (q . k) * scale with scale = 1/sqrt(d) (SS Eq. 1);
+    LSE = ln sum_j exp(s_j); O = sum_j exp(s_j - LSE) v_j.
+
+    ``requests`` / ``heads`` restrict the work (others left as NaN).
+    Returns O [B][R][Hq][d] and LSE [B][Hq][R] (float64); rows that are not
+    valid have O = 0 and LSE = -inf.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, R, Hq, d = q.shape
+    Hkv = k_block.shape[1]
+    G = Hq // Hkv
+    if vis.shape != (B, R, R) or k_block.shape[:3] != (B, Hkv, R) or Hq % Hkv:
+        raise ValueError("inconsistent shapes")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    n_soft = 0 if soft_k is None else soft_k.shape[1]
+    O = np.full((B, R, Hq, d), np.nan)
+    LSE = np.full((B, Hq, R), np.nan)
+    reqs = range(B) if requests is None else requests
+    hs = range(Hq) if heads is None else heads
+    for b in reqs:
+        S = prefix_k[b].shape[1]
+        # explicit dense additive mask over the concatenated columns
+        mask = np.full((R, S + n_soft + R), -np.inf)
+        for r in range(R):
+            if not valid[b, r]:
+                continue
+            mask[r, :S] = 0.0
+            if sees_soft[b, r]:
+                mask[r, S:S + n_soft] = 0.0
+            for c in range(R):
+                if vis[b, r, c]:
+                    mask[r, S + n_soft + c] = 0.0
+        for h in hs:
+            kvh = h // G
+            parts_k = [np.asarray(prefix_k[b][kvh], dtype=np.float64)]
+            parts_v = [np.asarray(prefix_v[b][kvh], dtype=np.float64)]
+            if n_soft:
+                parts_k.append(np.asarray(soft_k[kvh], dtype=np.float64))
+                parts_v.append(np.asarray(soft_v[kvh], dtype=np.float64))
+            parts_k.append(np.asarray(k_block[b, kvh], dtype=np.float64))
+            parts_v.append(np.asarray(v_block[b, kvh], dtype=np.float64))
+            Kc = np.concatenate(parts_k, axis=0)
+            Vc = np.concatenate(parts_v, axis=0)
+            s = (q[b, :, h, :] @ Kc.T) * scale + mask       # [R][cols]
+            for r in range(R):
+                if not valid[b, r]:
+                    O[b, r, h] = 0.0
+                    LSE[b, h, r] = -np.inf
+                    continue
+                m = s[r].max()
+                lse = m + math.log(np.exp(s[r] - m).sum())
+                p = np.exp(s[r] - lse)
+                O[b, r, h] = p @ Vc
+                LSE[b, h, r] = lse
+    return O, LSE
+
+
+def gather_paged(pages, page_table, seq_len, page_size):
+    """Logical per-request prefixes [Hkv][S_b][d] from a paged cache.
+
+    pages [n_pages][Hkv][page_size][d]; page_table[b][j] = physical page of
+    logical page j of request b.
+    """
+    out = []
+    for b in range(len(seq_len)):
+        S = int(seq_len[b])
+        Hkv, d = pages.shape[1], pages.shape[3]
+        kk = np.empty((Hkv, S, d), dtype=pages.dtype)
+        for t in range(S):
+            p = int(page_table[b][t // page_size])
+            kk[:, t] = pages[p, :, t % page_size]
+        out.append(kk)
+    return out
+
+
+# --------------------------------------------------------------------------
+# 3. vocab reduce
+# --------------------------------------------------------------------------
+
+def vocab_reduce(logits, proposal=None):
+    """Per row of logits [n][V]: argmax (lowest index on ties), LSE, z[prop].
+
+    LA sec. 2.4 needs the proposal's probability exp(z_prop - LSE); the
+    greedy walk of SS ("verification step", hard matching) needs the argmax.
+    """
+    z = np.asarray(logits, dtype=np.float64)
+    n = z.shape[0]
+    amax = np.empty(n, dtype=np.int64)
+    lse = np.empty(n)
+    zprop = np.full(n, np.nan)
+    for i in range(n):
+        row = z[i]
+        m = row.max()
+        amax[i] = int(np.nonzero(row == m)[0][0])
+        lse[i] = m + math.log(np.exp(row - m).sum())
+        if proposal is not None:
+            zprop[i] = row[int(proposal[i])]
+    return amax, lse, zprop
+
+
+# --------------------------------------------------------------------------
+# 4. acceptance
+# --------------------------------------------------------------------------
+
+def accept_threshold_chain(zprop, lse, n_props, tau):
+    """LA sec. 2.4: the longest prefix of proposals whose probabilities all
+    reach tau.  Row i judges proposal i.  Returns L (number accepted)."""
+    L = 0
+    while L < n_props and math.exp(zprop[L] - lse[L]) >= tau:
+        L += 1
+    return L
+
+
+def accept_greedy_tree(tokens, tree_parent, n_nodes, argmax_of_node):
+    """SS verification step (hard matching), also ConFu's tree verify.
+
+    From the root (node 0), repeatedly move to the child of the current node
+    whose token equals the target's greedy token at the current node; stop
+    when there is none.  Returns (path [root, ...], next_token) where
+    next_token is the target's greedy token at the last accepted node (the
+    correction token); beta = len(path) - 1 draft tokens are accepted.
+    Siblings are expected to carry distinct tokens; otherwise the child with
+    the lowest index is taken.
+    """
+    cur = 0
+    path = [0]
+    while True:
+        want = int(argmax_of_node[cur])
+        nxt = None
+        for c in range(n_nodes):
+            if int(tree_parent[c]) == cur and int(tokens[c]) == want:
+                nxt = c
+                break
+        if nxt is None:
+            return path, want
+        cur = nxt
+        path.append(cur)
+
+
+def accept(mode, tau, tokens, tree_parent, n_nodes, argmax, lse, zprop,
+           row_of=None):
+    """Acceptance for every request.
+
+    Chain mode (LA): proposal i of request b is judged by judge row i;
+    acc_len = L, path = [0, 1, ..., L-1], next_token = argmax of row L when
+    L < n_nodes else -1, last_node = L - 1.
+    Tree mode: path as ``accept_greedy_tree``; acc_len = len(path) (root
+    included), last_node = path[-1].
+    ``row_of[b][node]`` gives the judge row of a node (identity if None).
+    """
+    B = tokens.shape[0]
+    acc_len = np.zeros(B, dtype=np.int64)
+    paths = []
+    next_tok = np.zeros(B, dtype=np.int64)
+    last = np.zeros(B, dtype=np.int64)
+    for b in range(B):
+        n = int(n_nodes[b])
+        ro = (lambda j: j) if row_of is None else (lambda j, b=b: int(row_of[b][j]))
+        if mode == MODE_THRESH_CHAIN:
+            zp = [zprop[b][ro(i)] for i in range(n)]
+            ls = [lse[b][ro(i)] for i in range(n)]
+            L = accept_threshold_chain(zp, ls, n, tau)
+            acc_len[b] = L
+            paths.append(list(range(L)))
+            next_tok[b] = int(argmax[b][ro(L)]) if L < n else -1
+            last[b] = L - 1
+        else:
+            am = [int(argmax[b][ro(j)]) for j in range(n)]
+            path, nt = accept_greedy_tree(tokens[b], tree_parent[b], n, am)
+            acc_len[b] = len(path)
+            paths.append(path)
+            next_tok[b] = nt
+            last[b] = path[-1]
+    return acc_len, paths, next_tok, last
+
+
+# --------------------------------------------------------------------------
+# 5. commit
+# --------------------------------------------------------------------------
+
+def kv_commit_contiguous(K, V, seq_len, k_block, v_block, paths):
+    """Append accepted rows to a contiguous cache [B][Hkv][Smax][d].
+
+    Row paths[b][i] of the block goes to position seq_len[b] + i; every
+    other block row is dropped (LA sec. 3.2: speculative KV is not kept).
+    Returns new (K, V, seq_len) copies.
+    """
+    K = K.copy()
+    V = V.copy()
+    seq = np.array(seq_len, dtype=np.int64).copy()
+    for b, path in enumerate(paths):
+        for i, row in enumerate(path):
+            pos = int(seq[b]) + i
+            if pos >= K.shape[2]:
+                raise OverflowError("contiguous cache capacity exceeded")
+            K[b, :, pos] = k_block[b, :, row]
+            V[b, :, pos] = v_block[b, :, row]
+        seq[b] += len(path)
+    return K, V, seq
+
+
+def kv_commit_paged(Kp, Vp, page_table, seq_len, free_pages, free_head,
+                    k_block, v_block, paths, page_size):
+    """Append accepted rows to a paged cache [n_pages][Hkv][page][d].
+
+    Position t of request b lives in page page_table[b][t // page_size] at
+    slot t % page_size.  Requests are served in ascending b; each first fills
+    its partly used last page, then takes pages from
+    free_pages[free_head], free_pages[free_head + 1], ... in order.
+    Returns new (Kp, Vp, page_table, seq_len, free_head) copies.
+    """
+    Kp = Kp.copy()
+    Vp = Vp.copy()
+    pt = np.array(page_table).copy()
+    seq = np.array(seq_len, dtype=np.int64).copy()
+    head = int(free_head)
+    for b, path in enumerate(paths):
+        for i, row in enumerate(path):
+            pos = int(seq[b]) + i
+            j = pos // page_size
+            if pos % page_size == 0:
+                # a fresh page is needed for this position
+                if j >= pt.shape[1]:
+                    raise OverflowError("page table capacity exceeded")
+                if head >= len(free_pages):
+                    raise OverflowError("free page list exhausted")
+                pt[b, j] = free_pages[head]
+                head += 1
+            p = int(pt[b, j])
+            Kp[p, :, pos % page_size] = k_block[b, :, row]
+            Vp[p, :, pos % page_size] = v_block[b, :, row]
+        seq[b] += len(path)
+    return Kp, Vp, pt, seq, head

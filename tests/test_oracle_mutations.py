@@ -1,0 +1,91 @@
+"""The oracle's pins are sensitive: plausible mistakes planted in the oracle
+(on the CPU, by monkeypatching) make at least one pin fail."""
+
+import math
+import types
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle.specverify_oracle as so
+import test_oracle_accept_commit as tac
+import test_oracle_attention as tat
+import test_oracle_mask as tm
+
+
+def _expect_pin_failure(fn, *args):
+    with pytest.raises(AssertionError):
+        fn(*args)
+
+
+def test_wrong_softmax_scale_is_caught(monkeypatch):
+    fake = types.SimpleNamespace(sqrt=lambda x: x, log=math.log, exp=math.exp,
+                                 inf=math.inf)
+    monkeypatch.setattr(so, "math", fake)       # scale becomes 1/d
+    _expect_pin_failure(tat.test_chain_equals_causal_attention)
+    _expect_pin_failure(tat.test_single_visible_key)
+
+
+def test_dropped_self_visibility_is_caught(monkeypatch):
+    real = so.mask_build
+
+    def no_self(vparent, soft_flags=None):
+        vis, valid, sees = real(vparent, soft_flags)
+        vis = vis.copy()
+        for b in range(vis.shape[0]):
+            np.fill_diagonal(vis[b], False)
+        return vis, valid, sees
+
+    monkeypatch.setattr(oracle, "mask_build", no_self)
+    _expect_pin_failure(tm.test_la_verify_rows_equal_prefill_lookahead_rows)
+    _expect_pin_failure(tm.test_chain_is_lower_triangular)
+
+
+def test_parent_only_visibility_is_caught(monkeypatch):
+    """SS Eq. 4 read literally (immediate parent only) fails the pins."""
+    def parent_only(vparent, soft_flags=None):
+        vparent = np.asarray(vparent)
+        B, R = vparent.shape
+        vis = np.zeros((B, R, R), dtype=bool)
+        valid = vparent != so.VP_PAD
+        for b in range(B):
+            for r in range(R):
+                if valid[b, r]:
+                    vis[b, r, r] = True
+                    if vparent[b, r] >= 0:
+                        vis[b, r, vparent[b, r]] = True
+        sees = np.zeros((B, R), dtype=bool) if soft_flags is None else \
+            (np.asarray(soft_flags) != 0) & valid
+        return vis, valid, sees
+
+    monkeypatch.setattr(oracle, "mask_build", parent_only)
+    _expect_pin_failure(tm.test_full_tree_sizes_and_ancestors, 2, 3, 15)
+    _expect_pin_failure(tat.test_chain_equals_causal_attention)
+
+
+def test_strict_threshold_is_caught(monkeypatch):
+    def strict(zprop, lse, n, tau):
+        L = 0
+        while L < n and math.exp(zprop[L] - lse[L]) > tau + 1e-12:
+            L += 1
+        return L
+    monkeypatch.setattr(oracle, "accept_threshold_chain", strict)
+    _expect_pin_failure(tac.test_threshold_hand_worked)
+
+
+def test_walk_without_root_check_is_caught(monkeypatch):
+    """A walk that matches any node's token (not only the children of the
+    current node) fails the hand-worked tree pin."""
+    def sloppy(tokens, tree_parent, n_nodes, argmax_of_node):
+        cur, path = 0, [0]
+        while True:
+            want = int(argmax_of_node[cur])
+            nxt = next((c for c in range(1, n_nodes)
+                        if int(tokens[c]) == want and c not in path), None)
+            if nxt is None:
+                return path, want
+            cur = nxt
+            path.append(cur)
+    monkeypatch.setattr(oracle, "accept_greedy_tree", sloppy)
+    _expect_pin_failure(tac.test_greedy_walk_hand_worked)
