@@ -1,0 +1,309 @@
+/*
+ * libspecverify -- the single-forward-pass verification step of
+ * self-speculative decoding, for NVIDIA GB300 (sm_103a).
+ *
+ * One verification step, as the pages describe it:
+ *   1. spec_mask_build   which speculative rows see which block columns
+ *   2. spec_verify_attn  masked attention of the speculative rows over
+ *                        (committed KV prefix || soft prompt || the block)
+ *   3. spec_accept       vocab-wide argmax / log-sum-exp per judged row,
+ *                        then the LA threshold longest prefix or the greedy
+ *                        tree walk
+ *   4. kv_commit         append the accepted rows' K/V to the cache; every
+ *                        other speculative K/V row is dropped
+ *
+ * Sources, cited by page title and section / equation:
+ *   [LA]  "Lookahead Attention: Self-Speculative Verification via Parallel
+ *         Token Proposals": sec. 2.1-2.4, sec. 3.1 (mask M_LA), sec. 3.2
+ *         (lookahead KV discarded), sec. 3.3 (batched lookahead, padding).
+ *   [CF]  "ConFu: Contemplate the Future for Better Speculative Sampling"
+ *         (reading notes): key design 1 (soft prompt seen only by
+ *         contemplate tokens, one contemplate token per draft node, 2T
+ *         tokens in one verify pass).
+ *   [SS]  "Speculative Streaming: Fast LLM Inference without Auxiliary
+ *         Models": Eq. 1-2 (multi-stream attention), Eq. 4 and the text
+ *         after it (tree attention mask), batching with streams, the
+ *         verification step (hard matching, beta + 1 tokens advanced).
+ *
+ * Conventions for every call:
+ *   - All tensor arguments are DEVICE pointers owned by the caller, dense
+ *     and row-major in the layout stated; the library never frees them and
+ *     keeps no reference after the call returns.
+ *   - Calls are asynchronous on the caller's CUDA stream (`stream`, a
+ *     cudaStream_t; NULL = legacy default stream) and launch only this
+ *     library's kernels.  The library allocates no device memory: scratch
+ *     comes from a caller-provided workspace (spec_verify_attn).
+ *   - Errors visible on the host (bad sizes, NULL pointers, unsupported
+ *     dtype/shape, a too-small workspace) are returned before anything is
+ *     launched.  Errors only visible on the device (a bad parent pointer, a
+ *     page id out of range, a full cache) set bits in a per-device status
+ *     word and the kernel skips the offending work; nothing traps, nothing
+ *     spins.  spec_get_status() reads and clears that word.
+ *   - The status word is shared by all calls on a device: with concurrent
+ *     streams, an error bit cannot be attributed to one call.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPECVERIFY_VERSION 100
+
+typedef int spec_status_t;
+
+/* return codes */
+#define SPEC_OK              0
+#define SPEC_ERR_INVALID_ARG 1  /* NULL pointer, negative / inconsistent size */
+#define SPEC_ERR_UNSUPPORTED 2  /* dtype or shape this build does not handle */
+#define SPEC_ERR_BAD_TREE    3  /* reserved: tree errors are device-detected */
+#define SPEC_ERR_CAPACITY    4  /* workspace too small */
+#define SPEC_ERR_CUDA        5  /* a CUDA runtime call failed */
+#define SPEC_ERR_DEVICE      6  /* spec_get_status found device error bits */
+
+/* element types */
+#define SPEC_F32  0
+#define SPEC_BF16 1
+
+/* KV-cache layouts */
+#define SPEC_KV_CONTIGUOUS 0
+#define SPEC_KV_PAGED      1
+
+/* acceptance modes */
+#define SPEC_ACCEPT_THRESH_CHAIN 0  /* [LA] sec. 2.4 */
+#define SPEC_ACCEPT_GREEDY_TREE  1  /* [SS] verification step, [CF] */
+
+/* vparent codes (spec_mask_build) */
+#define SPEC_VP_ROOT (-1)   /* row sees the prefix and itself only */
+#define SPEC_VP_PAD  (-2)   /* padding row ([LA] sec. 3.3): sees nothing */
+
+/* row_flags bits (spec_mask_build output, spec_verify_attn input) */
+#define SPEC_ROW_VALID     1u
+#define SPEC_ROW_SEES_SOFT 2u
+
+/* device status bits (spec_get_status) */
+#define SPEC_DEV_BAD_TREE     0x01  /* vparent not an earlier valid row */
+#define SPEC_DEV_BAD_PAGE     0x02  /* page id outside [0, n_pages) */
+#define SPEC_DEV_SEQ_OVERFLOW 0x04  /* seq_len outside [0, cache capacity] */
+#define SPEC_DEV_CAPACITY     0x08  /* commit: cache or free list full */
+#define SPEC_DEV_BAD_INDEX    0x10  /* path / row_of / acc_len out of range */
+
+/* Maximum speculative rows per request (block columns). */
+#define SPEC_MAX_ROWS 256
+
+/*
+ * The committed KV cache ([LA] sec. 3.2, [SS] "no additional KV caching":
+ * only accepted tokens' K/V ever enter it).
+ *
+ * kind == SPEC_KV_CONTIGUOUS:
+ *   k, v : [batch][n_kv_heads][max_seq][head_dim]   (dtype)
+ *   request b's token t lives at k[b][h][t][:].
+ * kind == SPEC_KV_PAGED:
+ *   k, v : [n_pages][n_kv_heads][page_size][head_dim] (dtype)
+ *   page_table : int32 [batch][max_pages_per_seq]; token t of request b
+ *   lives in page page_table[b][t / page_size], slot t % page_size.
+ *   Entries past ceil(seq_len[b] / page_size) are unused.
+ */
+typedef struct spec_kv_desc {
+    int kind;
+    int dtype;
+    int n_kv_heads;
+    int head_dim;
+    void *k;
+    void *v;
+    int batch;
+    int max_seq;             /* contiguous: token capacity per request */
+    int n_pages;             /* paged */
+    int page_size;           /* paged: tokens per page (multiple of 16) */
+    int max_pages_per_seq;   /* paged: row length of page_table */
+    int32_t *page_table;     /* paged */
+} spec_kv_desc;
+
+/* Shape of one verify-attention call. */
+typedef struct spec_attn_desc {
+    int batch;         /* B */
+    int n_rows;        /* R: padded speculative rows per request (<= 256) */
+    int n_q_heads;     /* Hq (multiple of n_kv_heads) */
+    int n_kv_heads;    /* Hkv */
+    int head_dim;      /* d: 64 or 128 */
+    int dtype;         /* SPEC_BF16 or SPEC_F32, for q, kb, vb, soft, o, cache */
+    int n_soft;        /* soft-prompt KV entries (0 = none), <= 64 */
+    float scale;       /* softmax scale; 0 -> 1/sqrt(head_dim) ([SS] Eq. 1) */
+    int split_tokens;  /* prefix tokens per split; 0 = chosen by the library */
+} spec_attn_desc;
+
+/* Shape and rule of one acceptance call. */
+typedef struct spec_accept_desc {
+    int mode;          /* SPEC_ACCEPT_THRESH_CHAIN or SPEC_ACCEPT_GREEDY_TREE */
+    float tau;         /* threshold on the proposal probability (chain mode) */
+    int batch;         /* B */
+    int n_judge_rows;  /* Rj: logits rows per request */
+    int vocab;         /* V */
+    int logit_dtype;   /* SPEC_BF16 or SPEC_F32 */
+    int max_nodes;     /* N: row length of tokens / tree_parent / row_of */
+    int path_cap;      /* row length of path */
+} spec_accept_desc;
+
+/* Library version (SPECVERIFY_VERSION). */
+int spec_version(void);
+
+/* Human-readable name of a return code. */
+const char *spec_status_string(spec_status_t status);
+
+/*
+ * spec_mask_build -- visibility of the speculative block ([LA] sec. 3.1 in
+ * its verify form, [SS] Eq. 2 and Eq. 4 with the following text, [CF] key
+ * design 1).
+ *
+ *   vparent    int32 [batch][n_rows]: SPEC_VP_ROOT (-1): the row sees the
+ *              prefix and itself; SPEC_VP_PAD (-2): padding row; p >= 0:
+ *              the row sees everything row p sees, plus itself (p must be an
+ *              earlier, non-padding row: p < r).
+ *   soft_flags uint8 [batch][n_rows] or NULL: nonzero -> the row also sees
+ *              the soft-prompt columns (ConFu contemplate tokens).
+ *   vis        uint32 [batch][n_rows][ceil(n_rows/32)] out: bit c of word
+ *              c/32 of row r is set iff row r sees block column c.
+ *   row_flags  uint8 [batch][n_rows] out: SPEC_ROW_VALID | SPEC_ROW_SEES_SOFT.
+ *
+ * A row whose vparent chain is malformed gets vis = 0 and row_flags = 0
+ * and sets SPEC_DEV_BAD_TREE.  n_rows <= SPEC_MAX_ROWS.
+ */
+spec_status_t spec_mask_build(const int32_t *vparent, const uint8_t *soft_flags,
+                              int batch, int n_rows, uint32_t *vis,
+                              uint8_t *row_flags, void *stream);
+
+/*
+ * Bytes of workspace spec_verify_attn needs for this shape and cache
+ * (split partials: per request, KV head and split, the packed rows'
+ * running max, sum and unnormalised output in fp32).
+ */
+spec_status_t spec_verify_attn_workspace_size(const spec_attn_desc *attn,
+                                              const spec_kv_desc *cache,
+                                              size_t *bytes);
+
+/*
+ * spec_verify_attn -- masked attention of the speculative rows
+ * ([SS] Eq. 1-2, Eq. 4; [LA] sec. 3.1; [CF] key design 1).
+ *
+ *   q         [batch][n_rows][n_q_heads][head_dim]
+ *   cache     committed prefix (see spec_kv_desc); seq_len int32 [batch]
+ *             gives each request's prefix length S_b.
+ *   kb, vb    [batch][n_kv_heads][n_rows][head_dim]: the block's own K/V
+ *             (never aliases the cache).
+ *   soft_k/v  [n_kv_heads][n_soft][head_dim], or NULL when n_soft == 0.
+ *   vis, row_flags  from spec_mask_build.
+ *   o         out [batch][n_rows][n_q_heads][head_dim] (dtype)
+ *   lse       out fp32 [batch][n_q_heads][n_rows]: natural-log
+ *             log-sum-exp of the row's scaled scores.
+ *   workspace device scratch of >= spec_verify_attn_workspace_size bytes,
+ *             256-byte aligned; its contents on entry are ignored.
+ *
+ * For query head h the K/V head is h / (n_q_heads / n_kv_heads).  A valid
+ * row r sees prefix columns 0..S_b-1, the n_soft soft columns iff
+ * SPEC_ROW_SEES_SOFT, and block column c iff vis bit c; scores are
+ * (q . k) * scale.  Rows without SPEC_ROW_VALID get o = 0, lse = -inf.
+ * A seq_len outside [0, capacity] is clamped and sets SPEC_DEV_SEQ_OVERFLOW;
+ * a page id outside [0, n_pages) reads as zeros and sets SPEC_DEV_BAD_PAGE.
+ */
+spec_status_t spec_verify_attn(const spec_attn_desc *attn, const void *q,
+                               const spec_kv_desc *cache, const void *kb,
+                               const void *vb, const void *soft_k,
+                               const void *soft_v, const int32_t *seq_len,
+                               const uint32_t *vis, const uint8_t *row_flags,
+                               void *o, float *lse, void *workspace,
+                               size_t workspace_bytes, void *stream);
+
+/*
+ * spec_vocab_reduce -- per logits row ([LA] sec. 2.4 needs the proposal's
+ * probability, [SS] hard matching needs the greedy token):
+ *
+ *   logits    [n_rows][vocab] (dtype)
+ *   proposal  int32 [n_rows] or NULL
+ *   argmax    out int32 [n_rows]: index of the maximum, lowest on ties
+ *   lse       out fp32 [n_rows]: ln sum_j exp(z_j)
+ *   zprop     out fp32 [n_rows] (may be NULL iff proposal is NULL):
+ *             z[proposal[i]]; NaN if the proposal is outside [0, vocab).
+ */
+spec_status_t spec_vocab_reduce(const void *logits, int dtype, int n_rows,
+                                int vocab, const int32_t *proposal,
+                                int32_t *argmax, float *lse, float *zprop,
+                                void *stream);
+
+/*
+ * spec_accept -- the acceptance step.
+ *
+ * If `logits` ([batch][n_judge_rows][vocab]) is non-NULL, spec_vocab_reduce
+ * runs first and writes argmax / lse / zprop ([batch][n_judge_rows]); in
+ * chain mode the proposal of judge row i is tokens[b][i].  If `logits` is
+ * NULL, argmax / lse / zprop are read as inputs.
+ *
+ *   tokens      int32 [batch][max_nodes]: chain mode: proposal i of request
+ *               b; tree mode: draft token of node j (node 0 = root).
+ *   tree_parent int32 [batch][max_nodes] (tree mode): parent node, -1 for
+ *               the root; parents precede children.  Ignored in chain mode.
+ *   row_of      int32 [batch][max_nodes] or NULL (identity): judge row of
+ *               node j (tree mode).  Must be NULL in chain mode.
+ *   n_nodes     int32 [batch]: proposals (chain: k_b) or tree nodes.
+ *
+ * Chain mode ([LA] sec. 2.4): L = the largest l <= n_nodes[b] with
+ *   zprop_i - lse_i >= ln(tau) for all i < l (fp32, row i judges proposal i).
+ *   acc_len = L, path = 0..L-1, next_token = argmax of row L (or -1 when
+ *   L == n_nodes[b]), last_node = L - 1.
+ * Tree mode ([SS] verification step): from node 0 move to the child whose
+ *   token equals the argmax of the current node's judge row (lowest node
+ *   index on duplicate sibling tokens) until none matches.
+ *   acc_len = nodes on the path including the root (beta + 1),
+ *   path = those nodes, next_token = argmax at the last node (the
+ *   correction token), last_node = last node on the path.
+ * path entries past acc_len are set to -1.  A path longer than path_cap or
+ * an index out of range stops the walk and sets SPEC_DEV_BAD_INDEX.
+ */
+spec_status_t spec_accept(const spec_accept_desc *desc, const void *logits,
+                          const int32_t *tokens, const int32_t *tree_parent,
+                          const int32_t *row_of, const int32_t *n_nodes,
+                          int32_t *argmax, float *lse, float *zprop,
+                          int32_t *acc_len, int32_t *path, int32_t *next_token,
+                          int32_t *last_node, void *stream);
+
+/*
+ * kv_commit -- append each request's accepted block rows to the cache and
+ * drop the rest ([LA] sec. 3.2, [SS] lazy removal of pruned KV).
+ *
+ *   kb, vb    [batch][n_kv_heads][n_rows][head_dim], as for spec_verify_attn
+ *   path      int32 [batch][path_cap]: block rows to append, in order
+ *   acc_len   int32 [batch]: how many entries of path to append
+ *   seq_len   int32 [batch], in/out: += appended rows
+ *   free_pages int32 [n_free], free_head int32 [1] in/out (paged only;
+ *             NULL / 0 for contiguous caches).
+ *
+ * Row path[b][i] goes to token position seq_len[b] + i.  Paged caches:
+ * requests are served in ascending b; each first fills its partly used last
+ * page, then takes pages free_pages[*free_head], free_pages[*free_head+1],
+ * ... in order, recording them in page_table.
+ * A request that would exceed its capacity (max_seq, or max_pages_per_seq)
+ * is skipped and sets SPEC_DEV_CAPACITY; if the free list cannot serve all
+ * requests, nothing is written and SPEC_DEV_CAPACITY is set.  Out-of-range
+ * path entries are not written (SPEC_DEV_BAD_INDEX).
+ */
+spec_status_t kv_commit(const spec_kv_desc *cache, int batch, int n_rows,
+                        const void *kb, const void *vb, int path_cap,
+                        const int32_t *path, const int32_t *acc_len,
+                        int32_t *seq_len, const int32_t *free_pages,
+                        int n_free, int32_t *free_head, void *stream);
+
+/*
+ * spec_get_status -- synchronise `stream`, then read and clear the current
+ * device's status word.  *out receives the SPEC_DEV_* bits (0 = none).
+ * Returns SPEC_OK if no bit was set, SPEC_ERR_DEVICE otherwise.
+ */
+spec_status_t spec_get_status(void *stream, int32_t *out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

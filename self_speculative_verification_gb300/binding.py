@@ -1,0 +1,264 @@
+"""Python binding of the libspecverify C ABI (argument marshalling only).
+
+Every function here has the name of the C entry point it calls, checks the
+tensors it is handed (CUDA device, dtype, contiguity, shape), passes raw
+device pointers plus the current torch CUDA stream, and raises
+``SpecError`` on any non-zero return code.  No arithmetic of the
+verification step happens in Python: if the shared library is missing,
+``load_library`` raises and nothing runs.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_float, c_int, c_size_t, c_void_p
+
+import torch
+
+from . import _build
+
+# return codes / enums (include/specverify.h)
+SPEC_OK = 0
+SPEC_ERR_DEVICE = 6
+SPEC_F32 = 0
+SPEC_BF16 = 1
+SPEC_KV_CONTIGUOUS = 0
+SPEC_KV_PAGED = 1
+SPEC_ACCEPT_THRESH_CHAIN = 0
+SPEC_ACCEPT_GREEDY_TREE = 1
+SPEC_ROW_VALID = 1
+SPEC_ROW_SEES_SOFT = 2
+SPEC_DEV_BAD_TREE = 0x01
+SPEC_DEV_BAD_PAGE = 0x02
+SPEC_DEV_SEQ_OVERFLOW = 0x04
+SPEC_DEV_CAPACITY = 0x08
+SPEC_DEV_BAD_INDEX = 0x10
+
+EXPORTS = ("spec_version", "spec_status_string", "spec_mask_build",
+           "spec_verify_attn_workspace_size", "spec_verify_attn",
+           "spec_vocab_reduce", "spec_accept", "kv_commit", "spec_get_status")
+
+
+class SpecError(RuntimeError):
+    def __init__(self, fn, code, msg):
+        super().__init__(f"{fn} failed: {msg} (code {code})")
+        self.code = code
+
+
+class KvDesc(ctypes.Structure):
+    _fields_ = [("kind", c_int), ("dtype", c_int), ("n_kv_heads", c_int),
+                ("head_dim", c_int), ("k", c_void_p), ("v", c_void_p),
+                ("batch", c_int), ("max_seq", c_int), ("n_pages", c_int),
+                ("page_size", c_int), ("max_pages_per_seq", c_int),
+                ("page_table", c_void_p)]
+
+
+class AttnDesc(ctypes.Structure):
+    _fields_ = [("batch", c_int), ("n_rows", c_int), ("n_q_heads", c_int),
+                ("n_kv_heads", c_int), ("head_dim", c_int), ("dtype", c_int),
+                ("n_soft", c_int), ("scale", c_float), ("split_tokens", c_int)]
+
+
+class AcceptDesc(ctypes.Structure):
+    _fields_ = [("mode", c_int), ("tau", c_float), ("batch", c_int),
+                ("n_judge_rows", c_int), ("vocab", c_int), ("logit_dtype", c_int),
+                ("max_nodes", c_int), ("path_cap", c_int)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return os.environ.get("SPECVERIFY_LIB", _build.LIB)
+
+
+def load_library():
+    """Load libspecverify.so (built by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libspecverify is not built ({path} missing); "
+                           "run __graft_entry__.build() first")
+    lib = ctypes.CDLL(path)
+    vp = c_void_p
+    sig = {
+        "spec_version": ([], c_int),
+        "spec_status_string": ([c_int], ctypes.c_char_p),
+        "spec_mask_build": ([vp, vp, c_int, c_int, vp, vp, vp], c_int),
+        "spec_verify_attn_workspace_size": ([POINTER(AttnDesc), POINTER(KvDesc),
+                                             POINTER(c_size_t)], c_int),
+        "spec_verify_attn": ([POINTER(AttnDesc), vp, POINTER(KvDesc), vp, vp, vp, vp,
+                              vp, vp, vp, vp, vp, vp, c_size_t, vp], c_int),
+        "spec_vocab_reduce": ([vp, c_int, c_int, c_int, vp, vp, vp, vp, vp], c_int),
+        "spec_accept": ([POINTER(AcceptDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                         vp, vp, vp], c_int),
+        "kv_commit": ([POINTER(KvDesc), c_int, c_int, vp, vp, c_int, vp, vp, vp, vp,
+                       c_int, vp, vp], c_int),
+        "spec_get_status": ([vp, POINTER(ctypes.c_int32)], c_int),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    _lib = lib
+    return lib
+
+
+def _check(fn, code):
+    if code != SPEC_OK:
+        msg = load_library().spec_status_string(code).decode()
+        raise SpecError(fn, code, msg)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return c_void_p(stream.cuda_stream)
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return c_void_p(t.data_ptr())
+
+
+def spec_dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+# ----------------------------------------------------------------- descriptors
+
+def kv_desc_contiguous(k: torch.Tensor, v: torch.Tensor) -> KvDesc:
+    """k, v: [B][Hkv][max_seq][d]."""
+    if k.shape != v.shape or k.dim() != 4:
+        raise ValueError("k and v must be [B][Hkv][max_seq][d]")
+    _ptr(k, name="k"), _ptr(v, k.dtype, "v")
+    B, Hkv, S, d = k.shape
+    return KvDesc(SPEC_KV_CONTIGUOUS, spec_dtype(k), Hkv, d, k.data_ptr(), v.data_ptr(),
+                  B, S, 0, 0, 0, None)
+
+
+def kv_desc_paged(k: torch.Tensor, v: torch.Tensor, page_table: torch.Tensor) -> KvDesc:
+    """k, v: [n_pages][Hkv][page_size][d]; page_table int32 [B][max_pages]."""
+    if k.shape != v.shape or k.dim() != 4:
+        raise ValueError("k and v must be [n_pages][Hkv][page_size][d]")
+    _ptr(k, name="k"), _ptr(v, k.dtype, "v")
+    _ptr(page_table, torch.int32, "page_table")
+    P, Hkv, ps, d = k.shape
+    B, maxp = page_table.shape
+    return KvDesc(SPEC_KV_PAGED, spec_dtype(k), Hkv, d, k.data_ptr(), v.data_ptr(),
+                  B, 0, P, ps, maxp, page_table.data_ptr())
+
+
+def attn_desc(batch, n_rows, n_q_heads, n_kv_heads, head_dim, dtype, n_soft=0,
+              scale=0.0, split_tokens=0) -> AttnDesc:
+    return AttnDesc(batch, n_rows, n_q_heads, n_kv_heads, head_dim, dtype, n_soft,
+                    scale, split_tokens)
+
+
+def accept_desc(mode, tau, batch, n_judge_rows, vocab, logit_dtype, max_nodes,
+                path_cap) -> AcceptDesc:
+    return AcceptDesc(mode, tau, batch, n_judge_rows, vocab, logit_dtype, max_nodes,
+                      path_cap)
+
+
+# ------------------------------------------------------------------- entry points
+
+def spec_version() -> int:
+    return load_library().spec_version()
+
+
+def spec_mask_build(vparent, soft_flags, vis, row_flags, stream=None):
+    lib = load_library()
+    B, R = vparent.shape
+    W = (R + 31) // 32
+    if tuple(vis.shape) != (B, R, W) or tuple(row_flags.shape) != (B, R):
+        raise ValueError("vis must be [B][R][ceil(R/32)], row_flags [B][R]")
+    _check("spec_mask_build", lib.spec_mask_build(
+        _ptr(vparent, torch.int32, "vparent"), _ptr(soft_flags, torch.uint8, "soft_flags"),
+        B, R, _ptr(vis, torch.int32, "vis"), _ptr(row_flags, torch.uint8, "row_flags"),
+        _stream(stream)))
+
+
+def spec_verify_attn_workspace_size(attn: AttnDesc, cache: KvDesc) -> int:
+    lib = load_library()
+    n = c_size_t(0)
+    _check("spec_verify_attn_workspace_size",
+           lib.spec_verify_attn_workspace_size(ctypes.byref(attn), ctypes.byref(cache),
+                                               ctypes.byref(n)))
+    return n.value
+
+
+def spec_verify_attn(attn: AttnDesc, q, cache: KvDesc, kb, vb, soft_k, soft_v, seq_len,
+                     vis, row_flags, o, lse, workspace, stream=None):
+    lib = load_library()
+    dt = q.dtype
+    for name, t in (("kb", kb), ("vb", vb), ("o", o)):
+        _ptr(t, dt, name)
+    _check("spec_verify_attn", lib.spec_verify_attn(
+        ctypes.byref(attn), _ptr(q, name="q"), ctypes.byref(cache), _ptr(kb), _ptr(vb),
+        _ptr(soft_k, dt, "soft_k"), _ptr(soft_v, dt, "soft_v"),
+        _ptr(seq_len, torch.int32, "seq_len"), _ptr(vis, torch.int32, "vis"),
+        _ptr(row_flags, torch.uint8, "row_flags"), _ptr(o), _ptr(lse, torch.float32, "lse"),
+        _ptr(workspace, name="workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def spec_vocab_reduce(logits, proposal, argmax, lse, zprop, stream=None):
+    lib = load_library()
+    n, V = logits.shape
+    _check("spec_vocab_reduce", lib.spec_vocab_reduce(
+        _ptr(logits, name="logits"), spec_dtype(logits), n, V,
+        _ptr(proposal, torch.int32, "proposal"), _ptr(argmax, torch.int32, "argmax"),
+        _ptr(lse, torch.float32, "lse"), _ptr(zprop, torch.float32, "zprop"),
+        _stream(stream)))
+
+
+def spec_accept(desc: AcceptDesc, logits, tokens, tree_parent, row_of, n_nodes, argmax, lse,
+                zprop, acc_len, path, next_token, last_node, stream=None):
+    lib = load_library()
+    i32 = torch.int32
+    _check("spec_accept", lib.spec_accept(
+        ctypes.byref(desc), _ptr(logits, name="logits"), _ptr(tokens, i32, "tokens"),
+        _ptr(tree_parent, i32, "tree_parent"), _ptr(row_of, i32, "row_of"),
+        _ptr(n_nodes, i32, "n_nodes"), _ptr(argmax, i32, "argmax"),
+        _ptr(lse, torch.float32, "lse"), _ptr(zprop, torch.float32, "zprop"),
+        _ptr(acc_len, i32, "acc_len"), _ptr(path, i32, "path"),
+        _ptr(next_token, i32, "next_token"), _ptr(last_node, i32, "last_node"),
+        _stream(stream)))
+
+
+def kv_commit(cache: KvDesc, kb, vb, path, acc_len, seq_len, free_pages=None, free_head=None,
+              stream=None):
+    lib = load_library()
+    B, Hkv, R, d = kb.shape
+    i32 = torch.int32
+    n_free = 0 if free_pages is None else free_pages.numel()
+    _check("kv_commit", lib.kv_commit(
+        ctypes.byref(cache), B, R, _ptr(kb, name="kb"), _ptr(vb, kb.dtype, "vb"),
+        path.shape[1], _ptr(path, i32, "path"), _ptr(acc_len, i32, "acc_len"),
+        _ptr(seq_len, i32, "seq_len"), _ptr(free_pages, i32, "free_pages"), n_free,
+        _ptr(free_head, i32, "free_head"), _stream(stream)))
+
+
+def spec_get_status(stream=None) -> int:
+    """Synchronise, read and clear the device status word (SPEC_DEV_* bits)."""
+    lib = load_library()
+    out = ctypes.c_int32(0)
+    code = lib.spec_get_status(_stream(stream), ctypes.byref(out))
+    if code not in (SPEC_OK, SPEC_ERR_DEVICE):
+        _check("spec_get_status", code)
+    return out.value

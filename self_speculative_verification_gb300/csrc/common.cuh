@@ -1,0 +1,54 @@
+// Shared helpers of libspecverify's CUDA sources (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "specverify.h"
+
+namespace sv {
+
+// Device address of the per-device status word (SPEC_DEV_* bits) for the
+// current device; nullptr if it cannot be resolved.
+int *status_ptr();
+
+// Number of SMs of the current device (cached per device).
+int num_sms();
+
+inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline spec_status_t launch_status() {
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+__host__ __device__ inline long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ void raise_status(int *st, int bits) {
+    if (st) atomicOr(st, bits);
+}
+
+__device__ __forceinline__ float load_f(const float *p) { return *p; }
+__device__ __forceinline__ float load_f(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+
+__device__ __forceinline__ void store_f(float *p, float x) { *p = x; }
+__device__ __forceinline__ void store_f(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+}  // namespace sv

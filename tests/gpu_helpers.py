@@ -1,0 +1,196 @@
+"""Shared helpers of the GPU parity tests: run the oracle on a workload and
+compare the CUDA path's outputs with it.
+
+Tolerances (GPU vs float64 oracle):
+* bf16 attention outputs: max |O_gpu - O_ref| <= 1e-2 and
+  ||O_gpu - O_ref|| / ||O_ref|| <= 1e-2; LSE relative error <= 1e-3.
+* fp32 attention: max abs <= 2e-5, LSE relative <= 1e-5.
+* vocab reduce: argmax exact; LSE relative <= 1e-5; proposal logit exact.
+* mask, acceptance (lengths, paths, next tokens, last nodes) and the
+  committed cache: bit-exact.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from self_speculative_verification_gb300 import workloads as W
+from self_speculative_verification_gb300.device import DeviceStep
+
+TOL = {
+    "bf16": dict(o_abs=1e-2, o_rel_norm=1e-2, lse_rel=1e-3),
+    "f32": dict(o_abs=2e-5, o_rel_norm=1e-5, lse_rel=1e-5),
+}
+
+
+def require_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def unpack_vis(vis: np.ndarray, R: int) -> np.ndarray:
+    """[B][R][W] int32 words -> [B][R][R] bool (bit c of word c//32)."""
+    u = vis.astype(np.int64) & 0xFFFFFFFF
+    B = u.shape[0]
+    out = np.zeros((B, R, R), dtype=bool)
+    for c in range(R):
+        out[:, :, c] = (u[:, :, c // 32] >> (c % 32)) & 1
+    return out
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def check_mask(ds: DeviceStep):
+    wl = ds.wl
+    vis, valid, sees = oracle.mask_build(wl.vparent, wl.soft_flags)
+    got = unpack_vis(ds.vis.cpu().numpy(), wl.R)
+    assert np.array_equal(got, vis)
+    fl = ds.row_flags.cpu().numpy()
+    assert np.array_equal((fl & 1) != 0, valid)
+    assert np.array_equal((fl & 2) != 0, sees)
+    return vis, valid, sees
+
+
+def oracle_attention(wl, vis, valid, sees, requests=None, heads=None):
+    pk, pv = [], []
+    for b in range(wl.B):
+        if requests is None or b in requests:
+            k, v = wl.prefix_kv(b)
+        else:
+            k = v = np.zeros((wl.Hkv, 0, wl.d), dtype=np.float32)
+        pk.append(k)
+        pv.append(v)
+    return oracle.verify_attention(wl.q, pk, pv, wl.kb, wl.vb, vis, valid, sees,
+                                   soft_k=wl.soft_k, soft_v=wl.soft_v,
+                                   requests=requests, heads=heads)
+
+
+def check_attention(ds: DeviceStep, O_ref, L_ref, requests=None, heads=None):
+    wl = ds.wl
+    tol = TOL[wl.dtype]
+    O = f64(ds.o)
+    L = ds.lse.cpu().numpy().astype(np.float64)
+    bs = list(range(wl.B)) if requests is None else list(requests)
+    hs = list(range(wl.Hq)) if heads is None else list(heads)
+    Og = O[bs][:, :, hs]
+    Or = O_ref[bs][:, :, hs]
+    Lg = L[bs][:, hs]
+    Lr = L_ref[bs][:, hs]
+    assert np.isfinite(Og).all()
+    err = np.abs(Og - Or)
+    assert err.max() <= tol["o_abs"], f"max abs err {err.max()}"
+    nrm = np.linalg.norm(Or)
+    if nrm > 0:
+        assert np.linalg.norm(Og - Or) / nrm <= tol["o_rel_norm"], \
+            f"relative norm err {np.linalg.norm(Og - Or) / nrm}"
+    fin = np.isfinite(Lr)
+    assert np.array_equal(np.isfinite(Lg), fin)
+    assert np.all(Lg[~fin] == -np.inf)
+    rel = np.abs(Lg[fin] - Lr[fin]) / np.maximum(np.abs(Lr[fin]), 1e-30)
+    if rel.size:
+        assert rel.max() <= tol["lse_rel"], f"LSE rel err {rel.max()}"
+    return err.max(), (rel.max() if rel.size else 0.0)
+
+
+def oracle_accept(wl):
+    logits = wl.logits.reshape(wl.B * wl.Rj, wl.V)
+    prop = wl.tokens.reshape(-1) if wl.mode == "la" else None
+    am, lse, zp = oracle.vocab_reduce(logits, prop)
+    am, lse, zp = (a.reshape(wl.B, wl.Rj) for a in (am, lse, zp))
+    mode = oracle.MODE_THRESH_CHAIN if wl.mode == "la" else oracle.MODE_GREEDY_TREE
+    acc, paths, nxt, last = oracle.accept(mode, wl.tau, wl.tokens, wl.tree_parent,
+                                          wl.n_nodes, am, lse, zp)
+    return am, lse, zp, acc, paths, nxt, last
+
+
+def check_accept(ds: DeviceStep):
+    wl = ds.wl
+    am, lse, zp, acc, paths, nxt, last = oracle_accept(wl)
+    assert np.array_equal(ds.argmax.cpu().numpy(), am)
+    lg = ds.lse_v.cpu().numpy().astype(np.float64)
+    assert (np.abs(lg - lse) / np.abs(lse)).max() <= 1e-5
+    if wl.mode == "la":
+        assert np.array_equal(ds.zprop.cpu().numpy().astype(np.float64), zp)
+    acc_g = ds.acc_len.cpu().numpy()
+    path_g = ds.path.cpu().numpy()
+    assert acc_g.tolist() == acc.tolist()
+    assert acc_g.tolist() == wl.expect_acc_len.tolist()
+    for b in range(wl.B):
+        assert path_g[b, : acc_g[b]].tolist() == paths[b]
+        assert np.all(path_g[b, acc_g[b]:] == -1)
+    assert ds.next_token.cpu().numpy().tolist() == nxt.tolist()
+    assert ds.last_node.cpu().numpy().tolist() == last.tolist()
+    return acc, paths
+
+
+def cache_bits(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy()
+    return t.view(torch.int32).cpu().numpy()
+
+
+def block_bits(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Storage bits of a generator block array (float32 holding dtype values)."""
+    if dtype == "bf16":
+        return (x.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16).view(np.int16)
+    return x.astype(np.float32).view(np.int32)
+
+
+def check_commit(ds: DeviceStep, before_k, before_v, paths):
+    """The cache after the step equals the cache before it, except the new
+    slots, which hold the accepted rows' K/V bits; bookkeeping matches."""
+    wl = ds.wl
+    after_k = cache_bits(ds.k_cache)
+    after_v = cache_bits(ds.v_cache)
+    kb_bits = block_bits(wl.kb, wl.dtype)
+    vb_bits = block_bits(wl.vb, wl.dtype)
+    exp_k = before_k.copy()
+    exp_v = before_v.copy()
+    seq = wl.seq_len.astype(np.int64)
+    if wl.paged:
+        pt, seq2, head = wl.page_table.copy(), seq.copy(), 0
+        ps = wl.page_size
+        for b, path in enumerate(paths):
+            for i, row in enumerate(path):
+                pos = int(seq[b]) + i
+                j = pos // ps
+                if pos % ps == 0:
+                    pt[b, j] = wl.free_pages[head]
+                    head += 1
+                exp_k[pt[b, j], :, pos % ps] = kb_bits[b, :, row]
+                exp_v[pt[b, j], :, pos % ps] = vb_bits[b, :, row]
+            seq2[b] += len(path)
+        assert np.array_equal(ds.page_table.cpu().numpy(), pt)
+        assert int(ds.free_head.item()) == head
+    else:
+        seq2 = seq.copy()
+        for b, path in enumerate(paths):
+            for i, row in enumerate(path):
+                exp_k[b, :, int(seq[b]) + i] = kb_bits[b, :, row]
+                exp_v[b, :, int(seq[b]) + i] = vb_bits[b, :, row]
+            seq2[b] += len(path)
+    assert np.array_equal(after_k, exp_k)
+    assert np.array_equal(after_v, exp_v)
+    assert ds.seq_len.cpu().numpy().tolist() == seq2.tolist()
+
+
+def run_and_check(wl, split_tokens=0, requests=None, heads=None):
+    """Full parity check of one step on a (small) workload."""
+    ds = DeviceStep(wl, split_tokens=split_tokens)
+    before_k = cache_bits(ds.k_cache)
+    before_v = cache_bits(ds.v_cache)
+    ds.run()
+    torch.cuda.synchronize()
+    from self_speculative_verification_gb300 import binding
+    assert binding.spec_get_status() == 0
+    vis, valid, sees = check_mask(ds)
+    O_ref, L_ref = oracle_attention(wl, vis, valid, sees, requests, heads)
+    errs = check_attention(ds, O_ref, L_ref, requests, heads)
+    acc, paths = check_accept(ds)
+    check_commit(ds, before_k, before_v, paths)
+    return ds, errs
