@@ -1,0 +1,496 @@
+#!/usr/bin/env python
+"""Benchmark of the self-speculative verification step on GB300.
+
+One step = the whole hot path on one batch: spec_mask_build ->
+spec_verify_attn -> spec_accept (vocab reduce + acceptance) -> kv_commit,
+through the libspecverify C ABI, plus the restore of seq_len / free_head
+(two 4-byte-per-request device copies) so every step does the same work.
+
+Default workload: the long-context paged verify (64 requests, 32 q heads /
+8 KV heads, head_dim 128, bf16, 16-token pages, prefix ~ U[16384, 32768],
+8 lookahead rows, threshold acceptance over vocab 32000).
+
+Prints ONE JSON line (rank 0).  Metric: verified speculative tokens per
+second (candidate tokens judged per step / step time).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+  python bench.py --impl reference ...   # the CPU oracle, timed the same way
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verified spec tokens/s (attn+accept+commit)"
+UNIT = "tokens/s"
+L2_BYTES = 126 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------- helpers
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--config", default="long_paged")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-workers", type=int, default=0)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def workload_label(wl):
+    seq = f"S~U[{int(wl.seq_len.min())},{int(wl.seq_len.max())}]"
+    return (f"{wl.name}: B={wl.B} R={wl.R} Hq/Hkv={wl.Hq}/{wl.Hkv} d={wl.d} {wl.dtype} "
+            f"{'paged(16-token pages)' if wl.paged else 'contiguous'} KV, {seq}, "
+            f"n_soft={wl.n_soft}, V={wl.V}, {'threshold' if wl.mode == 'la' else 'greedy tree'}")
+
+
+def attn_algorithmic_bytes(wl):
+    """Bytes spec_verify_attn must move (nothing dense over masked columns)."""
+    e = 2 if wl.dtype == "bf16" else 4
+    W = (wl.R + 31) // 32
+    S = wl.seq_len.astype("int64")
+    prefix = int(S.sum()) * wl.Hkv * wl.d * 2 * e
+    block = wl.B * wl.R * wl.Hkv * wl.d * 2 * e
+    soft = wl.n_soft * wl.Hkv * wl.d * 2 * e
+    qo = wl.B * wl.R * wl.Hq * wl.d * e * 2
+    lse = wl.B * wl.Hq * wl.R * 4
+    ints = wl.B * 4 + wl.B * wl.R * (W * 4 + 1)
+    if wl.paged:
+        ints += int(((S + wl.page_size - 1) // wl.page_size).sum()) * 4
+    return prefix + block + soft + qo + lse + ints
+
+
+def step_algorithmic_bytes(wl, accepted_rows):
+    e = 2 if wl.dtype == "bf16" else 4
+    le = 2 if wl.logit_dtype == "bf16" else 4
+    logits = wl.B * wl.Rj * wl.V * le
+    accept_io = wl.B * wl.N * 4 * 3 + wl.B * wl.Rj * 12 + wl.B * (wl.path_cap + 3) * 4
+    commit = accepted_rows * wl.Hkv * wl.d * 2 * e * 2
+    mask = wl.B * wl.R * (4 + 1 + 1 + 4 * ((wl.R + 31) // 32))
+    return attn_algorithmic_bytes(wl) + logits + accept_io + commit + mask
+
+
+def kernel_sources_sha():
+    from self_speculative_verification_gb300 import _build
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(_build.CSRC)):
+        if f.startswith("attn") or f.startswith("verify_attn"):
+            with open(os.path.join(_build.CSRC, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config):
+    """DRAM bytes per spec_verify_attn call from the committed ncu summary,
+    or None if the attention sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        rec = d.get(config)
+        if rec and rec.get("source_sha") == kernel_sources_sha():
+            return rec.get("dram_bytes_per_call")
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), max=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        load = [r for r in rows if r["power"] > 0.3 * max(x["power"] for x in rows)] or rows
+        reasons = []
+        for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                          ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+            if any(r[key].lower() == "active" for r in load):
+                reasons.append(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load),
+                "sm_max_mhz": max(r["max"] for r in rows), "reasons": reasons,
+                "samples": len(load)}
+
+
+# --------------------------------------------------------------- CPU oracle
+
+def _oracle_worker(conn, config, seed, requests):
+    """Runs in a spawned process: the oracle on a sample of requests."""
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    import numpy as np
+    import oracle
+    from self_speculative_verification_gb300 import workloads as W
+    wl = W.make_workload(config, seed)
+    kv = {b: wl.prefix_kv(b) for b in requests}
+    empty = np.zeros((wl.Hkv, 0, wl.d), dtype=np.float32)
+    pk = [kv[b][0] if b in kv else empty for b in range(wl.B)]
+    pv = [kv[b][1] if b in kv else empty for b in range(wl.B)]
+    conn.send(("ready", sum(int(wl.n_nodes[b]) for b in requests)))
+    mode = oracle.MODE_THRESH_CHAIN if wl.mode == "la" else oracle.MODE_GREEDY_TREE
+    while True:
+        msg = conn.recv()
+        if msg == "stop":
+            break
+        t0 = time.perf_counter()
+        for b in requests:
+            vp = wl.vparent[b:b + 1]
+            vis, valid, sees = oracle.mask_build(vp, wl.soft_flags[b:b + 1])
+            O, L = oracle.verify_attention(
+                wl.q[b:b + 1], [pk[b]], [pv[b]], wl.kb[b:b + 1], wl.vb[b:b + 1], vis, valid,
+                sees, soft_k=wl.soft_k, soft_v=wl.soft_v)
+            prop = wl.tokens[b] if wl.mode == "la" else None
+            am, lse, zp = oracle.vocab_reduce(wl.logits[b], prop)
+            acc, paths, nxt, last = oracle.accept(
+                mode, wl.tau, wl.tokens[b:b + 1], wl.tree_parent[b:b + 1],
+                wl.n_nodes[b:b + 1], am[None], lse[None], zp[None])
+            # commit the accepted rows into the request's own logical cache
+            K = np.concatenate([pk[b], np.zeros((wl.Hkv, wl.R, wl.d), np.float32)], axis=1)
+            oracle.kv_commit_contiguous(K[None], K[None], [int(wl.seq_len[b])],
+                                        wl.kb[b:b + 1], wl.vb[b:b + 1], paths)
+        conn.send(("done", time.perf_counter() - t0))
+    conn.close()
+
+
+class OracleWorkers:
+    """A spawned pool of oracle processes, one request sample each."""
+
+    def __init__(self, config, seed, n_workers, B):
+        ctx = mp.get_context("spawn")
+        n = max(1, min(n_workers, B))
+        self.conns, self.procs = [], []
+        self.tokens = 0
+        self.requests = list(range(n))
+        for i in range(n):
+            a, b = ctx.Pipe()
+            p = ctx.Process(target=_oracle_worker, args=(b, config, seed, [i]), daemon=True)
+            p.start()
+            self.conns.append(a)
+            self.procs.append(p)
+        for c in self.conns:
+            tag, tok = c.recv()
+            self.tokens += tok
+        self.n = n
+
+    def step(self):
+        t0 = time.perf_counter()
+        for c in self.conns:
+            c.send("go")
+        times = [c.recv()[1] for c in self.conns]
+        return time.perf_counter() - t0, max(times)
+
+    def close(self):
+        for c in self.conns:
+            try:
+                c.send("stop")
+            except Exception:
+                pass
+        for p in self.procs:
+            p.join(timeout=10)
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle as it stands, timed on host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from self_speculative_verification_gb300 import workloads as W
+    cfg = W.CONFIGS[args.config]
+    cores = args.cpu_workers or host_cores()
+    workers = OracleWorkers(args.config, args.seed, cores, cfg["B"])
+    try:
+        for _ in range(args.warmup):
+            workers.step()
+        walls = [workers.step()[0] for _ in range(args.steps)]
+    finally:
+        workers.close()
+    wl = W.make_workload(args.config, args.seed)
+    t = sum(walls)
+    value = workers.tokens * len(walls) / t
+    sample = (f"requests 0..{workers.n - 1} of {args.config} (all heads, their logits rows), "
+              f"one per spawned process; each step re-runs the sample")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * t / len(walls), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_label(wl), "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": workers.n, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(args, wl):
+    cores = args.cpu_workers or host_cores()
+    workers = OracleWorkers(args.config, args.seed, cores, wl.B)
+    try:
+        workers.step()                       # warm
+        walls = [workers.step()[0] for _ in range(2)]
+    finally:
+        workers.close()
+    value = workers.tokens * len(walls) / sum(walls)
+    return {"value": value, "unit": UNIT, "cores": workers.n, "kind": "oracle",
+            "sample": f"requests 0..{workers.n - 1} of the workload (all heads, logits rows, "
+                      f"acceptance, commit), one per spawned process, best-effort float64 numpy"}
+
+
+# ------------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    # CPU baseline processes start (spawn) before the first GPU call
+    cpu = None
+    from self_speculative_verification_gb300 import workloads as W
+    from self_speculative_verification_gb300 import binding as bn
+    from self_speculative_verification_gb300.device import DeviceStep
+
+    wl = W.make_workload(args.config, args.seed + rank)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args, wl)
+
+    bn.load_library()
+    ds = DeviceStep(wl, device=dev, threads=16)
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+
+    attn_bytes = attn_algorithmic_bytes(wl)
+    footprint = attn_bytes + wl.B * wl.Rj * wl.V * 2
+    flush = footprint < 2 * L2_BYTES
+    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush else None
+
+    def step(ev=None):
+        ds.reset_state()
+        if ev is not None:
+            ev[0].record(stream)
+        ds.mask_build()
+        if ev is not None:
+            ev[1].record(stream)
+        ds.verify_attn()
+        if ev is not None:
+            ev[2].record(stream)
+        ds.accept_step()
+        if ev is not None:
+            ev[3].record(stream)
+        ds.commit()
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+        if flush:
+            flush_buf.random_()
+    torch.cuda.synchronize(dev)
+    assert bn.spec_get_status() == 0, "device status set during warm-up"
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    region = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        region[0].record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+            if flush:
+                flush_buf.random_()
+        region[1].record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    status = bn.spec_get_status()
+
+    per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)]
+                    for i in range(args.steps)])          # ms: mask, attn, accept, commit
+    step_ms = per.sum(axis=1)
+    region_ms = region[0].elapsed_time(region[1])
+    total_ms = float(step_ms.sum()) if flush else region_ms
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    tokens = wl.verified_tokens()
+    value = tokens * args.steps * world / (total_ms / 1e3)
+    attn_ms = float(per[:, 1].mean())
+    hbm, hbm_kind = peaks()
+    achieved = attn_bytes / (attn_ms / 1e3) / 1e9
+    accepted_rows = int(ds.acc_len.sum().item())
+
+    # e2e: host (pinned) inputs -> device, the four calls, results -> host
+    e2e = None
+    if args.e2e_steps > 0:
+        e2e = run_e2e(ds, args.e2e_steps, stream)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    ms_step = total_ms / args.steps
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": wl.dtype, "data": "synthetic",
+        "config": {
+            "workload": workload_label(wl),
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": ("flushed between steps (2x L2 buffer written)" if flush else
+                   f"inputs larger than L2 ({attn_bytes / 1e9:.2f} GB per step vs 126 MB L2)"),
+            "seed": args.seed,
+            "verified_tokens_per_step": tokens,
+            "accepted_rows_per_step": accepted_rows,
+            "per_call_ms": {"mask_build": float(per[:, 0].mean()), "verify_attn": attn_ms,
+                            "accept": float(per[:, 2].mean()), "kv_commit": float(per[:, 3].mean())},
+            "step_includes": "seq_len/free_head restore (2 small device copies)",
+            "step_algorithmic_bytes": step_algorithmic_bytes(wl, accepted_rows),
+        },
+        "roofline": {
+            "kernel": "spec_verify_attn (split kernel + combine kernel)",
+            "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "peak_kind": f"{hbm_kind} HBM copy bandwidth",
+            "algorithmic_bytes_per_call": attn_bytes,
+            "traffic": recorded_traffic(args.config),
+        },
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": DeviceStep.LAUNCHES_PER_STEP * args.steps,
+        "device_status": status,
+    }
+    line["clocks"] = clk.summary()
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(ds, steps, stream):
+    """The same step through the C ABI with host buffers: pinned host inputs
+    copied in, results (acceptance outputs) copied out, every step."""
+    import torch
+    inputs = [t for t in (ds.q, ds.kb, ds.vb, ds.soft_k, ds.soft_v, ds.vparent,
+                          ds.soft_flags, ds.logits, ds.tokens, ds.tree_parent, ds.n_nodes)
+              if t is not None]
+    outputs = [ds.acc_len, ds.path, ds.next_token, ds.last_node]
+    h_in = [t.cpu().pin_memory() for t in inputs]
+    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outputs]
+    bi = sum(t.numel() * t.element_size() for t in inputs)
+    bo = sum(t.numel() * t.element_size() for t in outputs)
+
+    def one():
+        for d, h in zip(inputs, h_in):
+            d.copy_(h, non_blocking=True)
+        ds.reset_state()
+        ds.run()
+        for h, d in zip(h_out, outputs):
+            h.copy_(d, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    dt = time.perf_counter() - t0
+    tokens = ds.wl.verified_tokens()
+    return {"value": tokens * steps / dt, "unit": UNIT, "h2d_bytes_per_step": bi,
+            "d2h_bytes_per_step": bo, "ms_per_step": 1e3 * dt / steps,
+            "timing": "host wall clock per step, stream synchronised each step"}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
