@@ -91,6 +91,7 @@ typedef int spec_status_t;
 #define SPEC_DEV_SEQ_OVERFLOW 0x04  /* seq_len outside [0, cache capacity] */
 #define SPEC_DEV_CAPACITY     0x08  /* commit: cache or free list full */
 #define SPEC_DEV_BAD_INDEX    0x10  /* path / row_of / acc_len out of range */
+#define SPEC_DEV_TIMEOUT      0x20  /* an internal pipeline wait expired */
 
 /* Maximum speculative rows per request (block columns). */
 #define SPEC_MAX_ROWS 256
@@ -207,7 +208,8 @@ spec_status_t spec_verify_attn_workspace_size(const spec_attn_desc *attn,
  * SPEC_ROW_SEES_SOFT, and block column c iff vis bit c; scores are
  * (q . k) * scale.  Rows without SPEC_ROW_VALID get o = 0, lse = -inf.
  * A seq_len outside [0, capacity] is clamped and sets SPEC_DEV_SEQ_OVERFLOW;
- * a page id outside [0, n_pages) reads as zeros and sets SPEC_DEV_BAD_PAGE.
+ * a page id outside [0, n_pages) is not read and sets SPEC_DEV_BAD_PAGE (the
+ * affected outputs are then unspecified).
  */
 spec_status_t spec_verify_attn(const spec_attn_desc *attn, const void *q,
                                const spec_kv_desc *cache, const void *kb,

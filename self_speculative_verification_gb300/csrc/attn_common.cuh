@@ -35,6 +35,7 @@ struct AttnParams {
     int *status;
     int B, R, Hq, Hkv, G, d, M, W, n_soft;
     int paged, max_seq, page_size, max_pages, n_pages, capacity;
+    long long cache_rows;    // rows of the cache viewed as [rows][d]
     int chunk, max_splits;
     int n_rb, rb_rows;       // row blocks of packed rows per (request, KV head)
     float scale_log2;        // softmax scale * log2(e)

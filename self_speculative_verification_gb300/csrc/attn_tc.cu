@@ -1,12 +1,805 @@
-// Tensor-core verify-attention kernel: not yet enabled in this build.
+// Tensor-core verify attention for bf16 (sm_103a).
+//
+// Same result as the CUDA-core kernel in verify_attn.cu ("Speculative
+// Streaming" Eq. 1-2 and Eq. 4, "Lookahead Attention" sec. 3.1, "ConFu" key
+// design 1): masked softmax attention of the speculative rows over
+// (committed prefix || soft prompt || block).
+//
+// Design (GB300):
+// * Work as one linear space of 64-token tiles.  A segment is one (request,
+//   KV head, row block): its prefix tiles, then its soft-prompt tiles, then
+//   its block tiles.  The persistent grid (one CTA per SM) cuts the space
+//   into equal contiguous ranges, so every CTA streams the same number of
+//   tiles whatever the prefix lengths; a CTA writes one fp32 partial
+//   (m, l, O) per segment it touches, and the combine kernel merges them.
+// * Warp specialisation: one producer warp issues TMA tile loads
+//   (cp.async.bulk.tensor, 128-byte swizzle) into a ring of shared-memory
+//   stages guarded by mbarriers; four consumer warps compute.  Paged caches
+//   load one box per page; contiguous caches one box per 64 tokens.
+// * Consumers: S = Q K^T and O += P V on tensor cores (m16n8k16 bf16, fp32
+//   accumulate), online softmax in registers (exp2 domain), masks applied
+//   as selects on the scores; K/V rows past the valid count of a ragged
+//   tile are never used (scores -> -inf, V fragments -> 0).
+// * Packed rows (GQA): packed row p = r * G + g of KV head h is query head
+//   h * G + g of speculative row r.  Warps tile the row block 16 rows at a
+//   time; when the block has fewer than 64 rows the warps also split the
+//   64 tokens of a tile and each writes its own partial.
+// * Every mbarrier wait is bounded (clock64); on expiry the kernel sets
+//   SPEC_DEV_TIMEOUT and stops, after waiting (bounded) for its own copies.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "attn_tc.cuh"
 
 namespace sv {
+namespace {
 
-bool tc_supported(const AttnParams &, int) { return false; }
+constexpr int kTile = 64;                 // tokens per tile
+constexpr int kHalfBytes = kTile * 128;   // one 64-token x 64-element bf16 box
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr long long kTimeoutCycles = 2000000000ll;
 
-int tc_rows_per_block(const AttnParams &) { return 64; }
+struct TcParams {
+    AttnParams a;
+    int n_ctas;
+    int soft_tiles;      // ceil(n_soft / 64)
+    int tail;            // soft_tiles + ceil(R / 64)
+    int box_rows;        // rows per cache box: 64 (contiguous) or page_size
+};
 
-spec_status_t launch_attn_tc(const AttnParams &, cudaStream_t) { return SPEC_ERR_UNSUPPORTED; }
+// ------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > kTimeoutCycles) return false;
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Address of 16-byte chunk `chunk` (0..7) of row `row` in a 128B-swizzled
+// [rows][128 B] box whose base is 1024-byte aligned.
+__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk) {
+    return base + row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+// -------------------------------------------------------------- schedule
+
+__device__ __forceinline__ int req_seq(const TcParams &P, int b) {
+    int S = P.a.seq_len[b];
+    return S < 0 ? 0 : (S > P.a.capacity ? P.a.capacity : S);
+}
+
+__device__ __forceinline__ int seg_tiles(const TcParams &P, int S) {
+    return ceil_div(S, kTile) + P.tail;
+}
+
+__device__ __forceinline__ long long req_tiles(const TcParams &P, int b) {
+    return (long long)seg_tiles(P, req_seq(P, b)) * P.a.Hkv * P.a.n_rb;
+}
+
+__device__ __forceinline__ long long warp_sum_ll(long long x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// Total tiles over all requests (every lane gets it).
+__device__ long long warp_total_tiles(const TcParams &P) {
+    const int lane = threadIdx.x & 31;
+    long long s = 0;
+    for (int b = lane; b < P.a.B; b += 32) s += req_tiles(P, b);
+    return warp_sum_ll(s);
+}
+
+// Tiles of requests before b (every lane gets it).
+__device__ long long warp_tiles_before(const TcParams &P, int b) {
+    const int lane = threadIdx.x & 31;
+    long long s = 0;
+    for (int i = lane; i < b; i += 32) s += req_tiles(P, i);
+    return warp_sum_ll(s);
+}
+
+// Request containing linear tile t (< total), and its first tile.
+__device__ void warp_locate(const TcParams &P, long long t, int *b_out, long long *start_out) {
+    const int lane = threadIdx.x & 31;
+    const int B = P.a.B;
+    const int per = ceil_div(B, 32);
+    const int lo = min(B, lane * per), hi = min(B, lo + per);
+    long long sum = 0;
+    for (int b = lo; b < hi; ++b) sum += req_tiles(P, b);
+    long long incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const long long excl = incl - sum;
+    const unsigned m = __ballot_sync(0xffffffffu, lo < hi && t >= excl && t < incl);
+    const int src = m ? __ffs(m) - 1 : 0;
+    long long acc = __shfl_sync(0xffffffffu, excl, src);
+    int b = src * per;
+    while (b < B - 1) {
+        const long long n = req_tiles(P, b);
+        if (t < acc + n) break;
+        acc += n;
+        ++b;
+    }
+    *b_out = b;
+    *start_out = acc;
+}
+
+// First tile of CTA i's range.
+__device__ __forceinline__ long long range_lo(long long T, int i, int n) { return T * i / n; }
+
+// CTA whose range holds tile t.
+__device__ __forceinline__ int cta_of(long long T, long long t, int n) {
+    long long i = ((t + 1) * n - 1) / T;
+    return (int)(i < n - 1 ? i : n - 1);
+}
+
+struct Cursor {
+    int b, h, rb;
+    int S, n_prefix, n_tiles;
+    int tile;
+};
+
+__device__ void cursor_init(const TcParams &P, long long t, Cursor &c) {
+    long long start;
+    warp_locate(P, t, &c.b, &start);
+    c.S = req_seq(P, c.b);
+    c.n_prefix = ceil_div(c.S, kTile);
+    c.n_tiles = c.n_prefix + P.tail;
+    const long long local = t - start;
+    const int seg = (int)(local / c.n_tiles);
+    c.tile = (int)(local % c.n_tiles);
+    c.h = seg / P.a.n_rb;
+    c.rb = seg % P.a.n_rb;
+}
+
+__device__ __forceinline__ void cursor_next(const TcParams &P, Cursor &c) {
+    if (++c.tile < c.n_tiles) return;
+    c.tile = 0;
+    if (++c.rb < P.a.n_rb) return;
+    c.rb = 0;
+    if (++c.h < P.a.Hkv) return;
+    c.h = 0;
+    if (++c.b < P.a.B) {
+        c.S = req_seq(P, c.b);
+        c.n_prefix = ceil_div(c.S, kTile);
+        c.n_tiles = c.n_prefix + P.tail;
+    }
+}
+
+enum { kPrefix = 0, kSoft = 1, kBlock = 2 };
+
+struct TileInfo {
+    int kind, base, nvalid, j;
+};
+
+__device__ __forceinline__ TileInfo tile_info(const TcParams &P, const Cursor &c) {
+    TileInfo ti;
+    if (c.tile < c.n_prefix) {
+        ti.kind = kPrefix;
+        ti.j = c.tile;
+        ti.base = c.tile * kTile;
+        ti.nvalid = min(kTile, c.S - ti.base);
+    } else if (c.tile - c.n_prefix < P.soft_tiles) {
+        ti.kind = kSoft;
+        ti.j = c.tile - c.n_prefix;
+        ti.base = ti.j * kTile;
+        ti.nvalid = min(kTile, P.a.n_soft - ti.base);
+    } else {
+        ti.kind = kBlock;
+        ti.j = c.tile - c.n_prefix - P.soft_tiles;
+        ti.base = ti.j * kTile;
+        ti.nvalid = min(kTile, P.a.R - ti.base);
+    }
+    return ti;
+}
+
+__device__ __forceinline__ size_t slot_row(const TcParams &P, int seg, int cta, int wc, int wcn,
+                                           int row) {
+    return ((size_t)(seg + cta) * wcn + wc) * P.a.rb_rows + row;
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <int D, int WR>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUtensorMap mk,
+               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mkb,
+               const __grid_constant__ CUtensorMap mvb, const __grid_constant__ CUtensorMap msk,
+               const __grid_constant__ CUtensorMap msv) {
+    constexpr int NH = D / 64;                       // 128-byte halves per row
+    constexpr int KV_BYTES = NH * kHalfBytes;        // K (or V) of one tile
+    constexpr int STAGE = 2 * KV_BYTES;
+    constexpr int NS = D == 128 ? 5 : 8;
+    constexpr int WC = kConsumerWarps / WR;          // warps splitting a tile's tokens
+    constexpr int TW = kTile / WC;                   // tokens per warp per tile
+    constexpr int NT = TW / 8;                       // n8 score tiles per warp
+    constexpr int ND = D / 8;                        // n8 output tiles
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * STAGE);
+    uint64_t *empty = full + NS;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const AttnParams &A = P.a;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+
+    const long long T = warp_total_tiles(P);
+    const int cta = blockIdx.x;
+    const long long t_begin = range_lo(T, cta, P.n_ctas);
+    const long long t_end = range_lo(T, cta + 1, P.n_ctas);
+    if (t_begin >= t_end) return;
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------ producer
+        Cursor c;
+        cursor_init(P, t_begin, c);          // warp-collective
+        if (lane != 0) return;
+        // the prefix is read once unless several row blocks share it
+        const uint64_t pol_keep = policy_evict_last();
+        const uint64_t pol_stream = A.n_rb == 1 ? policy_evict_first() : pol_keep;
+        long long k = 0;
+        bool ok = true;
+        for (long long t = t_begin; t < t_end; ++t, ++k) {
+            const int s = (int)(k % NS);
+            const uint32_t ph = (uint32_t)((k / NS) & 1);
+            if (!mbar_wait(&empty[s], ph ^ 1)) {
+                raise_status(A.status, SPEC_DEV_TIMEOUT);
+                ok = false;
+                break;
+            }
+            uint8_t *kbuf = smem + s * STAGE;
+            uint8_t *vbuf = kbuf + KV_BYTES;
+            const TileInfo ti = tile_info(P, c);
+            if (ti.kind == kPrefix && A.paged) {
+                const int ps = P.box_rows;
+                const int npg = kTile / ps;
+                int pages[4];
+                uint32_t bytes = 0;
+                for (int i = 0; i < npg; ++i) {
+                    const int tok = ti.base + i * ps;
+                    int pg = -1;
+                    if (tok < c.S) {
+                        pg = A.page_table[(size_t)c.b * A.max_pages + tok / ps];
+                        if (pg < 0 || pg >= A.n_pages) {
+                            raise_status(A.status, SPEC_DEV_BAD_PAGE);
+                            pg = -1;
+                        }
+                    }
+                    pages[i] = pg;
+                    if (pg >= 0) bytes += 2u * NH * ps * 128u;
+                }
+                mbar_arrive_expect_tx(&full[s], bytes);
+                for (int i = 0; i < npg; ++i) {
+                    if (pages[i] < 0) continue;
+                    const int row = (pages[i] * A.Hkv + c.h) * ps;
+                    for (int hh = 0; hh < NH; ++hh) {
+                        tma_load_2d(kbuf + hh * kHalfBytes + i * ps * 128, &mk, hh * 64, row,
+                                    &full[s], pol_stream);
+                        tma_load_2d(vbuf + hh * kHalfBytes + i * ps * 128, &mv, hh * 64, row,
+                                    &full[s], pol_stream);
+                    }
+                }
+            } else {
+                const CUtensorMap *km, *vm;
+                int row;
+                uint64_t pol = pol_keep;
+                if (ti.kind == kPrefix) {
+                    km = &mk;
+                    vm = &mv;
+                    row = (c.b * A.Hkv + c.h) * A.max_seq + ti.base;
+                    pol = pol_stream;
+                } else if (ti.kind == kSoft) {
+                    km = &msk;
+                    vm = &msv;
+                    row = c.h * A.n_soft + ti.base;
+                } else {
+                    km = &mkb;
+                    vm = &mvb;
+                    row = (c.b * A.Hkv + c.h) * A.R + ti.base;
+                }
+                mbar_arrive_expect_tx(&full[s], (uint32_t)STAGE);
+                for (int hh = 0; hh < NH; ++hh) {
+                    tma_load_2d(kbuf + hh * kHalfBytes, km, hh * 64, row, &full[s], pol);
+                    tma_load_2d(vbuf + hh * kHalfBytes, vm, hh * 64, row, &full[s], pol);
+                }
+            }
+            cursor_next(P, c);
+        }
+        // do not leave while copies into this CTA's shared memory are in flight
+        const long long last = k;
+        for (long long kk = last - 1; kk >= 0 && kk >= last - NS; --kk) {
+            if (!mbar_wait(&full[kk % NS], (uint32_t)((kk / NS) & 1))) {
+                raise_status(A.status, SPEC_DEV_TIMEOUT);
+                break;
+            }
+        }
+        (void)ok;
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    const int wr = warp % WR, wc = warp / WR;
+    const int g = lane >> 2, cq = lane & 3;
+    const int c0 = wc * TW;                  // first token of this warp in a tile
+    const uint32_t smem_base = smem_u32(smem);
+
+    uint32_t qf[D / 16][4];
+    float oacc[ND][4];
+    float m[2], l[2];
+    bool rvalid[2], rsoft[2];
+    int rrow[2];                             // speculative row r of the two rows
+    uint64_t vmask[2] = {0ull, 0ull};
+    int vmask_j = -1;
+
+    Cursor c;
+    cursor_init(P, t_begin, c);
+    bool seg_open = false;
+    long long k = 0;
+    for (long long t = t_begin; t < t_end; ++t, ++k) {
+        if (!seg_open) {
+            // new segment: load the rows' queries as A fragments, row flags
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int p = c.rb * A.rb_rows + wr * 16 + g + 8 * i;
+                rvalid[i] = false;
+                rsoft[i] = false;
+                rrow[i] = -1;
+                if (p < A.M) {
+                    const int r = p / A.G;
+                    const uint8_t fl = A.row_flags[(size_t)c.b * A.R + r];
+                    rvalid[i] = (fl & SPEC_ROW_VALID) != 0;
+                    rsoft[i] = rvalid[i] && (fl & SPEC_ROW_SEES_SOFT) != 0;
+                    rrow[i] = r;
+                }
+            }
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = e & 1;                     // a0,a2: row g; a1,a3: row g+8
+                    const int dcol = ks * 16 + 2 * cq + (e >> 1) * 8;
+                    uint32_t v = 0;
+                    if (rrow[i] >= 0) {
+                        const int p = c.rb * A.rb_rows + wr * 16 + g + 8 * i;
+                        const int hq = c.h * A.G + p % A.G;
+                        const __nv_bfloat16 *qr = static_cast<const __nv_bfloat16 *>(A.q) +
+                                                  (((size_t)c.b * A.R + rrow[i]) * A.Hq + hq) * D;
+                        v = *reinterpret_cast<const uint32_t *>(qr + dcol);
+                    }
+                    qf[ks][e] = v;
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < ND; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) oacc[nt][e] = 0.f;
+            m[0] = m[1] = -INFINITY;
+            l[0] = l[1] = 0.f;
+            vmask_j = -1;
+            seg_open = true;
+        }
+
+        const int s = (int)(k % NS);
+        const uint32_t ph = (uint32_t)((k / NS) & 1);
+        if (!mbar_wait(&full[s], ph)) {
+            raise_status(A.status, SPEC_DEV_TIMEOUT);
+            break;
+        }
+        const uint32_t kb = smem_base + s * STAGE;
+        const uint32_t vb = kb + KV_BYTES;
+        const TileInfo ti = tile_info(P, c);
+
+        if (ti.kind == kBlock && vmask_j != ti.j) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                uint64_t w = 0;
+                if (rrow[i] >= 0 && rvalid[i]) {
+                    const uint32_t *vr = A.vis + ((size_t)c.b * A.R + rrow[i]) * A.W;
+                    const int w0 = 2 * ti.j;
+                    w = vr[w0];
+                    if (w0 + 1 < A.W) w |= (uint64_t)vr[w0 + 1] << 32;
+                }
+                vmask[i] = w;
+            }
+            vmask_j = ti.j;
+        }
+
+        // ---- S = Q K^T for this warp's TW tokens
+        float sacc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t half = kb + (ks >> 2) * kHalfBytes;
+            const int chunk = (ks & 3) * 2 + ((lane >> 3) & 1);
+#pragma unroll
+            for (int np = 0; np < NT / 2; ++np) {
+                const int tok = c0 + np * 16 + (lane & 7) + ((lane >> 4) & 1) * 8;
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(swz(half, tok, chunk), b0, b1, b2, b3);
+                mma_bf16(sacc[2 * np], qf[ks], b0, b1);
+                mma_bf16(sacc[2 * np + 1], qf[ks], b2, b3);
+            }
+        }
+
+        // ---- mask, scale, online softmax (rows g and g+8 of the warp)
+        float tmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = e >> 1;
+                const int col = c0 + nt * 8 + 2 * cq + (e & 1);
+                bool vis = col < ti.nvalid;
+                if (ti.kind == kPrefix) vis = vis && rvalid[i];
+                else if (ti.kind == kSoft) vis = vis && rsoft[i];
+                else vis = vis && ((vmask[i] >> col) & 1ull);
+                const float x = vis ? sacc[nt][e] * A.scale_log2 : -INFINITY;
+                sacc[nt][e] = x;
+                tmax[i] = fmaxf(tmax[i], x);
+            }
+        }
+        float alpha[2], muse[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            tmax[i] = fmaxf(tmax[i], __shfl_xor_sync(0xffffffffu, tmax[i], 1));
+            tmax[i] = fmaxf(tmax[i], __shfl_xor_sync(0xffffffffu, tmax[i], 2));
+            const float mn = fmaxf(m[i], tmax[i]);
+            muse[i] = mn == -INFINITY ? 0.f : mn;
+            alpha[i] = exp2f(m[i] - muse[i]);
+            m[i] = mn;
+        }
+        uint32_t pa[TW / 16][4];
+        float rs[2] = {0.f, 0.f};
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const float p0 = exp2f(sacc[nt][0] - muse[0]);
+            const float p1 = exp2f(sacc[nt][1] - muse[0]);
+            const float p2 = exp2f(sacc[nt][2] - muse[1]);
+            const float p3 = exp2f(sacc[nt][3] - muse[1]);
+            rs[0] += p0 + p1;
+            rs[1] += p2 + p3;
+            pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16(p0, p1);
+            pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16(p2, p3);
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) l[i] = l[i] * alpha[i] + rs[i];
+#pragma unroll
+        for (int nt = 0; nt < ND; ++nt) {
+            oacc[nt][0] *= alpha[0];
+            oacc[nt][1] *= alpha[0];
+            oacc[nt][2] *= alpha[1];
+            oacc[nt][3] *= alpha[1];
+        }
+
+        // ---- O += P V
+        const bool ragged = ti.nvalid < kTile;
+#pragma unroll
+        for (int kk = 0; kk < TW / 16; ++kk) {
+            const int k0 = c0 + kk * 16;
+            const int tok = k0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+            uint32_t keep0 = 0xffffffffu, keep1 = 0xffffffffu;
+            if (ragged) {
+                const int t0 = k0 + 2 * cq, t1 = k0 + 8 + 2 * cq;
+                keep0 = (t0 < ti.nvalid ? 0x0000ffffu : 0u) | (t0 + 1 < ti.nvalid ? 0xffff0000u : 0u);
+                keep1 = (t1 < ti.nvalid ? 0x0000ffffu : 0u) | (t1 + 1 < ti.nvalid ? 0xffff0000u : 0u);
+            }
+#pragma unroll
+            for (int dp = 0; dp < D / 16; ++dp) {
+                const int dchunk = dp * 2 + (lane >> 4);         // 16-byte chunk of d
+                const uint32_t half = vb + (dchunk >> 3) * kHalfBytes;
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(swz(half, tok, dchunk & 7), b0, b1, b2, b3);
+                b0 &= keep0;
+                b1 &= keep1;
+                b2 &= keep0;
+                b3 &= keep1;
+                mma_bf16(oacc[2 * dp], pa[kk], b0, b1);
+                mma_bf16(oacc[2 * dp + 1], pa[kk], b2, b3);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+
+        // ---- segment done (or range done): write this warp's partial
+        const bool seg_end = (c.tile == c.n_tiles - 1) || (t == t_end - 1);
+        if (seg_end) {
+            const int seg = (c.b * A.Hkv + c.h) * A.n_rb + c.rb;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                float lt = l[i];
+                lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+                lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+                const size_t row = slot_row(P, seg, cta, wc, WC, wr * 16 + g + 8 * i);
+                float *po = A.part_o + row * D;
+#pragma unroll
+                for (int nt = 0; nt < ND; ++nt)
+                    *reinterpret_cast<float2 *>(po + nt * 8 + 2 * cq) =
+                        make_float2(oacc[nt][2 * i], oacc[nt][2 * i + 1]);
+                if (cq == 0) {
+                    A.part_ml[row * 2] = m[i];
+                    A.part_ml[row * 2 + 1] = lt;
+                }
+            }
+            seg_open = false;
+        }
+        cursor_next(P, c);
+    }
+}
+
+// Merge the partials of every (request, KV head, packed row): one warp each.
+template <int D>
+__global__ void __launch_bounds__(128) attn_tc_combine_kernel(const __grid_constant__ TcParams P,
+                                                               int wcn) {
+    const AttnParams &A = P.a;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int p = blockIdx.x * 4 + warp;
+    const int h = blockIdx.y, b = blockIdx.z;
+    if (p >= A.M) return;
+    const long long T = warp_total_tiles(P);
+    const int rb = p / A.rb_rows, rr = p % A.rb_rows;
+    const int S = req_seq(P, b);
+    const int nt = seg_tiles(P, S);
+    const long long s0 = warp_tiles_before(P, b) + (long long)(h * A.n_rb + rb) * nt;
+    const long long s1 = s0 + nt;
+    const int seg = (b * A.Hkv + h) * A.n_rb + rb;
+    const int first = cta_of(T, s0, P.n_ctas), last = cta_of(T, s1 - 1, P.n_ctas);
+
+    float mstar = -INFINITY;
+    for (int i = first; i <= last; ++i) {
+        const long long lo = range_lo(T, i, P.n_ctas), hi = range_lo(T, i + 1, P.n_ctas);
+        if (max(lo, s0) >= min(hi, s1)) continue;
+        for (int w = 0; w < wcn; ++w)
+            mstar = fmaxf(mstar, A.part_ml[slot_row(P, seg, i, w, wcn, rr) * 2]);
+    }
+    const int r = p / A.G, hq = h * A.G + p % A.G;
+    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(A.o) + (((size_t)b * A.R + r) * A.Hq + hq) * D;
+    float out[D / 32];
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) out[j] = 0.f;
+    float lse = -INFINITY;
+    if (mstar != -INFINITY) {
+        float L = 0.f;
+        for (int i = first; i <= last; ++i) {
+            const long long lo = range_lo(T, i, P.n_ctas), hi = range_lo(T, i + 1, P.n_ctas);
+            if (max(lo, s0) >= min(hi, s1)) continue;
+            for (int w = 0; w < wcn; ++w) {
+                const size_t row = slot_row(P, seg, i, w, wcn, rr);
+                const float ms = A.part_ml[row * 2];
+                if (ms == -INFINITY) continue;
+                const float wgt = exp2f(ms - mstar);
+                L = fmaf(wgt, A.part_ml[row * 2 + 1], L);
+                const float *po = A.part_o + row * D;
+#pragma unroll
+                for (int j = 0; j < D / 32; ++j) out[j] = fmaf(wgt, po[lane + 32 * j], out[j]);
+            }
+        }
+        const float inv = 1.f / L;
+#pragma unroll
+        for (int j = 0; j < D / 32; ++j) out[j] *= inv;
+        lse = (mstar + log2f(L)) * kLn2;
+    }
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) o[lane + 32 * j] = __float2bfloat16_rn(out[j]);
+    if (lane == 0) A.lse[((size_t)b * A.Hq + hq) * A.R + r] = lse;
+}
+
+// ------------------------------------------------------------------ host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 map over [rows][d] with a (64 x box_rows) box, 128-byte swizzle.
+bool make_map(CUtensorMap *map, const void *base, long long rows, int d, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    if (rows < 1) rows = 1;
+    cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int ns_for(int d) { return d == 128 ? 5 : 8; }
+
+size_t smem_bytes(int d) {
+    const int stage = 2 * (d / 64) * kHalfBytes;
+    return (size_t)ns_for(d) * stage + 2 * ns_for(d) * sizeof(uint64_t) + 1024;
+}
+
+int wr_for(int rb_rows) { return rb_rows / 16; }
+
+template <int D, int WR>
+spec_status_t launch_impl(const TcParams &P, const CUtensorMap *maps, cudaStream_t s) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    const size_t smem = smem_bytes(D);
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(attn_tc_kernel<D, WR>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    });
+    if (attr_err != cudaSuccess) return SPEC_ERR_CUDA;
+    attn_tc_kernel<D, WR><<<P.n_ctas, kThreads, smem, s>>>(P, maps[0], maps[1], maps[2], maps[3],
+                                                           maps[4], maps[5]);
+    spec_status_t st = launch_status();
+    if (st != SPEC_OK) return st;
+    dim3 grid(ceil_div(P.a.M, 4), P.a.Hkv, P.a.B);
+    attn_tc_combine_kernel<D><<<grid, 128, 0, s>>>(P, kConsumerWarps / WR);
+    return launch_status();
+}
+
+}  // namespace
+
+bool tc_supported(const AttnParams &P, int dtype) {
+    if (dtype != SPEC_BF16) return false;
+    if (P.d != 64 && P.d != 128) return false;
+    if (P.paged && P.page_size != 16 && P.page_size != 32 && P.page_size != 64) return false;
+    return true;
+}
+
+int tc_rows_per_block(const AttnParams &P) {
+    if (P.M <= 16) return 16;
+    if (P.M <= 32) return 32;
+    return 64;
+}
+
+int tc_num_ctas() { return num_sms(); }
+
+size_t tc_workspace_bytes(const AttnParams &P, size_t *off_ml) {
+    const int wc = kConsumerWarps / wr_for(P.rb_rows);
+    const size_t segs = (size_t)P.B * P.Hkv * P.n_rb;
+    const size_t rows = (segs + tc_num_ctas()) * wc * P.rb_rows;
+    const size_t o_bytes = (rows * P.d * sizeof(float) + 255) & ~size_t(255);
+    *off_ml = o_bytes;
+    return o_bytes + ((rows * 2 * sizeof(float) + 255) & ~size_t(255));
+}
+
+spec_status_t launch_attn_tc(const AttnParams &A, cudaStream_t s) {
+    TcParams P{};
+    P.a = A;
+    P.n_ctas = tc_num_ctas();
+    P.soft_tiles = ceil_div(A.n_soft, kTile);
+    P.tail = P.soft_tiles + ceil_div(A.R, kTile);
+    P.box_rows = A.paged ? A.page_size : kTile;
+    CUtensorMap maps[6];
+    const long long cache_rows = A.cache_rows;
+    const long long block_rows = (long long)A.B * A.Hkv * A.R;
+    bool ok = make_map(&maps[0], A.kc, cache_rows, A.d, P.box_rows) &&
+              make_map(&maps[1], A.vc, cache_rows, A.d, P.box_rows) &&
+              make_map(&maps[2], A.kb, block_rows, A.d, kTile) &&
+              make_map(&maps[3], A.vb, block_rows, A.d, kTile);
+    if (ok && A.n_soft > 0) {
+        ok = make_map(&maps[4], A.soft_k, (long long)A.Hkv * A.n_soft, A.d, kTile) &&
+             make_map(&maps[5], A.soft_v, (long long)A.Hkv * A.n_soft, A.d, kTile);
+    } else {
+        maps[4] = maps[2];
+        maps[5] = maps[3];
+    }
+    if (!ok) return SPEC_ERR_CUDA;
+    const int wr = wr_for(A.rb_rows);
+    if (A.d == 128) {
+        if (wr == 1) return launch_impl<128, 1>(P, maps, s);
+        if (wr == 2) return launch_impl<128, 2>(P, maps, s);
+        return launch_impl<128, 4>(P, maps, s);
+    }
+    if (wr == 1) return launch_impl<64, 1>(P, maps, s);
+    if (wr == 2) return launch_impl<64, 2>(P, maps, s);
+    return launch_impl<64, 4>(P, maps, s);
+}
 
 }  // namespace sv

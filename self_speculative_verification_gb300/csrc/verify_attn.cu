@@ -275,6 +275,7 @@ spec_status_t make_plan(const spec_attn_desc *a, const spec_kv_desc *c, Plan *ou
         P.paged = 0;
         P.max_seq = c->max_seq;
         P.capacity = c->max_seq;
+        P.cache_rows = (long long)c->batch * c->n_kv_heads * c->max_seq;
     } else if (c->kind == SPEC_KV_PAGED) {
         if (c->page_size <= 0 || c->max_pages_per_seq <= 0 || c->n_pages <= 0) return SPEC_ERR_INVALID_ARG;
         if (c->page_size != 16 && c->page_size != 32 && c->page_size != 64) return SPEC_ERR_UNSUPPORTED;
@@ -284,6 +285,7 @@ spec_status_t make_plan(const spec_attn_desc *a, const spec_kv_desc *c, Plan *ou
         P.max_pages = c->max_pages_per_seq;
         P.n_pages = c->n_pages;
         P.capacity = c->max_pages_per_seq * c->page_size;
+        P.cache_rows = (long long)c->n_pages * c->n_kv_heads * c->page_size;
     } else {
         return SPEC_ERR_INVALID_ARG;
     }
@@ -291,7 +293,11 @@ spec_status_t make_plan(const spec_attn_desc *a, const spec_kv_desc *c, Plan *ou
     P.scale_log2 = scale * kLog2e;
 
     Plan plan{};
-    plan.use_tc = tc_supported(P, a->dtype);
+    // TMA coordinates are 32-bit: the tensor-core path takes caches and
+    // blocks with fewer than 2^31 rows of head_dim elements.
+    plan.use_tc = tc_supported(P, a->dtype) && P.cache_rows < (1ll << 31) &&
+                  (long long)P.B * P.Hkv * P.R < (1ll << 31) &&
+                  (long long)P.Hkv * P.n_soft < (1ll << 31);
     P.rb_rows = plan.use_tc ? tc_rows_per_block(P) : kSimtRows;
     P.n_rb = ceil_div(P.M, P.rb_rows);
     if (a->split_tokens > 0) {
@@ -309,9 +315,13 @@ spec_status_t make_plan(const spec_attn_desc *a, const spec_kv_desc *c, Plan *ou
     }
     P.max_splits = P.capacity > 0 ? ceil_div(P.capacity, P.chunk) : 1;
     if (P.max_splits < 1) P.max_splits = 1;
-    const size_t nrow = (size_t)P.B * P.Hkv * P.max_splits * P.M;
-    plan.off_ml = align256(nrow * P.d * sizeof(float));
-    plan.ws_bytes = plan.off_ml + align256(nrow * 2 * sizeof(float));
+    if (plan.use_tc) {
+        plan.ws_bytes = tc_workspace_bytes(P, &plan.off_ml);
+    } else {
+        const size_t nrow = (size_t)P.B * P.Hkv * P.max_splits * P.M;
+        plan.off_ml = align256(nrow * P.d * sizeof(float));
+        plan.ws_bytes = plan.off_ml + align256(nrow * 2 * sizeof(float));
+    }
     plan.P = P;
     *out = plan;
     return SPEC_OK;
@@ -385,7 +395,8 @@ extern "C" spec_status_t spec_verify_attn(const spec_attn_desc *attn, const void
     P.part_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.off_ml);
     cudaStream_t s = sv::as_stream(stream);
     if (attn->dtype == SPEC_BF16) {
-        st = plan.use_tc ? sv::launch_attn_tc(P, s) : sv::launch_simt<__nv_bfloat16>(P, s);
+        if (plan.use_tc) return sv::launch_attn_tc(P, s);
+        st = sv::launch_simt<__nv_bfloat16>(P, s);
         if (st != SPEC_OK) return st;
         return sv::launch_combine<__nv_bfloat16>(P, s);
     }
