@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-workers", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch (small cases for profiling)")
     return ap.parse_args()
 
 
@@ -331,7 +333,7 @@ def run_gpu(args):
     from self_speculative_verification_gb300 import binding as bn
     from self_speculative_verification_gb300.device import DeviceStep
 
-    wl = W.make_workload(args.config, args.seed + rank)
+    wl = W.make_workload(args.config, args.seed + rank, B=args.batch or None)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args, wl)
 

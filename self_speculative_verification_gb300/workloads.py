@@ -341,7 +341,8 @@ def _seq_lengths(rng, spec, B):
 
 def make_workload(name: str, seed: int = 0, *, B=None, seq=None, V=None,
                   q_scale: float = 1.0, T=None, k_choices=None,
-                  paged=None, n_soft=None, slack_pages=None) -> Workload:
+                  paged=None, n_soft=None, slack_pages=None,
+                  page_order: str = "shuffled") -> Workload:
     """Build one seeded workload; keyword overrides shrink it for tests."""
     cfg = dict(CONFIGS[name])
     if B is not None:
@@ -495,6 +496,8 @@ def make_workload(name: str, seed: int = 0, *, B=None, seq=None, V=None,
         slack = B if slack_pages is None else slack_pages
         P = int(sum(need)) + slack
         perm = rng.permutation(P).astype(np.int32)
+        if page_order == "sequential":
+            perm = np.arange(P, dtype=np.int32)
         wl.max_pages = max(need) if B else 1
         wl.page_table = np.full((B, wl.max_pages), -1, dtype=np.int32)
         off = 0
