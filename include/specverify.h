@@ -104,9 +104,14 @@ typedef int spec_status_t;
  *   k, v : [batch][n_kv_heads][max_seq][head_dim]   (dtype)
  *   request b's token t lives at k[b][h][t][:].
  * kind == SPEC_KV_PAGED:
- *   k, v : [n_pages][n_kv_heads][page_size][head_dim] (dtype)
+ *   k, v : [n_pages][n_kv_heads][head_dim / 64][page_size][64] (dtype)
  *   page_table : int32 [batch][max_pages_per_seq]; token t of request b
- *   lives in page page_table[b][t / page_size], slot t % page_size.
+ *   lives in page page_table[b][t / page_size], slot t % page_size, and its
+ *   element j of KV head h is k[page][h][j / 64][t % page_size][j % 64].
+ *   Within one (page, head) the head dimension is split into 64-element
+ *   blocks, each holding page_size rows: one (page, head) is a single
+ *   contiguous 2-D tile, fetched by one tensor copy.  For head_dim = 64
+ *   this is [n_pages][n_kv_heads][page_size][64].
  *   Entries past ceil(seq_len[b] / page_size) are unused.
  */
 typedef struct spec_kv_desc {

@@ -45,7 +45,9 @@ reason in the design notes):
 * Tree root = node 0, always accepted; its K/V is committed first.
 * Padding rows (vparent = -2) see nothing: O = 0, LSE = -inf.
 * Paged cache: requests in ascending order take pages from the free list in
-  order, after filling their partly used tail page.
+  order, after filling their partly used tail page.  A page stores, per KV
+  head, the head dimension in blocks of ``blk`` elements, each block as
+  page_size rows: pages[p][h][j // blk][slot][j % blk].
 """
 
 from __future__ import annotations
@@ -202,17 +204,21 @@ def verify_attention(q, prefix_k, prefix_v, k_block, v_block, vis, valid,
 def gather_paged(pages, page_table, seq_len, page_size):
     """Logical per-request prefixes [Hkv][S_b][d] from a paged cache.
 
-    pages [n_pages][Hkv][page_size][d]; page_table[b][j] = physical page of
-    logical page j of request b.
+    pages [n_pages][Hkv][d // blk][page_size][blk]: element j of token t of
+    request b, KV head h is pages[page_table[b][t // page_size]][h]
+    [j // blk][t % page_size][j % blk].
     """
     out = []
+    P, Hkv, nblk, ps, blk = pages.shape
+    assert ps == page_size
+    d = nblk * blk
     for b in range(len(seq_len)):
         S = int(seq_len[b])
-        Hkv, d = pages.shape[1], pages.shape[3]
         kk = np.empty((Hkv, S, d), dtype=pages.dtype)
         for t in range(S):
             p = int(page_table[b][t // page_size])
-            kk[:, t] = pages[p, :, t % page_size]
+            for j in range(nblk):
+                kk[:, t, j * blk:(j + 1) * blk] = pages[p, :, j, t % page_size]
         out.append(kk)
     return out
 
@@ -345,10 +351,10 @@ def kv_commit_contiguous(K, V, seq_len, k_block, v_block, paths):
 
 def kv_commit_paged(Kp, Vp, page_table, seq_len, free_pages, free_head,
                     k_block, v_block, paths, page_size):
-    """Append accepted rows to a paged cache [n_pages][Hkv][page][d].
+    """Append accepted rows to a paged cache [n_pages][Hkv][d // blk][page][blk].
 
     Position t of request b lives in page page_table[b][t // page_size] at
-    slot t % page_size.  Requests are served in ascending b; each first fills
+    slot t % page_size (layout as ``gather_paged``).  Requests are served in ascending b; each first fills
     its partly used last page, then takes pages from
     free_pages[free_head], free_pages[free_head + 1], ... in order.
     Returns new (Kp, Vp, page_table, seq_len, free_head) copies.
@@ -371,7 +377,9 @@ def kv_commit_paged(Kp, Vp, page_table, seq_len, free_pages, free_head,
                 pt[b, j] = free_pages[head]
                 head += 1
             p = int(pt[b, j])
-            Kp[p, :, pos % page_size] = k_block[b, :, row]
-            Vp[p, :, pos % page_size] = v_block[b, :, row]
+            nblk, blk = Kp.shape[2], Kp.shape[4]
+            for jj in range(nblk):
+                Kp[p, :, jj, pos % page_size] = k_block[b, :, row, jj * blk:(jj + 1) * blk]
+                Vp[p, :, jj, pos % page_size] = v_block[b, :, row, jj * blk:(jj + 1) * blk]
         seq[b] += len(path)
     return Kp, Vp, pt, seq, head

@@ -152,12 +152,13 @@ def kv_desc_contiguous(k: torch.Tensor, v: torch.Tensor) -> KvDesc:
 
 
 def kv_desc_paged(k: torch.Tensor, v: torch.Tensor, page_table: torch.Tensor) -> KvDesc:
-    """k, v: [n_pages][Hkv][page_size][d]; page_table int32 [B][max_pages]."""
-    if k.shape != v.shape or k.dim() != 4:
-        raise ValueError("k and v must be [n_pages][Hkv][page_size][d]")
+    """k, v: [n_pages][Hkv][d / 64][page_size][64]; page_table int32 [B][max_pages]."""
+    if k.shape != v.shape or k.dim() != 5 or k.shape[4] != 64:
+        raise ValueError("k and v must be [n_pages][Hkv][d / 64][page_size][64]")
     _ptr(k, name="k"), _ptr(v, k.dtype, "v")
     _ptr(page_table, torch.int32, "page_table")
-    P, Hkv, ps, d = k.shape
+    P, Hkv, nblk, ps, _ = k.shape
+    d = nblk * 64
     B, maxp = page_table.shape
     return KvDesc(SPEC_KV_PAGED, spec_dtype(k), Hkv, d, k.data_ptr(), v.data_ptr(),
                   B, 0, P, ps, maxp, page_table.data_ptr())

@@ -45,7 +45,8 @@ struct TcParams {
     int n_ctas;
     int soft_tiles;      // ceil(n_soft / 64)
     int tail;            // soft_tiles + ceil(R / 64)
-    int box_rows;        // rows per cache box: 64 (contiguous) or page_size
+    int box_rows;        // rows per cache box: 64 (contiguous) or NH * page_size
+    int page_log2;       // log2(page_size) (paged)
 };
 
 // ------------------------------------------------------------ PTX helpers
@@ -145,10 +146,16 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// Address of 16-byte chunk `chunk` (0..7) of row `row` in a 128B-swizzled
-// [rows][128 B] box whose base is 1024-byte aligned.
-__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk) {
-    return base + row * 128 + ((chunk ^ (row & 7)) << 4);
+// Shared-memory address of 16-byte chunk `chunk` (0..7) of 64-element half
+// `hh` of token `tok` in one K or V tile.  A tile is a sequence of blocks of
+// 2^rbl tokens (64 for contiguous / soft / block tiles, page_size for paged
+// tiles); each block holds its NH halves one after another, each half as
+// 2^rbl rows of 128 bytes, 128B-swizzled (16-byte chunk index XOR row % 8;
+// every half starts on a 1024-byte boundary).
+template <int NH>
+__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int tok, int hh, int chunk, int rbl) {
+    const int row = ((((tok >> rbl) * NH + hh) << rbl) | (tok & ((1 << rbl) - 1)));
+    return base + row * 128 + ((chunk ^ (tok & 7)) << 4);
 }
 
 // -------------------------------------------------------------- schedule
@@ -353,7 +360,7 @@ attn_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUten
         const uint64_t pol_keep = policy_evict_last();
         // the prefix is read once unless several row blocks share it
         const uint64_t pol_stream = A.n_rb == 1 ? policy_evict_first() : pol_keep;
-        const int ps = P.box_rows;
+        const int ps = A.paged ? A.page_size : kTile;
         const int ppt = kTile / ps;          // pages per tile (paged)
         const int grp = 32 / ppt;            // tiles covered by one id per lane
 
@@ -415,10 +422,11 @@ attn_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUten
                 uint32_t bytes;
                 int nbox;
                 if (paged_tile) {
+                    // one box per (page, K or V): both halves of a page-head
                     bytes = 0;
                     for (int i = 0; i < ppt; ++i)
                         if (pages[i] >= 0) bytes += 2u * NH * ps * 128u;
-                    nbox = ppt * 2 * NH;
+                    nbox = ppt * 2;
                 } else {
                     bytes = (uint32_t)STAGE;
                     nbox = 2 * NH;
@@ -426,16 +434,15 @@ attn_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUten
                 if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
                 __syncwarp();
                 if (lane < nbox) {
-                    const int per_page = 2 * NH;
-                    const int i = paged_tile ? lane / per_page : 0;
-                    const int rem = paged_tile ? lane % per_page : lane;
-                    const int kv = rem / NH, hh = rem % NH;
-                    uint8_t *dst = kbuf + kv * KV_BYTES + hh * kHalfBytes;
                     if (paged_tile) {
+                        const int i = lane >> 1, kv = lane & 1;
                         if (pages[i] >= 0)
-                            tma_load_2d(dst + i * ps * 128, kv ? &mv : &mk, hh * 64,
-                                        (pages[i] * A.Hkv + tc.h) * ps, &full[s], pol_stream);
+                            tma_load_2d(kbuf + kv * KV_BYTES + i * NH * ps * 128, kv ? &mv : &mk,
+                                        0, (pages[i] * A.Hkv + tc.h) * NH * ps, &full[s],
+                                        pol_stream);
                     } else {
+                        const int kv = lane / NH, hh = lane % NH;
+                        uint8_t *dst = kbuf + kv * KV_BYTES + hh * kHalfBytes;
                         const CUtensorMap *map;
                         int row;
                         uint64_t pol = pol_keep;
@@ -542,6 +549,7 @@ attn_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUten
         const uint32_t kb = smem_base + s * STAGE;
         const uint32_t vb = kb + KV_BYTES;
         const TileInfo ti = tile_info(P, c);
+        const int rbl = (ti.kind == kPrefix && A.paged) ? P.page_log2 : 6;
 
         if (ti.kind == kBlock && vmask_j != ti.j) {
 #pragma unroll
@@ -567,13 +575,12 @@ attn_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUten
             for (int e = 0; e < 4; ++e) sacc[nt][e] = sacc2[nt][e] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t half = kb + (ks >> 2) * kHalfBytes;
             const int chunk = (ks & 3) * 2 + ((lane >> 3) & 1);
 #pragma unroll
             for (int np = 0; np < NT / 2; ++np) {
                 const int tok = c0 + np * 16 + (lane & 7) + ((lane >> 4) & 1) * 8;
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4(swz(half, tok, chunk), b0, b1, b2, b3);
+                ldsm_x4(tile_addr<NH>(kb, tok, ks >> 2, chunk, rbl), b0, b1, b2, b3);
                 if (NT <= 2 && (ks & 1)) {
                     mma_bf16(sacc2[2 * np], qf[ks], b0, b1);
                     mma_bf16(sacc2[2 * np + 1], qf[ks], b2, b3);
@@ -669,9 +676,8 @@ attn_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUten
 #pragma unroll
             for (int dp = 0; dp < D / 16; ++dp) {
                 const int dchunk = dp * 2 + (lane >> 4);         // 16-byte chunk of d
-                const uint32_t half = vb + (dchunk >> 3) * kHalfBytes;
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(swz(half, tok, dchunk & 7), b0, b1, b2, b3);
+                ldsm_x4_t(tile_addr<NH>(vb, tok, dchunk >> 3, dchunk & 7, rbl), b0, b1, b2, b3);
                 b0 &= keep0;
                 b1 &= keep1;
                 b2 &= keep0;
@@ -868,12 +874,16 @@ spec_status_t launch_attn_tc(const AttnParams &A, cudaStream_t s) {
     P.n_ctas = num_sms() * cfg.minb;
     P.soft_tiles = ceil_div(A.n_soft, kTile);
     P.tail = P.soft_tiles + ceil_div(A.R, kTile);
-    P.box_rows = A.paged ? A.page_size : kTile;
+    P.box_rows = A.paged ? (A.d / 64) * A.page_size : kTile;
+    P.page_log2 = A.page_size == 16 ? 4 : A.page_size == 32 ? 5 : 6;
     CUtensorMap maps[6];
-    const long long cache_rows = A.cache_rows;
+    // paged caches: [page][head][d / 64][page_size][64] viewed as rows of 64
+    // elements, one box = one (page, head); contiguous: rows of d elements
+    const long long cache_rows = A.paged ? A.cache_rows * (A.d / 64) : A.cache_rows;
+    const int cache_inner = A.paged ? 64 : A.d;
     const long long block_rows = (long long)A.B * A.Hkv * A.R;
-    bool ok = make_map(&maps[0], A.kc, cache_rows, A.d, P.box_rows) &&
-              make_map(&maps[1], A.vc, cache_rows, A.d, P.box_rows) &&
+    bool ok = make_map(&maps[0], A.kc, cache_rows, cache_inner, P.box_rows) &&
+              make_map(&maps[1], A.vc, cache_rows, cache_inner, P.box_rows) &&
               make_map(&maps[2], A.kb, block_rows, A.d, kTile) &&
               make_map(&maps[3], A.vb, block_rows, A.d, kTile);
     if (ok && A.n_soft > 0) {

@@ -26,6 +26,7 @@ struct CommitParams {
     int32_t *free_head;
     int n_free;
     int B, Hkv, R, path_cap, row_bytes;
+    int blk_bytes, vec_per_blk;    // paged: bytes / 16-byte vectors of a 64-element block
     int paged, max_seq, page_size, max_pages, n_pages, capacity;
     int *status;
 };
@@ -120,7 +121,7 @@ __global__ void __launch_bounds__(128) kv_commit_copy_kernel(CommitParams P) {
         const int pos = S + i;
         size_t dst;
         if (!P.paged) {
-            dst = (((size_t)b * P.Hkv + h) * P.max_seq + pos) * P.row_bytes;
+            dst = (((size_t)b * P.Hkv + h) * P.max_seq + pos) * P.row_bytes + (size_t)v * 16;
         } else {
             const int j = pos / P.page_size;
             const int page = j < used ? P.page_table[(size_t)b * P.max_pages + j]
@@ -129,13 +130,18 @@ __global__ void __launch_bounds__(128) kv_commit_copy_kernel(CommitParams P) {
                 if (v == 0) raise_status(P.status, SPEC_DEV_BAD_PAGE);
                 continue;
             }
-            dst = (((size_t)page * P.Hkv + h) * P.page_size + pos % P.page_size) * P.row_bytes;
+            // [page][head][d / 64][page_size][64]: 16-byte vector v of the row
+            // lies in 64-element block v / vec_per_blk
+            const int blk = v / P.vec_per_blk, vin = v % P.vec_per_blk;
+            dst = (((size_t)page * P.Hkv + h) * (P.row_bytes / P.blk_bytes) + blk) *
+                      P.page_size * P.blk_bytes +
+                  (size_t)(pos % P.page_size) * P.blk_bytes + (size_t)vin * 16;
         }
         const size_t src = (((size_t)b * P.Hkv + h) * P.R + row) * P.row_bytes;
         const uint4 kx = reinterpret_cast<const uint4 *>(P.kb + src)[v];
         const uint4 vx = reinterpret_cast<const uint4 *>(P.vb + src)[v];
-        reinterpret_cast<uint4 *>(P.kc + dst)[v] = kx;
-        reinterpret_cast<uint4 *>(P.vc + dst)[v] = vx;
+        *reinterpret_cast<uint4 *>(P.kc + dst) = kx;
+        *reinterpret_cast<uint4 *>(P.vc + dst) = vx;
     }
 }
 
@@ -197,6 +203,7 @@ extern "C" spec_status_t kv_commit(const spec_kv_desc *cache, int batch, int n_r
     const int es = cache->dtype == SPEC_BF16 ? 2 : 4;
     const int row_bytes = cache->head_dim * es;
     if (row_bytes % 16 != 0) return SPEC_ERR_UNSUPPORTED;
+    if (cache->kind == SPEC_KV_PAGED && cache->head_dim % 64 != 0) return SPEC_ERR_UNSUPPORTED;
     if (batch == 0) return SPEC_OK;
     if (!kb || !vb || !path || !acc_len || !seq_len || !cache->k || !cache->v)
         return SPEC_ERR_INVALID_ARG;
@@ -214,6 +221,8 @@ extern "C" spec_status_t kv_commit(const spec_kv_desc *cache, int batch, int n_r
     P.R = n_rows;
     P.path_cap = path_cap;
     P.row_bytes = row_bytes;
+    P.blk_bytes = 64 * es;
+    P.vec_per_blk = 64 * es / 16;
     if (cache->kind == SPEC_KV_CONTIGUOUS) {
         if (cache->max_seq < 0) return SPEC_ERR_INVALID_ARG;
         P.paged = 0;

@@ -20,6 +20,9 @@ namespace {
 constexpr int kSimtRows = 16;   // packed rows per CTA (4 warps x 4 rows)
 constexpr int kSimtCols = 32;   // columns per tile (one per lane)
 
+// First element of token t's K (or V) row for head h; element k of the row
+// is at row + (k / 64) * block_stride(P) + k % 64 (paged caches split the
+// head dimension into 64-element blocks of page_size rows).
 template <typename T>
 __device__ __forceinline__ const T *prefix_row(const AttnParams &P, const T *base, int b, int h,
                                                int t, bool *bad) {
@@ -29,7 +32,11 @@ __device__ __forceinline__ const T *prefix_row(const AttnParams &P, const T *bas
         *bad = true;
         return nullptr;
     }
-    return base + (((size_t)page * P.Hkv + h) * P.page_size + t % P.page_size) * P.d;
+    return base + ((size_t)page * P.Hkv + h) * P.page_size * P.d + (t % P.page_size) * 64;
+}
+
+__device__ __forceinline__ int block_stride(const AttnParams &P, int kind_prefix) {
+    return (kind_prefix && P.paged) ? P.page_size * 64 : 64;
 }
 
 // Column kinds of a tile.
@@ -132,8 +139,9 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnParams P) {
                     vr = vbp + (((size_t)b * P.Hkv + h) * P.R + c) * D;
                 }
                 if (kr) {
-                    kx = load_f(kr + k);
-                    vx = load_f(vr + k);
+                    const int off = (k >> 6) * block_stride(P, kind == kColPrefix) + (k & 63);
+                    kx = load_f(kr + off);
+                    vx = load_f(vr + off);
                 }
             }
             sk[j][k] = kx;
@@ -295,7 +303,7 @@ spec_status_t make_plan(const spec_attn_desc *a, const spec_kv_desc *c, Plan *ou
     Plan plan{};
     // TMA coordinates are 32-bit: the tensor-core path takes caches and
     // blocks with fewer than 2^31 rows of head_dim elements.
-    plan.use_tc = tc_supported(P, a->dtype) && P.cache_rows < (1ll << 31) &&
+    plan.use_tc = tc_supported(P, a->dtype) && P.cache_rows * (P.d / 64) < (1ll << 31) &&
                   (long long)P.B * P.Hkv * P.R < (1ll << 31) &&
                   (long long)P.Hkv * P.n_soft < (1ll << 31);
     P.rb_rows = plan.use_tc ? tc_rows_per_block(P) : kSimtRows;

@@ -65,8 +65,9 @@ def _fill_paged(wl: Workload, K, V, dt, threads=8, fill=math.nan):
                 t = to_dev(src, K.device, dt)                     # [Hkv][S][d]
                 pad = torch.full((wl.Hkv, npg * ps, wl.d), fill, dtype=dt, device=K.device)
                 pad[:, :S] = t
-                blk = pad.view(wl.Hkv, npg, ps, wl.d).permute(1, 0, 2, 3).contiguous()
-                dst.index_copy_(0, pages, blk)
+                # -> [page][Hkv][d / 64][page_size][64]
+                blk = pad.view(wl.Hkv, npg, ps, wl.d // 64, 64).permute(1, 0, 3, 2, 4)
+                dst.index_copy_(0, pages, blk.contiguous())
 
 
 class DeviceStep:
@@ -101,7 +102,7 @@ class DeviceStep:
         self.seq_len = to_dev(wl.seq_len.astype(np.int32), dev)
         self.seq_len0 = self.seq_len.clone()
         if wl.paged:
-            shape = (wl.n_pages, Hkv, wl.page_size, d)
+            shape = (wl.n_pages, Hkv, d // 64, wl.page_size, 64)
             self.k_cache = torch.empty(shape, dtype=dt, device=dev)
             self.v_cache = torch.empty(shape, dtype=dt, device=dev)
             _fill_paged(wl, self.k_cache, self.v_cache, dt, threads, fill)

@@ -182,9 +182,11 @@ class Workload:
         return K, Vc
 
     def paged_cache(self, fill=np.nan):
-        """K, V pages as [n_pages][Hkv][page][d]; unused slots hold ``fill``."""
+        """K, V pages as [n_pages][Hkv][d // 64][page][64] (the paged layout:
+        per head, the head dimension in 64-element blocks of page rows);
+        unused slots hold ``fill``."""
         assert self.paged
-        shape = (self.n_pages, self.Hkv, self.page_size, self.d)
+        shape = (self.n_pages, self.Hkv, self.d // 64, self.page_size, 64)
         K = np.full(shape, fill, dtype=np.float32)
         Vc = np.full(shape, fill, dtype=np.float32)
         for b in range(self.B):
@@ -194,14 +196,16 @@ class Workload:
 
 
 def place_request_pages(wl: Workload, b: int, k, v, Kp, Vp):
-    """Scatter request ``b``'s logical prefix [Hkv][S][d] into page arrays."""
+    """Scatter request ``b``'s logical prefix [Hkv][S][d] into page arrays
+    [n_pages][Hkv][d // 64][page][64]."""
     S = k.shape[1]
     ps = wl.page_size
     for j in range((S + ps - 1) // ps):
         p = int(wl.page_table[b, j])
         t0, t1 = j * ps, min(S, (j + 1) * ps)
-        Kp[p, :, : t1 - t0] = k[:, t0:t1]
-        Vp[p, :, : t1 - t0] = v[:, t0:t1]
+        for blk in range(wl.d // 64):
+            Kp[p, :, blk, : t1 - t0] = k[:, t0:t1, blk * 64:(blk + 1) * 64]
+            Vp[p, :, blk, : t1 - t0] = v[:, t0:t1, blk * 64:(blk + 1) * 64]
 
 
 # --------------------------------------------------------------------------

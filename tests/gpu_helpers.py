@@ -162,8 +162,9 @@ def check_commit(ds: DeviceStep, before_k, before_v, paths):
                 if pos % ps == 0:
                     pt[b, j] = wl.free_pages[head]
                     head += 1
-                exp_k[pt[b, j], :, pos % ps] = kb_bits[b, :, row]
-                exp_v[pt[b, j], :, pos % ps] = vb_bits[b, :, row]
+                nb = wl.d // 64
+                exp_k[pt[b, j], :, :, pos % ps] = kb_bits[b, :, row].reshape(wl.Hkv, nb, 64)
+                exp_v[pt[b, j], :, :, pos % ps] = vb_bits[b, :, row].reshape(wl.Hkv, nb, 64)
             seq2[b] += len(path)
         assert np.array_equal(ds.page_table.cpu().numpy(), pt)
         assert int(ds.free_head.item()) == head

@@ -139,8 +139,8 @@ def test_commit_paged_hand_worked():
     """
     rng = np.random.Generator(np.random.PCG64(2))
     P, Hkv, ps, d = 10, 1, 4, 2
-    Kp = rng.standard_normal((P, Hkv, ps, d))
-    Vp = rng.standard_normal((P, Hkv, ps, d))
+    Kp = rng.standard_normal((P, Hkv, 1, ps, d))      # one block of d elements
+    Vp = rng.standard_normal((P, Hkv, 1, ps, d))
     pt = np.array([[4, 0, -1], [6, 1, -1]])
     kb, vb = _rand_block(rng, 2, Hkv, 3, d)
     out = oracle.kv_commit_paged(Kp, Vp, pt, [5, 8], np.array([9, 7, 3]), 0,
@@ -148,18 +148,18 @@ def test_commit_paged_hand_worked():
     K2, V2, pt2, seq2, head = out
     assert seq2.tolist() == [8, 10] and head == 1
     assert pt2.tolist() == [[4, 0, -1], [6, 1, 9]]
-    assert np.array_equal(K2[0, 0, 1:4], kb[0, 0, [0, 1, 2]])
-    assert np.array_equal(K2[9, 0, 0:2], kb[1, 0, [2, 0]])
-    assert np.array_equal(V2[9, 0, 0:2], vb[1, 0, [2, 0]])
+    assert np.array_equal(K2[0, 0, 0, 1:4], kb[0, 0, [0, 1, 2]])
+    assert np.array_equal(K2[9, 0, 0, 0:2], kb[1, 0, [2, 0]])
+    assert np.array_equal(V2[9, 0, 0, 0:2], vb[1, 0, [2, 0]])
     touched = np.zeros((P, ps), dtype=bool)
     touched[0, 1:4] = True
     touched[9, 0:2] = True
-    diff = (K2 != Kp).any(axis=(1, 3)) | (V2 != Vp).any(axis=(1, 3))
+    diff = (K2 != Kp).any(axis=(1, 2, 4)) | (V2 != Vp).any(axis=(1, 2, 4))
     assert np.array_equal(diff, touched)
 
 
 def test_commit_paged_exhaustion():
-    Kp = np.zeros((3, 1, 2, 1))
+    Kp = np.zeros((3, 1, 1, 2, 1))
     kb = np.zeros((1, 1, 3, 1))
     with pytest.raises(OverflowError):
         oracle.kv_commit_paged(Kp, Kp, np.array([[0, -1, -1]]), [2],
