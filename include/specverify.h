@@ -32,7 +32,8 @@
  *   - Calls are asynchronous on the caller's CUDA stream (`stream`, a
  *     cudaStream_t; NULL = legacy default stream) and launch only this
  *     library's kernels.  The library allocates no device memory: scratch
- *     comes from a caller-provided workspace (spec_verify_attn).
+ *     comes from a caller-provided workspace (spec_verify_attn), or, for
+ *     spec_verify_attn_noalloc, from one fixed array inside the library.
  *   - Errors visible on the host (bad sizes, NULL pointers, unsupported
  *     dtype/shape, a too-small workspace) are returned before anything is
  *     launched.  Errors only visible on the device (a bad parent pointer, a
@@ -223,6 +224,44 @@ spec_status_t spec_verify_attn(const spec_attn_desc *attn, const void *q,
                                const uint32_t *vis, const uint8_t *row_flags,
                                void *o, float *lse, void *workspace,
                                size_t workspace_bytes, void *stream);
+
+/* Bytes of the fixed scratch array behind spec_verify_attn_noalloc. */
+#define SPEC_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/*
+ * spec_verify_attn_noalloc -- spec_verify_attn for callers that cannot
+ * allocate device memory.  The pages have no counterpart: this is a
+ * deployment variant of the same computation.
+ *
+ * Meant for callers that have no workspace to give: for example an engine
+ * that reserved all of the GPU's memory for its own KV-cache pool and allows
+ * no later allocation, or a plugin hook whose framework owns the memory and
+ * forbids allocating while it runs (cudaMalloc may also synchronise the
+ * whole device).  Arguments and results are exactly those of
+ * spec_verify_attn without `workspace` / `workspace_bytes`; the split
+ * partials go to a fixed array of SPEC_NOALLOC_SCRATCH_BYTES (64 MiB) that
+ * is part of the library, held on every GPU that loads the library's kernels
+ * until the process exits.
+ *
+ *   - Returns SPEC_ERR_CAPACITY, before launching anything, when the shape
+ *     needs more scratch than that (spec_verify_attn_workspace_size tells);
+ *     such shapes must use spec_verify_attn.
+ *   - Calls no allocating routine (no cudaMalloc, cudaFree or the like).
+ *   - The first call on each device resolves the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the previous
+ *     call's contents (nothing needs to start at zero: the kernels write each
+ *     partial before reading it).  Calls that can overlap on the GPU (other
+ *     streams, other host threads) race on the array and must be serialised
+ *     by the caller.
+ */
+spec_status_t spec_verify_attn_noalloc(const spec_attn_desc *attn, const void *q,
+                                       const spec_kv_desc *cache, const void *kb,
+                                       const void *vb, const void *soft_k,
+                                       const void *soft_v, const int32_t *seq_len,
+                                       const uint32_t *vis, const uint8_t *row_flags,
+                                       void *o, float *lse, void *stream);
 
 /*
  * spec_vocab_reduce -- per logits row ([LA] sec. 2.4 needs the proposal's

@@ -37,7 +37,9 @@ SPEC_DEV_BAD_INDEX = 0x10
 
 EXPORTS = ("spec_version", "spec_status_string", "spec_mask_build",
            "spec_verify_attn_workspace_size", "spec_verify_attn",
-           "spec_vocab_reduce", "spec_accept", "kv_commit", "spec_get_status")
+           "spec_verify_attn_noalloc", "spec_vocab_reduce", "spec_accept", "kv_commit",
+           "spec_get_status")
+SPEC_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class SpecError(RuntimeError):
@@ -92,6 +94,8 @@ def load_library():
                                              POINTER(c_size_t)], c_int),
         "spec_verify_attn": ([POINTER(AttnDesc), vp, POINTER(KvDesc), vp, vp, vp, vp,
                               vp, vp, vp, vp, vp, vp, c_size_t, vp], c_int),
+        "spec_verify_attn_noalloc": ([POINTER(AttnDesc), vp, POINTER(KvDesc), vp, vp, vp, vp,
+                                      vp, vp, vp, vp, vp, vp], c_int),
         "spec_vocab_reduce": ([vp, c_int, c_int, c_int, vp, vp, vp, vp, vp], c_int),
         "spec_accept": ([POINTER(AcceptDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                          vp, vp, vp], c_int),
@@ -215,6 +219,23 @@ def spec_verify_attn(attn: AttnDesc, q, cache: KvDesc, kb, vb, soft_k, soft_v, s
         _ptr(seq_len, torch.int32, "seq_len"), _ptr(vis, torch.int32, "vis"),
         _ptr(row_flags, torch.uint8, "row_flags"), _ptr(o), _ptr(lse, torch.float32, "lse"),
         _ptr(workspace, name="workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def spec_verify_attn_noalloc(attn: AttnDesc, q, cache: KvDesc, kb, vb, soft_k, soft_v,
+                             seq_len, vis, row_flags, o, lse, stream=None):
+    """spec_verify_attn without a workspace: for callers that cannot
+    allocate device memory; the library's own fixed scratch array is used
+    (shared by all calls on a device, so overlapping calls must not run)."""
+    lib = load_library()
+    dt = q.dtype
+    for name, t in (("kb", kb), ("vb", vb), ("o", o)):
+        _ptr(t, dt, name)
+    _check("spec_verify_attn_noalloc", lib.spec_verify_attn_noalloc(
+        ctypes.byref(attn), _ptr(q, name="q"), ctypes.byref(cache), _ptr(kb), _ptr(vb),
+        _ptr(soft_k, dt, "soft_k"), _ptr(soft_v, dt, "soft_v"),
+        _ptr(seq_len, torch.int32, "seq_len"), _ptr(vis, torch.int32, "vis"),
+        _ptr(row_flags, torch.uint8, "row_flags"), _ptr(o), _ptr(lse, torch.float32, "lse"),
         _stream(stream)))
 
 
