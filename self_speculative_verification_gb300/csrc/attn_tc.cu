@@ -724,6 +724,10 @@ __global__ void __launch_bounds__(128) attn_tc_combine_kernel(const __grid_const
     const int p = blockIdx.x * 4 + warp;
     const int h = blockIdx.y, b = blockIdx.z;
     if (p >= A.M) return;
+    if (p == 0 && h == 0 && lane == 0) {
+        const int S_raw = A.seq_len[b];
+        if (S_raw < 0 || S_raw > A.capacity) raise_status(A.status, SPEC_DEV_SEQ_OVERFLOW);
+    }
     const long long T = warp_total_tiles(P);
     const int rb = p / A.rb_rows, rr = p % A.rb_rows;
     const int S = req_seq(P, b);

@@ -346,7 +346,8 @@ def _seq_lengths(rng, spec, B):
 def make_workload(name: str, seed: int = 0, *, B=None, seq=None, V=None,
                   q_scale: float = 1.0, T=None, k_choices=None,
                   paged=None, n_soft=None, slack_pages=None,
-                  page_order: str = "shuffled") -> Workload:
+                  page_order: str = "shuffled", d=None, page_size=None,
+                  dtype=None) -> Workload:
     """Build one seeded workload; keyword overrides shrink it for tests."""
     cfg = dict(CONFIGS[name])
     if B is not None:
@@ -363,6 +364,10 @@ def make_workload(name: str, seed: int = 0, *, B=None, seq=None, V=None,
         cfg["paged"] = paged
     if n_soft is not None:
         cfg["n_soft"] = n_soft
+    if d is not None:
+        cfg["d"] = d
+    if dtype is not None:
+        cfg["dtype"] = dtype
     rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0x5EC])))
     B, Hq, Hkv, d, dt, Vv = (cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["d"],
                              cfg["dtype"], cfg["V"])
@@ -493,6 +498,8 @@ def make_workload(name: str, seed: int = 0, *, B=None, seq=None, V=None,
         node_depth=node_depth,
     )
     wl.max_seq = int(seq_len.max()) + R if B else R
+    if page_size is not None:
+        wl.page_size = page_size
     if wl.paged:
         ps = wl.page_size
         used = [(int(s) + ps - 1) // ps for s in seq_len]

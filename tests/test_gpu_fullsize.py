@@ -1,0 +1,69 @@
+"""Parity at the workloads' full sizes, in the launch configuration the
+benchmark times (library-chosen splits): the mask, the vocab reduce, the
+acceptance and the commit in full, the attention on sampled (request, head)
+pairs that the oracle computes one by one."""
+
+import numpy as np
+import pytest
+import torch
+
+import gpu_helpers as gh
+from self_speculative_verification_gb300 import binding as bn
+from self_speculative_verification_gb300 import workloads as W
+from self_speculative_verification_gb300.device import DeviceStep
+
+pytestmark = pytest.mark.gpu
+
+
+def _commit_expected_on_device(ds, k0, v0, paths):
+    """Expected cache after the commit, built on the device from the
+    snapshot, the oracle's paths and the page rule (pages from the table)."""
+    wl = ds.wl
+    ek, ev = k0.clone(), v0.clone()
+    pt = ds.page_table.cpu().numpy() if wl.paged else None
+    for b, path in enumerate(paths):
+        for i, row in enumerate(path):
+            pos = int(wl.seq_len[b]) + i
+            if wl.paged:
+                page, slot = int(pt[b, pos // wl.page_size]), pos % wl.page_size
+                nb = wl.d // 64
+                ek[page, :, :, slot] = ds.kb[b, :, row].view(wl.Hkv, nb, 64)
+                ev[page, :, :, slot] = ds.vb[b, :, row].view(wl.Hkv, nb, 64)
+            else:
+                ek[b, :, pos] = ds.kb[b, :, row]
+                ev[b, :, pos] = ds.vb[b, :, row]
+    return ek, ev
+
+
+@pytest.mark.parametrize("name", ["la7b", "confu", "ss", "long_paged"])
+def test_full_size_sampled(name):
+    gh.require_gpu()
+    wl = W.make_workload(name, 0)
+    ds = DeviceStep(wl, threads=16)
+    k0, v0 = ds.k_cache.clone(), ds.v_cache.clone()
+    ds.run()
+    torch.cuda.synchronize()
+    assert bn.spec_get_status() == 0
+    vis, valid, sees = gh.check_mask(ds)
+    reqs = sorted({0, wl.B // 2, wl.B - 1})
+    heads = sorted({0, wl.Hq // 2 + 1, wl.Hq - 1})
+    O_ref, L_ref = gh.oracle_attention(wl, vis, valid, sees, requests=reqs, heads=heads)
+    gh.check_attention(ds, O_ref, L_ref, requests=reqs, heads=heads)
+    acc, paths = gh.check_accept(ds)
+    # commit: whole cache compared bit for bit on the device
+    if wl.paged:
+        head = 0
+        pt = wl.page_table.copy()
+        for b, path in enumerate(paths):
+            S = int(wl.seq_len[b])
+            for i in range(len(path)):
+                pos = S + i
+                if pos % wl.page_size == 0:
+                    pt[b, pos // wl.page_size] = wl.free_pages[head]
+                    head += 1
+        assert np.array_equal(ds.page_table.cpu().numpy(), pt)
+        assert int(ds.free_head.item()) == head
+    ek, ev = _commit_expected_on_device(ds, k0, v0, paths)
+    assert torch.equal(ds.k_cache.view(torch.int16), ek.view(torch.int16))
+    assert torch.equal(ds.v_cache.view(torch.int16), ev.view(torch.int16))
+    assert ds.seq_len.cpu().numpy().tolist() == (wl.seq_len + acc).tolist()

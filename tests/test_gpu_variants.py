@@ -1,0 +1,50 @@
+"""GPU parity for the kernel variants the five workloads do not reach:
+head_dim 64 on the tensor-core path (16-, 32- and 64-row tiles), 32- and
+64-token pages, and fp32 inputs (CUDA-core path) on tree, soft-prompt and
+paged workloads."""
+
+import pytest
+
+import gpu_helpers as gh
+from self_speculative_verification_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _gpu():
+    gh.require_gpu()
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("la7b", dict(B=3, seq=("uniform", 100, 700), V=3000, d=64)),
+    ("long_paged", dict(B=3, seq=("uniform", 200, 900), V=3000, d=64)),
+    ("ss", dict(B=2, seq=("uniform", 100, 400), V=3000, d=64)),
+    ("confu", dict(B=2, seq=("uniform", 100, 400), V=3000, d=64)),
+])
+def test_head_dim_64_bf16(name, kw):
+    gh.run_and_check(W.make_workload(name, 21, **kw))
+
+
+@pytest.mark.parametrize("page_size", [32, 64])
+@pytest.mark.parametrize("d", [64, 128])
+def test_page_sizes(page_size, d):
+    wl = W.make_workload("long_paged", 22, B=3, seq=("uniform", 150, 700), V=3000,
+                         page_size=page_size, d=d)
+    gh.run_and_check(wl)
+    gh.run_and_check(wl, split_tokens=64)
+
+
+@pytest.mark.parametrize("name", ["ss", "confu", "long_paged", "la7b"])
+def test_fp32_cuda_core_path(name):
+    wl = W.make_workload(name, 23, B=2, seq=("uniform", 60, 300), V=2000, dtype="f32")
+    gh.run_and_check(wl)
+    gh.run_and_check(wl, split_tokens=64)
+
+
+def test_gqa_many_row_blocks():
+    """ConFu rows (120 x G=4 = 480 packed rows) over several row blocks,
+    with sharpened scores."""
+    wl = W.make_workload("confu", 24, B=3, seq=("uniform", 500, 1300), V=2000,
+                         q_scale=8.0)
+    gh.run_and_check(wl)
