@@ -8,10 +8,13 @@
 //
 // Accept: the LA threshold longest prefix, or the greedy walk down the draft
 // tree ("Speculative Streaming", verification step; "ConFu" tree verify).
+#include <cooperative_groups.h>
 #include <limits.h>
 #include <math.h>
 
 #include "common.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace sv {
 namespace {
@@ -67,43 +70,85 @@ template <> struct Vec<__nv_bfloat16> {
     }
 };
 
-// One CTA per row, 16-byte loads, one pass with a running (max, index, sum).
+// One thread-block cluster per row: CTA `rank` of the cluster reduces slice
+// `rank` of the row, kUnroll 16-byte loads in flight per thread, one pass
+// with a running (max, index, sum of exp).  Per batch of kUnroll * N
+// elements: the batch max first; the index search and the rescale of the
+// running sum only when the max rises (a thread visits its indices in
+// increasing order, so an equal later value never wins a tie); then one
+// FFMA + one ex2 per element.  Rank 0 merges the CTAs' results through
+// distributed shared memory.
+constexpr int kUnroll = 4;
+
+// 2^x by the hardware approximation (relative error ~2^-22); 2^-inf = 0.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kReduceThreads)
 vocab_reduce_kernel(const T *__restrict__ logits, int V, const int32_t *__restrict__ proposal,
                     int32_t *__restrict__ argmax, float *__restrict__ lse,
                     float *__restrict__ zprop) {
-    const int row = blockIdx.x;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int nc = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    const int row = blockIdx.x / nc;
     const T *z = logits + (size_t)row * V;
     Best best{-INFINITY, INT_MAX, 0.f};
     constexpr int N = Vec<T>::N;
-    const bool vec_ok = ((reinterpret_cast<uintptr_t>(z) & 15) == 0);
-    int done = 0;
-    if (vec_ok) {
+    if ((reinterpret_cast<uintptr_t>(z) & 15) == 0) {
         const int nv = V / N;
-        for (int i = threadIdx.x; i < nv; i += kReduceThreads) {
-            float x[N];
-            Vec<T>::load(z + (size_t)i * N, x);
-            float vm = x[0];
-            int vi = 0;
+        const int lo = (int)((long long)nv * rank / nc), hi = (int)((long long)nv * (rank + 1) / nc);
+        for (int i0 = lo + threadIdx.x; i0 < hi; i0 += kReduceThreads * kUnroll) {
+            float x[kUnroll][N];
 #pragma unroll
-            for (int j = 1; j < N; ++j)
-                if (x[j] > vm) { vm = x[j]; vi = j; }
-            if (vm > best.m) {
-                best.s = best.s * __expf(best.m - vm);
-                best.m = vm;
-                best.idx = i * N + vi;
-            } else if (vm == best.m && i * N + vi < best.idx) {
-                best.idx = i * N + vi;
+            for (int u = 0; u < kUnroll; ++u) {
+                const int i = i0 + u * kReduceThreads;
+                if (i < hi) {
+                    Vec<T>::load(z + (size_t)i * N, x[u]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < N; ++j) x[u][j] = -INFINITY;
+                }
             }
-            float acc = 0.f;
+            float bm = x[0][0];
 #pragma unroll
-            for (int j = 0; j < N; ++j) acc += __expf(x[j] - best.m);
-            best.s += acc;
+            for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+                for (int j = 0; j < N; ++j) bm = fmaxf(bm, x[u][j]);
+            if (bm > best.m) {
+                int bi = INT_MAX;
+#pragma unroll
+                for (int u = kUnroll - 1; u >= 0; --u)
+#pragma unroll
+                    for (int j = N - 1; j >= 0; --j)
+                        if (x[u][j] == bm) bi = (i0 + u * kReduceThreads) * N + j;
+                best.s *= ex2((best.m - bm) * kLog2e);
+                best.m = bm;
+                best.idx = bi;
+            }
+            const float mb = best.m * kLog2e;
+            float acc[N];
+#pragma unroll
+            for (int j = 0; j < N; ++j) acc[j] = 0.f;
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+                for (int j = 0; j < N; ++j) acc[j] += ex2(fmaf(x[u][j], kLog2e, -mb));
+#pragma unroll
+            for (int j = 1; j < N; ++j) acc[0] += acc[j];
+            best.s += acc[0];
         }
-        done = nv * N;
+        if (rank == nc - 1)
+            for (int i = nv * N + threadIdx.x; i < V; i += kReduceThreads)
+                best_push(best, load_f(z + i), i);
+    } else {
+        const int lo = (int)((long long)V * rank / nc), hi = (int)((long long)V * (rank + 1) / nc);
+        for (int i = lo + threadIdx.x; i < hi; i += kReduceThreads) best_push(best, load_f(z + i), i);
     }
-    for (int i = done + threadIdx.x; i < V; i += kReduceThreads) best_push(best, load_f(z + i), i);
 
     // block reduction: warps, then across warps
 #pragma unroll
@@ -115,12 +160,19 @@ vocab_reduce_kernel(const T *__restrict__ logits, int V, const int32_t *__restri
         best = best_merge(best, other);
     }
     __shared__ Best sb[kReduceThreads / 32];
+    __shared__ Best cta_best;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (lane == 0) sb[warp] = best;
     __syncthreads();
     if (threadIdx.x == 0) {
         Best r = sb[0];
         for (int w = 1; w < kReduceThreads / 32; ++w) r = best_merge(r, sb[w]);
+        cta_best = r;
+    }
+    cluster.sync();
+    if (rank == 0 && threadIdx.x == 0) {
+        Best r = cta_best;
+        for (int i = 1; i < nc; ++i) r = best_merge(r, *cluster.map_shared_rank(&cta_best, i));
         argmax[row] = r.idx == INT_MAX ? 0 : r.idx;
         lse[row] = r.m + logf(r.s);
         if (proposal && zprop) {
@@ -128,6 +180,7 @@ vocab_reduce_kernel(const T *__restrict__ logits, int V, const int32_t *__restri
             zprop[row] = (pidx >= 0 && pidx < V) ? load_f(z + pidx) : NAN;
         }
     }
+    cluster.sync();     // peers' shared memory stays alive until rank 0 has read it
 }
 
 struct AcceptParams {
@@ -179,8 +232,23 @@ __global__ void __launch_bounds__(128) accept_kernel(AcceptParams P) {
         last = L - 1;
         for (int i = lane; i < P.path_cap; i += 32) pth[i] = i < L ? i : -1;
     } else {
-        const int32_t *par = P.tree_parent + (size_t)b * P.N;
-        const int32_t *tok = P.tokens + (size_t)b * P.N;
+        // Node c's parent, token and judge row's argmax live in lane c % 32,
+        // slot c / 32; the walk is then shuffles and ballots only.
+        constexpr int kSlots = SPEC_MAX_ROWS / 32;
+        int par[kSlots], tok[kSlots], am[kSlots];   // am = -1: judge row out of range
+#pragma unroll
+        for (int k = 0; k < kSlots; ++k) {
+            const int c = k * 32 + lane;
+            par[k] = -3;
+            tok[k] = 0;
+            am[k] = -1;
+            if (c < n) {
+                par[k] = P.tree_parent[(size_t)b * P.N + c];
+                tok[k] = P.tokens[(size_t)b * P.N + c];
+                const int row = P.row_of ? P.row_of[(size_t)b * P.N + c] : c;
+                if (row >= 0 && row < P.Rj) am[k] = P.argmax[(size_t)b * P.Rj + row];
+            }
+        }
         int cur = 0;
         if (n == 0 || P.path_cap == 0) {
             if (lane == 0) raise_status(P.status, SPEC_DEV_BAD_INDEX);
@@ -188,24 +256,24 @@ __global__ void __launch_bounds__(128) accept_kernel(AcceptParams P) {
             len = 1;
             if (lane == 0) pth[0] = 0;
             while (true) {
-                const int row = P.row_of ? P.row_of[(size_t)b * P.N + cur] : cur;
-                if (row < 0 || row >= P.Rj) {
+                // argmax of the current node's judge row, from its lane
+                int want = 0;
+#pragma unroll
+                for (int k = 0; k < kSlots; ++k)
+                    if (k == (cur >> 5)) want = __shfl_sync(0xffffffffu, am[k], cur & 31);
+                if (want < 0) {           // judge row out of range
                     if (lane == 0) raise_status(P.status, SPEC_DEV_BAD_INDEX);
                     next = -1;
                     break;
                 }
-                const int want = P.argmax[(size_t)b * P.Rj + row];
                 next = want;
-                // children have larger indices than their parent
+                // lowest-index child of cur carrying the wanted token
                 int found = -1;
-                for (int base = cur + 1; base < n; base += 32) {
-                    const int c = base + lane;
-                    const bool hit = c < n && par[c] == cur && tok[c] == want;
-                    const unsigned bal = __ballot_sync(0xffffffffu, hit);
-                    if (bal) {
-                        found = base + __ffs(bal) - 1;
-                        break;
-                    }
+#pragma unroll
+                for (int k = 0; k < kSlots; ++k) {
+                    const unsigned bal = __ballot_sync(0xffffffffu, par[k] == cur && tok[k] == want &&
+                                                                         k * 32 + lane > cur);
+                    if (found < 0 && bal) found = k * 32 + __ffs(bal) - 1;
                 }
                 if (found < 0) break;
                 if (len >= P.path_cap) {
@@ -228,16 +296,46 @@ __global__ void __launch_bounds__(128) accept_kernel(AcceptParams P) {
     }
 }
 
+// CTAs per row: enough CTAs for ~8 per SM, each slice at least 16 KB.
+int cluster_size(int n_rows, int V, int dtype) {
+    const long long row_bytes = (long long)V * (dtype == SPEC_BF16 ? 2 : 4);
+    int nc = 1;
+    while (nc < 8 && row_bytes / (2 * nc) >= 16384 && (long long)n_rows * nc < 8ll * num_sms())
+        nc *= 2;
+    return nc;
+}
+
+template <typename T>
+spec_status_t launch_vocab_cluster(const void *logits, int n_rows, int V, int nc,
+                                   const int32_t *proposal, int32_t *argmax, float *lse,
+                                   float *zprop, cudaStream_t s) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)((long long)n_rows * nc), 1, 1);
+    cfg.blockDim = dim3(kReduceThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = nc;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, vocab_reduce_kernel<T>,
+                                             static_cast<const T *>(logits), V, proposal, argmax,
+                                             lse, zprop);
+    return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
 spec_status_t launch_vocab_reduce(const void *logits, int dtype, int n_rows, int V,
                                   const int32_t *proposal, int32_t *argmax, float *lse,
                                   float *zprop, cudaStream_t s) {
+    const int nc = cluster_size(n_rows, V, dtype);
+    if ((long long)n_rows * nc > 2147483647ll) return SPEC_ERR_UNSUPPORTED;
     if (dtype == SPEC_BF16)
-        vocab_reduce_kernel<__nv_bfloat16><<<n_rows, kReduceThreads, 0, s>>>(
-            static_cast<const __nv_bfloat16 *>(logits), V, proposal, argmax, lse, zprop);
-    else
-        vocab_reduce_kernel<float><<<n_rows, kReduceThreads, 0, s>>>(
-            static_cast<const float *>(logits), V, proposal, argmax, lse, zprop);
-    return launch_status();
+        return launch_vocab_cluster<__nv_bfloat16>(logits, n_rows, V, nc, proposal, argmax, lse,
+                                                   zprop, s);
+    return launch_vocab_cluster<float>(logits, n_rows, V, nc, proposal, argmax, lse, zprop, s);
 }
 
 }  // namespace
@@ -250,7 +348,6 @@ extern "C" spec_status_t spec_vocab_reduce(const void *logits, int dtype, int n_
     if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
     if (n_rows == 0) return SPEC_OK;
     if (!logits || !argmax || !lse || (proposal && !zprop)) return SPEC_ERR_INVALID_ARG;
-    if (n_rows > 2147483647 / 1) return SPEC_ERR_UNSUPPORTED;
     return sv::launch_vocab_reduce(logits, dtype, n_rows, vocab, proposal, argmax, lse, zprop,
                                    sv::as_stream(stream));
 }

@@ -300,6 +300,145 @@ __device__ __forceinline__ size_t slot_row(const TcParams &P, int seg, int cta, 
 
 // ---------------------------------------------------------------- kernel
 
+// Producer warp: streams the K/V tiles of [t_begin, t_end) into the stage
+// ring.  The whole warp walks the tiles; lane i issues box i of a tile.
+template <int D, int NS>
+__device__ __forceinline__ void run_producer(const TcParams &P, const CUtensorMap &mk, const CUtensorMap &mv,
+                             const CUtensorMap &mkb, const CUtensorMap &mvb,
+                             const CUtensorMap &msk, const CUtensorMap &msv, uint8_t *smem,
+                             uint64_t *full, uint64_t *empty, long long t_begin,
+                             long long t_end) {
+    constexpr int NH = D / 64;
+    constexpr int KV_BYTES = NH * kHalfBytes;
+    constexpr int STAGE = 2 * KV_BYTES;
+    const AttnParams &A = P.a;
+    const int lane = threadIdx.x & 31;
+    // The whole warp walks the tiles; lane 0 waits and issues the copies.
+    // For paged caches the warp loads the page ids of a group of tiles
+    // (one id per lane) one group ahead, so no page-table load sits
+    // between two tile issues.
+    Cursor gc;
+    cursor_init(P, t_begin, gc);         // warp-collective
+    const uint64_t pol_keep = policy_evict_last();
+    // the prefix is read once unless several row blocks share it
+    const uint64_t pol_stream = A.n_rb == 1 ? policy_evict_first() : pol_keep;
+    const int ps = A.paged ? A.page_size : kTile;
+    const int ppt = kTile / ps;          // pages per tile (paged)
+    const int grp = 32 / ppt;            // tiles covered by one id per lane
+
+    // raw page id of this lane's slot in the group whose first tile is
+    // t0, or kNoPage; checked only where it is used, so the load stays
+    // in flight while the current group is issued
+    constexpr int kNoPage = -2147483647 - 1;
+    auto load_ids = [&](const Cursor &start, long long t0) -> int {
+        if (!A.paged) return kNoPage;
+        const int j = lane / ppt;
+        if (t0 + j >= t_end) return kNoPage;
+        Cursor cc = start;
+        for (int i = 0; i < j; ++i) cursor_next(P, cc);
+        const TileInfo ti = tile_info(P, cc);
+        const int tok = ti.base + (lane % ppt) * ps;
+        if (ti.kind != kPrefix || tok >= cc.S) return kNoPage;
+        return A.page_table[(size_t)cc.b * A.max_pages + tok / ps];
+    };
+
+    long long k = 0;
+    bool ok = true;
+    int ids = load_ids(gc, t_begin);
+    for (long long g0 = t_begin; g0 < t_end && ok; g0 += grp) {
+        const int n_here = (int)min((long long)grp, t_end - g0);
+        Cursor ngc = gc;
+        for (int i = 0; i < n_here; ++i) cursor_next(P, ngc);
+        const int ids_next = load_ids(ngc, g0 + grp);
+        Cursor tc = gc;
+        for (int j = 0; j < n_here; ++j, ++k) {
+            int pages[4] = {-1, -1, -1, -1};
+            if (A.paged) {
+                for (int i = 0; i < ppt; ++i) {
+                    const int pg = __shfl_sync(0xffffffffu, ids, j * ppt + i);
+                    if (pg != kNoPage && (pg < 0 || pg >= A.n_pages)) {
+                        if (lane == 0) raise_status(A.status, SPEC_DEV_BAD_PAGE);
+                        pages[i] = -1;
+                    } else {
+                        pages[i] = pg == kNoPage ? -1 : pg;
+                    }
+                }
+            }
+            const int s = (int)(k % NS);
+            const uint32_t ph = (uint32_t)((k / NS) & 1);
+            bool got = true;
+            if (lane == 0) got = mbar_wait(&empty[s], ph ^ 1);
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) {
+                if (lane == 0) raise_status(A.status, SPEC_DEV_TIMEOUT);
+                ok = false;
+                ++k;
+                break;
+            }
+            // Boxes of this tile, one per lane: lane i loads box i.
+            // Paged prefix: box i = (page i / (2 NH), K or V, half);
+            // otherwise: box i = (K or V, half) of one 64-row box.
+            uint8_t *kbuf = smem + s * STAGE;
+            const TileInfo ti = tile_info(P, tc);
+            const bool paged_tile = ti.kind == kPrefix && A.paged;
+            uint32_t bytes;
+            int nbox;
+            if (paged_tile) {
+                // one box per (page, K or V): both halves of a page-head
+                bytes = 0;
+                for (int i = 0; i < ppt; ++i)
+                    if (pages[i] >= 0) bytes += 2u * NH * ps * 128u;
+                nbox = ppt * 2;
+            } else {
+                bytes = (uint32_t)STAGE;
+                nbox = 2 * NH;
+            }
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
+            __syncwarp();
+            if (lane < nbox) {
+                if (paged_tile) {
+                    const int i = lane >> 1, kv = lane & 1;
+                    if (pages[i] >= 0)
+                        tma_load_2d(kbuf + kv * KV_BYTES + i * NH * ps * 128, kv ? &mv : &mk,
+                                    0, (pages[i] * A.Hkv + tc.h) * NH * ps, &full[s],
+                                    pol_stream);
+                } else {
+                    const int kv = lane / NH, hh = lane % NH;
+                    uint8_t *dst = kbuf + kv * KV_BYTES + hh * kHalfBytes;
+                    const CUtensorMap *map;
+                    int row;
+                    uint64_t pol = pol_keep;
+                    if (ti.kind == kPrefix) {
+                        map = kv ? &mv : &mk;
+                        row = (tc.b * A.Hkv + tc.h) * A.max_seq + ti.base;
+                        pol = pol_stream;
+                    } else if (ti.kind == kSoft) {
+                        map = kv ? &msv : &msk;
+                        row = tc.h * A.n_soft + ti.base;
+                    } else {
+                        map = kv ? &mvb : &mkb;
+                        row = (tc.b * A.Hkv + tc.h) * A.R + ti.base;
+                    }
+                    tma_load_2d(dst, map, hh * 64, row, &full[s], pol);
+                }
+            }
+            cursor_next(P, tc);
+        }
+        gc = ngc;
+        ids = ids_next;
+    }
+    // do not leave while copies into this CTA's shared memory are in flight
+    if (lane == 0) {
+        const long long last = ok ? k : k - 1;       // the aborted tile issued nothing
+        for (long long kk = last - 1; kk >= 0 && kk >= last - NS; --kk) {
+            if (!mbar_wait(&full[kk % NS], (uint32_t)((kk / NS) & 1))) {
+                raise_status(A.status, SPEC_DEV_TIMEOUT);
+                break;
+            }
+        }
+    }
+}
+
 // D: head_dim; WR: 16-row warp groups per row block; NCW: consumer warps;
 // NS: pipeline stages; MINB: CTAs per SM the launch is sized for.
 template <int D, int WR, int NCW, int NS, int MINB>
@@ -350,131 +489,7 @@ attn_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUten
     if (t_begin >= t_end) return;
 
     if (warp == NCW) {
-        // ------------------------------------------------------ producer
-        // The whole warp walks the tiles; lane 0 waits and issues the copies.
-        // For paged caches the warp loads the page ids of a group of tiles
-        // (one id per lane) one group ahead, so no page-table load sits
-        // between two tile issues.
-        Cursor gc;
-        cursor_init(P, t_begin, gc);         // warp-collective
-        const uint64_t pol_keep = policy_evict_last();
-        // the prefix is read once unless several row blocks share it
-        const uint64_t pol_stream = A.n_rb == 1 ? policy_evict_first() : pol_keep;
-        const int ps = A.paged ? A.page_size : kTile;
-        const int ppt = kTile / ps;          // pages per tile (paged)
-        const int grp = 32 / ppt;            // tiles covered by one id per lane
-
-        // raw page id of this lane's slot in the group whose first tile is
-        // t0, or kNoPage; checked only where it is used, so the load stays
-        // in flight while the current group is issued
-        constexpr int kNoPage = -2147483647 - 1;
-        auto load_ids = [&](const Cursor &start, long long t0) -> int {
-            if (!A.paged) return kNoPage;
-            const int j = lane / ppt;
-            if (t0 + j >= t_end) return kNoPage;
-            Cursor cc = start;
-            for (int i = 0; i < j; ++i) cursor_next(P, cc);
-            const TileInfo ti = tile_info(P, cc);
-            const int tok = ti.base + (lane % ppt) * ps;
-            if (ti.kind != kPrefix || tok >= cc.S) return kNoPage;
-            return A.page_table[(size_t)cc.b * A.max_pages + tok / ps];
-        };
-
-        long long k = 0;
-        bool ok = true;
-        int ids = load_ids(gc, t_begin);
-        for (long long g0 = t_begin; g0 < t_end && ok; g0 += grp) {
-            const int n_here = (int)min((long long)grp, t_end - g0);
-            Cursor ngc = gc;
-            for (int i = 0; i < n_here; ++i) cursor_next(P, ngc);
-            const int ids_next = load_ids(ngc, g0 + grp);
-            Cursor tc = gc;
-            for (int j = 0; j < n_here; ++j, ++k) {
-                int pages[4] = {-1, -1, -1, -1};
-                if (A.paged) {
-                    for (int i = 0; i < ppt; ++i) {
-                        const int pg = __shfl_sync(0xffffffffu, ids, j * ppt + i);
-                        if (pg != kNoPage && (pg < 0 || pg >= A.n_pages)) {
-                            if (lane == 0) raise_status(A.status, SPEC_DEV_BAD_PAGE);
-                            pages[i] = -1;
-                        } else {
-                            pages[i] = pg == kNoPage ? -1 : pg;
-                        }
-                    }
-                }
-                const int s = (int)(k % NS);
-                const uint32_t ph = (uint32_t)((k / NS) & 1);
-                bool got = true;
-                if (lane == 0) got = mbar_wait(&empty[s], ph ^ 1);
-                got = __shfl_sync(0xffffffffu, got, 0);
-                if (!got) {
-                    if (lane == 0) raise_status(A.status, SPEC_DEV_TIMEOUT);
-                    ok = false;
-                    ++k;
-                    break;
-                }
-                // Boxes of this tile, one per lane: lane i loads box i.
-                // Paged prefix: box i = (page i / (2 NH), K or V, half);
-                // otherwise: box i = (K or V, half) of one 64-row box.
-                uint8_t *kbuf = smem + s * STAGE;
-                const TileInfo ti = tile_info(P, tc);
-                const bool paged_tile = ti.kind == kPrefix && A.paged;
-                uint32_t bytes;
-                int nbox;
-                if (paged_tile) {
-                    // one box per (page, K or V): both halves of a page-head
-                    bytes = 0;
-                    for (int i = 0; i < ppt; ++i)
-                        if (pages[i] >= 0) bytes += 2u * NH * ps * 128u;
-                    nbox = ppt * 2;
-                } else {
-                    bytes = (uint32_t)STAGE;
-                    nbox = 2 * NH;
-                }
-                if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
-                __syncwarp();
-                if (lane < nbox) {
-                    if (paged_tile) {
-                        const int i = lane >> 1, kv = lane & 1;
-                        if (pages[i] >= 0)
-                            tma_load_2d(kbuf + kv * KV_BYTES + i * NH * ps * 128, kv ? &mv : &mk,
-                                        0, (pages[i] * A.Hkv + tc.h) * NH * ps, &full[s],
-                                        pol_stream);
-                    } else {
-                        const int kv = lane / NH, hh = lane % NH;
-                        uint8_t *dst = kbuf + kv * KV_BYTES + hh * kHalfBytes;
-                        const CUtensorMap *map;
-                        int row;
-                        uint64_t pol = pol_keep;
-                        if (ti.kind == kPrefix) {
-                            map = kv ? &mv : &mk;
-                            row = (tc.b * A.Hkv + tc.h) * A.max_seq + ti.base;
-                            pol = pol_stream;
-                        } else if (ti.kind == kSoft) {
-                            map = kv ? &msv : &msk;
-                            row = tc.h * A.n_soft + ti.base;
-                        } else {
-                            map = kv ? &mvb : &mkb;
-                            row = (tc.b * A.Hkv + tc.h) * A.R + ti.base;
-                        }
-                        tma_load_2d(dst, map, hh * 64, row, &full[s], pol);
-                    }
-                }
-                cursor_next(P, tc);
-            }
-            gc = ngc;
-            ids = ids_next;
-        }
-        // do not leave while copies into this CTA's shared memory are in flight
-        if (lane == 0) {
-            const long long last = ok ? k : k - 1;       // the aborted tile issued nothing
-            for (long long kk = last - 1; kk >= 0 && kk >= last - NS; --kk) {
-                if (!mbar_wait(&full[kk % NS], (uint32_t)((kk / NS) & 1))) {
-                    raise_status(A.status, SPEC_DEV_TIMEOUT);
-                    break;
-                }
-            }
-        }
+        run_producer<D, NS>(P, mk, mv, mkb, mvb, msk, msv, smem, full, empty, t_begin, t_end);
         return;
     }
 
@@ -715,6 +730,513 @@ attn_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUten
     }
 }
 
+// ===================================================== tcgen05 / TMEM variant
+//
+// For row blocks of up to 128 packed rows (the compute-bound shapes: many
+// speculative rows x GQA heads per KV head).  Same schedule, producer,
+// partial slots and combine as attn_tc_kernel; the contraction runs on the
+// fifth-generation tensor cores:
+//   S = Q K^T  -> TMEM (fp32, lane = packed row, column = token), issued by
+//                 one thread as tcgen05.mma (bf16 x bf16 -> fp32), Q read from
+//                 TMEM (lane = row, two bf16 per column), K from the TMA tile;
+//   softmax    -> one thread per row reads its S row from TMEM, masks,
+//                 scales, exponentiates in the exp2 domain and writes P (bf16)
+//                 back to TMEM;
+//   O += P V   -> TMEM (fp32, 128 columns = head_dim), P from TMEM, V read as
+//                 an MN-major operand straight from the TMA tile.
+// Shared memory therefore carries only K/V tiles (6 stages).
+// The running max is raised only when a row's tile max exceeds it by more
+// than 2^8 (then O and l are rescaled in place); below that, p <= 256 and
+// the fp32 accumulators absorb it.  S and P are double-buffered so S(t) is
+// computed while the softmax works on tile t-1.
+namespace umma {
+
+constexpr int kRows = 128;              // rows per CTA tile (MMA M)
+constexpr int kSoftmaxWarps = 4;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kThreads = 6 * 32;
+constexpr int kNS = 6;                  // K/V stages
+constexpr int kTmemCols = 512;
+constexpr int kColO = 0;                // O: columns [0, 128)
+constexpr int kColS = 128;              // S buffer b: [128 + 64 b, 192 + 64 b)
+constexpr int kColQ = 256;              // Q buffer b: [256 + 128 b, 320 + 128 b), bf16 pairs
+constexpr int kColP = 320;              // P buffer b: [320 + 32 b, 352 + 32 b), bf16 pairs
+constexpr float kRescale = 8.f;         // log2 growth allowed before rescaling
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;             // descriptor version of the sm_100 family
+    d |= (uint64_t)2 << 61;             // 128-byte swizzle
+    return d;
+}
+
+// bf16 x bf16 -> fp32, M x N; a_mn / b_mn: operand stored MN-major.
+__host__ __device__ constexpr uint32_t idesc(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+           ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D (TMEM) (+)= A (TMEM, lane = row, two bf16 per column) x B (shared memory)
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id,
+                                    uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate));
+}
+
+__device__ __forceinline__ void commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31]));
+}
+
+__device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Byte offset, inside a K or V tile, of token `tok`'s first 128-byte row
+// (half 0); tiles are blocks of 2^rbl tokens, each block NH halves of
+// 2^rbl rows of 128 bytes (see tile_addr).
+template <int NH>
+__device__ __forceinline__ uint32_t row_off(int tok, int rbl) {
+    return (uint32_t)((((tok >> rbl) * NH) << rbl) + (tok & ((1 << rbl) - 1))) * 128u;
+}
+
+struct Shared {
+    uint64_t full[kNS], empty[kNS];
+    uint64_t s_full[2], p_full[2], o_upd[2];
+    uint64_t q_ready[2];                // Q buffer b holds segment n (n % 2 == b)
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+}  // namespace umma
+
+template <int D>
+__global__ void __launch_bounds__(umma::kThreads, 1)
+attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUtensorMap mk,
+                 const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mkb,
+                 const __grid_constant__ CUtensorMap mvb, const __grid_constant__ CUtensorMap msk,
+                 const __grid_constant__ CUtensorMap msv) {
+    using namespace umma;
+    static_assert(D == 128, "tcgen05 path is built for head_dim 128");
+    constexpr int NH = D / 64;
+    constexpr int KV_BYTES = NH * kHalfBytes;
+    constexpr int STAGE = 2 * KV_BYTES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Shared &sh = *reinterpret_cast<Shared *>(smem + kNS * STAGE);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const AttnParams &A = P.a;
+
+    if (threadIdx.x == kProducerWarp * 32) {
+        const CUtensorMap *maps[6] = {&mk, &mv, &mkb, &mvb, &msk, &msv};
+        for (int i = 0; i < 6; ++i)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(maps[i]))
+                         : "memory");
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kNS; ++s) {
+            mbar_init(&sh.full[s], 1);
+            mbar_init(&sh.empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sh.s_full[b], 1);
+            mbar_init(&sh.p_full[b], kSoftmaxWarps);
+            mbar_init(&sh.o_upd[b], 1);
+        }
+        mbar_init(&sh.q_ready[0], kSoftmaxWarps);
+        mbar_init(&sh.q_ready[1], kSoftmaxWarps);
+        mbar_init(&sh.drain, 1);
+        sh.abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&sh.tmem_base)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = sh.tmem_base;
+
+    const long long T = warp_total_tiles(P);
+    const int cta = blockIdx.x;
+    const long long t_begin = range_lo(T, cta, P.n_ctas);
+    const long long t_end = range_lo(T, cta + 1, P.n_ctas);
+    volatile int *abort = &sh.abort;
+
+    if (t_begin < t_end) {
+        if (warp == kProducerWarp) {
+            run_producer<D, kNS>(P, mk, mv, mkb, mvb, msk, msv, smem, sh.full, sh.empty, t_begin,
+                                 t_end);
+        } else if (warp == kMmaWarp) {
+            // --------------------------------------------------- MMA issuer
+            Cursor c;
+            cursor_init(P, t_begin, c);
+            if (lane == 0) {
+                const uint32_t id_pv = idesc(kRows, D, false, true);
+                const uint32_t id_s64 = idesc(kRows, kTile, false, false);
+                uint32_t a_q = tmem + kColQ;
+                int seg_n = 0;
+                int prev_rbl = 6, prev_stage = 0;
+                bool prev_first = true;
+                bool ok = true;
+                // O += P(j) V(j): A = P buffer j%2 (TMEM), B = V (MN-major smem)
+                auto issue_pv = [&](long long j, int rbl, int stage, bool first) -> bool {
+                    const int b = (int)(j & 1);
+                    if (!mbar_wait(&sh.p_full[b], (uint32_t)((j >> 1) & 1))) return false;
+                    fence_after();
+                    const uint32_t vb = smem_u32(smem + stage * STAGE + KV_BYTES);
+                    const uint32_t a_p = tmem + kColP + (uint32_t)b * (kTile / 2);
+                    if (rbl == 6) {
+                        const uint64_t vd = smem_desc(vb, kHalfBytes, 1024);
+#pragma unroll
+                        for (int ks = 0; ks < kTile / 16; ++ks)
+                            mma(tmem + kColO, a_p + ks * 8, vd + (uint64_t)((ks * 2048) >> 4),
+                                id_pv, (ks > 0 || !first) ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int ks = 0; ks < kTile / 16; ++ks)
+                            mma(tmem + kColO, a_p + ks * 8,
+                                smem_desc(vb + row_off<NH>(ks * 16, rbl), (1u << rbl) * 128u, 1024),
+                                id_pv, (ks > 0 || !first) ? 1u : 0u);
+                    }
+                    commit(&sh.o_upd[b]);
+                    commit(&sh.empty[stage]);
+                    return true;
+                };
+                long long k = 0;
+                for (long long t = t_begin; t < t_end && ok; ++t, ++k) {
+                    const TileInfo ti = tile_info(P, c);
+                    const bool new_seg = (k == 0) || (c.tile == 0);
+                    const int stage = (int)(k % kNS);
+                    const int rbl = (ti.kind == kPrefix && A.paged) ? P.page_log2 : 6;
+                    if (new_seg && k > 0) {
+                        ok = issue_pv(k - 1, prev_rbl, prev_stage, prev_first);
+                        if (!ok) break;
+                    }
+                    if (new_seg) {
+                        if (!mbar_wait(&sh.q_ready[seg_n & 1], (uint32_t)((seg_n >> 1) & 1))) {
+                            ok = false;
+                            break;
+                        }
+                        a_q = tmem + kColQ + (uint32_t)(seg_n & 1) * 128;
+                        ++seg_n;
+                        fence_after();
+                    }
+                    if (!mbar_wait(&sh.full[stage], (uint32_t)((k / kNS) & 1))) { ok = false; break; }
+                    // S(k) = Q K^T into S buffer k%2
+                    const uint32_t kb = smem_u32(smem + stage * STAGE);
+                    const uint32_t s_col = tmem + kColS + (uint32_t)(k & 1) * kTile;
+                    if (rbl == 6) {
+                        const uint64_t kd = smem_desc(kb, 16, 1024);
+#pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks)
+                            mma(s_col, a_q + ks * 8,
+                                kd + (uint64_t)((((ks >> 2) * kHalfBytes) + (ks & 3) * 32) >> 4),
+                                id_s64, ks > 0 ? 1u : 0u);
+                    } else {
+                        // paged tile: one MMA per page block (its 8-row groups
+                        // are contiguous only within the block)
+                        const int blk = 1 << rbl;
+                        const uint32_t id_s = idesc(kRows, blk, false, false);
+                        for (int i = 0; i < kTile / blk; ++i)
+#pragma unroll
+                            for (int ks = 0; ks < D / 16; ++ks) {
+                                const int hh = ks >> 2, kk = ks & 3;
+                                const uint32_t boff = (uint32_t)((i * NH + hh) * blk) * 128u + kk * 32;
+                                mma(s_col + i * blk, a_q + ks * 8, smem_desc(kb + boff, 16, 1024),
+                                    id_s, ks > 0 ? 1u : 0u);
+                            }
+                    }
+                    commit(&sh.s_full[k & 1]);
+                    if (!new_seg && k > 0) {
+                        ok = issue_pv(k - 1, prev_rbl, prev_stage, prev_first);
+                        if (!ok) break;
+                    }
+                    prev_rbl = rbl;
+                    prev_stage = stage;
+                    prev_first = new_seg;
+                    cursor_next(P, c);
+                }
+                if (ok && k > 0) ok = issue_pv(k - 1, prev_rbl, prev_stage, prev_first);
+                if (!ok) {
+                    raise_status(A.status, SPEC_DEV_TIMEOUT);
+                    *abort = 1;
+                }
+                // every MMA issued above has completed before TMEM is released
+                commit(&sh.drain);
+                if (!mbar_wait(&sh.drain, 0)) raise_status(A.status, SPEC_DEV_TIMEOUT);
+            }
+        } else {
+            // ------------------------------------------------------ softmax
+            const int r = warp * 32 + lane;                 // row of the CTA tile
+            const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+            Cursor c;
+            cursor_init(P, t_begin, c);
+            float m_used = -INFINITY, l = 0.f;
+            bool rvalid = false, rsoft = false;
+            int rrow = -1;
+            uint64_t vmask = 0;
+            int vmask_j = -1;
+            int seg_id = 0;
+            bool first = true;
+            long long k = 0;
+            const float sc = A.scale_log2;
+
+            // partial (m, l, O row) of this CTA for segment `seg`, after PV(j)
+            auto epilogue = [&](long long j, int seg) -> bool {
+                if (!mbar_wait(&sh.o_upd[j & 1], (uint32_t)((j >> 1) & 1))) return false;
+                fence_after();
+                const size_t row = slot_row(P, seg, cta, 0, 1, r);
+                float *po = A.part_o + row * D;
+#pragma unroll
+                for (int c32 = 0; c32 < D / 32; ++c32) {
+                    uint32_t v[32];
+                    ld32(tmem + lane_base + kColO + c32 * 32, v);
+                    wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4 *>(po + c32 * 32 + e) =
+                            make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                                        __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+                }
+                A.part_ml[row * 2] = m_used;
+                A.part_ml[row * 2 + 1] = l;
+                return true;
+            };
+
+            int seg_n = 0;
+            // this row's query for the segment at cursor cq -> TMEM Q buffer
+            // n % 2 (the bf16 pairs of a row, in order, are exactly the
+            // 32-bit columns the MMA reads), then signal that buffer
+            auto load_q = [&](const Cursor &cq, int n) {
+                const int p = cq.rb * kRows + r;
+                const uint4 *qsrc = nullptr;
+                if (p < A.M) {
+                    const int rr = p / A.G, hq = cq.h * A.G + p % A.G;
+                    qsrc = reinterpret_cast<const uint4 *>(
+                        static_cast<const __nv_bfloat16 *>(A.q) +
+                        (((size_t)cq.b * A.R + rr) * A.Hq + hq) * D);
+                }
+#pragma unroll
+                for (int c32 = 0; c32 < D / 64; ++c32) {
+                    uint32_t w[32];
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        const uint4 x = qsrc ? qsrc[c32 * 8 + v] : make_uint4(0u, 0u, 0u, 0u);
+                        w[4 * v] = x.x;
+                        w[4 * v + 1] = x.y;
+                        w[4 * v + 2] = x.z;
+                        w[4 * v + 3] = x.w;
+                    }
+                    st32(tmem + lane_base + kColQ + (uint32_t)(n & 1) * 128 + c32 * 32, w);
+                }
+                wait_st();
+                fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.q_ready[n & 1]);
+            };
+            bool ok = true;
+            for (long long t = t_begin; t < t_end; ++t, ++k) {
+                if (*abort) { ok = false; break; }
+                const TileInfo ti = tile_info(P, c);
+                const bool new_seg = (k == 0) || (c.tile == 0);
+                if (new_seg) {
+                    if (k > 0 && !(ok = epilogue(k - 1, seg_id))) break;
+                    seg_id = (c.b * A.Hkv + c.h) * A.n_rb + c.rb;
+                    if (k == 0) load_q(c, 0);        // first segment of this CTA
+                    // the next segment's queries go to the other buffer now,
+                    // while this segment runs (its last S MMAs are complete:
+                    // the epilogue above waited for the final PV)
+                    const long long left = c.n_tiles - c.tile;
+                    if (t + left < t_end) {
+                        Cursor cn = c;
+                        cn.tile = cn.n_tiles - 1;
+                        cursor_next(P, cn);
+                        load_q(cn, seg_n + 1);
+                    }
+                    // this row's flags for the segment
+                    const int p = c.rb * kRows + r;
+                    rvalid = rsoft = false;
+                    rrow = -1;
+                    if (p < A.M) {
+                        rrow = p / A.G;
+                        const uint8_t fl = A.row_flags[(size_t)c.b * A.R + rrow];
+                        rvalid = (fl & SPEC_ROW_VALID) != 0;
+                        rsoft = rvalid && (fl & SPEC_ROW_SEES_SOFT) != 0;
+                    }
+                    ++seg_n;
+                    m_used = -INFINITY;
+                    l = 0.f;
+                    vmask_j = -1;
+                    first = true;
+                }
+                if (ti.kind == kBlock && vmask_j != ti.j) {
+                    uint64_t w = 0;
+                    if (rrow >= 0 && rvalid) {
+                        const uint32_t *vr = A.vis + ((size_t)c.b * A.R + rrow) * A.W;
+                        w = vr[2 * ti.j];
+                        if (2 * ti.j + 1 < A.W) w |= (uint64_t)vr[2 * ti.j + 1] << 32;
+                    }
+                    vmask = w;
+                    vmask_j = ti.j;
+                }
+                // S row of this tile
+                if (!mbar_wait(&sh.s_full[k & 1], (uint32_t)((k >> 1) & 1))) { ok = false; break; }
+                fence_after();
+                float x[kTile];
+                {
+                    uint32_t v[32];
+                    const uint32_t sa = tmem + lane_base + kColS + (uint32_t)(k & 1) * kTile;
+                    ld32(sa, v);
+                    wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(v[e]);
+                    ld32(sa + 32, v);
+                    wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[32 + e] = __uint_as_float(v[e]);
+                }
+                // columns this row sees in this tile, as one 64-bit mask
+                const uint64_t valid_cols =
+                    ti.nvalid >= kTile ? ~0ull : ((1ull << ti.nvalid) - 1ull);
+                uint64_t vm;
+                if (ti.kind == kPrefix) vm = rvalid ? valid_cols : 0ull;
+                else if (ti.kind == kSoft) vm = rsoft ? valid_cols : 0ull;
+                else vm = vmask & valid_cols;
+                float tm = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < kTile; ++e) {
+                    x[e] = ((vm >> e) & 1ull) ? x[e] * sc : -INFINITY;
+                    tm = fmaxf(tm, x[e]);
+                }
+                // raise the reference max only when it grew by more than 2^8
+                if (tm > m_used + kRescale || (m_used == -INFINITY && tm != -INFINITY)) {
+                    const float alpha = (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - tm);
+                    if (!first && m_used != -INFINITY) {
+                        // O holds PV(k-1): wait for it, then scale this row in place
+                        if (!mbar_wait(&sh.o_upd[(k - 1) & 1], (uint32_t)(((k - 1) >> 1) & 1))) {
+                            ok = false;
+                            break;
+                        }
+                        fence_after();
+#pragma unroll
+                        for (int c32 = 0; c32 < D / 32; ++c32) {
+                            uint32_t v[32];
+                            const uint32_t oa = tmem + lane_base + kColO + c32 * 32;
+                            ld32(oa, v);
+                            wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                            st32(oa, v);
+                        }
+                        wait_st();
+                    }
+                    l *= alpha;
+                    m_used = tm;
+                }
+                const float mu = m_used == -INFINITY ? 0.f : m_used;
+                // P buffer k%2 was last read by PV(k-2)
+                if (k >= 2 && !mbar_wait(&sh.o_upd[k & 1], (uint32_t)(((k - 2) >> 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                float rs = 0.f;
+                {
+                    uint32_t w[32];
+#pragma unroll
+                    for (int e = 0; e < kTile / 2; ++e) {
+                        const float p0 = fast_exp2(x[2 * e] - mu);
+                        const float p1 = fast_exp2(x[2 * e + 1] - mu);
+                        rs += p0 + p1;
+                        w[e] = pack_bf16(p0, p1);
+                    }
+                    st32(tmem + lane_base + kColP + (uint32_t)(k & 1) * (kTile / 2), w);
+                }
+                l += rs;
+                if (ti.nvalid < kTile) {
+                    // V rows past the valid count hold whatever the copy left
+                    // (stale or unwritten shared memory, cache slots past S_b):
+                    // P is 0 there, but 0 x NaN is NaN, so clear them
+                    const int rbl = (ti.kind == kPrefix && A.paged) ? P.page_log2 : 6;
+                    uint8_t *vt = smem + (int)(k % kNS) * STAGE + KV_BYTES;
+                    const int nchunk = (kTile - ti.nvalid) * NH * 8;
+                    for (int i = r; i < nchunk; i += kSoftmaxWarps * 32) {
+                        const int tok = ti.nvalid + i / (NH * 8), rem = i % (NH * 8);
+                        const int hh = rem >> 3, ch = rem & 7;
+                        *reinterpret_cast<uint4 *>(vt + row_off<NH>(tok, rbl) +
+                                                   hh * ((1 << rbl) * 128) + ch * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                }
+                wait_st();
+                fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.p_full[k & 1]);
+                first = false;
+                cursor_next(P, c);
+            }
+            if (ok && k > 0) ok = epilogue(k - 1, seg_id);
+            if (!ok) {
+                raise_status(A.status, SPEC_DEV_TIMEOUT);
+                *abort = 1;
+            }
+        }
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == kMmaWarp)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols));
+}
+
 // Merge the partials of every (request, KV head, packed row): one warp each.
 template <int D>
 __global__ void __launch_bounds__(128) attn_tc_combine_kernel(const __grid_constant__ TcParams P,
@@ -846,6 +1368,26 @@ spec_status_t launch_impl(const TcParams &P, const CUtensorMap *maps, cudaStream
     return launch_status();
 }
 
+spec_status_t launch_umma(const TcParams &P, const CUtensorMap *maps, cudaStream_t s) {
+    constexpr int D = 128;
+    constexpr size_t smem = (size_t)umma::kNS * 2 * (D / 64) * kHalfBytes +   // K/V stages
+                            sizeof(umma::Shared) + 1024;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(attn_umma_kernel<D>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    });
+    if (attr_err != cudaSuccess) return SPEC_ERR_CUDA;
+    attn_umma_kernel<D><<<P.n_ctas, umma::kThreads, smem, s>>>(P, maps[0], maps[1], maps[2],
+                                                                 maps[3], maps[4], maps[5]);
+    spec_status_t st = launch_status();
+    if (st != SPEC_OK) return st;
+    dim3 grid(ceil_div(P.a.M, 4), P.a.Hkv, P.a.B);
+    attn_tc_combine_kernel<D><<<grid, 128, 0, s>>>(P, 1);
+    return launch_status();
+}
+
 }  // namespace
 
 bool tc_supported(const AttnParams &P, int dtype) {
@@ -855,17 +1397,26 @@ bool tc_supported(const AttnParams &P, int dtype) {
     return true;
 }
 
+// The tcgen05 kernel takes 128-row blocks: worth it once a KV head carries
+// at least 64 packed rows (the contraction, not HBM, is then the bound).
+bool umma_selected(const AttnParams &P) { return P.d == 128 && P.M >= 64; }
+
 int tc_rows_per_block(const AttnParams &P) {
+    if (umma_selected(P)) return umma::kRows;
     if (P.M <= 16) return 16;
     if (P.M <= 32) return 32;
     return 64;
 }
 
 size_t tc_workspace_bytes(const AttnParams &P, size_t *off_ml) {
-    const TcConfig cfg = choose(P);
-    const int wc = cfg.ncw / cfg.wr;
+    int wc = 1, ctas = num_sms();
+    if (!umma_selected(P)) {
+        const TcConfig cfg = choose(P);
+        wc = cfg.ncw / cfg.wr;
+        ctas = num_sms() * cfg.minb;
+    }
     const size_t segs = (size_t)P.B * P.Hkv * P.n_rb;
-    const size_t rows = (segs + (size_t)num_sms() * cfg.minb) * wc * P.rb_rows;
+    const size_t rows = (segs + (size_t)ctas) * wc * P.rb_rows;
     const size_t o_bytes = (rows * P.d * sizeof(float) + 255) & ~size_t(255);
     *off_ml = o_bytes;
     return o_bytes + ((rows * 2 * sizeof(float) + 255) & ~size_t(255));
@@ -874,7 +1425,8 @@ size_t tc_workspace_bytes(const AttnParams &P, size_t *off_ml) {
 spec_status_t launch_attn_tc(const AttnParams &A, cudaStream_t s) {
     TcParams P{};
     P.a = A;
-    const TcConfig cfg = choose(A);
+    const bool use_umma = umma_selected(A);
+    const TcConfig cfg = use_umma ? TcConfig{8, 4, 0, 1} : choose(A);
     P.n_ctas = num_sms() * cfg.minb;
     P.soft_tiles = ceil_div(A.n_soft, kTile);
     P.tail = P.soft_tiles + ceil_div(A.R, kTile);
@@ -898,6 +1450,7 @@ spec_status_t launch_attn_tc(const AttnParams &A, cudaStream_t s) {
         maps[5] = maps[3];
     }
     if (!ok) return SPEC_ERR_CUDA;
+    if (use_umma) return launch_umma(P, maps, s);
     if (A.d == 128) {
         if (cfg.wr == 1) return launch_impl<128, 1, 4, 3, 2>(P, maps, s);
         if (cfg.wr == 2) return launch_impl<128, 2, 4, 3, 2>(P, maps, s);

@@ -34,7 +34,9 @@ __global__ void mask_build_kernel(const int32_t *__restrict__ vparent,
             // c is a valid row index here; its parent must be -1 or an
             // earlier row that is not padding.
             while (true) {
-                words[c >> 5] |= 1u << (c & 31);
+#pragma unroll
+                for (int w = 0; w < kMaxWords; ++w)
+                    if (w == (c >> 5)) words[w] |= 1u << (c & 31);
                 const int p = svp[c];
                 if (p == SPEC_VP_ROOT) break;
                 if (p < 0 || p >= c || svp[p] == SPEC_VP_PAD) {
