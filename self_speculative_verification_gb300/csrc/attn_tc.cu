@@ -863,7 +863,7 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Shared &sh = *reinterpret_cast<Shared *>(smem + kNS * STAGE);
+    Shared &sh = *reinterpret_cast<Shared *>(smem + kNS * STAGE + kRows * D * 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const AttnParams &A = P.a;
@@ -1015,59 +1015,57 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
             // ------------------------------------------------------ softmax
             const int r = warp * 32 + lane;                 // row of the CTA tile
             const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+            uint8_t *qstage = smem + kNS * STAGE;           // [128 rows][D * 2 B]
             Cursor c;
             cursor_init(P, t_begin, c);
             float m_used = -INFINITY, l = 0.f;
-            bool rvalid = false, rsoft = false;
-            int rrow = -1;
+            bool rvalid = false, rsoft = false, warp_rows = false;
+            int rrow = -1, seg_n = 0, vmask_j = -1;
+            int seg_b = 0, seg_h = 0, seg_rb = 0, seg_id = 0;
             uint64_t vmask = 0;
-            int vmask_j = -1;
-            int seg_id = 0;
-            bool first = true;
+            bool first = true, seg_whole = false;
             long long k = 0;
             const float sc = A.scale_log2;
 
-            // partial (m, l, O row) of this CTA for segment `seg`, after PV(j)
-            auto epilogue = [&](long long j, int seg) -> bool {
-                if (!mbar_wait(&sh.o_upd[j & 1], (uint32_t)((j >> 1) & 1))) return false;
-                fence_after();
-                const size_t row = slot_row(P, seg, cta, 0, 1, r);
-                float *po = A.part_o + row * D;
-#pragma unroll
-                for (int c32 = 0; c32 < D / 32; ++c32) {
-                    uint32_t v[32];
-                    ld32(tmem + lane_base + kColO + c32 * 32, v);
-                    wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4 *>(po + c32 * 32 + e) =
-                            make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                                        __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-                }
-                A.part_ml[row * 2] = m_used;
-                A.part_ml[row * 2 + 1] = l;
-                return true;
-            };
-
-            int seg_n = 0;
-            // this row's query for the segment at cursor cq -> TMEM Q buffer
-            // n % 2 (the bf16 pairs of a row, in order, are exactly the
-            // 32-bit columns the MMA reads), then signal that buffer
-            auto load_q = [&](const Cursor &cq, int n) {
+            // this row's query for the segment at cursor cq (nullptr: padding)
+            auto q_row = [&](const Cursor &cq) -> const uint4 * {
                 const int p = cq.rb * kRows + r;
-                const uint4 *qsrc = nullptr;
-                if (p < A.M) {
-                    const int rr = p / A.G, hq = cq.h * A.G + p % A.G;
-                    qsrc = reinterpret_cast<const uint4 *>(
-                        static_cast<const __nv_bfloat16 *>(A.q) +
-                        (((size_t)cq.b * A.R + rr) * A.Hq + hq) * D);
+                if (p >= A.M) return nullptr;
+                const int rr = p / A.G, hq = cq.h * A.G + p % A.G;
+                return reinterpret_cast<const uint4 *>(
+                    static_cast<const __nv_bfloat16 *>(A.q) + (((size_t)cq.b * A.R + rr) * A.Hq + hq) * D);
+            };
+            // start copying a query row into this thread's staging row
+            // (16-byte chunk v at chunk v ^ (r % 16): conflict-free reads)
+            auto stage_q = [&](const uint4 *src) {
+                if (src) {
+#pragma unroll
+                    for (int v = 0; v < D / 8; ++v) {
+                        const uint32_t dst = smem_u32(qstage + r * (D * 2) + ((v ^ (r & 15)) << 4));
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
+                                     "l"(src + v)
+                                     : "memory");
+                    }
                 }
+                asm volatile("cp.async.commit_group;" ::: "memory");
+            };
+            // query row -> TMEM Q buffer n % 2 (the bf16 pairs of a row, in
+            // order, are exactly the 32-bit columns the MMA reads); from
+            // global memory, or from this thread's staging row
+            auto put_q = [&](const uint4 *src, bool staged, int n) {
+                if (staged) asm volatile("cp.async.wait_all;" ::: "memory");
 #pragma unroll
                 for (int c32 = 0; c32 < D / 64; ++c32) {
                     uint32_t w[32];
 #pragma unroll
                     for (int v = 0; v < 8; ++v) {
-                        const uint4 x = qsrc ? qsrc[c32 * 8 + v] : make_uint4(0u, 0u, 0u, 0u);
+                        const int vi = c32 * 8 + v;
+                        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+                        if (src) {
+                            x = staged ? *reinterpret_cast<const uint4 *>(
+                                             qstage + r * (D * 2) + ((vi ^ (r & 15)) << 4))
+                                       : src[vi];
+                        }
                         w[4 * v] = x.x;
                         w[4 * v + 1] = x.y;
                         w[4 * v + 2] = x.z;
@@ -1080,27 +1078,93 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh.q_ready[n & 1]);
             };
+            // end of this CTA's part of a segment (after PV(j)): a segment
+            // wholly inside this CTA's range writes its final O (bf16) and
+            // LSE; otherwise the (m, l, O) partial goes to the workspace
+            auto epilogue = [&](long long j) -> bool {
+                if (!mbar_wait(&sh.o_upd[j & 1], (uint32_t)((j >> 1) & 1))) return false;
+                fence_after();
+                const int p = seg_rb * kRows + r;
+                if (p >= A.M) return true;
+                if (seg_whole) {
+                    const int rr = p / A.G, hq = seg_h * A.G + p % A.G;
+                    const float inv = l > 0.f ? 1.f / l : 0.f;
+                    uint4 *dst = reinterpret_cast<uint4 *>(
+                        static_cast<__nv_bfloat16 *>(A.o) + (((size_t)seg_b * A.R + rr) * A.Hq + hq) * D);
+#pragma unroll
+                    for (int c32 = 0; c32 < D / 32; ++c32) {
+                        uint32_t v[32];
+                        ld32(tmem + lane_base + kColO + c32 * 32, v);
+                        wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; e += 8)
+                            dst[(c32 * 32 + e) / 8] = make_uint4(
+                                pack_bf16(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv),
+                                pack_bf16(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv),
+                                pack_bf16(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv),
+                                pack_bf16(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv));
+                    }
+                    A.lse[((size_t)seg_b * A.Hq + hq) * A.R + rr] =
+                        l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+                } else {
+                    const size_t row = slot_row(P, seg_id, cta, 0, 1, r);
+                    float *po = A.part_o + row * D;
+#pragma unroll
+                    for (int c32 = 0; c32 < D / 32; ++c32) {
+                        uint32_t v[32];
+                        ld32(tmem + lane_base + kColO + c32 * 32, v);
+                        wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4)
+                            *reinterpret_cast<float4 *>(po + c32 * 32 + e) =
+                                make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                                            __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+                    }
+                    A.part_ml[row * 2] = m_used;
+                    A.part_ml[row * 2 + 1] = l;
+                }
+                return true;
+            };
+
             bool ok = true;
             for (long long t = t_begin; t < t_end; ++t, ++k) {
                 if (*abort) { ok = false; break; }
                 const TileInfo ti = tile_info(P, c);
                 const bool new_seg = (k == 0) || (c.tile == 0);
                 if (new_seg) {
-                    if (k > 0 && !(ok = epilogue(k - 1, seg_id))) break;
+                    if (k > 0 && !(ok = epilogue(k - 1))) break;
+                    seg_b = c.b;
+                    seg_h = c.h;
+                    seg_rb = c.rb;
                     seg_id = (c.b * A.Hkv + c.h) * A.n_rb + c.rb;
-                    if (k == 0) load_q(c, 0);        // first segment of this CTA
-                    // the next segment's queries go to the other buffer now,
-                    // while this segment runs (its last S MMAs are complete:
-                    // the epilogue above waited for the final PV)
-                    const long long left = c.n_tiles - c.tile;
-                    if (t + left < t_end) {
-                        Cursor cn = c;
-                        cn.tile = cn.n_tiles - 1;
-                        cursor_next(P, cn);
-                        load_q(cn, seg_n + 1);
+                    const long long seg_lo = t - c.tile;
+                    seg_whole = seg_lo >= t_begin && seg_lo + c.n_tiles <= t_end;
+                    // the next two segments of this range, if any
+                    const long long t_next = t + (c.n_tiles - c.tile);
+                    Cursor cn = c;
+                    cn.tile = cn.n_tiles - 1;
+                    cursor_next(P, cn);
+                    const bool has_next = t_next < t_end;
+                    const bool has_next2 = has_next && t_next + cn.n_tiles < t_end;
+                    Cursor cnn = cn;
+                    if (has_next2) {
+                        cnn.tile = cnn.n_tiles - 1;
+                        cursor_next(P, cnn);
                     }
+                    // Q(seg_n) is in TMEM buffer seg_n % 2 already (except at
+                    // the first segment); Q(seg_n + 1) goes to the other
+                    // buffer now (its previous S MMAs finished: the epilogue
+                    // waited for the last PV); Q(seg_n + 2) starts staging.
+                    if (k == 0) {
+                        put_q(q_row(c), false, 0);
+                        if (has_next) put_q(q_row(cn), false, 1);
+                    } else if (has_next) {
+                        put_q(q_row(cn), true, seg_n + 1);
+                    }
+                    if (has_next2) stage_q(q_row(cnn));
                     // this row's flags for the segment
                     const int p = c.rb * kRows + r;
+                    warp_rows = c.rb * kRows + warp * 32 < A.M;
                     rvalid = rsoft = false;
                     rrow = -1;
                     if (p < A.M) {
@@ -1125,80 +1189,85 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                     vmask = w;
                     vmask_j = ti.j;
                 }
-                // S row of this tile
                 if (!mbar_wait(&sh.s_full[k & 1], (uint32_t)((k >> 1) & 1))) { ok = false; break; }
                 fence_after();
-                float x[kTile];
-                {
-                    uint32_t v[32];
-                    const uint32_t sa = tmem + lane_base + kColS + (uint32_t)(k & 1) * kTile;
-                    ld32(sa, v);
-                    wait_ld();
+                if (warp_rows) {
+                    float x[kTile];
+                    {
+                        uint32_t v[32];
+                        const uint32_t sa = tmem + lane_base + kColS + (uint32_t)(k & 1) * kTile;
+                        ld32(sa, v);
+                        wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(v[e]);
-                    ld32(sa + 32, v);
-                    wait_ld();
+                        for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(v[e]);
+                        ld32(sa + 32, v);
+                        wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) x[32 + e] = __uint_as_float(v[e]);
-                }
-                // columns this row sees in this tile, as one 64-bit mask
-                const uint64_t valid_cols =
-                    ti.nvalid >= kTile ? ~0ull : ((1ull << ti.nvalid) - 1ull);
-                uint64_t vm;
-                if (ti.kind == kPrefix) vm = rvalid ? valid_cols : 0ull;
-                else if (ti.kind == kSoft) vm = rsoft ? valid_cols : 0ull;
-                else vm = vmask & valid_cols;
-                float tm = -INFINITY;
-#pragma unroll
-                for (int e = 0; e < kTile; ++e) {
-                    x[e] = ((vm >> e) & 1ull) ? x[e] * sc : -INFINITY;
-                    tm = fmaxf(tm, x[e]);
-                }
-                // raise the reference max only when it grew by more than 2^8
-                if (tm > m_used + kRescale || (m_used == -INFINITY && tm != -INFINITY)) {
-                    const float alpha = (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - tm);
-                    if (!first && m_used != -INFINITY) {
-                        // O holds PV(k-1): wait for it, then scale this row in place
-                        if (!mbar_wait(&sh.o_upd[(k - 1) & 1], (uint32_t)(((k - 1) >> 1) & 1))) {
-                            ok = false;
-                            break;
-                        }
-                        fence_after();
-#pragma unroll
-                        for (int c32 = 0; c32 < D / 32; ++c32) {
-                            uint32_t v[32];
-                            const uint32_t oa = tmem + lane_base + kColO + c32 * 32;
-                            ld32(oa, v);
-                            wait_ld();
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                            st32(oa, v);
-                        }
-                        wait_st();
+                        for (int e = 0; e < 32; ++e) x[32 + e] = __uint_as_float(v[e]);
                     }
-                    l *= alpha;
-                    m_used = tm;
-                }
-                const float mu = m_used == -INFINITY ? 0.f : m_used;
-                // P buffer k%2 was last read by PV(k-2)
-                if (k >= 2 && !mbar_wait(&sh.o_upd[k & 1], (uint32_t)(((k - 2) >> 1) & 1))) {
-                    ok = false;
-                    break;
-                }
-                float rs = 0.f;
-                {
+                    // columns this row sees in this tile, as one 64-bit mask
+                    const uint64_t valid_cols =
+                        ti.nvalid >= kTile ? ~0ull : ((1ull << ti.nvalid) - 1ull);
+                    uint64_t vm;
+                    if (ti.kind == kPrefix) vm = rvalid ? valid_cols : 0ull;
+                    else if (ti.kind == kSoft) vm = rsoft ? valid_cols : 0ull;
+                    else vm = vmask & valid_cols;
+                    float tmv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) tmv[e] = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < kTile; ++e) {
+                        x[e] = ((vm >> e) & 1ull) ? x[e] * sc : -INFINITY;
+                        tmv[e & 7] = fmaxf(tmv[e & 7], x[e]);
+                    }
+                    const float tm = fmaxf(fmaxf(fmaxf(tmv[0], tmv[1]), fmaxf(tmv[2], tmv[3])),
+                                           fmaxf(fmaxf(tmv[4], tmv[5]), fmaxf(tmv[6], tmv[7])));
+                    // raise the reference max only when it grew by more than 2^8
+                    if (tm > m_used + kRescale || (m_used == -INFINITY && tm != -INFINITY)) {
+                        const float alpha = (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - tm);
+                        if (!first && m_used != -INFINITY) {
+                            // O holds PV(k-1): wait for it, then scale this row in place
+                            if (!mbar_wait(&sh.o_upd[(k - 1) & 1], (uint32_t)(((k - 1) >> 1) & 1))) {
+                                ok = false;
+                                break;
+                            }
+                            fence_after();
+#pragma unroll
+                            for (int c32 = 0; c32 < D / 32; ++c32) {
+                                uint32_t v[32];
+                                const uint32_t oa = tmem + lane_base + kColO + c32 * 32;
+                                ld32(oa, v);
+                                wait_ld();
+#pragma unroll
+                                for (int e = 0; e < 32; ++e)
+                                    v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                                st32(oa, v);
+                            }
+                            wait_st();
+                        }
+                        l *= alpha;
+                        m_used = tm;
+                    }
+                    const float mu = m_used == -INFINITY ? 0.f : m_used;
+                    // P buffer k%2 was last read by PV(k-2)
+                    if (k >= 2 && !mbar_wait(&sh.o_upd[k & 1], (uint32_t)(((k - 2) >> 1) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    float rsv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) rsv[e] = 0.f;
                     uint32_t w[32];
 #pragma unroll
                     for (int e = 0; e < kTile / 2; ++e) {
                         const float p0 = fast_exp2(x[2 * e] - mu);
                         const float p1 = fast_exp2(x[2 * e + 1] - mu);
-                        rs += p0 + p1;
+                        rsv[e & 7] += p0 + p1;
                         w[e] = pack_bf16(p0, p1);
                     }
                     st32(tmem + lane_base + kColP + (uint32_t)(k & 1) * (kTile / 2), w);
+                    l += ((rsv[0] + rsv[1]) + (rsv[2] + rsv[3])) + ((rsv[4] + rsv[5]) + (rsv[6] + rsv[7]));
                 }
-                l += rs;
                 if (ti.nvalid < kTile) {
                     // V rows past the valid count hold whatever the copy left
                     // (stale or unwritten shared memory, cache slots past S_b):
@@ -1222,7 +1291,8 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                 first = false;
                 cursor_next(P, c);
             }
-            if (ok && k > 0) ok = epilogue(k - 1, seg_id);
+            if (ok && k > 0) ok = epilogue(k - 1);
+            asm volatile("cp.async.wait_all;" ::: "memory");
             if (!ok) {
                 raise_status(A.status, SPEC_DEV_TIMEOUT);
                 *abort = 1;
@@ -1240,7 +1310,7 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
 // Merge the partials of every (request, KV head, packed row): one warp each.
 template <int D>
 __global__ void __launch_bounds__(128) attn_tc_combine_kernel(const __grid_constant__ TcParams P,
-                                                               int wcn) {
+                                                               int wcn, int whole_done) {
     const AttnParams &A = P.a;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int p = blockIdx.x * 4 + warp;
@@ -1258,6 +1328,8 @@ __global__ void __launch_bounds__(128) attn_tc_combine_kernel(const __grid_const
     const long long s1 = s0 + nt;
     const int seg = (b * A.Hkv + h) * A.n_rb + rb;
     const int first = cta_of(T, s0, P.n_ctas), last = cta_of(T, s1 - 1, P.n_ctas);
+    // segments inside one CTA's range were finished by the attention kernel
+    if (whole_done && first == last) return;
 
     float mstar = -INFINITY;
     for (int i = first; i <= last; ++i) {
@@ -1364,13 +1436,14 @@ spec_status_t launch_impl(const TcParams &P, const CUtensorMap *maps, cudaStream
     spec_status_t st = launch_status();
     if (st != SPEC_OK) return st;
     dim3 grid(ceil_div(P.a.M, 4), P.a.Hkv, P.a.B);
-    attn_tc_combine_kernel<D><<<grid, 128, 0, s>>>(P, NCW / WR);
+    attn_tc_combine_kernel<D><<<grid, 128, 0, s>>>(P, NCW / WR, 0);
     return launch_status();
 }
 
 spec_status_t launch_umma(const TcParams &P, const CUtensorMap *maps, cudaStream_t s) {
     constexpr int D = 128;
     constexpr size_t smem = (size_t)umma::kNS * 2 * (D / 64) * kHalfBytes +   // K/V stages
+                            (size_t)umma::kRows * D * 2 +                    // query staging
                             sizeof(umma::Shared) + 1024;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -1384,7 +1457,7 @@ spec_status_t launch_umma(const TcParams &P, const CUtensorMap *maps, cudaStream
     spec_status_t st = launch_status();
     if (st != SPEC_OK) return st;
     dim3 grid(ceil_div(P.a.M, 4), P.a.Hkv, P.a.B);
-    attn_tc_combine_kernel<D><<<grid, 128, 0, s>>>(P, 1);
+    attn_tc_combine_kernel<D><<<grid, 128, 0, s>>>(P, 1, 1);
     return launch_status();
 }
 
