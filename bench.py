@@ -133,6 +133,24 @@ def recorded_traffic(config):
     return None
 
 
+def max_over_ranks(x: float, device="cpu") -> float:
+    """Largest value of x over the ranks of the default process group (x
+    itself without one).  The bench takes the slowest rank's time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_step: int, steps: int, world: int, total_ms: float) -> float:
+    """Whole-job verified tokens per second: every rank runs its own replica
+    (weak scaling), all ranks' tokens over the slowest rank's time."""
+    return tokens_per_step * steps * world / (total_ms / 1e3)
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling while the timed region runs."""
 
@@ -393,13 +411,10 @@ def run_gpu(args):
     step_ms = per.sum(axis=1)
     region_ms = region[0].elapsed_time(region[1])
     total_ms = float(step_ms.sum()) if flush else region_ms
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev)
 
     tokens = wl.verified_tokens()
-    value = tokens * args.steps * world / (total_ms / 1e3)
+    value = job_throughput(tokens, args.steps, world, total_ms)
     attn_ms = float(per[:, 1].mean())
     hbm, hbm_kind = peaks()
     achieved = attn_bytes / (attn_ms / 1e3) / 1e9
