@@ -48,3 +48,14 @@ def test_gqa_many_row_blocks():
     wl = W.make_workload("confu", 24, B=3, seq=("uniform", 500, 1300), V=2000,
                          q_scale=8.0)
     gh.run_and_check(wl)
+
+
+@pytest.mark.parametrize("name", ["ss", "confu"])
+@pytest.mark.parametrize("page_size", [16, 32, 64])
+def test_many_rows_on_paged_cache(name, page_size):
+    """>= 64 packed rows per KV head (the tcgen05 kernel) on paged caches:
+    one MMA per page block for S, V fetched per page block for PV."""
+    wl = W.make_workload(name, 25, B=2, seq=("uniform", 150, 700), V=2000, paged=True,
+                         page_size=page_size)
+    gh.run_and_check(wl)
+    gh.run_and_check(wl, split_tokens=64)
