@@ -86,6 +86,41 @@ def la_prefill_mask(n: int, k: int) -> np.ndarray:
     return m
 
 
+def la_prefill_attention(q, k, v, n, scale=None):
+    """Attention of all n + k positions under the full LA mask (LA sec. 3.1).
+
+    q, k, v: [L][d] with L = n + k (n originals, then k lookahead rows);
+    returns O [L][d] and LSE [L] (float64): softmax(q K^T * scale + M) V with
+    M the additive 0 / -inf form of ``la_prefill_mask(n, L - n)``.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    L, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    mask = np.where(la_prefill_mask(n, L - n), 0.0, -np.inf)
+    s = (q @ k.T) * scale + mask
+    O = np.empty((L, d))
+    LSE = np.empty(L)
+    for i in range(L):
+        m = s[i].max()
+        LSE[i] = m + math.log(np.exp(s[i] - m).sum())
+        O[i] = np.exp(s[i] - LSE[i]) @ v
+    return O, LSE
+
+
+def la_prefill_vparent(n: int, k: int) -> np.ndarray:
+    """Parent pointers whose closure is M_LA (LA sec. 3.1): original i's
+    parent is i - 1 (causal), every lookahead row's parent is the last
+    original (it then sees all originals and itself)."""
+    vp = np.empty(n + k, dtype=np.int64)
+    vp[0] = VP_ROOT
+    vp[1:n] = np.arange(n - 1)
+    vp[n:] = n - 1 if n > 0 else VP_ROOT
+    return vp
+
+
 def mask_build(vparent: np.ndarray, soft_flags=None):
     """Visibility of the speculative block, per request.
 
