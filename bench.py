@@ -15,6 +15,11 @@ second (candidate tokens judged per step / step time).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
   python bench.py --impl reference ...   # the CPU oracle, timed the same way
+
+``--config la_prefill`` times the prefill form of Lookahead Attention
+(spec_la_prefill_attn: 4 requests x (4096 + 8) positions, 32 heads, head_dim
+128, bf16) instead; its metric is prefill positions per second and its
+roofline is the tensor-core one.
 """
 
 from __future__ import annotations
@@ -108,25 +113,31 @@ def step_algorithmic_bytes(wl, accepted_rows):
     return attn_algorithmic_bytes(wl) + logits + accept_io + commit + mask
 
 
-def kernel_sources_sha():
+VERIFY_SOURCES = ("attn", "verify_attn", "ptx_")
+PREFILL_SOURCES = ("la_prefill", "ptx_")
+
+
+def kernel_sources_sha(prefixes=VERIFY_SOURCES):
+    """Hash of the CUDA sources (file names starting with ``prefixes``) that
+    a recorded traffic figure was taken from."""
     from self_speculative_verification_gb300 import _build
     h = hashlib.sha256()
     for f in sorted(os.listdir(_build.CSRC)):
-        if f.startswith("attn") or f.startswith("verify_attn"):
+        if f.startswith(prefixes):
             with open(os.path.join(_build.CSRC, f), "rb") as fh:
                 h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(config):
-    """DRAM bytes per spec_verify_attn call from the committed ncu summary,
-    or None if the attention sources changed since it was taken."""
+def recorded_traffic(config, prefixes=VERIFY_SOURCES):
+    """DRAM bytes per call of the workload's dominant kernel from the
+    committed ncu summary, or None if its sources changed since."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         rec = d.get(config)
-        if rec and rec.get("source_sha") == kernel_sources_sha():
+        if rec and rec.get("source_sha") == kernel_sources_sha(prefixes):
             return rec.get("dram_bytes_per_call")
     except Exception:
         pass
@@ -501,8 +512,242 @@ def run_e2e(ds, steps, stream):
             "timing": "host wall clock per step, stream synchronised each step"}
 
 
+# ------------------------------------------------------ prefill-form LA
+
+PREFILL_METRIC = "LA prefill positions/s (full M_LA attention, all heads)"
+
+
+def prefill_flops(wl):
+    """Algorithmic FLOPs of one call: 4 d per visible (query, key) pair per
+    head (QK^T and PV), nothing over masked pairs.  Original i sees i + 1
+    keys; each lookahead position sees the n originals and itself."""
+    pairs = wl.n * (wl.n + 1) // 2 + wl.k * (wl.n + 1)
+    return 4 * wl.d * pairs * wl.B * wl.Hq
+
+
+def prefill_label(wl):
+    return (f"la_prefill: B={wl.B} n={wl.n} k={wl.k} (L={wl.L}) Hq/Hkv={wl.Hq}/{wl.Hkv} "
+            f"d={wl.d} bf16, full M_LA mask")
+
+
+def _prefill_oracle_worker(conn, cfg, seed, pairs):
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    import oracle
+    from self_speculative_verification_gb300 import workloads as W
+    wl = W.make_prefill(seed, **cfg)
+    G = wl.Hq // wl.Hkv
+    conn.send("ready")
+    while True:
+        if conn.recv() == "stop":
+            break
+        t0 = time.perf_counter()
+        for b, h in pairs:
+            oracle.la_prefill_attention(wl.q[b, :, h], wl.kk[b, :, h // G], wl.v[b, :, h // G],
+                                        wl.n)
+        conn.send(time.perf_counter() - t0)
+    conn.close()
+
+
+def prefill_oracle(cfg, seed, cores, warm, steps):
+    """The oracle on one (request, head) slice per spawned process; returns
+    (positions/s equivalent over all heads, processes, wall seconds per step)."""
+    ctx = mp.get_context("spawn")
+    n = max(1, min(cores, cfg["B"] * cfg["Hq"]))
+    pairs = [(i % cfg["B"], i // cfg["B"]) for i in range(n)]
+    conns, procs = [], []
+    for i in range(n):
+        a, b = ctx.Pipe()
+        p = ctx.Process(target=_prefill_oracle_worker, args=(b, cfg, seed, [pairs[i]]),
+                        daemon=True)
+        p.start()
+        conns.append(a)
+        procs.append(p)
+    for c in conns:
+        c.recv()
+    walls = []
+    try:
+        for i in range(warm + steps):
+            t0 = time.perf_counter()
+            for c in conns:
+                c.send("go")
+            for c in conns:
+                c.recv()
+            if i >= warm:
+                walls.append(time.perf_counter() - t0)
+    finally:
+        for c in conns:
+            try:
+                c.send("stop")
+            except Exception:
+                pass
+        for p in procs:
+            p.join(timeout=10)
+    L = cfg["n"] + cfg["k"]
+    wall = sum(walls) / len(walls)
+    # n slices of L positions each = n / Hq of a full-head pass over L positions
+    return n * L / cfg["Hq"] / wall, n, wall
+
+
+def run_prefill_reference(args):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    from self_speculative_verification_gb300 import workloads as W
+    cfg = dict(W.PREFILL_CONFIGS[args.config])
+    cores = args.cpu_workers or host_cores()
+    value, n, wall = prefill_oracle(cfg, args.seed, cores, min(args.warmup, 1),
+                                    max(1, min(args.steps, 3)))
+    wl = W.make_prefill(args.seed, B=1, n=1, k=0, Hq=1, Hkv=1)   # label only
+    sample = (f"{n} (request, head) slices of {args.config}, one per spawned process, "
+              f"float64 numpy; each step re-runs the sample")
+    line = {
+        "impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": "positions/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * wall, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"la_prefill: B={cfg['B']} n={cfg['n']} k={cfg['k']} "
+                               f"Hq/Hkv={cfg['Hq']}/{cfg['Hkv']} d={cfg['d']}",
+                   "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "positions/s", "cores": n, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    del wl
+    print(json.dumps(line), flush=True)
+
+
+def run_prefill_gpu(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from self_speculative_verification_gb300 import workloads as W
+    from self_speculative_verification_gb300 import binding as bn
+
+    cfg = dict(W.PREFILL_CONFIGS[args.config])
+    if args.batch:
+        cfg["B"] = args.batch
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, n, wall = prefill_oracle(cfg, args.seed, args.cpu_workers or host_cores(), 0, 1)
+        cpu = {"value": v, "unit": "positions/s", "cores": n, "kind": "oracle",
+               "sample": f"{n} (request, head) slices of the workload, one per spawned "
+                         f"process, float64 numpy, scaled to all heads"}
+    wl = W.make_prefill(args.seed + rank, **cfg)
+    bn.load_library()
+    q = torch.from_numpy(wl.q).to(dev, torch.bfloat16)
+    k = torch.from_numpy(wl.kk).to(dev, torch.bfloat16)
+    v = torch.from_numpy(wl.v).to(dev, torch.bfloat16)
+    o = torch.empty_like(q)
+    lse = torch.empty((wl.B, wl.Hq, wl.L), dtype=torch.float32, device=dev)
+    desc = bn.prefill_desc(wl.B, wl.n, wl.k, wl.Hq, wl.Hkv, wl.d)
+    stream = torch.cuda.current_stream(dev)
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v))
+    flush = in_bytes < 2 * L2_BYTES
+    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush else None
+
+    for _ in range(args.warmup):
+        bn.spec_la_prefill_attn(desc, q, k, v, o, lse, stream)
+        if flush:
+            flush_buf.random_()
+    torch.cuda.synchronize(dev)
+    assert bn.spec_get_status() == 0, "device status set during warm-up"
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        for e0, e1 in evs:
+            e0.record(stream)
+            bn.spec_la_prefill_attn(desc, q, k, v, o, lse, stream)
+            e1.record(stream)
+            if flush:
+                flush_buf.random_()
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    status = bn.spec_get_status()
+    times = np.array([a.elapsed_time(b) for a, b in evs])
+    total_ms = max_over_ranks(float(times.sum()), dev)
+    positions = wl.B * wl.L
+    value = positions * args.steps * world / (total_ms / 1e3)
+    flops = prefill_flops(wl)
+    call_ms = float(times.mean())
+    achieved = flops / (call_ms / 1e3) / 1e12
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, peak_kind = float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        peak, peak_kind = 1900.0, "fallback"
+
+    # e2e: pinned host q/k/v in, o/lse out, every call
+    h_in = [t.cpu().pin_memory() for t in (q, k, v)]
+    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (o, lse)]
+    e2e = None
+    if args.e2e_steps > 0:
+        def one():
+            for d, h in zip((q, k, v), h_in):
+                d.copy_(h, non_blocking=True)
+            bn.spec_la_prefill_attn(desc, q, k, v, o, lse, stream)
+            for h, d in zip(h_out, (o, lse)):
+                h.copy_(d, non_blocking=True)
+            stream.synchronize()
+        for _ in range(2):
+            one()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            one()
+        dt = time.perf_counter() - t0
+        e2e = {"value": positions * args.e2e_steps / dt, "unit": "positions/s",
+               "h2d_bytes_per_step": in_bytes,
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in (o, lse)),
+               "ms_per_step": 1e3 * dt / args.e2e_steps}
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": PREFILL_METRIC, "value": value, "unit": "positions/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": prefill_label(wl), "seed": args.seed,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": ("flushed between calls" if flush else
+                          f"inputs larger than L2 ({in_bytes / 1e9:.2f} GB vs 126 MB)")},
+        "roofline": {"kernel": "la_prefill_kernel", "bound": "tensor", "achieved": achieved,
+                     "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_kind": f"{peak_kind} dense bf16 (burst)",
+                     "algorithmic_flops_per_call": flops,
+                     "traffic": recorded_traffic(args.config, PREFILL_SOURCES)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "device_status": status,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
+    from self_speculative_verification_gb300 import workloads as W
+    if args.config in W.PREFILL_CONFIGS:
+        if args.impl == "reference":
+            run_prefill_reference(args)
+        else:
+            run_prefill_gpu(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -155,6 +155,18 @@ typedef struct spec_accept_desc {
     int path_cap;      /* row length of path */
 } spec_accept_desc;
 
+/* Shape of one prefill-form Lookahead Attention call. */
+typedef struct spec_prefill_desc {
+    int batch;         /* B */
+    int n_orig;        /* n: original positions per request (>= 1) */
+    int n_look;        /* k: lookahead positions per request (>= 0) */
+    int n_q_heads;     /* Hq (multiple of n_kv_heads) */
+    int n_kv_heads;    /* Hkv */
+    int head_dim;      /* d: 128 */
+    int dtype;         /* SPEC_BF16 */
+    float scale;       /* softmax scale; 0 -> 1/sqrt(head_dim) */
+} spec_prefill_desc;
+
 /* Library version (SPECVERIFY_VERSION). */
 int spec_version(void);
 
@@ -224,6 +236,28 @@ spec_status_t spec_verify_attn(const spec_attn_desc *attn, const void *q,
                                const uint32_t *vis, const uint8_t *row_flags,
                                void *o, float *lse, void *workspace,
                                size_t workspace_bytes, void *stream);
+
+/*
+ * spec_la_prefill_attn -- the prefill form of Lookahead Attention ([LA]
+ * sec. 3.1): the n original and k lookahead positions of each request attend
+ * in one pass under the full (n + k) x (n + k) mask M_LA.
+ *
+ *   q, o   [batch][n + k][n_q_heads][head_dim] (bf16); positions 0..n-1 are
+ *          the originals, n..n+k-1 the lookahead tokens.
+ *   k, v   [batch][n + k][n_kv_heads][head_dim] (bf16)
+ *   lse    out fp32 [batch][n_q_heads][n + k]: natural-log log-sum-exp of
+ *          each position's scaled scores.
+ *
+ * Position i < n sees keys 0..i (causal attention over the originals);
+ * position i >= n sees keys 0..n-1 and itself.  For query head h the K/V
+ * head is h / (n_q_heads / n_kv_heads); scores are (q . k) * scale.  q, k
+ * and v must be 16-byte aligned.  No workspace: each query tile is finished
+ * by one CTA.  Returns SPEC_ERR_UNSUPPORTED unless dtype is SPEC_BF16 and
+ * head_dim is 128.
+ */
+spec_status_t spec_la_prefill_attn(const spec_prefill_desc *desc, const void *q,
+                                   const void *k, const void *v, void *o,
+                                   float *lse, void *stream);
 
 /* Bytes of the fixed scratch array behind spec_verify_attn_noalloc. */
 #define SPEC_NOALLOC_SCRATCH_BYTES (64u << 20)

@@ -20,6 +20,10 @@ from . import _build
 
 # return codes / enums (include/specverify.h)
 SPEC_OK = 0
+SPEC_ERR_INVALID_ARG = 1
+SPEC_ERR_UNSUPPORTED = 2
+SPEC_ERR_CAPACITY = 4
+SPEC_ERR_CUDA = 5
 SPEC_ERR_DEVICE = 6
 SPEC_F32 = 0
 SPEC_BF16 = 1
@@ -38,7 +42,7 @@ SPEC_DEV_BAD_INDEX = 0x10
 EXPORTS = ("spec_version", "spec_status_string", "spec_mask_build",
            "spec_verify_attn_workspace_size", "spec_verify_attn",
            "spec_verify_attn_noalloc", "spec_vocab_reduce", "spec_accept", "kv_commit",
-           "spec_get_status")
+           "spec_get_status", "spec_la_prefill_attn")
 SPEC_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -66,6 +70,12 @@ class AcceptDesc(ctypes.Structure):
     _fields_ = [("mode", c_int), ("tau", c_float), ("batch", c_int),
                 ("n_judge_rows", c_int), ("vocab", c_int), ("logit_dtype", c_int),
                 ("max_nodes", c_int), ("path_cap", c_int)]
+
+
+class PrefillDesc(ctypes.Structure):
+    _fields_ = [("batch", c_int), ("n_orig", c_int), ("n_look", c_int),
+                ("n_q_heads", c_int), ("n_kv_heads", c_int), ("head_dim", c_int),
+                ("dtype", c_int), ("scale", c_float)]
 
 
 _lib = None
@@ -102,6 +112,7 @@ def load_library():
         "kv_commit": ([POINTER(KvDesc), c_int, c_int, vp, vp, c_int, vp, vp, vp, vp,
                        c_int, vp, vp], c_int),
         "spec_get_status": ([vp, POINTER(ctypes.c_int32)], c_int),
+        "spec_la_prefill_attn": ([POINTER(PrefillDesc), vp, vp, vp, vp, vp, vp], c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -181,6 +192,11 @@ def accept_desc(mode, tau, batch, n_judge_rows, vocab, logit_dtype, max_nodes,
 
 
 # ------------------------------------------------------------------- entry points
+
+def prefill_desc(batch, n_orig, n_look, n_q_heads, n_kv_heads, head_dim, dtype=SPEC_BF16,
+                 scale=0.0) -> PrefillDesc:
+    return PrefillDesc(batch, n_orig, n_look, n_q_heads, n_kv_heads, head_dim, dtype, scale)
+
 
 def spec_version() -> int:
     return load_library().spec_version()
@@ -284,3 +300,14 @@ def spec_get_status(stream=None) -> int:
     if code not in (SPEC_OK, SPEC_ERR_DEVICE):
         _check("spec_get_status", code)
     return out.value
+
+
+def spec_la_prefill_attn(desc: PrefillDesc, q, k, v, o, lse, stream=None):
+    """Prefill-form Lookahead Attention: q, o [B][n+k][Hq][d]; k, v
+    [B][n+k][Hkv][d] (bf16); lse [B][Hq][n+k] fp32."""
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _ptr(t, torch.bfloat16, name)
+    _check("spec_la_prefill_attn", lib.spec_la_prefill_attn(
+        ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+        _ptr(lse, torch.float32, "lse"), _stream(stream)))

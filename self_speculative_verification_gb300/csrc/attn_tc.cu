@@ -32,13 +32,13 @@
 #include <mutex>
 
 #include "attn_tc.cuh"
+#include "ptx_sm103.cuh"
 
 namespace sv {
 namespace {
 
 constexpr int kTile = 64;                 // tokens per tile
 constexpr int kHalfBytes = kTile * 128;   // one 64-token x 64-element bf16 box
-constexpr long long kTimeoutCycles = 2000000000ll;
 
 struct TcParams {
     AttnParams a;
@@ -49,67 +49,7 @@ struct TcParams {
     int page_log2;       // log2(page_size) (paged)
 };
 
-// ------------------------------------------------------------ PTX helpers
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity))
-        if (clock64() - t0 > kTimeoutCycles) return false;
-    return true;
-}
-
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
-                                            uint64_t *bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ uint64_t policy_evict_first() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ __forceinline__ uint64_t policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
+// -------------------------------------------- mma.sync helpers
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                         uint32_t &r3) {
@@ -132,18 +72,6 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// 2^x with the hardware approximation (max relative error ~2^-22); 2^-inf = 0.
-__device__ __forceinline__ float fast_exp2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
 }
 
 // Shared-memory address of 16-byte chunk `chunk` (0..7) of 64-element half
@@ -751,6 +679,8 @@ attn_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUten
 // computed while the softmax works on tile t-1.
 namespace umma {
 
+using namespace tc5;
+
 constexpr int kRows = 128;              // rows per CTA tile (MMA M)
 constexpr int kSoftmaxWarps = 4;
 constexpr int kProducerWarp = 4;
@@ -763,72 +693,6 @@ constexpr int kColS = 128;              // S buffer b: [128 + 64 b, 192 + 64 b)
 constexpr int kColQ = 256;              // Q buffer b: [256 + 128 b, 320 + 128 b), bf16 pairs
 constexpr int kColP = 320;              // P buffer b: [320 + 32 b, 352 + 32 b), bf16 pairs
 constexpr float kRescale = 8.f;         // log2 growth allowed before rescaling
-
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = (uint64_t)((addr >> 4) & 0x3FFFu);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;             // descriptor version of the sm_100 family
-    d |= (uint64_t)2 << 61;             // 128-byte swizzle
-    return d;
-}
-
-// bf16 x bf16 -> fp32, M x N; a_mn / b_mn: operand stored MN-major.
-__host__ __device__ constexpr uint32_t idesc(int M, int N, bool a_mn, bool b_mn) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
-           ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-// D (TMEM) (+)= A (TMEM, lane = row, two bf16 per column) x B (shared memory)
-__device__ __forceinline__ void mma(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id,
-                                    uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate));
-}
-
-__device__ __forceinline__ void commit(uint64_t *bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
-        : "r"(taddr));
-}
-
-__device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
-            taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-        "r"(r[29]), "r"(r[30]), "r"(r[31]));
-}
-
-__device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Byte offset, inside a K or V tile, of token `tok`'s first 128-byte row
 // (half 0); tiles are blocks of 2^rbl tokens, each block NH halves of
@@ -1084,8 +948,11 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
             auto epilogue = [&](long long j) -> bool {
                 if (!mbar_wait(&sh.o_upd[j & 1], (uint32_t)((j >> 1) & 1))) return false;
                 fence_after();
+                // tcgen05.ld is warp-collective: a warp with any real row
+                // loads, and only its real rows store
+                if (!warp_rows) return true;
                 const int p = seg_rb * kRows + r;
-                if (p >= A.M) return true;
+                const bool row_ok = p < A.M;
                 if (seg_whole) {
                     const int rr = p / A.G, hq = seg_h * A.G + p % A.G;
                     const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -1096,6 +963,7 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                         uint32_t v[32];
                         ld32(tmem + lane_base + kColO + c32 * 32, v);
                         wait_ld();
+                        if (!row_ok) continue;
 #pragma unroll
                         for (int e = 0; e < 32; e += 8)
                             dst[(c32 * 32 + e) / 8] = make_uint4(
@@ -1104,9 +972,11 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                                 pack_bf16(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv),
                                 pack_bf16(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv));
                     }
-                    A.lse[((size_t)seg_b * A.Hq + hq) * A.R + rr] =
-                        l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+                    if (row_ok)
+                        A.lse[((size_t)seg_b * A.Hq + hq) * A.R + rr] =
+                            l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
                 } else {
+                    // partial slots hold all kRows rows of a segment
                     const size_t row = slot_row(P, seg_id, cta, 0, 1, r);
                     float *po = A.part_o + row * D;
 #pragma unroll
@@ -1372,23 +1242,9 @@ __global__ void __launch_bounds__(128) attn_tc_combine_kernel(const __grid_const
 
 // ------------------------------------------------------------------ host
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
 // 2-D bf16 map over [rows][d] with a (64 x box_rows) box, 128-byte swizzle.
 bool make_map(CUtensorMap *map, const void *base, long long rows, int d, int box_rows) {
-    auto fn = encode_fn();
+    auto fn = tensor_map_encoder();
     if (!fn) return false;
     if (rows < 1) rows = 1;
     cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
@@ -1532,6 +1388,20 @@ spec_status_t launch_attn_tc(const AttnParams &A, cudaStream_t s) {
     if (cfg.wr == 1) return launch_impl<64, 1, 4, 6, 2>(P, maps, s);
     if (cfg.wr == 2) return launch_impl<64, 2, 4, 6, 2>(P, maps, s);
     return launch_impl<64, 4, 8, 8, 1>(P, maps, s);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
 }
 
 }  // namespace sv

@@ -522,3 +522,47 @@ def make_workload(name: str, seed: int = 0, *, B=None, seq=None, V=None,
 
 def config_names():
     return list(CONFIGS)
+
+
+# --------------------------------------------------------------------------
+# prefill form of Lookahead Attention
+# --------------------------------------------------------------------------
+
+#: Prefill-form LA ("Lookahead Attention" sec. 3.1, the full (n + k) mask):
+#: n prompt positions plus k lookahead positions per request, with the
+#: LLaMA-7B attention shape of the LA verify workload (32 heads MHA,
+#: head_dim 128, bf16).  n = 4096 is the top of that workload's prefix range
+#: and k = 8 its largest lookahead count.
+PREFILL_CONFIGS = {
+    "la_prefill": dict(B=4, n=4096, k=8, Hq=32, Hkv=32, d=128),
+}
+
+
+@dataclass
+class PrefillWorkload:
+    """Inputs of one prefill-form LA call (bf16-representable float32)."""
+
+    B: int
+    n: int
+    k: int
+    Hq: int
+    Hkv: int
+    d: int
+    q: np.ndarray      # [B][n + k][Hq][d]
+    kk: np.ndarray     # [B][n + k][Hkv][d]
+    v: np.ndarray      # [B][n + k][Hkv][d]
+
+    @property
+    def L(self) -> int:
+        return self.n + self.k
+
+
+def make_prefill(seed: int = 0, *, B: int, n: int, k: int, Hq: int, Hkv: int,
+                 d: int = 128, q_scale: float = 1.0) -> PrefillWorkload:
+    """q, K, V ~ N(0, 1) / 8 (q times ``q_scale``), rounded to bf16."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    L = n + k
+    q = _normal(rng, (B, L, Hq, d), VALUE_SCALE * q_scale, "bf16")
+    kk = _normal(rng, (B, L, Hkv, d), VALUE_SCALE, "bf16")
+    v = _normal(rng, (B, L, Hkv, d), VALUE_SCALE, "bf16")
+    return PrefillWorkload(B, n, k, Hq, Hkv, d, q, kk, v)
