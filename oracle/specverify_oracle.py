@@ -11,7 +11,8 @@ what one verification step computes:
   2. ``verify_attention`` masked softmax attention over
                           (committed prefix || soft prompt || block)
   3. ``vocab_reduce``     per judged row: argmax, log-sum-exp, proposal logit
-  4. ``accept``           threshold longest prefix, or greedy tree walk
+  4. ``accept``           threshold longest prefix, or greedy tree walk;
+     ``accept_soft``      soft matching (ratio test + residual draw)
   5. ``kv_commit``        append the accepted rows' K/V to the cache
 
 Sources (page title, section / equation):
@@ -356,6 +357,106 @@ def accept(mode, tau, tokens, tree_parent, n_nodes, argmax, lse, zprop,
             paths.append(path)
             next_tok[b] = nt
             last[b] = path[-1]
+    return acc_len, paths, next_tok, last
+
+
+# --------------------------------------------------------------------------
+# 4b. soft matching
+# --------------------------------------------------------------------------
+#
+# "Speculative Streaming", verification step: soft matching accepts a drafted
+# token x with probability min(1, p_target(x) / p_draft(x)) (the rejection
+# sampling of Leviathan et al. that the page invokes), continues down the
+# branch until a rejection, and samples one correction token at the
+# rejection point from the main stream.  Readings: children of a node are
+# tried in index order and the first accepted one is followed; each try is
+# an independent test against the same p and q; the correction token is
+# drawn from the normalised residual max(0, p - q) of the stop node (q = 0
+# when the stop node has no drafted children, i.e. the bonus token is drawn
+# from p); p and q are softmax(z / T).  The uniforms are inputs.
+
+def softmax_t(z, temperature=1.0):
+    """softmax(z / T) in float64."""
+    z = np.asarray(z, dtype=np.float64) / float(temperature)
+    m = z.max()
+    e = np.exp(z - m)
+    return e / e.sum()
+
+
+def residual_sample(p, q, u):
+    """Inverse-CDF draw from max(0, p - q) normalised (from p when q is None
+    or the residual has no mass): the smallest v whose cumulative mass
+    exceeds u times the total."""
+    p = np.asarray(p, dtype=np.float64)
+    r = p.copy() if q is None else np.maximum(0.0, p - np.asarray(q, dtype=np.float64))
+    c = np.cumsum(r)
+    if not c[-1] > 0.0:
+        c = np.cumsum(p)
+    v = int(np.searchsorted(c, float(u) * c[-1], side="right"))
+    return min(v, len(c) - 1)
+
+
+def accept_soft_tree(tokens, tree_parent, n_nodes, p_of, q_of, u_accept):
+    """Soft-matching walk from the root (node 0).
+
+    p_of(c): the target distribution at node c (over the token after c);
+    q_of(c): the draft distribution c's children were drafted from, or None.
+    Child x of the current node (index order) is accepted iff
+    u_accept[x] * q(x) < p(x), i.e. u < p / q.  Returns the path.
+    """
+    cur = 0
+    path = [0]
+    while True:
+        nxt = None
+        p = None
+        for c in range(n_nodes):
+            if int(tree_parent[c]) != cur or c <= cur:
+                continue
+            if p is None:
+                p = p_of(cur)
+                q = q_of(cur)
+            x = int(tokens[c])
+            qx = 0.0 if q is None else float(q[x])
+            if float(u_accept[c]) * qx < float(p[x]):
+                nxt = c
+                break
+        if nxt is None:
+            return path
+        cur = nxt
+        path.append(cur)
+
+
+def accept_soft(logits, draft_logits, tokens, tree_parent, row_of, child_draft_row,
+                n_nodes, u_accept, u_sample, temperature=1.0):
+    """Soft-matching acceptance for every request.
+
+    logits [B][Rj][V] (target), draft_logits [B][Rd][V]; row_of[b][c]: judge
+    row of node c (identity if None); child_draft_row[b][c]: draft row of
+    c's children (-1: none).  Returns (acc_len, paths, next_token,
+    last_node) like ``accept`` in tree mode; next_token is the residual
+    draw at the last node with u_sample[b].
+    """
+    B = len(tokens)
+    acc_len = np.zeros(B, dtype=np.int64)
+    paths, next_tok, last = [], np.zeros(B, dtype=np.int64), np.zeros(B, dtype=np.int64)
+    for b in range(B):
+        def row(c, b=b):
+            return c if row_of is None else int(row_of[b][c])
+
+        def p_of(c, b=b):
+            return softmax_t(logits[b][row(c)], temperature)
+
+        def q_of(c, b=b):
+            dr = int(child_draft_row[b][c])
+            return None if dr < 0 else softmax_t(draft_logits[b][dr], temperature)
+
+        path = accept_soft_tree(tokens[b], tree_parent[b], int(n_nodes[b]), p_of, q_of,
+                                u_accept[b])
+        c = path[-1]
+        acc_len[b] = len(path)
+        paths.append(path)
+        last[b] = c
+        next_tok[b] = residual_sample(p_of(c), q_of(c), u_sample[b])
     return acc_len, paths, next_tok, last
 
 

@@ -89,3 +89,36 @@ def test_walk_without_root_check_is_caught(monkeypatch):
             path.append(cur)
     monkeypatch.setattr(oracle, "accept_greedy_tree", sloppy)
     _expect_pin_failure(tac.test_greedy_walk_hand_worked)
+
+
+# ---------------------------------------------------------------- soft matching
+
+import test_oracle_soft as tos
+
+
+def test_inverted_acceptance_ratio_is_caught(monkeypatch):
+    def inverted(tokens, tree_parent, n_nodes, p_of, q_of, u_accept):
+        swapped = lambda c: q_of(c)
+        return so.accept_soft_tree(tokens, tree_parent, n_nodes, swapped,
+                                   lambda c: p_of(c), u_accept)
+
+    monkeypatch.setattr(oracle, "accept_soft_tree", inverted)
+    _expect_pin_failure(tos.test_single_draft_output_is_target_distribution, 0)
+    _expect_pin_failure(tos.test_hand_worked_tree)
+
+
+def test_residual_without_draft_subtraction_is_caught(monkeypatch):
+    monkeypatch.setattr(oracle, "residual_sample",
+                        lambda p, q, u: so.residual_sample(p, None, u))
+    _expect_pin_failure(tos.test_single_draft_output_is_target_distribution, 1)
+
+
+def test_residual_sign_flip_is_caught(monkeypatch):
+    def flipped(p, q, u):
+        if q is None:
+            return so.residual_sample(p, None, u)
+        return so.residual_sample(q, p, u)
+
+    monkeypatch.setattr(oracle, "residual_sample", flipped)
+    _expect_pin_failure(tos.test_single_draft_output_is_target_distribution, 2)
+    _expect_pin_failure(tos.test_hand_worked_tree)
