@@ -84,7 +84,8 @@ def workload_label(wl):
     seq = f"S~U[{int(wl.seq_len.min())},{int(wl.seq_len.max())}]"
     return (f"{wl.name}: B={wl.B} R={wl.R} Hq/Hkv={wl.Hq}/{wl.Hkv} d={wl.d} {wl.dtype} "
             f"{'paged(16-token pages)' if wl.paged else 'contiguous'} KV, {seq}, "
-            f"n_soft={wl.n_soft}, V={wl.V}, {'threshold' if wl.mode == 'la' else 'greedy tree'}")
+            f"n_soft={wl.n_soft}, V={wl.V}, "
+            f"{'threshold' if wl.mode == 'la' else 'soft matching' if wl.soft else 'greedy tree'}")
 
 
 def attn_algorithmic_bytes(wl):
@@ -107,6 +108,9 @@ def step_algorithmic_bytes(wl, accepted_rows):
     e = 2 if wl.dtype == "bf16" else 4
     le = 2 if wl.logit_dtype == "bf16" else 4
     logits = wl.B * wl.Rj * wl.V * le
+    if wl.soft:
+        # draft rows once, plus the stop rows' second read for the residual draw
+        logits += wl.draft_logits.shape[0] * wl.draft_logits.shape[1] * wl.V * le
     accept_io = wl.B * wl.N * 4 * 3 + wl.B * wl.Rj * 12 + wl.B * (wl.path_cap + 3) * 4
     commit = accepted_rows * wl.Hkv * wl.d * 2 * e * 2
     mask = wl.B * wl.R * (4 + 1 + 1 + 4 * ((wl.R + 31) // 32))
@@ -244,11 +248,18 @@ def _oracle_worker(conn, config, seed, requests):
             O, L = oracle.verify_attention(
                 wl.q[b:b + 1], [pk[b]], [pv[b]], wl.kb[b:b + 1], wl.vb[b:b + 1], vis, valid,
                 sees, soft_k=wl.soft_k, soft_v=wl.soft_v)
-            prop = wl.tokens[b] if wl.mode == "la" else None
-            am, lse, zp = oracle.vocab_reduce(wl.logits[b], prop)
-            acc, paths, nxt, last = oracle.accept(
-                mode, wl.tau, wl.tokens[b:b + 1], wl.tree_parent[b:b + 1],
-                wl.n_nodes[b:b + 1], am[None], lse[None], zp[None])
+            if wl.soft:
+                acc, paths, nxt, last = oracle.accept_soft(
+                    wl.logits[b:b + 1], wl.draft_logits[b:b + 1], wl.tokens[b:b + 1],
+                    wl.tree_parent[b:b + 1], None, wl.child_draft_row[b:b + 1],
+                    wl.n_nodes[b:b + 1], wl.u_accept[b:b + 1], wl.u_sample[b:b + 1],
+                    wl.temperature)
+            else:
+                prop = wl.tokens[b] if wl.mode == "la" else None
+                am, lse, zp = oracle.vocab_reduce(wl.logits[b], prop)
+                acc, paths, nxt, last = oracle.accept(
+                    mode, wl.tau, wl.tokens[b:b + 1], wl.tree_parent[b:b + 1],
+                    wl.n_nodes[b:b + 1], am[None], lse[None], zp[None])
             # commit the accepted rows into the request's own logical cache
             K = np.concatenate([pk[b], np.zeros((wl.Hkv, wl.R, wl.d), np.float32)], axis=1)
             oracle.kv_commit_contiguous(K[None], K[None], [int(wl.seq_len[b])],
@@ -468,7 +479,7 @@ def run_gpu(args):
         },
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": DeviceStep.LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": ds.launches_per_step * args.steps,
         "device_status": status,
     }
     line["clocks"] = clk.summary()
@@ -482,7 +493,8 @@ def run_e2e(ds, steps, stream):
     copied in, results (acceptance outputs) copied out, every step."""
     import torch
     inputs = [t for t in (ds.q, ds.kb, ds.vb, ds.soft_k, ds.soft_v, ds.vparent,
-                          ds.soft_flags, ds.logits, ds.tokens, ds.tree_parent, ds.n_nodes)
+                          ds.soft_flags, ds.logits, ds.tokens, ds.tree_parent, ds.n_nodes,
+                          ds.draft_logits, ds.child_draft_row, ds.u_accept, ds.u_sample)
               if t is not None]
     outputs = [ds.acc_len, ds.path, ds.next_token, ds.last_node]
     h_in = [t.cpu().pin_memory() for t in inputs]

@@ -167,6 +167,18 @@ typedef struct spec_prefill_desc {
     float scale;       /* softmax scale; 0 -> 1/sqrt(head_dim) */
 } spec_prefill_desc;
 
+/* Shape of one soft-matching acceptance call. */
+typedef struct spec_soft_desc {
+    int batch;          /* B */
+    int n_judge_rows;   /* Rj: target logits rows per request */
+    int n_draft_rows;   /* Rd: draft logits rows per request (0 = none) */
+    int vocab;          /* V (<= 1,048,576) */
+    int logit_dtype;    /* SPEC_BF16 or SPEC_F32, target and draft logits */
+    int max_nodes;      /* N: row length of tokens / tree_parent / row_of */
+    int path_cap;       /* row length of path */
+    float temperature;  /* T > 0: p = softmax(z / T), q = softmax(z_d / T) */
+} spec_soft_desc;
+
 /* Library version (SPECVERIFY_VERSION). */
 int spec_version(void);
 
@@ -236,6 +248,45 @@ spec_status_t spec_verify_attn(const spec_attn_desc *attn, const void *q,
                                const uint32_t *vis, const uint8_t *row_flags,
                                void *o, float *lse, void *workspace,
                                size_t workspace_bytes, void *stream);
+
+/*
+ * spec_accept_soft -- acceptance by soft matching ([SS] verification step:
+ * a drafted token x is accepted with probability min(1, p(x) / q(x)), the
+ * rejection sampling of Leviathan et al.; one correction token is sampled
+ * at the rejection point).
+ *
+ *   logits          [batch][n_judge_rows][vocab]: target (main-stream) logits.
+ *   draft_logits    [batch][n_draft_rows][vocab]: the draft distributions.
+ *   tokens, tree_parent, row_of, n_nodes: the draft tree as in spec_accept
+ *                   (tree mode); row_of NULL = identity.
+ *   child_draft_row int32 [batch][max_nodes]: the draft row node c's children
+ *                   were drafted from, -1 if none.  May be NULL only when
+ *                   n_draft_rows == 0 (every q is then 0).
+ *   u_accept        fp32 [batch][max_nodes]: uniform in [0, 1) used when node
+ *                   c is tested.
+ *   u_sample        fp32 [batch]: uniform in [0, 1) for the correction token.
+ *   lse_t, lse_d    fp32 out [batch][n_judge_rows], [batch][n_draft_rows]:
+ *                   ln sum exp(z / T) of each row (scratch the call fills).
+ *   acc_len, path, next_token, last_node: out, as spec_accept (tree mode).
+ *
+ * From node 0, the children c of the current node are tried in index
+ * order: c (token x) is accepted iff u_accept[c] * q(x) < p(x), with p the
+ * softmax(z / T) of the current node's judge row and q that of its
+ * child_draft_row; the first accepted child becomes the current node.  When
+ * none is accepted, next_token is drawn from max(0, p - q) normalised (from
+ * p when the node has no draft row or p <= q everywhere): the smallest v
+ * whose cumulative mass exceeds u_sample[b] times the total (fp32 sums).
+ * Malformed indices set SPEC_DEV_BAD_INDEX.  Three launches: two vocab
+ * reductions (target, draft) and one walk-and-draw kernel.
+ */
+spec_status_t spec_accept_soft(const spec_soft_desc *desc, const void *logits,
+                               const void *draft_logits, const int32_t *tokens,
+                               const int32_t *tree_parent, const int32_t *row_of,
+                               const int32_t *child_draft_row, const int32_t *n_nodes,
+                               const float *u_accept, const float *u_sample,
+                               float *lse_t, float *lse_d, int32_t *acc_len,
+                               int32_t *path, int32_t *next_token, int32_t *last_node,
+                               void *stream);
 
 /*
  * spec_la_prefill_attn -- the prefill form of Lookahead Attention ([LA]

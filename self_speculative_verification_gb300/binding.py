@@ -42,7 +42,7 @@ SPEC_DEV_BAD_INDEX = 0x10
 EXPORTS = ("spec_version", "spec_status_string", "spec_mask_build",
            "spec_verify_attn_workspace_size", "spec_verify_attn",
            "spec_verify_attn_noalloc", "spec_vocab_reduce", "spec_accept", "kv_commit",
-           "spec_get_status", "spec_la_prefill_attn")
+           "spec_get_status", "spec_la_prefill_attn", "spec_accept_soft")
 SPEC_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -70,6 +70,12 @@ class AcceptDesc(ctypes.Structure):
     _fields_ = [("mode", c_int), ("tau", c_float), ("batch", c_int),
                 ("n_judge_rows", c_int), ("vocab", c_int), ("logit_dtype", c_int),
                 ("max_nodes", c_int), ("path_cap", c_int)]
+
+
+class SoftDesc(ctypes.Structure):
+    _fields_ = [("batch", c_int), ("n_judge_rows", c_int), ("n_draft_rows", c_int),
+                ("vocab", c_int), ("logit_dtype", c_int), ("max_nodes", c_int),
+                ("path_cap", c_int), ("temperature", c_float)]
 
 
 class PrefillDesc(ctypes.Structure):
@@ -113,6 +119,7 @@ def load_library():
                        c_int, vp, vp], c_int),
         "spec_get_status": ([vp, POINTER(ctypes.c_int32)], c_int),
         "spec_la_prefill_attn": ([POINTER(PrefillDesc), vp, vp, vp, vp, vp, vp], c_int),
+        "spec_accept_soft": ([POINTER(SoftDesc)] + [vp] * 16, c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -196,6 +203,12 @@ def accept_desc(mode, tau, batch, n_judge_rows, vocab, logit_dtype, max_nodes,
 def prefill_desc(batch, n_orig, n_look, n_q_heads, n_kv_heads, head_dim, dtype=SPEC_BF16,
                  scale=0.0) -> PrefillDesc:
     return PrefillDesc(batch, n_orig, n_look, n_q_heads, n_kv_heads, head_dim, dtype, scale)
+
+
+def soft_desc(batch, n_judge_rows, n_draft_rows, vocab, logit_dtype, max_nodes, path_cap,
+              temperature=1.0) -> SoftDesc:
+    return SoftDesc(batch, n_judge_rows, n_draft_rows, vocab, logit_dtype, max_nodes, path_cap,
+                    temperature)
 
 
 def spec_version() -> int:
@@ -311,3 +324,20 @@ def spec_la_prefill_attn(desc: PrefillDesc, q, k, v, o, lse, stream=None):
     _check("spec_la_prefill_attn", lib.spec_la_prefill_attn(
         ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
         _ptr(lse, torch.float32, "lse"), _stream(stream)))
+
+
+def spec_accept_soft(desc: SoftDesc, logits, draft_logits, tokens, tree_parent, row_of,
+                     child_draft_row, n_nodes, u_accept, u_sample, lse_t, lse_d, acc_len, path,
+                     next_token, last_node, stream=None):
+    """Soft-matching acceptance (ratio test down the tree, residual draw)."""
+    lib = load_library()
+    i32, f32 = torch.int32, torch.float32
+    _check("spec_accept_soft", lib.spec_accept_soft(
+        ctypes.byref(desc), _ptr(logits, name="logits"),
+        _ptr(draft_logits, logits.dtype, "draft_logits"), _ptr(tokens, i32, "tokens"),
+        _ptr(tree_parent, i32, "tree_parent"), _ptr(row_of, i32, "row_of"),
+        _ptr(child_draft_row, i32, "child_draft_row"), _ptr(n_nodes, i32, "n_nodes"),
+        _ptr(u_accept, f32, "u_accept"), _ptr(u_sample, f32, "u_sample"),
+        _ptr(lse_t, f32, "lse_t"), _ptr(lse_d, f32, "lse_d"), _ptr(acc_len, i32, "acc_len"),
+        _ptr(path, i32, "path"), _ptr(next_token, i32, "next_token"),
+        _ptr(last_node, i32, "last_node"), _stream(stream)))

@@ -7,7 +7,8 @@
 // greedy token) need.
 //
 // Accept: the LA threshold longest prefix, or the greedy walk down the draft
-// tree ("Speculative Streaming", verification step; "ConFu" tree verify).
+// tree ("Speculative Streaming", verification step; "ConFu" tree verify);
+// spec_accept_soft: the soft-matching walk and the residual draw.
 #include <cooperative_groups.h>
 #include <limits.h>
 #include <math.h>
@@ -27,25 +28,26 @@ struct Best {
     float s;     // sum of exp(z - m)
 };
 
-__device__ __forceinline__ void best_push(Best &b, float z, int i) {
+// inv_t: 1 / temperature (the sums are of exp(z / T)).
+__device__ __forceinline__ void best_push(Best &b, float z, int i, float inv_t) {
     if (z > b.m) {
-        b.s = b.s * __expf(b.m - z) + 1.f;
+        b.s = b.s * __expf((b.m - z) * inv_t) + 1.f;
         b.m = z;
         b.idx = i;
     } else {
-        b.s += __expf(z - b.m);
+        b.s += __expf((z - b.m) * inv_t);
         if (z == b.m && i < b.idx) b.idx = i;
     }
 }
 
-__device__ __forceinline__ Best best_merge(Best a, Best b) {
+__device__ __forceinline__ Best best_merge(Best a, Best b, float inv_t) {
     if (b.m > a.m || (b.m == a.m && b.idx < a.idx)) {
         Best t = a;
         a = b;
         b = t;
     }
     // a has the larger max (or equal max with the lower index)
-    if (b.m != -INFINITY) a.s += b.s * __expf(b.m - a.m);
+    if (b.m != -INFINITY) a.s += b.s * __expf((b.m - a.m) * inv_t);
     return a;
 }
 
@@ -91,7 +93,8 @@ template <typename T>
 __global__ void __launch_bounds__(kReduceThreads)
 vocab_reduce_kernel(const T *__restrict__ logits, int V, const int32_t *__restrict__ proposal,
                     int32_t *__restrict__ argmax, float *__restrict__ lse,
-                    float *__restrict__ zprop) {
+                    float *__restrict__ zprop, float inv_t) {
+    const float c2 = kLog2e * inv_t;
     cg::cluster_group cluster = cg::this_cluster();
     const int nc = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
@@ -126,28 +129,29 @@ vocab_reduce_kernel(const T *__restrict__ logits, int V, const int32_t *__restri
 #pragma unroll
                     for (int j = N - 1; j >= 0; --j)
                         if (x[u][j] == bm) bi = (i0 + u * kReduceThreads) * N + j;
-                best.s *= ex2((best.m - bm) * kLog2e);
+                best.s *= ex2((best.m - bm) * c2);
                 best.m = bm;
                 best.idx = bi;
             }
-            const float mb = best.m * kLog2e;
+            const float mb = best.m * c2;
             float acc[N];
 #pragma unroll
             for (int j = 0; j < N; ++j) acc[j] = 0.f;
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u)
 #pragma unroll
-                for (int j = 0; j < N; ++j) acc[j] += ex2(fmaf(x[u][j], kLog2e, -mb));
+                for (int j = 0; j < N; ++j) acc[j] += ex2(fmaf(x[u][j], c2, -mb));
 #pragma unroll
             for (int j = 1; j < N; ++j) acc[0] += acc[j];
             best.s += acc[0];
         }
         if (rank == nc - 1)
             for (int i = nv * N + threadIdx.x; i < V; i += kReduceThreads)
-                best_push(best, load_f(z + i), i);
+                best_push(best, load_f(z + i), i, inv_t);
     } else {
         const int lo = (int)((long long)V * rank / nc), hi = (int)((long long)V * (rank + 1) / nc);
-        for (int i = lo + threadIdx.x; i < hi; i += kReduceThreads) best_push(best, load_f(z + i), i);
+        for (int i = lo + threadIdx.x; i < hi; i += kReduceThreads)
+            best_push(best, load_f(z + i), i, inv_t);
     }
 
     // block reduction: warps, then across warps
@@ -157,7 +161,7 @@ vocab_reduce_kernel(const T *__restrict__ logits, int V, const int32_t *__restri
         other.m = __shfl_xor_sync(0xffffffffu, best.m, o);
         other.idx = __shfl_xor_sync(0xffffffffu, best.idx, o);
         other.s = __shfl_xor_sync(0xffffffffu, best.s, o);
-        best = best_merge(best, other);
+        best = best_merge(best, other, inv_t);
     }
     __shared__ Best sb[kReduceThreads / 32];
     __shared__ Best cta_best;
@@ -166,15 +170,16 @@ vocab_reduce_kernel(const T *__restrict__ logits, int V, const int32_t *__restri
     __syncthreads();
     if (threadIdx.x == 0) {
         Best r = sb[0];
-        for (int w = 1; w < kReduceThreads / 32; ++w) r = best_merge(r, sb[w]);
+        for (int w = 1; w < kReduceThreads / 32; ++w) r = best_merge(r, sb[w], inv_t);
         cta_best = r;
     }
     cluster.sync();
     if (rank == 0 && threadIdx.x == 0) {
         Best r = cta_best;
-        for (int i = 1; i < nc; ++i) r = best_merge(r, *cluster.map_shared_rank(&cta_best, i));
-        argmax[row] = r.idx == INT_MAX ? 0 : r.idx;
-        lse[row] = r.m + logf(r.s);
+        for (int i = 1; i < nc; ++i)
+            r = best_merge(r, *cluster.map_shared_rank(&cta_best, i), inv_t);
+        if (argmax) argmax[row] = r.idx == INT_MAX ? 0 : r.idx;
+        lse[row] = r.m * inv_t + logf(r.s);
         if (proposal && zprop) {
             const int pidx = proposal[row];
             zprop[row] = (pidx >= 0 && pidx < V) ? load_f(z + pidx) : NAN;
@@ -308,7 +313,7 @@ int cluster_size(int n_rows, int V, int dtype) {
 template <typename T>
 spec_status_t launch_vocab_cluster(const void *logits, int n_rows, int V, int nc,
                                    const int32_t *proposal, int32_t *argmax, float *lse,
-                                   float *zprop, cudaStream_t s) {
+                                   float *zprop, float inv_t, cudaStream_t s) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)((long long)n_rows * nc), 1, 1);
     cfg.blockDim = dim3(kReduceThreads, 1, 1);
@@ -323,19 +328,240 @@ spec_status_t launch_vocab_cluster(const void *logits, int n_rows, int V, int nc
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, vocab_reduce_kernel<T>,
                                              static_cast<const T *>(logits), V, proposal, argmax,
-                                             lse, zprop);
+                                             lse, zprop, inv_t);
     return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 spec_status_t launch_vocab_reduce(const void *logits, int dtype, int n_rows, int V,
                                   const int32_t *proposal, int32_t *argmax, float *lse,
-                                  float *zprop, cudaStream_t s) {
+                                  float *zprop, cudaStream_t s, float inv_t = 1.f) {
     const int nc = cluster_size(n_rows, V, dtype);
     if ((long long)n_rows * nc > 2147483647ll) return SPEC_ERR_UNSUPPORTED;
     if (dtype == SPEC_BF16)
         return launch_vocab_cluster<__nv_bfloat16>(logits, n_rows, V, nc, proposal, argmax, lse,
-                                                   zprop, s);
-    return launch_vocab_cluster<float>(logits, n_rows, V, nc, proposal, argmax, lse, zprop, s);
+                                                   zprop, inv_t, s);
+    return launch_vocab_cluster<float>(logits, n_rows, V, nc, proposal, argmax, lse, zprop, inv_t,
+                                       s);
+}
+
+// ------------------------------------------------------------ soft matching
+//
+// "Speculative Streaming", verification step with soft matching: a drafted
+// token x (child of the current node) is accepted with probability
+// min(1, p(x) / q(x)), decided as u_x * q(x) < p(x); children are tried in
+// index order and the first accepted one is followed.  At the stop node one
+// correction token is drawn from the normalised residual max(0, p - q) (from
+// p when the node has no drafted children or the residual has no mass), as
+// the smallest v whose cumulative mass exceeds u_b times the total.
+// p = softmax(z / T) of the node's judge row, q = softmax(z_d / T) of the
+// draft row its children were drafted from.
+
+constexpr int kSoftThreads = 512;
+constexpr int kSoftTile = 256;             // vocab entries per tile: 8 per lane
+constexpr int kMaxSoftTiles = 4096;        // vocab <= 1,048,576
+
+struct SoftParams {
+    int B, Rj, Rd, N, V, path_cap;
+    float inv_t;
+    const void *logits, *draft;
+    const int32_t *tokens, *tree_parent, *row_of, *child_draft_row, *n_nodes;
+    const float *u_accept, *u_sample, *lse_t, *lse_d;
+    int32_t *acc_len, *path, *next_token, *last_node;
+    int *status;
+};
+
+template <typename T>
+__device__ __forceinline__ float prob_at(const T *row, int v, float lse, float inv_t) {
+    return __expf(fmaf(load_f(row + v), inv_t, -lse));
+}
+
+// One CTA per request: thread 0 walks the tree, then the CTA draws the
+// correction token (tile sums, a scan over tiles, a scan inside the tile).
+template <typename T>
+__global__ void __launch_bounds__(kSoftThreads) soft_accept_kernel(SoftParams P) {
+    __shared__ float s_tile[kMaxSoftTiles];
+    __shared__ int s_row, s_drow, s_hit;
+    __shared__ float s_total, s_base;
+    const int b = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const T *Z = static_cast<const T *>(P.logits);
+    const T *ZD = static_cast<const T *>(P.draft);
+
+    if (threadIdx.x == 0) {
+        int n = P.n_nodes[b];
+        if (n < 0 || n > P.N) {
+            raise_status(P.status, SPEC_DEV_BAD_INDEX);
+            n = n < 0 ? 0 : P.N;
+        }
+        int32_t *pth = P.path + (size_t)b * P.path_cap;
+        const size_t nb = (size_t)b * P.N;
+        int len = 0, cur = 0, row = -1, drow = -1;
+        if (n == 0 || P.path_cap == 0) {
+            raise_status(P.status, SPEC_DEV_BAD_INDEX);
+        } else {
+            len = 1;
+            pth[0] = 0;
+            while (true) {
+                row = P.row_of ? P.row_of[nb + cur] : cur;
+                if (row < 0 || row >= P.Rj) {
+                    raise_status(P.status, SPEC_DEV_BAD_INDEX);
+                    row = -1;
+                    break;
+                }
+                drow = P.child_draft_row ? P.child_draft_row[nb + cur] : -1;
+                if (drow < -1 || drow >= P.Rd) {
+                    raise_status(P.status, SPEC_DEV_BAD_INDEX);
+                    drow = -1;
+                }
+                const T *zt = Z + ((size_t)b * P.Rj + row) * P.V;
+                const float lt = P.lse_t[(size_t)b * P.Rj + row];
+                const T *zd = drow >= 0 ? ZD + ((size_t)b * P.Rd + drow) * P.V : nullptr;
+                const float ld = drow >= 0 ? P.lse_d[(size_t)b * P.Rd + drow] : 0.f;
+                int found = -1;
+                for (int c = cur + 1; c < n; ++c) {
+                    if (P.tree_parent[nb + c] != cur) continue;
+                    const int x = P.tokens[nb + c];
+                    if (x < 0 || x >= P.V) {
+                        raise_status(P.status, SPEC_DEV_BAD_INDEX);
+                        continue;
+                    }
+                    const float p = prob_at(zt, x, lt, P.inv_t);
+                    const float q = zd ? prob_at(zd, x, ld, P.inv_t) : 0.f;
+                    if (P.u_accept[nb + c] * q < p) {
+                        found = c;
+                        break;
+                    }
+                }
+                if (found < 0) break;
+                if (len >= P.path_cap) {
+                    raise_status(P.status, SPEC_DEV_BAD_INDEX);
+                    break;
+                }
+                pth[len++] = found;
+                cur = found;
+            }
+        }
+        for (int i = len; i < P.path_cap; ++i) pth[i] = -1;
+        P.acc_len[b] = len;
+        P.last_node[b] = len > 0 ? cur : -1;
+        s_row = row;
+        s_drow = drow;
+    }
+    __syncthreads();
+    const int row = s_row;
+    if (row < 0) {
+        if (threadIdx.x == 0) P.next_token[b] = -1;
+        return;
+    }
+    const int drow = s_drow;
+    const T *zt = Z + ((size_t)b * P.Rj + row) * P.V;
+    const float lt = P.lse_t[(size_t)b * P.Rj + row];
+    const T *zd = drow >= 0 ? ZD + ((size_t)b * P.Rd + drow) * P.V : nullptr;
+    const float ld = drow >= 0 ? P.lse_d[(size_t)b * P.Rd + drow] : 0.f;
+    const int ntiles = (P.V + kSoftTile - 1) / kSoftTile;
+    bool resid = zd != nullptr;
+    auto mass = [&](int v) -> float {
+        if (v >= P.V) return 0.f;
+        const float p = prob_at(zt, v, lt, P.inv_t);
+        return resid ? fmaxf(0.f, p - prob_at(zd, v, ld, P.inv_t)) : p;
+    };
+    for (int pass = 0; pass < 2; ++pass) {
+        for (int t = warp; t < ntiles; t += kSoftThreads / 32) {
+            const int v0 = t * kSoftTile + lane * 8;
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc += mass(v0 + e);
+            acc = warp_sum(acc);
+            if (lane == 0) s_tile[t] = acc;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            float acc = 0.f;
+            for (int t = lane; t < ntiles; t += 32) acc += s_tile[t];
+            acc = warp_sum(acc);
+            if (lane == 0) s_total = acc;
+        }
+        __syncthreads();
+        if (s_total > 0.f || !resid) break;
+        resid = false;           // p == q: draw from p
+        __syncthreads();
+    }
+    if (warp != 0) return;
+    // the tile holding the target: lane l scans tiles [l K, (l + 1) K)
+    const float total = s_total;
+    const float target = P.u_sample[b] * total;
+    const int K = (ntiles + 31) / 32;
+    const int t0 = min(lane * K, ntiles), t1 = min(t0 + K, ntiles);
+    float lsum = 0.f;
+    for (int t = t0; t < t1; ++t) lsum += s_tile[t];
+    float incl = lsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const unsigned hitl = __ballot_sync(0xffffffffu, incl > target && t0 < t1);
+    int tile = -1;
+    float base = 0.f;
+    if (hitl) {
+        const int L = __ffs(hitl) - 1;
+        if (lane == L) {
+            float run = incl - lsum;
+            for (int t = t0; t < t1; ++t) {
+                if (run + s_tile[t] > target) {
+                    tile = t;
+                    break;
+                }
+                run += s_tile[t];
+            }
+            if (tile < 0) tile = t1 - 1;
+            base = run;
+        }
+        tile = __shfl_sync(0xffffffffu, tile, L);
+        base = __shfl_sync(0xffffffffu, base, L);
+    } else {
+        // rounding put the target at the very end: the last tile with mass
+        int last = -1;
+        for (int t = lane; t < ntiles; t += 32)
+            if (s_tile[t] > 0.f) last = t;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+        tile = last < 0 ? 0 : last;
+        base = -INFINITY;        // take the last element with mass below
+    }
+    // inside the tile: lane l holds elements [l * 8, l * 8 + 8)
+    const int v0 = tile * kSoftTile + lane * 8;
+    float m[8], part = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        m[e] = mass(v0 + e);
+        part += m[e];
+    }
+    float ip = part;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, ip, o);
+        if (lane >= o) ip += y;
+    }
+    int mine = -1, lastpos = -1;
+    float run = base + (ip - part);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        run += m[e];
+        if (mine < 0 && m[e] > 0.f && run > target) mine = v0 + e;
+        if (m[e] > 0.f) lastpos = v0 + e;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, mine >= 0);
+    int tok;
+    if (hit) {
+        tok = __shfl_sync(0xffffffffu, mine, __ffs(hit) - 1);
+    } else {
+        tok = lastpos;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tok = max(tok, __shfl_xor_sync(0xffffffffu, tok, o));
+        if (tok < 0) tok = 0;
+    }
+    if (lane == 0) P.next_token[b] = tok;
 }
 
 }  // namespace
@@ -407,4 +633,71 @@ extern "C" spec_status_t spec_accept(const spec_accept_desc *d, const void *logi
     if (!P.status) return SPEC_ERR_CUDA;
     sv::accept_kernel<<<sv::ceil_div(P.B, 4), 128, 0, s>>>(P);
     return sv::launch_status();
+}
+
+extern "C" spec_status_t spec_accept_soft(const spec_soft_desc *d, const void *logits,
+                                          const void *draft_logits, const int32_t *tokens,
+                                          const int32_t *tree_parent, const int32_t *row_of,
+                                          const int32_t *child_draft_row, const int32_t *n_nodes,
+                                          const float *u_accept, const float *u_sample,
+                                          float *lse_t, float *lse_d, int32_t *acc_len,
+                                          int32_t *path, int32_t *next_token, int32_t *last_node,
+                                          void *stream) {
+    using namespace sv;
+    if (!d) return SPEC_ERR_INVALID_ARG;
+    if (d->batch < 0 || d->n_judge_rows <= 0 || d->n_draft_rows < 0 || d->vocab <= 0 ||
+        d->max_nodes <= 0 || d->path_cap < 0 || !(d->temperature > 0.f) ||
+        !(d->temperature < INFINITY))
+        return SPEC_ERR_INVALID_ARG;
+    if (d->logit_dtype != SPEC_F32 && d->logit_dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+    if ((d->vocab + kSoftTile - 1) / kSoftTile > kMaxSoftTiles) return SPEC_ERR_UNSUPPORTED;
+    if (d->batch == 0) return SPEC_OK;
+    if (!logits || !tokens || !tree_parent || !n_nodes || !u_accept || !u_sample || !lse_t ||
+        !acc_len || !path || !next_token || !last_node)
+        return SPEC_ERR_INVALID_ARG;
+    if (d->n_draft_rows > 0 && (!draft_logits || !lse_d || !child_draft_row))
+        return SPEC_ERR_INVALID_ARG;
+    const long long rows = (long long)d->batch * d->n_judge_rows;
+    const long long drows = (long long)d->batch * d->n_draft_rows;
+    if (rows > 2147483647ll || drows > 2147483647ll) return SPEC_ERR_UNSUPPORTED;
+    cudaStream_t s = as_stream(stream);
+    const float inv_t = 1.f / d->temperature;
+    spec_status_t st = launch_vocab_reduce(logits, d->logit_dtype, (int)rows, d->vocab, nullptr,
+                                           nullptr, lse_t, nullptr, s, inv_t);
+    if (st != SPEC_OK) return st;
+    if (drows > 0) {
+        st = launch_vocab_reduce(draft_logits, d->logit_dtype, (int)drows, d->vocab, nullptr,
+                                 nullptr, lse_d, nullptr, s, inv_t);
+        if (st != SPEC_OK) return st;
+    }
+    SoftParams P{};
+    P.B = d->batch;
+    P.Rj = d->n_judge_rows;
+    P.Rd = d->n_draft_rows;
+    P.N = d->max_nodes;
+    P.V = d->vocab;
+    P.path_cap = d->path_cap;
+    P.inv_t = inv_t;
+    P.logits = logits;
+    P.draft = d->n_draft_rows > 0 ? draft_logits : nullptr;
+    P.tokens = tokens;
+    P.tree_parent = tree_parent;
+    P.row_of = row_of;
+    P.child_draft_row = d->n_draft_rows > 0 ? child_draft_row : nullptr;
+    P.n_nodes = n_nodes;
+    P.u_accept = u_accept;
+    P.u_sample = u_sample;
+    P.lse_t = lse_t;
+    P.lse_d = lse_d;
+    P.acc_len = acc_len;
+    P.path = path;
+    P.next_token = next_token;
+    P.last_node = last_node;
+    P.status = status_ptr();
+    if (!P.status) return SPEC_ERR_CUDA;
+    if (d->logit_dtype == SPEC_BF16)
+        soft_accept_kernel<__nv_bfloat16><<<P.B, kSoftThreads, 0, s>>>(P);
+    else
+        soft_accept_kernel<float><<<P.B, kSoftThreads, 0, s>>>(P);
+    return launch_status();
 }

@@ -142,6 +142,21 @@ class DeviceStep:
         mode = bn.SPEC_ACCEPT_THRESH_CHAIN if wl.mode == "la" else bn.SPEC_ACCEPT_GREEDY_TREE
         self.accept = bn.accept_desc(mode, wl.tau, B, wl.Rj, wl.V, bn.spec_dtype(self.logits),
                                      wl.N, wl.path_cap)
+        # soft matching: draft distributions, uniforms, per-row LSE scratch
+        self.draft_logits = self.child_draft_row = self.u_accept = self.u_sample = None
+        self.lse_d = None
+        if wl.soft:
+            Rd = wl.draft_logits.shape[1]
+            self.draft_logits = to_dev(wl.draft_logits, dev, ldt)
+            self.child_draft_row = to_dev(wl.child_draft_row.astype(np.int32), dev)
+            self.u_accept = to_dev(wl.u_accept.astype(np.float32), dev)
+            self.u_sample = to_dev(wl.u_sample.astype(np.float32), dev)
+            self.lse_d = torch.zeros((B, max(Rd, 1)), dtype=torch.float32, device=dev)
+            self.soft = bn.soft_desc(B, wl.Rj, Rd, wl.V, bn.spec_dtype(self.logits), wl.N,
+                                     wl.path_cap, wl.temperature)
+        # kernel launches of one run() (see libspecverify's sources): mask 1,
+        # attention 2, accept 2 (soft: 3), commit 2
+        self.launches_per_step = 8 if wl.soft else 7
 
     # the four calls ---------------------------------------------------------
     def mask_build(self, stream=None):
@@ -153,6 +168,13 @@ class DeviceStep:
                             self.lse, self.workspace, stream)
 
     def accept_step(self, stream=None):
+        if self.wl.soft:
+            bn.spec_accept_soft(self.soft, self.logits, self.draft_logits, self.tokens,
+                                self.tree_parent, None, self.child_draft_row, self.n_nodes,
+                                self.u_accept, self.u_sample, self.lse_v, self.lse_d,
+                                self.acc_len, self.path, self.next_token, self.last_node,
+                                stream)
+            return
         tree = self.wl.mode != "la"
         bn.spec_accept(self.accept, self.logits, self.tokens,
                        self.tree_parent if tree else None, None, self.n_nodes,
@@ -181,5 +203,5 @@ class DeviceStep:
             if page_table:
                 self.page_table.copy_(self.page_table0)
 
-    # number of kernel launches of one run() (see libspecverify's sources)
+    # kernel launches of one run() with threshold / greedy acceptance
     LAUNCHES_PER_STEP = 7   # mask 1, attention 2, accept 2, commit 2

@@ -57,6 +57,11 @@ CONFIGS = {
     "ss": dict(mode="ss", B=32, Hq=32, Hkv=32, d=128, dtype="bf16",
                seq=("uniform", 128, 1024), T=16, gamma=3, branch=4,
                V=50272, paged=False),
+    # the SS workload verified with soft matching ("Speculative Streaming",
+    # verification step; T = 1 as in the page's top-k sampling runs)
+    "ss_soft": dict(mode="ss", B=32, Hq=32, Hkv=32, d=128, dtype="bf16",
+                    seq=("uniform", 128, 1024), T=16, gamma=3, branch=4,
+                    V=50272, paged=False, soft=True, temperature=1.0),
     "long_paged": dict(mode="la", B=64, Hq=32, Hkv=8, d=128, dtype="bf16",
                        seq=("uniform", 16384, 32768), k_choices=(8,), R=8,
                        V=32000, paged=True),
@@ -140,6 +145,13 @@ class Workload:
     expect_acc_len: np.ndarray   # int32 [B]
     expect_path: np.ndarray      # int32 [B][path_cap], -1 padded
     node_depth: np.ndarray = field(default=None)   # int32 [B][N]
+    # soft matching (tree workloads with ``soft``): draft distributions,
+    # draft row of each node's children (-1: none), the uniforms
+    draft_logits: Optional[np.ndarray] = None     # [B][Rd][V]
+    child_draft_row: Optional[np.ndarray] = None  # int32 [B][N]
+    u_accept: Optional[np.ndarray] = None         # float32 [B][N]
+    u_sample: Optional[np.ndarray] = None         # float32 [B]
+    temperature: float = 1.0
     # contiguous cache capacity / paged bookkeeping
     max_seq: int = 0
     page_size: int = PAGE_SIZE
@@ -151,6 +163,10 @@ class Workload:
     @property
     def G(self) -> int:
         return self.Hq // self.Hkv
+
+    @property
+    def soft(self) -> bool:
+        return self.draft_logits is not None
 
     def prefix_kv(self, b: int):
         """The committed K/V prefix of request ``b``: two [Hkv][S_b][d] arrays.
@@ -332,6 +348,75 @@ def _plant_margin_row(rng, V, dtype, target, margin):
     return z
 
 
+def _plant_probs_row(rng, V, dtype, probs):
+    """Logit row whose softmax puts probability probs[t] on each token t of
+    ``probs`` (their sum below 1) before storage rounding; other logits
+    ~ N(0, 1)."""
+    z = _to_storage(rng.standard_normal(V, dtype=np.float32), dtype).astype(np.float64)
+    if probs:
+        mask = np.ones(V, dtype=bool)
+        mask[list(probs)] = False
+        rest = z[mask]
+        mo = rest.max()
+        log_rest = mo + math.log(np.exp(rest - mo).sum())
+        s = sum(probs.values())
+        assert s < 1.0
+        for t, p in probs.items():
+            z[t] = math.log(p / (1.0 - s)) + log_rest
+    return _to_storage(z.astype(np.float32), dtype)
+
+
+def _plant_soft(rng, tree_parent, node_depth, tokens, D, V, dtype, path_cap):
+    """Soft-matching decisions planted with a wide margin around each
+    uniform.  Along the planted walk, the tested children of the current
+    node get draft probabilities q ~ U[0.01, 0.04] and target probabilities
+    p = ratio * q with ratio >= 1.6 u (accepted child) or ratio <= 0.6 u
+    (rejected ones), so storage rounding (a few percent on p and q) never
+    flips a decision.  Returns target logits [B][T][V], draft logits
+    [B][D][V] (row g: the distribution of depth-(g+1) candidates),
+    child_draft_row, u_accept, u_sample and the planted paths."""
+    B, T = tree_parent.shape
+    child_draft_row = np.where(node_depth < D, node_depth, -1).astype(np.int32)
+    u_accept = rng.random((B, T), dtype=np.float32)
+    u_sample = rng.random(B, dtype=np.float32)
+    logits = np.empty((B, T, V), dtype=np.float32)
+    draft = np.empty((B, D, V), dtype=np.float32)
+    expect_len = np.zeros(B, dtype=np.int32)
+    expect_path = np.full((B, path_cap), -1, dtype=np.int32)
+    for b in range(B):
+        par = tree_parent[b]
+        p_plant, q_plant = {}, {}
+        cur, path = 0, [0]
+        while True:
+            kids = [int(c) for c in np.nonzero(par == cur)[0]]
+            if not kids:
+                break
+            acc_i = int(rng.integers(len(kids))) if rng.random() < MATCH_P else -1
+            tested = kids if acc_i < 0 else kids[: acc_i + 1]
+            pp = p_plant.setdefault(cur, {})
+            qq = q_plant.setdefault(int(child_draft_row[b, cur]), {})
+            for i, c in enumerate(tested):
+                x, u = int(tokens[b, c]), float(u_accept[b, c])
+                qx = float(rng.uniform(0.01, 0.04))
+                if i == acc_i:
+                    ratio = max(1.6 * u, float(rng.uniform(0.3, 2.5)))
+                else:
+                    ratio = u * float(rng.uniform(0.1, 0.6))
+                qq[x] = qx
+                pp[x] = ratio * qx
+            if acc_i < 0:
+                break
+            cur = kids[acc_i]
+            path.append(cur)
+        for j in range(T):
+            logits[b, j] = _plant_probs_row(rng, V, dtype, p_plant.get(j, {}))
+        for g in range(D):
+            draft[b, g] = _plant_probs_row(rng, V, dtype, q_plant.get(g, {}))
+        expect_len[b] = len(path)
+        expect_path[b, : len(path)] = path
+    return logits, draft, child_draft_row, u_accept, u_sample, expect_len, expect_path
+
+
 # --------------------------------------------------------------------------
 # builders
 # --------------------------------------------------------------------------
@@ -374,6 +459,7 @@ def make_workload(name: str, seed: int = 0, *, B=None, seq=None, V=None,
     seq_len = _seq_lengths(rng, cfg["seq"], B)
     layout = cfg["mode"]
 
+    soft = {}
     if layout == "la":
         R = cfg["R"]
         k_b = rng.choice(np.array(cfg["k_choices"]), size=B).astype(np.int32)
@@ -440,42 +526,50 @@ def make_workload(name: str, seed: int = 0, *, B=None, seq=None, V=None,
         soft_flags = np.stack(softs)
         R = vparent.shape[1]
         n_nodes = np.full(B, T, dtype=np.int32)
-        # plant the accepted path: from the root, with prob MATCH_P make the
-        # target argmax equal to one (uniformly chosen) child's token.
-        argtok = np.empty((B, T), dtype=np.int64)
-        expect_len = np.zeros(B, dtype=np.int32)
-        expect_path = np.full((B, path_cap), -1, dtype=np.int32)
-        for b in range(B):
-            par = tree_parent[b]
-            planted = np.zeros(T, dtype=bool)
-            cur = 0
-            expect_path[b, 0] = 0
-            expect_len[b] = 1
-            while True:
-                kids = np.nonzero(par == cur)[0]
-                planted[cur] = True
-                if len(kids) and rng.random() < MATCH_P:
-                    c = int(kids[int(rng.integers(len(kids)))])
-                    argtok[b, cur] = tokens[b, c]
-                    cur = c
-                    expect_path[b, expect_len[b]] = c
-                    expect_len[b] += 1
-                else:
-                    kid_tok = set(int(t) for t in tokens[b, kids])
-                    while True:
-                        t = int(rng.integers(Vv))
-                        if t not in kid_tok:
-                            break
-                    argtok[b, cur] = t
-                    break
-            for j in range(T):
-                if not planted[j]:
-                    argtok[b, j] = int(rng.integers(Vv))
-        logits = np.empty((B, Rj, Vv), dtype=np.float32)
-        for b in range(B):
-            for j in range(T):
-                logits[b, j] = _plant_margin_row(rng, Vv, dt, int(argtok[b, j]),
-                                                 GREEDY_MARGIN)
+        soft = {}
+        if cfg.get("soft"):
+            (logits, draft, cdr, u_acc, u_smp, expect_len,
+             expect_path) = _plant_soft(rng, tree_parent, node_depth, tokens, max_depth, Vv, dt,
+                                        path_cap)
+            soft = dict(draft_logits=draft, child_draft_row=cdr, u_accept=u_acc,
+                        u_sample=u_smp, temperature=float(cfg.get("temperature", 1.0)))
+        else:
+            # plant the accepted path: from the root, with prob MATCH_P make the
+            # target argmax equal to one (uniformly chosen) child's token.
+            argtok = np.empty((B, T), dtype=np.int64)
+            expect_len = np.zeros(B, dtype=np.int32)
+            expect_path = np.full((B, path_cap), -1, dtype=np.int32)
+            for b in range(B):
+                par = tree_parent[b]
+                planted = np.zeros(T, dtype=bool)
+                cur = 0
+                expect_path[b, 0] = 0
+                expect_len[b] = 1
+                while True:
+                    kids = np.nonzero(par == cur)[0]
+                    planted[cur] = True
+                    if len(kids) and rng.random() < MATCH_P:
+                        c = int(kids[int(rng.integers(len(kids)))])
+                        argtok[b, cur] = tokens[b, c]
+                        cur = c
+                        expect_path[b, expect_len[b]] = c
+                        expect_len[b] += 1
+                    else:
+                        kid_tok = set(int(t) for t in tokens[b, kids])
+                        while True:
+                            t = int(rng.integers(Vv))
+                            if t not in kid_tok:
+                                break
+                        argtok[b, cur] = t
+                        break
+                for j in range(T):
+                    if not planted[j]:
+                        argtok[b, j] = int(rng.integers(Vv))
+            logits = np.empty((B, Rj, Vv), dtype=np.float32)
+            for b in range(B):
+                for j in range(T):
+                    logits[b, j] = _plant_margin_row(rng, Vv, dt, int(argtok[b, j]),
+                                                     GREEDY_MARGIN)
         mode = "tree"
 
     q = _normal(rng, (B, R, Hq, d), VALUE_SCALE * q_scale, dt)
@@ -495,7 +589,7 @@ def make_workload(name: str, seed: int = 0, *, B=None, seq=None, V=None,
         vparent=vparent, soft_flags=soft_flags, tokens=tokens,
         tree_parent=tree_parent, n_nodes=n_nodes, logits=logits,
         expect_acc_len=expect_len, expect_path=expect_path,
-        node_depth=node_depth,
+        node_depth=node_depth, **soft,
     )
     wl.max_seq = int(seq_len.max()) + R if B else R
     if page_size is not None:

@@ -108,8 +108,68 @@ def oracle_accept(wl):
     return am, lse, zp, acc, paths, nxt, last
 
 
+# A sampled correction token is unique only away from the boundaries of the
+# residual CDF.  The kernel sums fp32 masses in at most ~25 sequential
+# rounding steps (8 per lane, a 32-lane tree, a few tiles per lane, a
+# 32-lane scan) and its probabilities carry ~1e-6 relative error, so its
+# cumulative sums stay within 1e-5 of the total of the float64 ones; a draw
+# that differs from the oracle's must lie within that band of the boundary.
+CDF_TOL = 1e-5
+
+
+def residual_mass(wl, b, c):
+    p = oracle.softmax_t(wl.logits[b, c], wl.temperature)
+    dr = int(wl.child_draft_row[b, c])
+    if dr < 0:
+        return p
+    r = np.maximum(0.0, p - oracle.softmax_t(wl.draft_logits[b, dr], wl.temperature))
+    return r if r.sum() > 0 else p
+
+
+def check_soft_draw(wl, b, c, got, want):
+    """``got`` is the oracle's draw ``want``, or a neighbour across a CDF
+    boundary the fp32 sums cannot resolve."""
+    if got == want:
+        return
+    r = residual_mass(wl, b, c)
+    cum = np.cumsum(r)
+    target = float(wl.u_sample[b]) * cum[-1]
+    tol = CDF_TOL * cum[-1]
+    lo = cum[got - 1] if got > 0 else 0.0
+    assert r[got] > 0, f"request {b}: drawn token {got} has no residual mass"
+    assert lo - tol <= target <= cum[got] + tol, \
+        f"request {b}: drawn {got}, oracle {want}, target {target} outside [{lo}, {cum[got]}]"
+
+
+def check_accept_soft(ds: DeviceStep):
+    wl = ds.wl
+    acc, paths, nxt, last = oracle.accept_soft(
+        wl.logits, wl.draft_logits, wl.tokens, wl.tree_parent, None, wl.child_draft_row,
+        wl.n_nodes, wl.u_accept, wl.u_sample, wl.temperature)
+    acc_g = ds.acc_len.cpu().numpy()
+    path_g = ds.path.cpu().numpy()
+    assert acc_g.tolist() == acc.tolist()
+    assert acc_g.tolist() == wl.expect_acc_len.tolist()
+    for b in range(wl.B):
+        assert path_g[b, : acc_g[b]].tolist() == paths[b]
+        assert np.all(path_g[b, acc_g[b]:] == -1)
+    assert ds.last_node.cpu().numpy().tolist() == last.tolist()
+    lse_ref = np.array([[np.log(np.exp(wl.logits[b, j].astype(np.float64) / wl.temperature
+                                        - (wl.logits[b, j].max() / wl.temperature)).sum())
+                         + wl.logits[b, j].max() / wl.temperature for j in range(wl.Rj)]
+                        for b in range(wl.B)])
+    lg = ds.lse_v.cpu().numpy().astype(np.float64)
+    assert (np.abs(lg - lse_ref) / np.abs(lse_ref)).max() <= 1e-5
+    nxt_g = ds.next_token.cpu().numpy()
+    for b in range(wl.B):
+        check_soft_draw(wl, b, int(last[b]), int(nxt_g[b]), int(nxt[b]))
+    return acc, paths
+
+
 def check_accept(ds: DeviceStep):
     wl = ds.wl
+    if wl.soft:
+        return check_accept_soft(ds)
     am, lse, zp, acc, paths, nxt, last = oracle_accept(wl)
     assert np.array_equal(ds.argmax.cpu().numpy(), am)
     lg = ds.lse_v.cpu().numpy().astype(np.float64)

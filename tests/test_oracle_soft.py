@@ -139,3 +139,23 @@ def test_greedy_limit_is_hard_matching(seed):
     c = path[-1]
     nxt = oracle.residual_sample(oracle.softmax_t(z[c], tiny), q[c] if q[c].any() else None, 0.5)
     assert nxt == g_next
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_planted_soft_walk(seed):
+    """The generator plants each soft decision with a wide margin; the
+    oracle's walk must follow the planted path exactly."""
+    wl = W.make_workload("ss_soft", seed, B=6, V=3000)
+    acc, paths, nxt, last = oracle.accept_soft(
+        wl.logits, wl.draft_logits, wl.tokens, wl.tree_parent, None, wl.child_draft_row,
+        wl.n_nodes, wl.u_accept, wl.u_sample, wl.temperature)
+    assert acc.tolist() == wl.expect_acc_len.tolist()
+    for b in range(wl.B):
+        assert paths[b] == wl.expect_path[b, : acc[b]].tolist()
+        assert last[b] == paths[b][-1]
+        # the correction token has residual mass at the last node
+        c = paths[b][-1]
+        p = oracle.softmax_t(wl.logits[b, c], wl.temperature)
+        dr = int(wl.child_draft_row[b, c])
+        r = p if dr < 0 else np.maximum(0, p - oracle.softmax_t(wl.draft_logits[b, dr]))
+        assert r[nxt[b]] > 0
