@@ -17,5 +17,6 @@ from .specverify_oracle import (  # noqa: F401
     la_prefill_mask, la_prefill_attention, la_prefill_vparent, mask_build, verify_attention, gather_paged,
     vocab_reduce, accept, accept_threshold_chain, accept_greedy_tree,
     softmax_t, residual_sample, accept_soft_tree, accept_soft,
+    topk_tokens, draft_tree, prune_tree, ss_block_vparent,
     kv_commit_contiguous, kv_commit_paged,
 )

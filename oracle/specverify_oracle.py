@@ -13,6 +13,7 @@ what one verification step computes:
   3. ``vocab_reduce``     per judged row: argmax, log-sum-exp, proposal logit
   4. ``accept``           threshold longest prefix, or greedy tree walk;
      ``accept_soft``      soft matching (ratio test + residual draw)
+     ``draft_tree``, ``prune_tree``, ``ss_block_vparent``: the next draft
   5. ``kv_commit``        append the accepted rows' K/V to the cache
 
 Sources (page title, section / equation):
@@ -458,6 +459,88 @@ def accept_soft(logits, draft_logits, tokens, tree_parent, row_of, child_draft_r
         last[b] = c
         next_tok[b] = residual_sample(p_of(c), q_of(c), u_sample[b])
     return acc_len, paths, next_tok, last
+
+
+# --------------------------------------------------------------------------
+# 4c. tree draft construction and pruning
+# --------------------------------------------------------------------------
+#
+# "Speculative Streaming", tree draft construction: the top-k tokens of
+# each speculative stream's logits at the accepted position; stream-j
+# tokens are the parents of stream-(j+1) tokens and stream-1 tokens the
+# children of the root (the correction token); 1 + sum_g k^g nodes,
+# flattened.  Parallel tree pruning: an edge (parent p, child c) survives
+# iff softmax(early-exit logits at p)[token of c] reaches the threshold;
+# a failing edge prunes the subtree under c.  Batching with streams: every
+# surviving node carries gamma stream rows.  Readings: ties in top-k go to
+# the lower token id; "falls below" prunes, so p >= threshold survives; the
+# tree is flattened breadth-first (a node's children after all nodes of
+# its level's predecessors, in parent order, then in top-k order), and
+# pruning keeps that order.
+
+def topk_tokens(z, k):
+    """The k token ids of largest logit, largest first, ties to the lower id."""
+    z = np.asarray(z, dtype=np.float64)
+    order = np.lexsort((np.arange(len(z)), -z))
+    return order[:k].astype(np.int64)
+
+
+def draft_tree(stream_logits, k, root_token):
+    """Full k-ary draft tree from gamma stream logit rows: (tokens, parent,
+    depth) in breadth-first order; node 0 is the root."""
+    gamma = len(stream_logits)
+    top = [topk_tokens(stream_logits[j], k) for j in range(gamma)]
+    tokens, parent, depth = [int(root_token)], [-1], [0]
+    frontier = [0]
+    for g in range(1, gamma + 1):
+        nxt = []
+        for p in frontier:
+            for i in range(k):
+                tokens.append(int(top[g - 1][i]))
+                parent.append(p)
+                depth.append(g)
+                nxt.append(len(tokens) - 1)
+        frontier = nxt
+    return np.array(tokens), np.array(parent), np.array(depth)
+
+
+def prune_tree(tokens, parent, early_logits, threshold):
+    """Keep node c (> 0) iff its parent is kept and
+    softmax(early_logits[parent[c]])[tokens[c]] >= threshold; the root is
+    always kept.  Survivors keep their order.  Returns (tokens', parent'
+    with new indices, keep_map: new index or -1 per old node)."""
+    n = len(tokens)
+    keep_map = np.full(n, -1, dtype=np.int64)
+    new_tok, new_par = [], []
+    probs = {}
+    for c in range(n):
+        p = int(parent[c])
+        if c == 0:
+            ok = True
+        else:
+            if p not in probs:
+                probs[p] = softmax_t(early_logits[p])
+            ok = keep_map[p] >= 0 and probs[p][int(tokens[c])] >= threshold
+        if ok:
+            keep_map[c] = len(new_tok)
+            new_tok.append(int(tokens[c]))
+            new_par.append(-1 if c == 0 else int(keep_map[p]))
+    return np.array(new_tok), np.array(new_par), keep_map
+
+
+def ss_block_vparent(parent, gamma, n_rows):
+    """Parent pointers of the flattened SS block for a tree of n nodes: row j
+    < n is node j (it sees its ancestors); row n + j*gamma + (s-1) is stream
+    s of node j (stream 1 sees node j's view, stream s > 1 the view of
+    stream s-1); rows past n(1 + gamma) up to n_rows are padding."""
+    n = len(parent)
+    vp = np.full(n_rows, VP_PAD, dtype=np.int64)
+    for j in range(n):
+        vp[j] = VP_ROOT if parent[j] < 0 else int(parent[j])
+        for s in range(1, gamma + 1):
+            r = n + j * gamma + (s - 1)
+            vp[r] = j if s == 1 else r - 1
+    return vp
 
 
 # --------------------------------------------------------------------------

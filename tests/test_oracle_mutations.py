@@ -122,3 +122,35 @@ def test_residual_sign_flip_is_caught(monkeypatch):
     monkeypatch.setattr(oracle, "residual_sample", flipped)
     _expect_pin_failure(tos.test_single_draft_output_is_target_distribution, 2)
     _expect_pin_failure(tos.test_hand_worked_tree)
+
+
+# ------------------------------------------------------------ draft trees
+
+import test_oracle_draft as tod
+
+
+def test_prune_without_parent_closure_is_caught(monkeypatch):
+    def no_closure(tokens, parent, early_logits, threshold):
+        n = len(tokens)
+        keep = np.full(n, -1, dtype=np.int64)
+        nt, npar = [], []
+        for c in range(n):
+            ok = c == 0 or so.softmax_t(early_logits[int(parent[c])])[int(tokens[c])] >= threshold
+            if ok:
+                keep[c] = len(nt)
+                nt.append(int(tokens[c]))
+                npar.append(-1 if c == 0 else int(keep[int(parent[c])]))
+        return np.array(nt), np.array(npar), keep
+
+    monkeypatch.setattr(oracle, "prune_tree", no_closure)
+    _expect_pin_failure(tod.test_prune_hand_worked)
+
+
+def test_topk_ties_to_higher_id_is_caught(monkeypatch):
+    def high_ties(z, k):
+        z = np.asarray(z, dtype=np.float64)
+        order = np.lexsort((-np.arange(len(z)), -z))
+        return order[:k]
+
+    monkeypatch.setattr(oracle, "topk_tokens", high_ties)
+    _expect_pin_failure(tod.test_topk_brute_force, 0, 3)
