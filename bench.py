@@ -19,7 +19,9 @@ second (candidate tokens judged per step / step time).
 ``--config la_prefill`` times the prefill form of Lookahead Attention
 (spec_la_prefill_attn: 4 requests x (4096 + 8) positions, 32 heads, head_dim
 128, bf16) instead; its metric is prefill positions per second and its
-roofline is the tensor-core one.
+roofline is the tensor-core one.  ``--config ss_draft`` times the next
+draft (spec_draft_tree + spec_prune_tree: 32 requests, 3 streams, top-4,
+vocab 50272); its metric is draft-tree nodes per second.
 """
 
 from __future__ import annotations
@@ -751,9 +753,231 @@ def run_prefill_gpu(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------- draft trees
+
+DRAFT_METRIC = "SS draft-tree nodes/s (top-k tree construction + pruning)"
+
+
+def draft_algorithmic_bytes(dw):
+    """Stream rows and the inner nodes' early-exit rows are read once; the
+    tree arrays (tokens, parents, keep map, block parent pointers) are
+    written."""
+    e = 2 if dw.dtype == "bf16" else 4
+    inner = dw.N - dw.k ** dw.gamma
+    logits = dw.B * (dw.gamma + inner) * dw.V * e
+    arrays = dw.B * dw.N * 4 * (2 + 2 + 1 + 2 * (1 + dw.gamma))
+    return logits + arrays
+
+
+def _draft_oracle_worker(conn, cfg, seed, requests):
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    import oracle
+    from self_speculative_verification_gb300 import workloads as W
+    dw = W.make_draft(seed, **cfg)
+    conn.send("ready")
+    while conn.recv() != "stop":
+        t0 = time.perf_counter()
+        for b in requests:
+            tok, par, _ = oracle.draft_tree(dw.stream_logits[b], dw.k, dw.root_token[b])
+            t2, p2, km = oracle.prune_tree(tok, par, dw.early_logits[b], dw.threshold)
+            oracle.ss_block_vparent(p2, dw.gamma, dw.N * (1 + dw.gamma))
+        conn.send(time.perf_counter() - t0)
+    conn.close()
+
+
+def draft_oracle(cfg, seed, cores, warm, steps):
+    ctx = mp.get_context("spawn")
+    n = max(1, min(cores, cfg["B"]))
+    conns, procs = [], []
+    for i in range(n):
+        a, b = ctx.Pipe()
+        p = ctx.Process(target=_draft_oracle_worker, args=(b, cfg, seed, [i]), daemon=True)
+        p.start()
+        conns.append(a)
+        procs.append(p)
+    for c in conns:
+        c.recv()
+    walls = []
+    try:
+        for i in range(warm + steps):
+            t0 = time.perf_counter()
+            for c in conns:
+                c.send("go")
+            for c in conns:
+                c.recv()
+            if i >= warm:
+                walls.append(time.perf_counter() - t0)
+    finally:
+        for c in conns:
+            try:
+                c.send("stop")
+            except Exception:
+                pass
+        for p in procs:
+            p.join(timeout=10)
+    N = 1 + sum(cfg["k"] ** g for g in range(1, cfg["gamma"] + 1))
+    wall = sum(walls) / len(walls)
+    return n * N / wall, n, wall
+
+
+def run_draft_reference(args):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    from self_speculative_verification_gb300 import workloads as W
+    cfg = dict(W.DRAFT_CONFIGS[args.config])
+    value, n, wall = draft_oracle(cfg, args.seed, args.cpu_workers or host_cores(),
+                                  min(args.warmup, 1), max(1, min(args.steps, 3)))
+    sample = (f"requests 0..{n - 1} of {args.config}, one per spawned process, float64 "
+              f"numpy; each step re-runs the sample")
+    line = {
+        "impl": "reference", "metric": DRAFT_METRIC, "value": value, "unit": "nodes/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * wall, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.config}: {cfg}", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "nodes/s", "cores": n, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "nodes/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_draft_gpu(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from self_speculative_verification_gb300 import workloads as W
+    from self_speculative_verification_gb300 import binding as bn
+
+    cfg = dict(W.DRAFT_CONFIGS[args.config])
+    if args.batch:
+        cfg["B"] = args.batch
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, n, wall = draft_oracle(cfg, args.seed, args.cpu_workers or host_cores(), 0, 1)
+        cpu = {"value": v, "unit": "nodes/s", "cores": n, "kind": "oracle",
+               "sample": f"requests 0..{n - 1} of the workload, one per spawned process, "
+                         f"float64 numpy"}
+    dw = W.make_draft(args.seed + rank, **cfg)
+    bn.load_library()
+    B, N, g = dw.B, dw.N, dw.gamma
+    R = N * (1 + g)
+    ldt = torch.bfloat16 if dw.dtype == "bf16" else torch.float32
+    i32 = torch.int32
+    stream_l = torch.from_numpy(dw.stream_logits).to(dev, ldt)
+    early = torch.from_numpy(dw.early_logits).to(dev, ldt)
+    root = torch.from_numpy(dw.root_token).to(dev)
+    tok, par, t2, p2, keep = (torch.zeros((B, N), dtype=i32, device=dev) for _ in range(5))
+    nn, n2 = torch.zeros(B, dtype=i32, device=dev), torch.zeros(B, dtype=i32, device=dev)
+    vp_full, vp = (torch.zeros((B, R), dtype=i32, device=dev) for _ in range(2))
+    spec_dt = bn.SPEC_BF16 if dw.dtype == "bf16" else bn.SPEC_F32
+    ddesc = bn.DraftDesc(B, g, g, dw.k, dw.V, spec_dt, N, R)
+    pdesc = bn.PruneDesc(B, N, dw.V, spec_dt, dw.threshold, g, R)
+    stream = torch.cuda.current_stream(dev)
+    in_bytes = draft_algorithmic_bytes(dw)
+    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        bn.spec_draft_tree(ddesc, stream_l, None, root, tok, par, nn, vp_full, stream)
+        bn.spec_prune_tree(pdesc, tok, par, nn, early, keep, t2, p2, n2, vp, stream)
+
+    for _ in range(args.warmup):
+        step()
+        flush_buf.random_()
+    torch.cuda.synchronize(dev)
+    assert bn.spec_get_status() == 0, "device status set during warm-up"
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        for e0, e1 in evs:
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            flush_buf.random_()
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    status = bn.spec_get_status()
+    times = np.array([a.elapsed_time(b) for a, b in evs])
+    total_ms = max_over_ranks(float(times.sum()), dev)
+    value = B * N * args.steps * world / (total_ms / 1e3)
+    step_ms = float(times.mean())
+    hbm, hbm_kind = peaks()
+    achieved = in_bytes / (step_ms / 1e3) / 1e9
+
+    e2e = None
+    if args.e2e_steps > 0:
+        h_in = [t.cpu().pin_memory() for t in (stream_l, early, root)]
+        outs = (t2, p2, n2, vp)
+        h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+
+        def one():
+            for d, h in zip((stream_l, early, root), h_in):
+                d.copy_(h, non_blocking=True)
+            step()
+            for h, d in zip(h_out, outs):
+                h.copy_(d, non_blocking=True)
+            stream.synchronize()
+        for _ in range(2):
+            one()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            one()
+        dt = time.perf_counter() - t0
+        e2e = {"value": B * N * args.e2e_steps / dt, "unit": "nodes/s",
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_in),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in h_out),
+               "ms_per_step": 1e3 * dt / args.e2e_steps}
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": DRAFT_METRIC, "value": value, "unit": "nodes/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dw.dtype,
+        "data": "synthetic",
+        "config": {"workload": f"{args.config}: B={B} gamma={g} k={dw.k} V={dw.V} {dw.dtype} "
+                               f"threshold={dw.threshold} ({N} nodes per full tree)",
+                   "seed": args.seed, "l2": "flushed between steps (2x L2 buffer written)",
+                   "survivors_per_step": int(n2.sum().item()),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"kernel": "draft_tree_kernel + prune_edge_kernel + prune_compact_kernel",
+                     "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "peak_kind": f"{hbm_kind} HBM copy bandwidth",
+                     "algorithmic_bytes_per_call": in_bytes, "traffic": None},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "device_status": status,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
     from self_speculative_verification_gb300 import workloads as W
+    if args.config in W.DRAFT_CONFIGS:
+        if args.impl == "reference":
+            run_draft_reference(args)
+        else:
+            run_draft_gpu(args)
+        return
     if args.config in W.PREFILL_CONFIGS:
         if args.impl == "reference":
             run_prefill_reference(args)

@@ -11,6 +11,8 @@
  *                        tree walk
  *   4. kv_commit         append the accepted rows' K/V to the cache; every
  *                        other speculative K/V row is dropped
+ * and, around it: spec_accept_soft (soft matching), spec_draft_tree and
+ * spec_prune_tree (the next draft), spec_la_prefill_attn (prefill-form LA).
  *
  * Sources, cited by page title and section / equation:
  *   [LA]  "Lookahead Attention: Self-Speculative Verification via Parallel
@@ -179,6 +181,29 @@ typedef struct spec_soft_desc {
     float temperature;  /* T > 0: p = softmax(z / T), q = softmax(z_d / T) */
 } spec_soft_desc;
 
+/* Shape of one draft-tree construction call. */
+typedef struct spec_draft_desc {
+    int batch;          /* B */
+    int n_stream_rows;  /* rows per request in stream_logits */
+    int gamma;          /* speculative streams (tree depth) */
+    int k;              /* tokens per stream (1..8) */
+    int vocab;          /* V (>= k) */
+    int logit_dtype;    /* SPEC_BF16 or SPEC_F32 */
+    int max_nodes;      /* row length of tokens / tree_parent (>= 1 + sum k^g) */
+    int vparent_rows;   /* row length of vparent (>= nodes * (1 + gamma)) */
+} spec_draft_desc;
+
+/* Shape and threshold of one tree-pruning call. */
+typedef struct spec_prune_desc {
+    int batch;          /* B */
+    int max_nodes;      /* N (<= 1024): row length of the tree arrays */
+    int vocab;          /* V */
+    int logit_dtype;    /* SPEC_BF16 or SPEC_F32 (early-exit logits) */
+    float threshold;    /* an edge survives iff its probability >= threshold */
+    int gamma;          /* stream rows per node in vparent */
+    int vparent_rows;   /* row length of vparent (>= N * (1 + gamma)) */
+} spec_prune_desc;
+
 /* Library version (SPECVERIFY_VERSION). */
 int spec_version(void);
 
@@ -276,8 +301,11 @@ spec_status_t spec_verify_attn(const spec_attn_desc *attn, const void *q,
  * none is accepted, next_token is drawn from max(0, p - q) normalised (from
  * p when the node has no draft row or p <= q everywhere): the smallest v
  * whose cumulative mass exceeds u_sample[b] times the total (fp32 sums).
- * Malformed indices set SPEC_DEV_BAD_INDEX.  Three launches: two vocab
- * reductions (target, draft) and one walk-and-draw kernel.
+ * max_nodes <= SPEC_MAX_ROWS (else SPEC_ERR_UNSUPPORTED).  A malformed index
+ * anywhere in the tree (parent, token, judge or draft row) or a path longer
+ * than path_cap sets SPEC_DEV_BAD_INDEX; the malformed node is never
+ * accepted.  Three launches: two vocab reductions (target, draft) and one
+ * test-walk-draw kernel.
  */
 spec_status_t spec_accept_soft(const spec_soft_desc *desc, const void *logits,
                                const void *draft_logits, const int32_t *tokens,
@@ -287,6 +315,64 @@ spec_status_t spec_accept_soft(const spec_soft_desc *desc, const void *logits,
                                float *lse_t, float *lse_d, int32_t *acc_len,
                                int32_t *path, int32_t *next_token, int32_t *last_node,
                                void *stream);
+
+/*
+ * spec_draft_tree -- the next step's draft tree ([SS] tree draft
+ * construction, batching with streams).
+ *
+ *   stream_logits [batch][n_stream_rows][vocab]: the speculative streams'
+ *                 logits; request b's streams 1..gamma are rows
+ *                 stream_row[b] .. stream_row[b] + gamma - 1 (stream_row
+ *                 NULL: rows 0..gamma-1).
+ *   root_token    int32 [batch]: the root's token (the correction token).
+ *   tokens, tree_parent  int32 out [batch][max_nodes]; n_nodes int32 out
+ *                 [batch] = 1 + sum_{g=1..gamma} k^g.
+ *   vparent       int32 out [batch][vparent_rows] or NULL: the flattened
+ *                 block for spec_mask_build (see below).
+ *
+ * The top-k tokens of stream j (largest logit first, ties to the lower
+ * token id) are the candidates at depth j; every depth-(j-1) node gets all
+ * k of them as children.  The tree is flattened breadth-first: node 0 is
+ * the root, depth g holds k^g nodes, node off(g) + m has parent
+ * off(g-1) + m / k and the (m % k)-th token of stream g.  vparent: row j < n
+ * is node j (SPEC_VP_ROOT for the root, else its parent), row
+ * n + j*gamma + (s-1) is stream s of node j (parent: node j for s = 1, the
+ * row of stream s-1 otherwise), later rows SPEC_VP_PAD.  Entries past n are
+ * -1.  A stream row outside [0, n_stream_rows) sets SPEC_DEV_BAD_INDEX.
+ */
+spec_status_t spec_draft_tree(const spec_draft_desc *desc, const void *stream_logits,
+                              const int32_t *stream_row, const int32_t *root_token,
+                              int32_t *tokens, int32_t *tree_parent, int32_t *n_nodes,
+                              int32_t *vparent, void *stream);
+
+/*
+ * spec_prune_tree -- subtree pruning by early-exit probability ([SS]
+ * parallel tree pruning).
+ *
+ *   tokens, tree_parent, n_nodes  the tree (parents precede children, node 0
+ *                 the root), e.g. from spec_draft_tree.
+ *   early_logits  [batch][max_nodes][vocab]: early-exit logits at each node.
+ *   keep_map      int32 out [batch][max_nodes]: a node's index in the pruned
+ *                 tree, or -1.
+ *   tokens_out, parent_out  int32 out [batch][max_nodes]: the pruned tree,
+ *                 survivors in their original order, parents renumbered;
+ *                 entries past n_out are -1.  Must not alias the inputs.
+ *   n_out         int32 out [batch].
+ *   vparent       int32 out [batch][vparent_rows] or NULL: the pruned tree's
+ *                 flattened block (layout as in spec_draft_tree).
+ *
+ * The edge from node p to its child c survives iff
+ * exp(z_p[token c] - ln sum exp z_p) >= threshold (fp32), z_p the early-exit
+ * logits at p; c survives iff its edge and its parent survive.  The root
+ * always survives.  A parent index that does not precede its node sets
+ * SPEC_DEV_BAD_TREE (that node is dropped); a token outside the vocabulary
+ * sets SPEC_DEV_BAD_INDEX.  Two launches.
+ */
+spec_status_t spec_prune_tree(const spec_prune_desc *desc, const int32_t *tokens,
+                              const int32_t *tree_parent, const int32_t *n_nodes,
+                              const void *early_logits, int32_t *keep_map,
+                              int32_t *tokens_out, int32_t *parent_out, int32_t *n_out,
+                              int32_t *vparent, void *stream);
 
 /*
  * spec_la_prefill_attn -- the prefill form of Lookahead Attention ([LA]
@@ -389,7 +475,8 @@ spec_status_t spec_vocab_reduce(const void *logits, int dtype, int n_rows,
  *   index on duplicate sibling tokens) until none matches.
  *   acc_len = nodes on the path including the root (beta + 1),
  *   path = those nodes, next_token = argmax at the last node (the
- *   correction token), last_node = last node on the path.
+ *   correction token), last_node = last node on the path.  Tree mode takes
+ *   max_nodes <= SPEC_MAX_ROWS (else SPEC_ERR_UNSUPPORTED).
  * path entries past acc_len are set to -1.  A path longer than path_cap or
  * an index out of range stops the walk and sets SPEC_DEV_BAD_INDEX.
  */

@@ -42,7 +42,8 @@ SPEC_DEV_BAD_INDEX = 0x10
 EXPORTS = ("spec_version", "spec_status_string", "spec_mask_build",
            "spec_verify_attn_workspace_size", "spec_verify_attn",
            "spec_verify_attn_noalloc", "spec_vocab_reduce", "spec_accept", "kv_commit",
-           "spec_get_status", "spec_la_prefill_attn", "spec_accept_soft")
+           "spec_get_status", "spec_la_prefill_attn", "spec_accept_soft", "spec_draft_tree",
+           "spec_prune_tree")
 SPEC_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -76,6 +77,18 @@ class SoftDesc(ctypes.Structure):
     _fields_ = [("batch", c_int), ("n_judge_rows", c_int), ("n_draft_rows", c_int),
                 ("vocab", c_int), ("logit_dtype", c_int), ("max_nodes", c_int),
                 ("path_cap", c_int), ("temperature", c_float)]
+
+
+class DraftDesc(ctypes.Structure):
+    _fields_ = [("batch", c_int), ("n_stream_rows", c_int), ("gamma", c_int), ("k", c_int),
+                ("vocab", c_int), ("logit_dtype", c_int), ("max_nodes", c_int),
+                ("vparent_rows", c_int)]
+
+
+class PruneDesc(ctypes.Structure):
+    _fields_ = [("batch", c_int), ("max_nodes", c_int), ("vocab", c_int),
+                ("logit_dtype", c_int), ("threshold", c_float), ("gamma", c_int),
+                ("vparent_rows", c_int)]
 
 
 class PrefillDesc(ctypes.Structure):
@@ -120,6 +133,8 @@ def load_library():
         "spec_get_status": ([vp, POINTER(ctypes.c_int32)], c_int),
         "spec_la_prefill_attn": ([POINTER(PrefillDesc), vp, vp, vp, vp, vp, vp], c_int),
         "spec_accept_soft": ([POINTER(SoftDesc)] + [vp] * 16, c_int),
+        "spec_draft_tree": ([POINTER(DraftDesc)] + [vp] * 8, c_int),
+        "spec_prune_tree": ([POINTER(PruneDesc)] + [vp] * 10, c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -341,3 +356,29 @@ def spec_accept_soft(desc: SoftDesc, logits, draft_logits, tokens, tree_parent, 
         _ptr(lse_t, f32, "lse_t"), _ptr(lse_d, f32, "lse_d"), _ptr(acc_len, i32, "acc_len"),
         _ptr(path, i32, "path"), _ptr(next_token, i32, "next_token"),
         _ptr(last_node, i32, "last_node"), _stream(stream)))
+
+
+def spec_draft_tree(desc: DraftDesc, stream_logits, stream_row, root_token, tokens, tree_parent,
+                    n_nodes, vparent=None, stream=None):
+    """Top-k per stream -> complete k-ary draft tree (+ the block's vparent)."""
+    lib = load_library()
+    i32 = torch.int32
+    _check("spec_draft_tree", lib.spec_draft_tree(
+        ctypes.byref(desc), _ptr(stream_logits, name="stream_logits"),
+        _ptr(stream_row, i32, "stream_row"), _ptr(root_token, i32, "root_token"),
+        _ptr(tokens, i32, "tokens"), _ptr(tree_parent, i32, "tree_parent"),
+        _ptr(n_nodes, i32, "n_nodes"), _ptr(vparent, i32, "vparent"), _stream(stream)))
+
+
+def spec_prune_tree(desc: PruneDesc, tokens, tree_parent, n_nodes, early_logits, keep_map,
+                    tokens_out, parent_out, n_out, vparent=None, stream=None):
+    """Drop subtrees whose edge probability under the early-exit logits is
+    below the threshold; compact the survivors."""
+    lib = load_library()
+    i32 = torch.int32
+    _check("spec_prune_tree", lib.spec_prune_tree(
+        ctypes.byref(desc), _ptr(tokens, i32, "tokens"), _ptr(tree_parent, i32, "tree_parent"),
+        _ptr(n_nodes, i32, "n_nodes"), _ptr(early_logits, name="early_logits"),
+        _ptr(keep_map, i32, "keep_map"), _ptr(tokens_out, i32, "tokens_out"),
+        _ptr(parent_out, i32, "parent_out"), _ptr(n_out, i32, "n_out"),
+        _ptr(vparent, i32, "vparent"), _stream(stream)))

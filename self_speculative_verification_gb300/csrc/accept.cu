@@ -14,6 +14,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "logits.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -51,27 +52,6 @@ __device__ __forceinline__ Best best_merge(Best a, Best b, float inv_t) {
     return a;
 }
 
-template <typename T> struct Vec;
-template <> struct Vec<float> {
-    static constexpr int N = 4;
-    __device__ static void load(const float *p, float *out) {
-        const float4 v = *reinterpret_cast<const float4 *>(p);
-        out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
-    }
-};
-template <> struct Vec<__nv_bfloat16> {
-    static constexpr int N = 8;
-    __device__ static void load(const __nv_bfloat16 *p, float *out) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(p);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            out[2 * i] = __uint_as_float(w[i] << 16);
-            out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-        }
-    }
-};
-
 // One thread-block cluster per row: CTA `rank` of the cluster reduces slice
 // `rank` of the row, kUnroll 16-byte loads in flight per thread, one pass
 // with a running (max, index, sum of exp).  Per batch of kUnroll * N
@@ -82,12 +62,6 @@ template <> struct Vec<__nv_bfloat16> {
 // distributed shared memory.
 constexpr int kUnroll = 4;
 
-// 2^x by the hardware approximation (relative error ~2^-22); 2^-inf = 0.
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 
 template <typename T>
 __global__ void __launch_bounds__(kReduceThreads)
@@ -301,11 +275,14 @@ __global__ void __launch_bounds__(128) accept_kernel(AcceptParams P) {
     }
 }
 
-// CTAs per row: enough CTAs for ~8 per SM, each slice at least 16 KB.
+// CTAs per row: the smallest power of two giving at least two CTAs per SM
+// (at most 8, each slice at least 16 KB).  Measured on GB300 (bf16, L2
+// cold, CUDA-graph timing): 512 x 50272 logits take 15.8 us with one CTA
+// per row against 22.3 us with four; 96 rows need four to fill the GPU.
 int cluster_size(int n_rows, int V, int dtype) {
     const long long row_bytes = (long long)V * (dtype == SPEC_BF16 ? 2 : 4);
     int nc = 1;
-    while (nc < 8 && row_bytes / (2 * nc) >= 16384 && (long long)n_rows * nc < 8ll * num_sms())
+    while (nc < 8 && row_bytes / (2 * nc) >= 16384 && (long long)n_rows * nc < 2ll * num_sms())
         nc *= 2;
     return nc;
 }
@@ -375,26 +352,61 @@ __device__ __forceinline__ float prob_at(const T *row, int v, float lse, float i
     return __expf(fmaf(load_f(row + v), inv_t, -lse));
 }
 
-// One CTA per request: thread 0 walks the tree, then the CTA draws the
-// correction token (tile sums, a scan over tiles, a scan inside the tile).
+// One CTA per request.  Every node's test against its parent's rows is
+// independent of the walk, so all threads evaluate them at once; thread 0
+// then walks the tree in shared memory, and the CTA draws the correction
+// token (tile sums, a scan over tiles, a scan inside the tile).
 template <typename T>
 __global__ void __launch_bounds__(kSoftThreads) soft_accept_kernel(SoftParams P) {
     __shared__ float s_tile[kMaxSoftTiles];
-    __shared__ int s_row, s_drow, s_hit;
-    __shared__ float s_total, s_base;
+    __shared__ int s_par[SPEC_MAX_ROWS];
+    __shared__ uint8_t s_acc[SPEC_MAX_ROWS];
+    __shared__ int s_row, s_drow;
+    __shared__ float s_total;
     const int b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const T *Z = static_cast<const T *>(P.logits);
     const T *ZD = static_cast<const T *>(P.draft);
+    const size_t nb = (size_t)b * P.N;
 
-    if (threadIdx.x == 0) {
-        int n = P.n_nodes[b];
-        if (n < 0 || n > P.N) {
-            raise_status(P.status, SPEC_DEV_BAD_INDEX);
-            n = n < 0 ? 0 : P.N;
+    int n = P.n_nodes[b];
+    if (n < 0 || n > P.N) {
+        if (threadIdx.x == 0) raise_status(P.status, SPEC_DEV_BAD_INDEX);
+        n = n < 0 ? 0 : P.N;
+    }
+    // row / draft row of node c's judge distribution (-1 / -2: malformed)
+    auto rows_of = [&](int c, int &row, int &drow) {
+        row = P.row_of ? P.row_of[nb + c] : c;
+        if (row < 0 || row >= P.Rj) row = -1;
+        drow = P.child_draft_row ? P.child_draft_row[nb + c] : -1;
+        if (drow < -1 || drow >= P.Rd) drow = -2;
+    };
+    // 1. node c (token x, parent a) is accepted iff u_c q_a(x) < p_a(x)
+    for (int c = threadIdx.x; c < n; c += kSoftThreads) {
+        const int a = P.tree_parent[nb + c];
+        s_par[c] = a;
+        uint8_t acc = 0;
+        if (c > 0 && a >= 0 && a < c) {
+            int row, drow;
+            rows_of(a, row, drow);
+            const int x = P.tokens[nb + c];
+            if (row < 0 || drow == -2 || x < 0 || x >= P.V) {
+                raise_status(P.status, SPEC_DEV_BAD_INDEX);
+            } else {
+                const float p = prob_at(Z + ((size_t)b * P.Rj + row) * P.V, x,
+                                        P.lse_t[(size_t)b * P.Rj + row], P.inv_t);
+                const float q = drow >= 0 ? prob_at(ZD + ((size_t)b * P.Rd + drow) * P.V, x,
+                                                    P.lse_d[(size_t)b * P.Rd + drow], P.inv_t)
+                                          : 0.f;
+                acc = P.u_accept[nb + c] * q < p;
+            }
         }
+        s_acc[c] = acc;
+    }
+    __syncthreads();
+    // 2. the walk: the lowest-index accepted child of the current node
+    if (threadIdx.x == 0) {
         int32_t *pth = P.path + (size_t)b * P.path_cap;
-        const size_t nb = (size_t)b * P.N;
         int len = 0, cur = 0, row = -1, drow = -1;
         if (n == 0 || P.path_cap == 0) {
             raise_status(P.status, SPEC_DEV_BAD_INDEX);
@@ -402,36 +414,12 @@ __global__ void __launch_bounds__(kSoftThreads) soft_accept_kernel(SoftParams P)
             len = 1;
             pth[0] = 0;
             while (true) {
-                row = P.row_of ? P.row_of[nb + cur] : cur;
-                if (row < 0 || row >= P.Rj) {
-                    raise_status(P.status, SPEC_DEV_BAD_INDEX);
-                    row = -1;
-                    break;
-                }
-                drow = P.child_draft_row ? P.child_draft_row[nb + cur] : -1;
-                if (drow < -1 || drow >= P.Rd) {
-                    raise_status(P.status, SPEC_DEV_BAD_INDEX);
-                    drow = -1;
-                }
-                const T *zt = Z + ((size_t)b * P.Rj + row) * P.V;
-                const float lt = P.lse_t[(size_t)b * P.Rj + row];
-                const T *zd = drow >= 0 ? ZD + ((size_t)b * P.Rd + drow) * P.V : nullptr;
-                const float ld = drow >= 0 ? P.lse_d[(size_t)b * P.Rd + drow] : 0.f;
                 int found = -1;
-                for (int c = cur + 1; c < n; ++c) {
-                    if (P.tree_parent[nb + c] != cur) continue;
-                    const int x = P.tokens[nb + c];
-                    if (x < 0 || x >= P.V) {
-                        raise_status(P.status, SPEC_DEV_BAD_INDEX);
-                        continue;
-                    }
-                    const float p = prob_at(zt, x, lt, P.inv_t);
-                    const float q = zd ? prob_at(zd, x, ld, P.inv_t) : 0.f;
-                    if (P.u_accept[nb + c] * q < p) {
+                for (int c = cur + 1; c < n; ++c)
+                    if (s_par[c] == cur && s_acc[c]) {
                         found = c;
                         break;
                     }
-                }
                 if (found < 0) break;
                 if (len >= P.path_cap) {
                     raise_status(P.status, SPEC_DEV_BAD_INDEX);
@@ -439,6 +427,11 @@ __global__ void __launch_bounds__(kSoftThreads) soft_accept_kernel(SoftParams P)
                 }
                 pth[len++] = found;
                 cur = found;
+            }
+            rows_of(cur, row, drow);
+            if (row < 0 || drow == -2) {
+                raise_status(P.status, SPEC_DEV_BAD_INDEX);
+                drow = -1;
             }
         }
         for (int i = len; i < P.path_cap; ++i) pth[i] = -1;
@@ -453,26 +446,60 @@ __global__ void __launch_bounds__(kSoftThreads) soft_accept_kernel(SoftParams P)
         if (threadIdx.x == 0) P.next_token[b] = -1;
         return;
     }
+    // 3. the correction token
     const int drow = s_drow;
     const T *zt = Z + ((size_t)b * P.Rj + row) * P.V;
     const float lt = P.lse_t[(size_t)b * P.Rj + row];
     const T *zd = drow >= 0 ? ZD + ((size_t)b * P.Rd + drow) * P.V : nullptr;
     const float ld = drow >= 0 ? P.lse_d[(size_t)b * P.Rd + drow] : 0.f;
     const int ntiles = (P.V + kSoftTile - 1) / kSoftTile;
+    const bool vec = (reinterpret_cast<uintptr_t>(zt) & 15) == 0 &&
+                     (reinterpret_cast<uintptr_t>(zd) & 15) == 0;
     bool resid = zd != nullptr;
-    auto mass = [&](int v) -> float {
-        if (v >= P.V) return 0.f;
-        const float p = prob_at(zt, v, lt, P.inv_t);
-        return resid ? fmaxf(0.f, p - prob_at(zd, v, ld, P.inv_t)) : p;
-    };
-    for (int pass = 0; pass < 2; ++pass) {
-        for (int t = warp; t < ntiles; t += kSoftThreads / 32) {
-            const int v0 = t * kSoftTile + lane * 8;
-            float acc = 0.f;
+    const float c2 = P.inv_t * kLog2e, lt2 = lt * kLog2e, ld2 = ld * kLog2e;
+    // masses of the 8 entries v0 .. v0 + 7 (0 past the vocabulary)
+    auto mass8 = [&](int v0, float (&m)[8]) {
+        float a[8], q[8];
+        if (vec && v0 + 8 <= P.V) {
+            load8(zt + v0, a);
+            if (resid) load8(zd + v0, q);
+        } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc += mass(v0 + e);
-            acc = warp_sum(acc);
-            if (lane == 0) s_tile[t] = acc;
+            for (int e = 0; e < 8; ++e) {
+                a[e] = v0 + e < P.V ? load_f(zt + v0 + e) : -INFINITY;
+                q[e] = (resid && v0 + e < P.V) ? load_f(zd + v0 + e) : -INFINITY;
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float p = ex2(fmaf(a[e], c2, -lt2));
+            m[e] = resid ? fmaxf(0.f, p - ex2(fmaf(q[e], c2, -ld2))) : p;
+        }
+    };
+    constexpr int kWarps = kSoftThreads / 32;
+    for (int pass = 0; pass < 2; ++pass) {
+        for (int t = warp; t < ntiles; t += 2 * kWarps) {
+            const int t2 = t + kWarps;
+            float m0[8], m1[8];
+            mass8(t * kSoftTile + lane * 8, m0);
+            if (t2 < ntiles) {
+                mass8(t2 * kSoftTile + lane * 8, m1);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) m1[e] = 0.f;
+            }
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                s0 += m0[e];
+                s1 += m1[e];
+            }
+            s0 = warp_sum(s0);
+            s1 = warp_sum(s1);
+            if (lane == 0) {
+                s_tile[t] = s0;
+                if (t2 < ntiles) s_tile[t2] = s1;
+            }
         }
         __syncthreads();
         if (warp == 0) {
@@ -483,7 +510,7 @@ __global__ void __launch_bounds__(kSoftThreads) soft_accept_kernel(SoftParams P)
         }
         __syncthreads();
         if (s_total > 0.f || !resid) break;
-        resid = false;           // p == q: draw from p
+        resid = false;           // p <= q everywhere: draw from p
         __syncthreads();
     }
     if (warp != 0) return;
@@ -529,14 +556,12 @@ __global__ void __launch_bounds__(kSoftThreads) soft_accept_kernel(SoftParams P)
         tile = last < 0 ? 0 : last;
         base = -INFINITY;        // take the last element with mass below
     }
-    // inside the tile: lane l holds elements [l * 8, l * 8 + 8)
+    // inside the tile: lane l holds entries [l * 8, l * 8 + 8)
     const int v0 = tile * kSoftTile + lane * 8;
     float m[8], part = 0.f;
+    mass8(v0, m);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        m[e] = mass(v0 + e);
-        part += m[e];
-    }
+    for (int e = 0; e < 8; ++e) part += m[e];
     float ip = part;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -597,8 +622,9 @@ extern "C" spec_status_t spec_accept(const spec_accept_desc *d, const void *logi
         if (row_of || !zprop) return SPEC_ERR_INVALID_ARG;
         if (!(d->tau > 0.f) || d->tau > 1.f) return SPEC_ERR_INVALID_ARG;
         if (logits && d->max_nodes != d->n_judge_rows) return SPEC_ERR_INVALID_ARG;
-    } else if (!tree_parent) {
-        return SPEC_ERR_INVALID_ARG;
+    } else {
+        if (!tree_parent) return SPEC_ERR_INVALID_ARG;
+        if (d->max_nodes > SPEC_MAX_ROWS) return SPEC_ERR_UNSUPPORTED;   // walk keeps nodes in registers
     }
     cudaStream_t s = sv::as_stream(stream);
     if (logits) {
@@ -651,6 +677,7 @@ extern "C" spec_status_t spec_accept_soft(const spec_soft_desc *d, const void *l
         return SPEC_ERR_INVALID_ARG;
     if (d->logit_dtype != SPEC_F32 && d->logit_dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
     if ((d->vocab + kSoftTile - 1) / kSoftTile > kMaxSoftTiles) return SPEC_ERR_UNSUPPORTED;
+    if (d->max_nodes > SPEC_MAX_ROWS) return SPEC_ERR_UNSUPPORTED;
     if (d->batch == 0) return SPEC_OK;
     if (!logits || !tokens || !tree_parent || !n_nodes || !u_accept || !u_sample || !lse_t ||
         !acc_len || !path || !next_token || !last_node)

@@ -1177,30 +1177,14 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                      "r"(kTmemCols));
 }
 
-// Merge the partials of every (request, KV head, packed row): one warp each.
+// Merge packed row p of segment seg (request b, KV head h; tiles [s0, s1),
+// partials from CTAs first..last, wcn per CTA) into the final O and LSE.
+// One warp.
 template <int D>
-__global__ void __launch_bounds__(128) attn_tc_combine_kernel(const __grid_constant__ TcParams P,
-                                                               int wcn, int whole_done) {
+__device__ void merge_row(const TcParams &P, int wcn, long long T, int b, int h, int seg,
+                          long long s0, long long s1, int first, int last, int p, int lane) {
     const AttnParams &A = P.a;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int p = blockIdx.x * 4 + warp;
-    const int h = blockIdx.y, b = blockIdx.z;
-    if (p >= A.M) return;
-    if (p == 0 && h == 0 && lane == 0) {
-        const int S_raw = A.seq_len[b];
-        if (S_raw < 0 || S_raw > A.capacity) raise_status(A.status, SPEC_DEV_SEQ_OVERFLOW);
-    }
-    const long long T = warp_total_tiles(P);
-    const int rb = p / A.rb_rows, rr = p % A.rb_rows;
-    const int S = req_seq(P, b);
-    const int nt = seg_tiles(P, S);
-    const long long s0 = warp_tiles_before(P, b) + (long long)(h * A.n_rb + rb) * nt;
-    const long long s1 = s0 + nt;
-    const int seg = (b * A.Hkv + h) * A.n_rb + rb;
-    const int first = cta_of(T, s0, P.n_ctas), last = cta_of(T, s1 - 1, P.n_ctas);
-    // segments inside one CTA's range were finished by the attention kernel
-    if (whole_done && first == last) return;
-
+    const int rr = p % A.rb_rows;
     float mstar = -INFINITY;
     for (int i = first; i <= last; ++i) {
         const long long lo = range_lo(T, i, P.n_ctas), hi = range_lo(T, i + 1, P.n_ctas);
@@ -1238,6 +1222,72 @@ __global__ void __launch_bounds__(128) attn_tc_combine_kernel(const __grid_const
 #pragma unroll
     for (int j = 0; j < D / 32; ++j) o[lane + 32 * j] = __float2bfloat16_rn(out[j]);
     if (lane == 0) A.lse[((size_t)b * A.Hq + hq) * A.R + r] = lse;
+}
+
+__device__ __forceinline__ void check_seq_len(const AttnParams &A, int b) {
+    const int S_raw = A.seq_len[b];
+    if (S_raw < 0 || S_raw > A.capacity) raise_status(A.status, SPEC_DEV_SEQ_OVERFLOW);
+}
+
+// mma.sync path: every segment has partials.  One warp per (request, KV
+// head, packed row).
+template <int D>
+__global__ void __launch_bounds__(128) attn_tc_combine_kernel(const __grid_constant__ TcParams P,
+                                                               int wcn) {
+    const AttnParams &A = P.a;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int p = blockIdx.x * 4 + warp;
+    const int h = blockIdx.y, b = blockIdx.z;
+    if (p >= A.M) return;
+    if (p == 0 && h == 0 && lane == 0) check_seq_len(A, b);
+    const long long T = warp_total_tiles(P);
+    const int rb = p / A.rb_rows;
+    const int nt = seg_tiles(P, req_seq(P, b));
+    const long long s0 = warp_tiles_before(P, b) + (long long)(h * A.n_rb + rb) * nt;
+    const long long s1 = s0 + nt;
+    const int seg = (b * A.Hkv + h) * A.n_rb + rb;
+    merge_row<D>(P, wcn, T, b, h, seg, s0, s1, cta_of(T, s0, P.n_ctas),
+                 cta_of(T, s1 - 1, P.n_ctas), p, lane);
+}
+
+// tcgen05 path: a segment wholly inside one CTA's range already holds its
+// final output; a split segment contains at least one boundary between
+// consecutive CTA ranges.  CTA i here takes the boundary between attention
+// CTAs i and i + 1 and merges the segment across it when that boundary is
+// the segment's first, so only split segments cost work (at most
+// n_ctas - 1 of them).
+constexpr int kUmmaCombineThreads = 512;
+
+template <int D>
+__global__ void __launch_bounds__(kUmmaCombineThreads)
+attn_umma_combine_kernel(const __grid_constant__ TcParams P) {
+    const AttnParams &A = P.a;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (blockIdx.x == 0)
+        for (int b = threadIdx.x; b < A.B; b += kUmmaCombineThreads) check_seq_len(A, b);
+    const long long T = warp_total_tiles(P);
+    const long long tb = range_lo(T, blockIdx.x + 1, P.n_ctas);
+    if (tb <= 0 || tb >= T) return;
+    int b;
+    long long start;
+    warp_locate(P, tb, &b, &start);
+    const int nt = seg_tiles(P, req_seq(P, b));
+    const int segi = (int)((tb - start) / nt);
+    const long long s0 = start + (long long)segi * nt, s1 = s0 + nt;
+    if (s0 == tb) return;                       // the boundary starts a segment
+    const int first = cta_of(T, s0, P.n_ctas);
+    if (first != (int)blockIdx.x) return;        // not this segment's first boundary
+    const int last = cta_of(T, s1 - 1, P.n_ctas);
+    const int h = segi / A.n_rb, rb = segi % A.n_rb;
+    const int seg = (b * A.Hkv + h) * A.n_rb + rb;
+    const int p_hi = min(A.M, (rb + 1) * A.rb_rows);
+    for (int p = rb * A.rb_rows + warp; p < p_hi; p += kUmmaCombineThreads / 32)
+        merge_row<D>(P, 1, T, b, h, seg, s0, s1, first, last, p, lane);
+}
+
+// Single-CTA launches have no boundary: only the seq_len check remains.
+__global__ void check_seq_len_kernel(const __grid_constant__ TcParams P) {
+    for (int b = threadIdx.x; b < P.a.B; b += blockDim.x) check_seq_len(P.a, b);
 }
 
 // ------------------------------------------------------------------ host
@@ -1292,7 +1342,7 @@ spec_status_t launch_impl(const TcParams &P, const CUtensorMap *maps, cudaStream
     spec_status_t st = launch_status();
     if (st != SPEC_OK) return st;
     dim3 grid(ceil_div(P.a.M, 4), P.a.Hkv, P.a.B);
-    attn_tc_combine_kernel<D><<<grid, 128, 0, s>>>(P, NCW / WR, 0);
+    attn_tc_combine_kernel<D><<<grid, 128, 0, s>>>(P, NCW / WR);
     return launch_status();
 }
 
@@ -1312,8 +1362,10 @@ spec_status_t launch_umma(const TcParams &P, const CUtensorMap *maps, cudaStream
                                                                  maps[3], maps[4], maps[5]);
     spec_status_t st = launch_status();
     if (st != SPEC_OK) return st;
-    dim3 grid(ceil_div(P.a.M, 4), P.a.Hkv, P.a.B);
-    attn_tc_combine_kernel<D><<<grid, 128, 0, s>>>(P, 1, 1);
+    if (P.n_ctas > 1)
+        attn_umma_combine_kernel<D><<<P.n_ctas - 1, kUmmaCombineThreads, 0, s>>>(P);
+    else
+        check_seq_len_kernel<<<1, 32, 0, s>>>(P);
     return launch_status();
 }
 

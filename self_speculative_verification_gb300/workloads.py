@@ -660,3 +660,81 @@ def make_prefill(seed: int = 0, *, B: int, n: int, k: int, Hq: int, Hkv: int,
     kk = _normal(rng, (B, L, Hkv, d), VALUE_SCALE, "bf16")
     v = _normal(rng, (B, L, Hkv, d), VALUE_SCALE, "bf16")
     return PrefillWorkload(B, n, k, Hq, Hkv, d, q, kk, v)
+
+
+# --------------------------------------------------------------------------
+# tree draft construction and pruning ("Speculative Streaming")
+# --------------------------------------------------------------------------
+
+#: The next step's draft for the SS workload: gamma = 3 streams, top-k = 4
+#: per stream (the page sweeps gamma in {3, 4} and k from 1 up), OPT-6.7B's
+#: vocabulary, pruning threshold 0.05 (the page gives none).
+DRAFT_CONFIGS = {
+    "ss_draft": dict(B=32, gamma=3, k=4, V=50272, dtype="bf16", threshold=0.05),
+}
+
+
+@dataclass
+class DraftWorkload:
+    """Inputs of one draft construction + pruning, with planted outcomes."""
+
+    B: int
+    gamma: int
+    k: int
+    V: int
+    dtype: str
+    threshold: float
+    stream_logits: np.ndarray    # [B][gamma][V]
+    root_token: np.ndarray       # int32 [B]
+    early_logits: np.ndarray     # [B][N][V]: early-exit logits at each node
+    expect_top: np.ndarray       # int32 [B][gamma][k]: planted top-k per stream
+    expect_keep: np.ndarray      # bool [B][N]: planted survivors
+
+    @property
+    def N(self) -> int:
+        return 1 + sum(self.k ** g for g in range(1, self.gamma + 1))
+
+
+def make_draft(seed: int = 0, *, B=32, gamma=3, k=4, V=50272, dtype="bf16",
+               threshold=0.05, keep_p=0.7) -> DraftWorkload:
+    """Stream rows ~ N(0, 1) with k planted winners (logits 10 - 0.5 i, the
+    middle two tied so the lower id must come first); early-exit rows
+    ~ N(0, 1) with, at every inner node, each child token planted at a
+    probability >= 1.6 x threshold (kept, with prob keep_p) or <= 0.6 x
+    threshold (pruned)."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0xD7A])))
+    parent, depth = full_tree(k, gamma)
+    N = len(parent)
+    stream = np.empty((B, gamma, V), dtype=np.float32)
+    top = np.empty((B, gamma, k), dtype=np.int32)
+    for b in range(B):
+        for j in range(gamma):
+            z = rng.standard_normal(V, dtype=np.float32)
+            ids = rng.choice(V, size=k, replace=False)
+            vals = [10.0 - 0.5 * i for i in range(k)]
+            if k >= 3:
+                vals[2] = vals[1]                      # a tie at ranks 1 and 2
+            for t, val in zip(ids, vals):
+                z[t] = val
+            order = sorted(range(k), key=lambda i: (-vals[i], int(ids[i])))
+            top[b, j] = [int(ids[i]) for i in order]
+            stream[b, j] = _to_storage(z, dtype)
+    root = rng.integers(0, V, B).astype(np.int32)
+    early = np.empty((B, N, V), dtype=np.float32)
+    keep = np.zeros((B, N), dtype=bool)
+    for b in range(B):
+        keep[b, 0] = True
+        edge = {}
+        for p in range(N):
+            probs = {}
+            if depth[p] < gamma:
+                kids = np.nonzero(parent == p)[0]
+                for i, c in enumerate(kids):
+                    ok = rng.random() < keep_p
+                    edge[int(c)] = ok
+                    lo, hi = (1.6, 4.0) if ok else (0.1, 0.6)
+                    probs[int(top[b, depth[p], i])] = threshold * float(rng.uniform(lo, hi))
+            early[b, p] = _plant_probs_row(rng, V, dtype, probs)
+        for c in range(1, N):
+            keep[b, c] = keep[b, parent[c]] and edge[c]
+    return DraftWorkload(B, gamma, k, V, dtype, threshold, stream, root, early, top, keep)

@@ -114,3 +114,17 @@ def test_prune_closure_and_limits(seed):
     assert (km >= 0).sum() == len(t2)
     assert (oracle.prune_tree(tok, par, early, 0.0)[2] >= 0).all()
     assert (oracle.prune_tree(tok, par, early, 1.5)[2] >= 0).sum() == 1
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_planted_draft_workload(seed):
+    """The generator plants top-k winners (with a tie) and every pruning
+    decision with a margin; the oracle must recover them."""
+    d = W.make_draft(seed, B=3, V=2000)
+    for b in range(d.B):
+        for j in range(d.gamma):
+            assert oracle.topk_tokens(d.stream_logits[b, j], d.k).tolist() == \
+                d.expect_top[b, j].tolist()
+        tok, par, _ = oracle.draft_tree(d.stream_logits[b], d.k, d.root_token[b])
+        _, _, km = oracle.prune_tree(tok, par, d.early_logits[b], d.threshold)
+        assert np.array_equal(km >= 0, d.expect_keep[b])
