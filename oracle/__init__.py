@@ -18,5 +18,6 @@ from .specverify_oracle import (  # noqa: F401
     vocab_reduce, accept, accept_threshold_chain, accept_greedy_tree,
     softmax_t, residual_sample, accept_soft_tree, accept_soft,
     topk_tokens, draft_tree, prune_tree, ss_block_vparent,
+    rotate_stream_values, future_gather,
     kv_commit_contiguous, kv_commit_paged,
 )

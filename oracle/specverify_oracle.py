@@ -14,6 +14,7 @@ what one verification step computes:
   4. ``accept``           threshold longest prefix, or greedy tree walk;
      ``accept_soft``      soft matching (ratio test + residual draw)
      ``draft_tree``, ``prune_tree``, ``ss_block_vparent``: the next draft
+     ``rotate_stream_values`` (SS Eq. 7), ``future_gather`` (ConFu hand-off)
   5. ``kv_commit``        append the accepted rows' K/V to the cache
 
 Sources (page title, section / equation):
@@ -541,6 +542,40 @@ def ss_block_vparent(parent, gamma, n_rows):
             r = n + j * gamma + (s - 1)
             vp[r] = j if s == 1 else r - 1
     return vp
+
+
+# --------------------------------------------------------------------------
+# 4d. stream value rotation and the ConFu future-token hand-off
+# --------------------------------------------------------------------------
+
+def rotate_stream_values(vb, n_nodes, gamma, eps):
+    """"Speculative Streaming" Eq. 7 (value rotation): the value vector of
+    stream s of node j is node j's value vector times e^{i eps s}.  Reading:
+    consecutive pairs (v[2i], v[2i+1]) are the real and imaginary parts.
+    vb [B][Hkv][R][d] (block values in the SS layout: rows 0..T_b-1 the
+    nodes, row T_b + j*gamma + (s-1) stream s of node j); returns a float64
+    copy with the stream rows rewritten."""
+    out = np.array(vb, dtype=np.float64, copy=True)
+    B = out.shape[0]
+    for b in range(B):
+        T = int(n_nodes[b])
+        for j in range(T):
+            for s in range(1, gamma + 1):
+                r = T + j * gamma + (s - 1)
+                c, sn = math.cos(eps * s), math.sin(eps * s)
+                re, im = out[b, :, j, 0::2], out[b, :, j, 1::2]
+                out[b, :, r, 0::2] = re * c - im * sn
+                out[b, :, r, 1::2] = re * sn + im * c
+    return out
+
+
+def future_gather(o, last_node, row_offset):
+    """"ConFu" key design 1: the future prediction handed to the next round
+    is the output of the contemplate token attached to the last accepted
+    node, block row row_offset + last_node (row_offset = T).  o
+    [B][R][Hq][d] -> [B][Hq][d]."""
+    o = np.asarray(o)
+    return np.stack([o[b, row_offset + int(last_node[b])] for b in range(o.shape[0])])
 
 
 # --------------------------------------------------------------------------

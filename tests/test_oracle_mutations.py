@@ -154,3 +154,33 @@ def test_topk_ties_to_higher_id_is_caught(monkeypatch):
 
     monkeypatch.setattr(oracle, "topk_tokens", high_ties)
     _expect_pin_failure(tod.test_topk_brute_force, 0, 3)
+
+
+# ------------------------------------------------------ stream value rotation
+
+import test_oracle_stream_ops as tso
+
+
+def test_rotation_sign_flip_is_caught(monkeypatch):
+    monkeypatch.setattr(oracle, "rotate_stream_values",
+                        lambda vb, n, g, eps: so.rotate_stream_values(vb, n, g, -eps))
+    _expect_pin_failure(tso.test_rotation_is_complex_multiplication)
+
+
+def test_rotation_by_node_index_is_caught(monkeypatch):
+    """Rotating by eps * (node index) instead of eps * (stream index)."""
+    def by_node(vb, n_nodes, gamma, eps):
+        out = np.array(vb, dtype=np.float64, copy=True)
+        for b in range(out.shape[0]):
+            T = int(n_nodes[b])
+            for j in range(T):
+                for s in range(1, gamma + 1):
+                    r = T + j * gamma + (s - 1)
+                    c, sn = math.cos(eps * (j + 1)), math.sin(eps * (j + 1))
+                    re, im = out[b, :, j, 0::2], out[b, :, j, 1::2]
+                    out[b, :, r, 0::2] = re * c - im * sn
+                    out[b, :, r, 1::2] = re * sn + im * c
+        return out
+
+    monkeypatch.setattr(oracle, "rotate_stream_values", by_node)
+    _expect_pin_failure(tso.test_rotation_is_complex_multiplication)
