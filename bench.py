@@ -389,22 +389,26 @@ def run_gpu(args):
     flush = footprint < 2 * L2_BYTES
     flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush else None
 
+    # the step's calls in order (rotation / gather only where the workload
+    # has them); events bracket each call on the launching stream
+    stages = [(n, f) for n, f in (("stream_rotate", ds.rotate_values if ds.rotate else None),
+                                  ("mask_build", ds.mask_build),
+                                  ("verify_attn", ds.verify_attn),
+                                  ("accept", ds.accept_step),
+                                  ("future_gather",
+                                   ds.gather_future if ds.future is not None else None),
+                                  ("kv_commit", ds.commit)) if f is not None]
+    n_st = len(stages)
+    i_attn = [n for n, _ in stages].index("verify_attn")
+
     def step(ev=None):
         ds.reset_state()
+        for i, (_, f) in enumerate(stages):
+            if ev is not None:
+                ev[i].record(stream)
+            f()
         if ev is not None:
-            ev[0].record(stream)
-        ds.mask_build()
-        if ev is not None:
-            ev[1].record(stream)
-        ds.verify_attn()
-        if ev is not None:
-            ev[2].record(stream)
-        ds.accept_step()
-        if ev is not None:
-            ev[3].record(stream)
-        ds.commit()
-        if ev is not None:
-            ev[4].record(stream)
+            ev[n_st].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -413,7 +417,8 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
     assert bn.spec_get_status() == 0, "device status set during warm-up"
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_st + 1)]
+           for _ in range(args.steps)]
     region = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     if world > 1:
         dist.barrier()
@@ -430,8 +435,8 @@ def run_gpu(args):
         dist.barrier()
     status = bn.spec_get_status()
 
-    per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)]
-                    for i in range(args.steps)])          # ms: mask, attn, accept, commit
+    per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(n_st)]
+                    for i in range(args.steps)])          # ms per stage
     step_ms = per.sum(axis=1)
     region_ms = region[0].elapsed_time(region[1])
     total_ms = float(step_ms.sum()) if flush else region_ms
@@ -439,7 +444,7 @@ def run_gpu(args):
 
     tokens = wl.verified_tokens()
     value = job_throughput(tokens, args.steps, world, total_ms)
-    attn_ms = float(per[:, 1].mean())
+    attn_ms = float(per[:, i_attn].mean())
     hbm, hbm_kind = peaks()
     achieved = attn_bytes / (attn_ms / 1e3) / 1e9
     accepted_rows = int(ds.acc_len.sum().item())
@@ -467,8 +472,7 @@ def run_gpu(args):
             "seed": args.seed,
             "verified_tokens_per_step": tokens,
             "accepted_rows_per_step": accepted_rows,
-            "per_call_ms": {"mask_build": float(per[:, 0].mean()), "verify_attn": attn_ms,
-                            "accept": float(per[:, 2].mean()), "kv_commit": float(per[:, 3].mean())},
+            "per_call_ms": {n: float(per[:, i].mean()) for i, (n, _) in enumerate(stages)},
             "step_includes": "seq_len/free_head restore (2 small device copies)",
             "step_algorithmic_bytes": step_algorithmic_bytes(wl, accepted_rows),
         },
@@ -499,6 +503,8 @@ def run_e2e(ds, steps, stream):
                           ds.draft_logits, ds.child_draft_row, ds.u_accept, ds.u_sample)
               if t is not None]
     outputs = [ds.acc_len, ds.path, ds.next_token, ds.last_node]
+    if ds.future is not None:
+        outputs.append(ds.future)
     h_in = [t.cpu().pin_memory() for t in inputs]
     h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outputs]
     bi = sum(t.numel() * t.element_size() for t in inputs)

@@ -12,7 +12,9 @@
  *   4. kv_commit         append the accepted rows' K/V to the cache; every
  *                        other speculative K/V row is dropped
  * and, around it: spec_accept_soft (soft matching), spec_draft_tree and
- * spec_prune_tree (the next draft), spec_la_prefill_attn (prefill-form LA).
+ * spec_prune_tree (the next draft), spec_stream_rotate_values (stream values
+ * by rotation), spec_future_gather (ConFu's future token),
+ * spec_la_prefill_attn (prefill-form LA).
  *
  * Sources, cited by page title and section / equation:
  *   [LA]  "Lookahead Attention: Self-Speculative Verification via Parallel
@@ -204,6 +206,17 @@ typedef struct spec_prune_desc {
     int vparent_rows;   /* row length of vparent (>= N * (1 + gamma)) */
 } spec_prune_desc;
 
+/* Shape of one stream value rotation call. */
+typedef struct spec_rotate_desc {
+    int batch;          /* B */
+    int n_rows;         /* R: rows of the block per (request, KV head) */
+    int n_kv_heads;     /* Hkv */
+    int head_dim;       /* d (multiple of 8) */
+    int dtype;          /* SPEC_BF16 or SPEC_F32 */
+    int gamma;          /* streams per node (<= 64) */
+    float eps;          /* rotation angle per stream index, radians */
+} spec_rotate_desc;
+
 /* Library version (SPECVERIFY_VERSION). */
 int spec_version(void);
 
@@ -373,6 +386,46 @@ spec_status_t spec_prune_tree(const spec_prune_desc *desc, const int32_t *tokens
                               const void *early_logits, int32_t *keep_map,
                               int32_t *tokens_out, int32_t *parent_out, int32_t *n_out,
                               int32_t *vparent, void *stream);
+
+/*
+ * spec_stream_rotate_values -- stream values by rotation ([SS] Eq. 7,
+ * V_tn = V_t e^{i eps n}, 0 <= eps <= pi / (2N) with N the maximum sequence
+ * length plus the number of streams).
+ *
+ *   n_nodes  int32 [batch]: T_b, the nodes of request b's block.
+ *   vb       [batch][n_kv_heads][n_rows][head_dim] (dtype), in place: the
+ *            block values in the SS layout (rows 0..T_b-1 the nodes, row
+ *            T_b + j*gamma + (s-1) stream s of node j).
+ *
+ * For every node j and stream s = 1..gamma, the stream row's value vector
+ * becomes node j's value vector with each pair (v[2i], v[2i+1]), read as
+ * v[2i] + i v[2i+1], multiplied by e^{i eps s} (fp32, then the storage
+ * type).  Node rows and rows past T_b (1 + gamma) are not touched; the
+ * block keys are the caller's.  A request with T_b (1 + gamma) > n_rows is
+ * skipped and sets SPEC_DEV_BAD_INDEX.  vb must be 16-byte aligned.  Run it
+ * before spec_verify_attn.
+ */
+spec_status_t spec_stream_rotate_values(const spec_rotate_desc *desc, const int32_t *n_nodes,
+                                        void *vb, void *stream);
+
+/*
+ * spec_future_gather -- the future-token hand-off ([CF] key design 1: the
+ * future prediction of the contemplate token attached to the last accepted
+ * node goes to the next round's draft).
+ *
+ *   o          [batch][n_rows][row_elems] (dtype): e.g. spec_verify_attn's
+ *              output with row_elems = n_q_heads * head_dim.
+ *   last_node  int32 [batch]: from spec_accept.
+ *   out        [batch][row_elems] (dtype) out: row row_offset + last_node[b]
+ *              of request b (row_offset = T for the ConFu layout, whose
+ *              contemplate token of node j is row T + j).
+ *
+ * Rows must be whole multiples of 16 bytes and o, out 16-byte aligned.  A
+ * row outside [0, n_rows) writes zeros and sets SPEC_DEV_BAD_INDEX.
+ */
+spec_status_t spec_future_gather(int batch, int n_rows, int row_elems, int dtype,
+                                 const void *o, const int32_t *last_node, int row_offset,
+                                 void *out, void *stream);
 
 /*
  * spec_la_prefill_attn -- the prefill form of Lookahead Attention ([LA]

@@ -43,7 +43,7 @@ EXPORTS = ("spec_version", "spec_status_string", "spec_mask_build",
            "spec_verify_attn_workspace_size", "spec_verify_attn",
            "spec_verify_attn_noalloc", "spec_vocab_reduce", "spec_accept", "kv_commit",
            "spec_get_status", "spec_la_prefill_attn", "spec_accept_soft", "spec_draft_tree",
-           "spec_prune_tree")
+           "spec_prune_tree", "spec_stream_rotate_values", "spec_future_gather")
 SPEC_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -91,6 +91,11 @@ class PruneDesc(ctypes.Structure):
                 ("vparent_rows", c_int)]
 
 
+class RotateDesc(ctypes.Structure):
+    _fields_ = [("batch", c_int), ("n_rows", c_int), ("n_kv_heads", c_int),
+                ("head_dim", c_int), ("dtype", c_int), ("gamma", c_int), ("eps", c_float)]
+
+
 class PrefillDesc(ctypes.Structure):
     _fields_ = [("batch", c_int), ("n_orig", c_int), ("n_look", c_int),
                 ("n_q_heads", c_int), ("n_kv_heads", c_int), ("head_dim", c_int),
@@ -135,6 +140,8 @@ def load_library():
         "spec_accept_soft": ([POINTER(SoftDesc)] + [vp] * 16, c_int),
         "spec_draft_tree": ([POINTER(DraftDesc)] + [vp] * 8, c_int),
         "spec_prune_tree": ([POINTER(PruneDesc)] + [vp] * 10, c_int),
+        "spec_stream_rotate_values": ([POINTER(RotateDesc), vp, vp, vp], c_int),
+        "spec_future_gather": ([c_int, c_int, c_int, c_int, vp, vp, c_int, vp, vp], c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -382,3 +389,23 @@ def spec_prune_tree(desc: PruneDesc, tokens, tree_parent, n_nodes, early_logits,
         _ptr(keep_map, i32, "keep_map"), _ptr(tokens_out, i32, "tokens_out"),
         _ptr(parent_out, i32, "parent_out"), _ptr(n_out, i32, "n_out"),
         _ptr(vparent, i32, "vparent"), _stream(stream)))
+
+
+def spec_stream_rotate_values(desc: RotateDesc, n_nodes, vb, stream=None):
+    """Stream rows of the block values := their node's values rotated by
+    e^{i eps s} (in place)."""
+    lib = load_library()
+    _check("spec_stream_rotate_values", lib.spec_stream_rotate_values(
+        ctypes.byref(desc), _ptr(n_nodes, torch.int32, "n_nodes"), _ptr(vb, name="vb"),
+        _stream(stream)))
+
+
+def spec_future_gather(o, last_node, row_offset, out, stream=None):
+    """out[b] = o[b][row_offset + last_node[b]] (o: [B][R][...])."""
+    lib = load_library()
+    B, R = o.shape[0], o.shape[1]
+    row = o[0, 0].numel()
+    _ptr(out, o.dtype, "out")
+    _check("spec_future_gather", lib.spec_future_gather(
+        B, R, row, spec_dtype(o), _ptr(o, name="o"), _ptr(last_node, torch.int32, "last_node"),
+        row_offset, _ptr(out), _stream(stream)))

@@ -154,9 +154,20 @@ class DeviceStep:
             self.lse_d = torch.zeros((B, max(Rd, 1)), dtype=torch.float32, device=dev)
             self.soft = bn.soft_desc(B, wl.Rj, Rd, wl.V, bn.spec_dtype(self.logits), wl.N,
                                      wl.path_cap, wl.temperature)
+        # stream values by rotation (SS): the block's stream V rows are
+        # rewritten from their node rows before the attention
+        self.rotate = None
+        if wl.rotation_eps is not None:
+            self.rotate = bn.RotateDesc(B, R, Hkv, d, bn.spec_dtype(self.vb), wl.gamma,
+                                        wl.rotation_eps)
+        # ConFu: the contemplate output of the last accepted node (row T + j)
+        self.future = None
+        if wl.layout == "confu":
+            self.future = torch.zeros((B, Hq, d), dtype=dt, device=dev)
         # kernel launches of one run() (see libspecverify's sources): mask 1,
-        # attention 2, accept 2 (soft: 3), commit 2
-        self.launches_per_step = 8 if wl.soft else 7
+        # attention 2, accept 2 (soft: 3), commit 2, rotation 1, gather 1
+        self.launches_per_step = (7 + (1 if wl.soft else 0) + (1 if self.rotate else 0) +
+                                  (1 if self.future is not None else 0))
 
     # the four calls ---------------------------------------------------------
     def mask_build(self, stream=None):
@@ -185,11 +196,23 @@ class DeviceStep:
         bn.kv_commit(self.cache, self.kb, self.vb, self.path, self.acc_len, self.seq_len,
                      self.free_pages, self.free_head, stream)
 
+    def rotate_values(self, stream=None):
+        if self.rotate is not None:
+            bn.spec_stream_rotate_values(self.rotate, self.n_nodes, self.vb, stream)
+
+    def gather_future(self, stream=None):
+        if self.future is not None:
+            bn.spec_future_gather(self.o, self.last_node, self.wl.N, self.future, stream)
+
     def run(self, stream=None):
-        """One whole verification step (mask, attention, accept, commit)."""
+        """One whole verification step (mask, attention, accept, commit; the
+        stream-value rotation first and the ConFu future gather after the
+        acceptance where the workload has them)."""
+        self.rotate_values(stream)
         self.mask_build(stream)
         self.verify_attn(stream)
         self.accept_step(stream)
+        self.gather_future(stream)
         self.commit(stream)
 
     def reset_state(self, page_table: bool = False):

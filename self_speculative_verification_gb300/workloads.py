@@ -62,6 +62,11 @@ CONFIGS = {
     "ss_soft": dict(mode="ss", B=32, Hq=32, Hkv=32, d=128, dtype="bf16",
                     seq=("uniform", 128, 1024), T=16, gamma=3, branch=4,
                     V=50272, paged=False, soft=True, temperature=1.0),
+    # the SS workload with stream values by rotation ("Speculative Streaming"
+    # Eq. 7): eps at the page's upper bound pi / (2N), N = max sequence + streams
+    "ss_rot": dict(mode="ss", B=32, Hq=32, Hkv=32, d=128, dtype="bf16",
+                   seq=("uniform", 128, 1024), T=16, gamma=3, branch=4,
+                   V=50272, paged=False, value_rotation=True),
     "long_paged": dict(mode="la", B=64, Hq=32, Hkv=8, d=128, dtype="bf16",
                        seq=("uniform", 16384, 32768), k_choices=(8,), R=8,
                        V=32000, paged=True),
@@ -152,6 +157,9 @@ class Workload:
     u_accept: Optional[np.ndarray] = None         # float32 [B][N]
     u_sample: Optional[np.ndarray] = None         # float32 [B]
     temperature: float = 1.0
+    # stream values by rotation (SS layout): angle per stream index, or None
+    rotation_eps: Optional[float] = None
+    gamma: int = 0
     # contiguous cache capacity / paged bookkeeping
     max_seq: int = 0
     page_size: int = PAGE_SIZE
@@ -592,6 +600,10 @@ def make_workload(name: str, seed: int = 0, *, B=None, seq=None, V=None,
         node_depth=node_depth, **soft,
     )
     wl.max_seq = int(seq_len.max()) + R if B else R
+    if layout == "ss":
+        wl.gamma = gamma
+        if cfg.get("value_rotation"):
+            wl.rotation_eps = math.pi / (2.0 * (wl.max_seq + gamma))
     if page_size is not None:
         wl.page_size = page_size
     if wl.paged:

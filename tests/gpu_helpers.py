@@ -56,6 +56,15 @@ def check_mask(ds: DeviceStep):
     return vis, valid, sees
 
 
+def block_values(wl):
+    """The block V the attention sees: the generator's, with the stream rows
+    rotated when the workload has stream values by rotation (SS Eq. 7)."""
+    if wl.rotation_eps is None:
+        return wl.vb
+    rot = oracle.rotate_stream_values(wl.vb, wl.n_nodes, wl.gamma, wl.rotation_eps)
+    return W.round_bf16(rot.astype(np.float32)) if wl.dtype == "bf16" else rot
+
+
 def oracle_attention(wl, vis, valid, sees, requests=None, heads=None):
     pk, pv = [], []
     for b in range(wl.B):
@@ -65,7 +74,7 @@ def oracle_attention(wl, vis, valid, sees, requests=None, heads=None):
             k = v = np.zeros((wl.Hkv, 0, wl.d), dtype=np.float32)
         pk.append(k)
         pv.append(v)
-    return oracle.verify_attention(wl.q, pk, pv, wl.kb, wl.vb, vis, valid, sees,
+    return oracle.verify_attention(wl.q, pk, pv, wl.kb, block_values(wl), vis, valid, sees,
                                    soft_k=wl.soft_k, soft_v=wl.soft_v,
                                    requests=requests, heads=heads)
 
@@ -254,4 +263,9 @@ def run_and_check(wl, split_tokens=0, requests=None, heads=None):
     errs = check_attention(ds, O_ref, L_ref, requests, heads)
     acc, paths = check_accept(ds)
     check_commit(ds, before_k, before_v, paths)
+    if ds.future is not None:
+        # ConFu hand-off: bit-identical to the contemplate row of the last node
+        want = oracle.future_gather(ds.o.cpu().float().numpy(), ds.last_node.cpu().numpy(),
+                                    wl.N)
+        assert np.array_equal(ds.future.cpu().float().numpy(), want)
     return ds, errs

@@ -34,7 +34,8 @@ def test_header_declares_the_boundary():
     for n in ("spec_mask_build", "spec_verify_attn", "spec_verify_attn_workspace_size",
               "spec_vocab_reduce", "spec_accept", "kv_commit", "spec_get_status",
               "spec_version", "spec_status_string", "spec_la_prefill_attn",
-              "spec_accept_soft", "spec_draft_tree", "spec_prune_tree"):
+              "spec_accept_soft", "spec_draft_tree", "spec_prune_tree",
+              "spec_stream_rotate_values", "spec_future_gather"):
         assert n in names
     assert set(names) == set(binding.EXPORTS) | set(n for n in names if n not in binding.EXPORTS)
 
@@ -97,6 +98,7 @@ int main(void) {
   printf("spec_soft_desc %zu\n", sizeof(spec_soft_desc));
   printf("spec_draft_desc %zu\n", sizeof(spec_draft_desc));
   printf("spec_prune_desc %zu\n", sizeof(spec_prune_desc));
+  printf("spec_rotate_desc %zu\n", sizeof(spec_rotate_desc));
   F(spec_kv_desc, k); F(spec_kv_desc, batch); F(spec_kv_desc, page_table);
   F(spec_attn_desc, scale); F(spec_attn_desc, split_tokens);
   F(spec_accept_desc, tau); F(spec_accept_desc, path_cap);
@@ -104,6 +106,7 @@ int main(void) {
   F(spec_soft_desc, n_draft_rows); F(spec_soft_desc, path_cap); F(spec_soft_desc, temperature);
   F(spec_draft_desc, k); F(spec_draft_desc, vparent_rows);
   F(spec_prune_desc, threshold); F(spec_prune_desc, vparent_rows);
+  F(spec_rotate_desc, gamma); F(spec_rotate_desc, eps);
   return 0;
 }
 '''
@@ -122,12 +125,14 @@ int main(void) {
     assert int(out["spec_soft_desc"]) == ctypes.sizeof(binding.SoftDesc)
     assert int(out["spec_draft_desc"]) == ctypes.sizeof(binding.DraftDesc)
     assert int(out["spec_prune_desc"]) == ctypes.sizeof(binding.PruneDesc)
+    assert int(out["spec_rotate_desc"]) == ctypes.sizeof(binding.RotateDesc)
     for struct, cls in (("spec_kv_desc", binding.KvDesc), ("spec_attn_desc", binding.AttnDesc),
                         ("spec_accept_desc", binding.AcceptDesc),
                         ("spec_prefill_desc", binding.PrefillDesc),
                         ("spec_soft_desc", binding.SoftDesc),
                         ("spec_draft_desc", binding.DraftDesc),
-                        ("spec_prune_desc", binding.PruneDesc)):
+                        ("spec_prune_desc", binding.PruneDesc),
+                        ("spec_rotate_desc", binding.RotateDesc)):
         for key, val in out.items():
             if key.startswith(struct + "."):
                 field = key.split(".")[1]
