@@ -5,25 +5,30 @@
 // every original and itself, and no other lookahead position.
 //
 // Design (GB300, tcgen05):
-// * A unit is one 128-row query tile m of one (request, query head); it
-//   needs key tiles 0..m.  Units are paired (NM-1-p, p), so every work item
-//   costs NM + 1 key tiles (NM: query tiles per head), and the persistent
+// * A unit is a pair of consecutive 128-row query tiles A = 2t and
+//   B = 2t + 1 of one (request, query head); they share the K/V tiles
+//   0..2t (B also takes tile 2t + 1, its diagonal).  Units are paired
+//   (NB-1-p, p) so every work item costs about the same; the persistent
 //   grid (one CTA per SM) takes the items round-robin.  Items are numbered
 //   (request, head)-major with heads of one KV group adjacent, so the CTAs
-//   working on one KV head at a time read the same K/V tiles at about the
-//   same time and share them through L2.
-// * Warp roles: warp 4 issues TMA loads (each unit's Q tile into one of two
-//   Q buffers; K and V tiles into a five-slot ring), warp 5 issues the MMAs
-//   from one thread, warps 0-3 run the softmax with one query row per
-//   thread.
-// * S = Q K^T: both operands K-major in shared memory (128-byte swizzle),
-//   fp32 result in TMEM, double-buffered so S(t+1) is computed while the
-//   softmax works on S(t).  P (bf16) goes back to TMEM; O += P V takes P
-//   from TMEM and V (MN-major) from shared memory, accumulating in TMEM.
+//   working on one KV head at a time share its K/V tiles through L2.
+// * Warp roles: warps 0-3 run the softmax of tile A and warps 4-7 that of
+//   tile B (one query row per thread), warp 8 issues TMA loads (the unit's
+//   two Q tiles; K and V tiles into a five-slot ring), warp 9 issues the
+//   MMAs from one thread.
+// * Per tile, TMEM holds O (128 fp32 columns) and S (128 fp32 columns);
+//   P (bf16) is written over the first 64 columns of S, which the next S
+//   MMA of the same tile overwrites only after the PV MMA that reads it
+//   (tcgen05 MMAs of one thread run in issue order).  The MMA thread
+//   interleaves the tiles -- PV_A(j), S_A(j+1), PV_B(j), S_B(j+1) -- so the
+//   tensor core works on one tile while the other tile's softmax runs.
+// * Softmax of a tile row: the whole S row in registers (four TMEM loads in
+//   flight), the masked maximum, then P = exp2(s - m) written chunk by chunk.
+//   The running max is raised only when it grows by more than 2^8 (then O
+//   and l are rescaled in place); O holds every earlier PV of the tile by
+//   then, since the S MMA the softmax waits for was issued after them.
 // * The mask is evaluated only on key tiles that reach the diagonal or hold
-//   keys >= n; every other tile is wholly visible.  The running max is
-//   raised only when it grows by more than 2^8 (then O and l are rescaled
-//   in place).
+//   keys >= n; every other tile is wholly visible.
 // * Every wait is bounded; on expiry the kernel sets SPEC_DEV_TIMEOUT,
 //   stops issuing work, waits (bounded) for its own copies and MMAs, frees
 //   its TMEM and returns.
@@ -39,25 +44,38 @@ namespace {
 namespace lap {
 
 constexpr int kD = 128;                  // head_dim
-constexpr int kM = 128;                  // query rows per unit (MMA M)
+constexpr int kM = 128;                  // query rows per tile (MMA M)
 constexpr int kN = 128;                  // keys per key tile (MMA N of S)
 constexpr int kHalf = 128 * 128;         // one 128-row x 64-element bf16 box
 constexpr int kTileBytes = 2 * kHalf;    // one Q, K or V tile: 32 KB
 constexpr int kSlots = 5;                // K/V ring slots
-constexpr int kSoftmaxWarps = 4;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kThreads = 6 * 32;
+constexpr int kGroupWarps = 4;           // softmax warps per query tile
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;              // warps 10, 11 complete the third warpgroup
+constexpr int kThreads = 12 * 32;
+// Registers a thread, split by setmaxnreg: the launch gives every thread
+// kLaunchRegs (the most a 384-thread CTA can have); the two softmax
+// warpgroups raise theirs to kSoftmaxRegs and the third lowers to
+// kOtherRegs: 8 * 32 * 184 + 4 * 32 * 128 = 63488 <= 384 * 168 = 64512.
+// The split must fit the launch allocation, or the raise would wait
+// forever.
+constexpr int kLaunchRegs = 168;
+constexpr int kSoftmaxRegs = 184;
+constexpr int kOtherRegs = 128;
+static_assert(8 * 32 * kSoftmaxRegs + 4 * 32 * kOtherRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr int kTmemCols = 512;
-constexpr int kColO = 0;                 // O: columns [0, 128)
-constexpr int kColS = 128;               // S buffer b: [128 + 128 b, 256 + 128 b)
-constexpr int kColP = 384;               // P buffer b: [384 + 64 b, 448 + 64 b), bf16 pairs
+// TMEM columns of tile x (0 = A, 1 = B): O at [256 x, 256 x + 128), S at
+// [256 x + 128, 256 x + 256), P over the first 64 columns of S
+__host__ __device__ constexpr uint32_t col_o(int x) { return 256u * (uint32_t)x; }
+__host__ __device__ constexpr uint32_t col_s(int x) { return 256u * (uint32_t)x + 128u; }
 constexpr float kRescale = 8.f;          // log2 growth allowed before rescaling
 
 struct Params {
     int B, L, n;          // requests, positions per request (n + k), originals
     int Hq, Hkv, G;       // query heads, KV heads, Hq / Hkv
-    int NM, NP, n_items;  // query tiles per head, items per head, total items
+    int NM, NB, NP;       // query tiles, tile pairs, items per head
+    int n_items;
     float scale_log2;     // softmax scale * log2(e)
     __nv_bfloat16 *o;
     float *lse;
@@ -65,10 +83,9 @@ struct Params {
 };
 
 struct Shared {
-    uint64_t q_full[2], q_empty[2];
+    uint64_t q_full, q_empty;
     uint64_t full[kSlots], empty[kSlots];
-    uint64_t s_full[2], p_full[2], o_upd[2];
-    uint64_t o_free;
+    uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -77,17 +94,50 @@ struct Shared {
 constexpr size_t kSmemBytes = 2 * (size_t)kTileBytes + kSlots * (size_t)kTileBytes +
                               sizeof(Shared) + 1024;
 
+// Unit: query tiles 2t (A) and 2t + 1 (B, if it exists) of (b, hq).
 struct Unit {
-    int b, hq, m;
+    int b, hq, t;
 };
 
-// The units of item w: query tiles NM-1-p and p of one (request, head).
 __device__ __forceinline__ int units_of(const Params &P, int w, Unit (&u)[2]) {
     const int bh = w / P.NP, p = w % P.NP;
     const int b = bh / P.Hq, hq = bh % P.Hq;
-    u[0] = Unit{b, hq, P.NM - 1 - p};
+    u[0] = Unit{b, hq, P.NB - 1 - p};
     u[1] = Unit{b, hq, p};
-    return (P.NM - 1 - p == p) ? 1 : 2;
+    return (P.NB - 1 - p == p) ? 1 : 2;
+}
+
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// packed pairs of fp32 for the f32x2 arithmetic
+__device__ __forceinline__ uint64_t pair(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpair(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// last key tile of query tile X of unit t, or -1 if the tile does not exist
+__device__ __forceinline__ int last_tile(const Params &P, int t, int X) {
+    const int m = 2 * t + X;
+    return m < P.NM ? m : -1;
 }
 
 }  // namespace lap
@@ -100,7 +150,7 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *qbuf = smem;                          // 2 Q tiles
+    uint8_t *qbuf = smem;                          // Q tiles A and B
     uint8_t *ring = smem + 2 * kTileBytes;         // kSlots K / V tiles
     Shared &sh = *reinterpret_cast<Shared *>(ring + kSlots * kTileBytes);
 
@@ -113,18 +163,18 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
                          : "memory");
     }
     if (threadIdx.x == 0) {
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&sh.q_full[b], 1);
-            mbar_init(&sh.q_empty[b], 1);
-            mbar_init(&sh.s_full[b], 1);
-            mbar_init(&sh.p_full[b], kSoftmaxWarps);
-            mbar_init(&sh.o_upd[b], 1);
+        mbar_init(&sh.q_full, 1);
+        mbar_init(&sh.q_empty, 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&sh.s_full[x], 1);
+            mbar_init(&sh.p_full[x], kGroupWarps);
+            mbar_init(&sh.o_done[x], 1);
+            mbar_init(&sh.o_free[x], kGroupWarps);
         }
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(&sh.full[s], 1);
             mbar_init(&sh.empty[s], 1);
         }
-        mbar_init(&sh.o_free, kSoftmaxWarps);
         mbar_init(&sh.drain, 1);
         sh.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -142,255 +192,292 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
     const uint32_t tmem = sh.tmem_base;
     volatile int *abort = &sh.abort;
 
-    if (warp == kProducerWarp) {
-        // ------------------------------------------------------ producer
-        if (lane == 0) {
-            const uint64_t pol_q = policy_evict_first();
-            const uint64_t pol_kv = policy_evict_last();
-            long long ld = 0;          // K/V loads issued
-            int nq = 0;                // Q loads issued
-            bool ok = true;
-            for (int w = blockIdx.x; w < P.n_items && ok; w += gridDim.x) {
-                Unit u[2];
-                const int nu = units_of(P, w, u);
-                for (int s = 0; s < nu && ok; ++s) {
-                    const Unit &U = u[s];
-                    const int qb = nq & 1;
-                    if (*abort || !mbar_wait(&sh.q_empty[qb], (uint32_t)(((nq >> 1) & 1) ^ 1))) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&sh.q_full[qb], (uint32_t)kTileBytes);
-                    for (int hh = 0; hh < 2; ++hh)
-                        tma_load_4d(qbuf + qb * kTileBytes + hh * kHalf, &mq, hh * 64, U.hq,
-                                    U.m * kM, U.b, &sh.q_full[qb], pol_q);
-                    ++nq;
-                    const int hk = U.hq / P.G;
-                    for (int j = 0; j <= U.m && ok; ++j) {
-                        for (int kv = 0; kv < 2; ++kv) {
-                            const int slot = (int)(ld % kSlots);
-                            if (*abort ||
-                                !mbar_wait(&sh.empty[slot], (uint32_t)(((ld / kSlots) & 1) ^ 1))) {
-                                ok = false;
-                                break;
-                            }
-                            mbar_arrive_expect_tx(&sh.full[slot], (uint32_t)kTileBytes);
+    if (warp >= kProducerWarp) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
+        if (warp == kProducerWarp) {
+            // ------------------------------------------------------ producer
+            if (lane == 0) {
+                const uint64_t pol_q = policy_evict_first();
+                const uint64_t pol_kv = policy_evict_last();
+                long long ld = 0;          // K/V loads issued
+                int nu = 0;                // units (Q loads) issued
+                bool ok = true;
+                for (int w = blockIdx.x; w < P.n_items && ok; w += gridDim.x) {
+                    Unit u[2];
+                    const int nus = units_of(P, w, u);
+                    for (int s = 0; s < nus && ok; ++s) {
+                        const Unit &U = u[s];
+                        const int mA = last_tile(P, U.t, 0), mB = last_tile(P, U.t, 1);
+                        const int jmax = mB >= 0 ? mB : mA;
+                        if (*abort || !mbar_wait(&sh.q_empty, (uint32_t)((nu & 1) ^ 1))) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&sh.q_full, (uint32_t)(mB >= 0 ? 2 : 1) * kTileBytes);
+                        for (int x = 0; x < (mB >= 0 ? 2 : 1); ++x)
                             for (int hh = 0; hh < 2; ++hh)
-                                tma_load_4d(ring + slot * kTileBytes + hh * kHalf, kv ? &mv : &mk,
-                                            hh * 64, hk, j * kN, U.b, &sh.full[slot], pol_kv);
-                            ++ld;
+                                tma_load_4d(qbuf + x * kTileBytes + hh * kHalf, &mq, hh * 64, U.hq,
+                                            (2 * U.t + x) * kM, U.b, &sh.q_full, pol_q);
+                        ++nu;
+                        const int hk = U.hq / P.G;
+                        for (int j = 0; j <= jmax && ok; ++j) {
+                            for (int kv = 0; kv < 2; ++kv) {
+                                const int slot = (int)(ld % kSlots);
+                                if (*abort ||
+                                    !mbar_wait(&sh.empty[slot], (uint32_t)(((ld / kSlots) & 1) ^ 1))) {
+                                    ok = false;
+                                    break;
+                                }
+                                mbar_arrive_expect_tx(&sh.full[slot], (uint32_t)kTileBytes);
+                                for (int hh = 0; hh < 2; ++hh)
+                                    tma_load_4d(ring + slot * kTileBytes + hh * kHalf, kv ? &mv : &mk,
+                                                hh * 64, hk, j * kN, U.b, &sh.full[slot], pol_kv);
+                                ++ld;
+                            }
                         }
                     }
                 }
-            }
-            if (!ok) {
-                raise_status(P.status, SPEC_DEV_TIMEOUT);
-                *abort = 1;
-            }
-            // do not leave while copies into this CTA's shared memory are in
-            // flight (earlier loads were consumed, hence complete)
-            for (long long i = ld - 1; i >= 0 && i >= ld - kSlots; --i)
-                if (!mbar_wait(&sh.full[i % kSlots], (uint32_t)((i / kSlots) & 1))) {
+                if (!ok) {
                     raise_status(P.status, SPEC_DEV_TIMEOUT);
-                    break;
+                    *abort = 1;
                 }
-            for (int i = nq - 1; i >= 0 && i >= nq - 2; --i)
-                if (!mbar_wait(&sh.q_full[i & 1], (uint32_t)((i >> 1) & 1))) {
-                    raise_status(P.status, SPEC_DEV_TIMEOUT);
-                    break;
-                }
-        }
-    } else if (warp == kMmaWarp) {
-        // --------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            const uint32_t id_s = idesc(kM, kN, false, false);
-            const uint32_t id_pv = idesc(kM, kD, false, true);
-            long long k = 0, ld = 0;   // key tiles processed, K/V loads consumed
-            int un = 0;                // units started
-            bool ok = true;
-            // PV of the previous key tile: its V slot / load index, whether
-            // it starts its unit, and that unit's number
-            long long pv_ld = 0;
-            bool pv_first = false;
-            int pv_un = 0;
-            auto issue_pv = [&](long long t) -> bool {
-                const int b = (int)(t & 1);
-                const int vslot = (int)(pv_ld % kSlots);
-                if (!mbar_wait(&sh.p_full[b], (uint32_t)((t >> 1) & 1))) return false;
-                if (!mbar_wait(&sh.full[vslot], (uint32_t)((pv_ld / kSlots) & 1))) return false;
-                // a unit's first PV overwrites O: the previous unit's
-                // epilogue must have read it
-                if (pv_first && pv_un > 0 &&
-                    !mbar_wait(&sh.o_free, (uint32_t)((pv_un - 1) & 1)))
-                    return false;
-                fence_after();
-                const uint64_t vd = smem_desc(smem_u32(ring + vslot * kTileBytes), kHalf, 1024);
-                const uint32_t a_p = tmem + kColP + (uint32_t)b * (kN / 2);
-#pragma unroll
-                for (int ks = 0; ks < kN / 16; ++ks)
-                    mma(tmem + kColO, a_p + ks * 8, vd + (uint64_t)((ks * 2048) >> 4), id_pv,
-                        (ks > 0 || !pv_first) ? 1u : 0u);
-                commit(&sh.o_upd[b]);
-                commit(&sh.empty[vslot]);
-                return true;
-            };
-            for (int w = blockIdx.x; w < P.n_items && ok; w += gridDim.x) {
-                Unit u[2];
-                const int nu = units_of(P, w, u);
-                for (int s = 0; s < nu && ok; ++s, ++un) {
-                    const int m = u[s].m;
-                    const int qb = un & 1;
-                    if (*abort || !mbar_wait(&sh.q_full[qb], (uint32_t)((un >> 1) & 1))) {
-                        ok = false;
+                // do not leave while copies into this CTA's shared memory are in
+                // flight (earlier loads were consumed, hence complete)
+                for (long long i = ld - 1; i >= 0 && i >= ld - kSlots; --i)
+                    if (!mbar_wait(&sh.full[i % kSlots], (uint32_t)((i / kSlots) & 1))) {
+                        raise_status(P.status, SPEC_DEV_TIMEOUT);
                         break;
                     }
-                    const uint64_t qd = smem_desc(smem_u32(qbuf + qb * kTileBytes), 16, 1024);
-                    for (int j = 0; j <= m; ++j) {
-                        const int kslot = (int)(ld % kSlots);
+                if (nu > 0 && !mbar_wait(&sh.q_full, (uint32_t)((nu - 1) & 1)))
+                    raise_status(P.status, SPEC_DEV_TIMEOUT);
+            }
+        } else if (warp == kMmaWarp) {
+            // --------------------------------------------------- MMA issuer
+            if (lane == 0) {
+                const uint32_t id_s = idesc(kM, kN, false, false);
+                const uint32_t id_pv = idesc(kM, kD, false, true);
+                long long ld = 0;              // K/V loads consumed
+                int nu = 0;                    // units started
+                int np[2] = {0, 0};            // P hand-offs taken, per tile
+                int nact[2] = {0, 0};          // units in which the tile took part
+                bool ok = true;
+                const uint64_t qd[2] = {smem_desc(smem_u32(qbuf), 16, 1024),
+                                        smem_desc(smem_u32(qbuf + kTileBytes), 16, 1024)};
+                auto issue_s = [&](int x, int kslot) {
+                    const uint64_t kd = smem_desc(smem_u32(ring + kslot * kTileBytes), 16, 1024);
+    #pragma unroll
+                    for (int ks = 0; ks < kD / 16; ++ks) {
+                        const uint64_t off = (uint64_t)((((ks >> 2) * kHalf) + (ks & 3) * 32) >> 4);
+                        mma_ss(tmem + col_s(x), qd[x] + off, kd + off, id_s, ks > 0 ? 1u : 0u);
+                    }
+                    commit(&sh.s_full[x]);
+                };
+                // O_x += P_x V(j); the tile's first PV of a unit overwrites O_x,
+                // after the previous unit's epilogue of that tile read it
+                auto issue_pv = [&](int x, int vslot, bool first) -> bool {
+                    if (!mbar_wait(&sh.p_full[x], (uint32_t)(np[x] & 1))) return false;
+                    ++np[x];
+                    if (first && nact[x] > 0 &&
+                        !mbar_wait(&sh.o_free[x], (uint32_t)((nact[x] - 1) & 1)))
+                        return false;
+                    fence_after();
+                    const uint64_t vd = smem_desc(smem_u32(ring + vslot * kTileBytes), kHalf, 1024);
+    #pragma unroll
+                    for (int ks = 0; ks < kN / 16; ++ks)
+                        mma(tmem + col_o(x), tmem + col_s(x) + ks * 8,
+                            vd + (uint64_t)((ks * 2048) >> 4), id_pv, (ks > 0 || !first) ? 1u : 0u);
+                    return true;
+                };
+                for (int w = blockIdx.x; w < P.n_items && ok; w += gridDim.x) {
+                    Unit u[2];
+                    const int nus = units_of(P, w, u);
+                    for (int s = 0; s < nus && ok; ++s, ++nu) {
+                        const int m[2] = {last_tile(P, u[s].t, 0), last_tile(P, u[s].t, 1)};
+                        const int jmax = m[1] >= 0 ? m[1] : m[0];
+                        if (*abort || !mbar_wait(&sh.q_full, (uint32_t)(nu & 1))) {
+                            ok = false;
+                            break;
+                        }
+                        // S(0) of both tiles
+                        int kslot = (int)(ld % kSlots);
                         if (!mbar_wait(&sh.full[kslot], (uint32_t)((ld / kSlots) & 1))) {
                             ok = false;
                             break;
                         }
                         fence_after();
-                        // S(k) = Q K^T into S buffer k % 2 (free: PV(k-2),
-                        // issued last iteration, waited for its softmax)
-                        const uint64_t kd = smem_desc(smem_u32(ring + kslot * kTileBytes), 16, 1024);
-                        const uint32_t s_col = tmem + kColS + (uint32_t)(k & 1) * kN;
-#pragma unroll
-                        for (int ks = 0; ks < kD / 16; ++ks) {
-                            const uint64_t off = (uint64_t)((((ks >> 2) * kHalf) + (ks & 3) * 32) >> 4);
-                            mma_ss(s_col, qd + off, kd + off, id_s, ks > 0 ? 1u : 0u);
-                        }
-                        commit(&sh.s_full[k & 1]);
+                        for (int x = 0; x < 2; ++x)
+                            if (m[x] >= 0) issue_s(x, kslot);
                         commit(&sh.empty[kslot]);
-                        if (j == m) commit(&sh.q_empty[qb]);
-                        if (k > 0 && !issue_pv(k - 1)) {
-                            ok = false;
-                            break;
-                        }
-                        pv_ld = ld + 1;
-                        pv_first = j == 0;
-                        pv_un = un;
-                        ld += 2;
-                        ++k;
-                    }
-                }
-            }
-            if (ok && k > 0) ok = issue_pv(k - 1);
-            if (!ok) {
-                raise_status(P.status, SPEC_DEV_TIMEOUT);
-                *abort = 1;
-            }
-            // every MMA issued above has completed before TMEM is released
-            commit(&sh.drain);
-            if (!mbar_wait(&sh.drain, 0)) raise_status(P.status, SPEC_DEV_TIMEOUT);
-        }
-    } else {
-        // ------------------------------------------------------ softmax
-        const int r = warp * 32 + lane;                 // row of the query tile
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        const float sc = P.scale_log2;
-        long long k = 0;
-        bool ok = true;
-        for (int w = blockIdx.x; w < P.n_items && ok; w += gridDim.x) {
-            Unit u[2];
-            const int nu = units_of(P, w, u);
-            for (int s = 0; s < nu && ok; ++s) {
-                const Unit &U = u[s];
-                const int i = U.m * kM + r;              // this thread's position
-                float m_used = -INFINITY, l = 0.f;
-                for (int j = 0; j <= U.m; ++j, ++k) {
-                    if (*abort || !mbar_wait(&sh.s_full[k & 1], (uint32_t)((k >> 1) & 1))) {
-                        ok = false;
-                        break;
-                    }
-                    fence_after();
-                    float x[kN];
-                    {
-                        const uint32_t sa = tmem + lane_base + kColS + (uint32_t)(k & 1) * kN;
-#pragma unroll
-                        for (int c = 0; c < kN / 32; ++c) {
-                            uint32_t v[32];
-                            ld32(sa + c * 32, v);
-                            wait_ld();
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[e]);
-                        }
-                    }
-                    // key c is visible iff c <= i and (c < n or c == i)
-                    if (j == U.m || (j + 1) * kN > P.n) {
-                        const int c0 = j * kN;
-#pragma unroll
-                        for (int e = 0; e < kN; ++e) {
-                            const int c = c0 + e;
-                            const bool vis = c <= i && (c < P.n || c == i);
-                            x[e] = vis ? x[e] : -INFINITY;
-                        }
-                    }
-                    float tmv[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) tmv[e] = -INFINITY;
-#pragma unroll
-                    for (int e = 0; e < kN; ++e) tmv[e & 7] = fmaxf(tmv[e & 7], x[e]);
-                    const float traw = fmaxf(fmaxf(fmaxf(tmv[0], tmv[1]), fmaxf(tmv[2], tmv[3])),
-                                             fmaxf(fmaxf(tmv[4], tmv[5]), fmaxf(tmv[6], tmv[7])));
-                    const float tm = traw == -INFINITY ? -INFINITY : traw * sc;
-                    // raise the reference max only when it grew by more than 2^8
-                    if (tm > m_used + kRescale || (m_used == -INFINITY && tm != -INFINITY)) {
-                        const float alpha = (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - tm);
-                        if (j > 0 && m_used != -INFINITY) {
-                            // O holds PV(k-1): wait for it, then scale this row
-                            if (!mbar_wait(&sh.o_upd[(k - 1) & 1], (uint32_t)(((k - 1) >> 1) & 1))) {
+                        if (jmax == 0) commit(&sh.q_empty);
+                        ++ld;
+                        for (int j = 0; j <= jmax && ok; ++j) {
+                            const int vslot = (int)(ld % kSlots);
+                            if (!mbar_wait(&sh.full[vslot], (uint32_t)((ld / kSlots) & 1))) {
                                 ok = false;
                                 break;
                             }
+                            ++ld;
+                            const bool next = j + 1 <= jmax;
+                            if (next) {
+                                kslot = (int)(ld % kSlots);
+                                if (!mbar_wait(&sh.full[kslot], (uint32_t)((ld / kSlots) & 1))) {
+                                    ok = false;
+                                    break;
+                                }
+                            }
                             fence_after();
+                            for (int x = 0; x < 2 && ok; ++x) {
+                                if (m[x] < 0 || j > m[x]) continue;
+                                if (!issue_pv(x, vslot, j == 0)) {
+                                    ok = false;
+                                    break;
+                                }
+                                if (j == m[x]) commit(&sh.o_done[x]);
+                                if (x == 1) commit(&sh.empty[vslot]);
+                                if (next && j + 1 <= m[x]) issue_s(x, kslot);
+                            }
+                            if (!ok) break;
+                            if (m[1] < 0 || j > m[1]) commit(&sh.empty[vslot]);
+                            if (next) {
+                                commit(&sh.empty[kslot]);
+                                if (j + 1 == jmax) commit(&sh.q_empty);
+                                ++ld;
+                            }
+                        }
+                        for (int x = 0; x < 2; ++x)
+                            if (m[x] >= 0) ++nact[x];
+                    }
+                }
+                if (!ok) {
+                    raise_status(P.status, SPEC_DEV_TIMEOUT);
+                    *abort = 1;
+                }
+                // every MMA issued above has completed before TMEM is released
+                commit(&sh.drain);
+                if (!mbar_wait(&sh.drain, 0)) raise_status(P.status, SPEC_DEV_TIMEOUT);
+            }
+        }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
+        // ------------------------------------------------------ softmax
+        const int x = warp / kGroupWarps;               // query tile A (0) or B (1)
+        const int r = (warp % kGroupWarps) * 32 + lane; // row of the tile
+        const uint32_t lane_base = (uint32_t)((warp % kGroupWarps) * 32) << 16;
+        const uint32_t tS = tmem + lane_base + col_s(x), tO = tmem + lane_base + col_o(x);
+        const float sc = P.scale_log2;
+        int ns = 0, nact = 0;      // S hand-offs taken; units this tile took part in
+        bool ok = true;
+        for (int w = blockIdx.x; w < P.n_items && ok; w += gridDim.x) {
+            Unit u[2];
+            const int nus = units_of(P, w, u);
+            for (int s = 0; s < nus && ok; ++s) {
+                const Unit &U = u[s];
+                const int mX = last_tile(P, U.t, x);
+                if (mX < 0) continue;
+                const int i = mX * kM + r;               // this thread's position
+                float m_used = -INFINITY, l = 0.f;
+                for (int j = 0; j <= mX; ++j) {
+                    if (*abort || !mbar_wait(&sh.s_full[x], (uint32_t)(ns & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    ++ns;
+                    fence_after();
+                    const bool masked = j == mX || (j + 1) * kN > P.n;
+                    const int c0 = j * kN;
+                    // visibility of keys lo .. lo + 31 for this row: key c is
+                    // visible iff c <= i and (c < n or c == i)
+                    auto vis_bits = [&](int lo) -> uint32_t {
+                        if (!masked) return 0xffffffffu;
+                        const int di = i - lo, dn = P.n - lo;
+                        const uint32_t le = di < 0 ? 0u : di >= 31 ? 0xffffffffu
+                                                                   : (2u << di) - 1u;
+                        const uint32_t lt = dn <= 0 ? 0u : dn >= 32 ? 0xffffffffu
+                                                                    : (1u << dn) - 1u;
+                        const uint32_t self = (di >= 0 && di < 32) ? (1u << di) : 0u;
+                        return (le & lt) | self;
+                    };
+                    // the S row: four TMEM loads in flight, one wait (each
+                    // wait_ld ties its registers; the later ones return at once)
+                    uint32_t v[kN / 32][32];
 #pragma unroll
-                            for (int c32 = 0; c32 < kD / 32; ++c32) {
-                                uint32_t v[32];
-                                const uint32_t oa = tmem + lane_base + kColO + c32 * 32;
-                                ld32(oa, v);
-                                wait_ld();
+                    for (int c = 0; c < kN / 32; ++c) ld32(tS + c * 32, v[c]);
+#pragma unroll
+                    for (int c = 0; c < kN / 32; ++c) wait_ld(v[c]);
+                    // masked tiles: invisible scores become -inf in place
+                    if (masked) {
+#pragma unroll
+                        for (int c = 0; c < kN / 32; ++c) {
+                            const uint32_t vm = vis_bits(c0 + c * 32);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                v[c][e] = ((vm >> e) & 1u) ? v[c][e] : 0xff800000u;
+                        }
+                    }
+                    // the row maximum (three-input max, four chains)
+                    float tmv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                    for (int c = 0; c < kN / 32; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; e += 8)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                tmv[q] = max3(tmv[q], __uint_as_float(v[c][e + 2 * q]),
+                                              __uint_as_float(v[c][e + 2 * q + 1]));
+                    const float traw = fmaxf(fmaxf(tmv[0], tmv[1]), fmaxf(tmv[2], tmv[3]));
+                    const float tm = traw == -INFINITY ? -INFINITY : traw * sc;
+                    if (tm > m_used + kRescale || (m_used == -INFINITY && tm != -INFINITY)) {
+                        const float alpha = (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - tm);
+                        if (j > 0 && m_used != -INFINITY) {
+                            // O holds every earlier PV of this tile (issued
+                            // before the S just waited for): rescale it
+#pragma unroll 1
+                            for (int c = 0; c < kD / 32; ++c) {
+                                uint32_t o[32];
+                                ld32(tO + c * 32, o);
+                                wait_ld(o);
 #pragma unroll
                                 for (int e = 0; e < 32; ++e)
-                                    v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                                st32(oa, v);
+                                    o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                                st32(tO + c * 32, o);
                             }
-                            wait_st();
                         }
                         l *= alpha;
                         m_used = tm;
                     }
                     const float mu = m_used == -INFINITY ? 0.f : m_used;
-                    // P buffer k % 2 was last read by PV(k-2)
-                    if (k >= 2 && !mbar_wait(&sh.o_upd[k & 1], (uint32_t)(((k - 2) >> 1) & 1))) {
-                        ok = false;
-                        break;
-                    }
-                    float rsv[8];
+                    // P = exp2(s * scale - mu) (pairs: one f32x2 FMA, two ex2,
+                    // one f32x2 add, one pack) over the first 64 columns of S
+                    const uint64_t sc2 = pair(sc, sc), nmu2 = pair(-mu, -mu);
+                    uint64_t rs2[2] = {pair(0.f, 0.f), pair(0.f, 0.f)};
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) rsv[e] = 0.f;
+                    for (int c = 0; c < kN / 32; ++c) {
+                        uint32_t pw[16];
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t pw[32];
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const float p0 = fast_exp2(fmaf(x[h * 64 + 2 * e], sc, -mu));
-                            const float p1 = fast_exp2(fmaf(x[h * 64 + 2 * e + 1], sc, -mu));
-                            rsv[e & 7] += p0 + p1;
+                        for (int e = 0; e < 16; ++e) {
+                            float t0, t1;
+                            unpair(fma2(pair(__uint_as_float(v[c][2 * e]),
+                                             __uint_as_float(v[c][2 * e + 1])),
+                                        sc2, nmu2),
+                                   t0, t1);
+                            const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+                            rs2[e & 1] = add2(rs2[e & 1], pair(p0, p1));
                             pw[e] = pack_bf16(p0, p1);
                         }
-                        st32(tmem + lane_base + kColP + (uint32_t)(k & 1) * (kN / 2) + h * 32, pw);
+                        st16(tS + c * 16, pw);
                     }
-                    l += ((rsv[0] + rsv[1]) + (rsv[2] + rsv[3])) + ((rsv[4] + rsv[5]) + (rsv[6] + rsv[7]));
+                    float rs[4];
+                    unpair(rs2[0], rs[0], rs[1]);
+                    unpair(rs2[1], rs[2], rs[3]);
+                    l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
                     wait_st();
                     fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&sh.p_full[k & 1]);
+                    if (lane == 0) mbar_arrive(&sh.p_full[x]);
                 }
                 if (!ok) break;
                 // epilogue: O / l (bf16) and the LSE of this row
-                if (!mbar_wait(&sh.o_upd[(k - 1) & 1], (uint32_t)(((k - 1) >> 1) & 1))) {
+                if (!mbar_wait(&sh.o_done[x], (uint32_t)(nact & 1))) {
                     ok = false;
                     break;
                 }
@@ -399,15 +486,15 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
                 const float inv = l > 0.f ? 1.f / l : 0.f;
                 uint4 *dst = reinterpret_cast<uint4 *>(
                     P.o + (((size_t)U.b * P.L + (row_ok ? i : 0)) * P.Hq + U.hq) * kD);
-#pragma unroll
-                for (int c32 = 0; c32 < kD / 32; ++c32) {
+#pragma unroll 1
+                for (int c = 0; c < kD / 32; ++c) {
                     uint32_t v[32];
-                    ld32(tmem + lane_base + kColO + c32 * 32, v);
-                    wait_ld();
+                    ld32(tO + c * 32, v);
+                    wait_ld(v);
                     if (!row_ok) continue;
 #pragma unroll
                     for (int e = 0; e < 32; e += 8)
-                        dst[(c32 * 32 + e) / 8] = make_uint4(
+                        dst[(c * 32 + e) / 8] = make_uint4(
                             pack_bf16(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv),
                             pack_bf16(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv),
                             pack_bf16(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv),
@@ -418,7 +505,8 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
                         l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
                 fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.o_free);
+                if (lane == 0) mbar_arrive(&sh.o_free[x]);
+                ++nact;
             }
         }
         if (!ok) {
@@ -482,7 +570,8 @@ extern "C" spec_status_t spec_la_prefill_attn(const spec_prefill_desc *desc, con
     P.Hkv = Hkv;
     P.G = Hq / Hkv;
     P.NM = (int)ceil_div_ll(L, lap::kM);
-    P.NP = (P.NM + 1) / 2;
+    P.NB = (P.NM + 1) / 2;
+    P.NP = (P.NB + 1) / 2;
     const long long items = (long long)B * Hq * P.NP;
     if (items > 0x7fffffffll) return SPEC_ERR_UNSUPPORTED;
     P.n_items = (int)items;
