@@ -1062,36 +1062,43 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                 if (!mbar_wait(&sh.s_full[k & 1], (uint32_t)((k >> 1) & 1))) { ok = false; break; }
                 fence_after();
                 if (warp_rows) {
-                    float x[kTile];
+                    // the S row: both TMEM loads in flight, one wait
+                    uint32_t v[2][32];
                     {
-                        uint32_t v[32];
                         const uint32_t sa = tmem + lane_base + kColS + (uint32_t)(k & 1) * kTile;
-                        ld32(sa, v);
-                        wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(v[e]);
-                        ld32(sa + 32, v);
-                        wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) x[32 + e] = __uint_as_float(v[e]);
+                        ld32(sa, v[0]);
+                        ld32(sa + 32, v[1]);
+                        wait_ld(v[0]);
+                        wait_ld(v[1]);
                     }
-                    // columns this row sees in this tile, as one 64-bit mask
+                    // columns this row sees in this tile, as one 64-bit mask;
+                    // the others become -inf in place
                     const uint64_t valid_cols =
                         ti.nvalid >= kTile ? ~0ull : ((1ull << ti.nvalid) - 1ull);
                     uint64_t vm;
                     if (ti.kind == kPrefix) vm = rvalid ? valid_cols : 0ull;
                     else if (ti.kind == kSoft) vm = rsoft ? valid_cols : 0ull;
                     else vm = vmask & valid_cols;
-                    float tmv[8];
+                    if (vm != ~0ull) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) tmv[e] = -INFINITY;
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t hm = (uint32_t)(vm >> (32 * h));
 #pragma unroll
-                    for (int e = 0; e < kTile; ++e) {
-                        x[e] = ((vm >> e) & 1ull) ? x[e] * sc : -INFINITY;
-                        tmv[e & 7] = fmaxf(tmv[e & 7], x[e]);
+                            for (int e = 0; e < 32; ++e)
+                                v[h][e] = ((hm >> e) & 1u) ? v[h][e] : 0xff800000u;
+                        }
                     }
-                    const float tm = fmaxf(fmaxf(fmaxf(tmv[0], tmv[1]), fmaxf(tmv[2], tmv[3])),
-                                           fmaxf(fmaxf(tmv[4], tmv[5]), fmaxf(tmv[6], tmv[7])));
+                    float tmv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int e = 0; e < 32; e += 8)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                tmv[q] = max3(tmv[q], __uint_as_float(v[h][e + 2 * q]),
+                                              __uint_as_float(v[h][e + 2 * q + 1]));
+                    const float traw = fmaxf(fmaxf(tmv[0], tmv[1]), fmaxf(tmv[2], tmv[3]));
+                    const float tm = traw == -INFINITY ? -INFINITY : traw * sc;
                     // raise the reference max only when it grew by more than 2^8
                     if (tm > m_used + kRescale || (m_used == -INFINITY && tm != -INFINITY)) {
                         const float alpha = (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - tm);
@@ -1104,14 +1111,14 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                             fence_after();
 #pragma unroll
                             for (int c32 = 0; c32 < D / 32; ++c32) {
-                                uint32_t v[32];
+                                uint32_t o[32];
                                 const uint32_t oa = tmem + lane_base + kColO + c32 * 32;
-                                ld32(oa, v);
-                                wait_ld();
+                                ld32(oa, o);
+                                wait_ld(o);
 #pragma unroll
                                 for (int e = 0; e < 32; ++e)
-                                    v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                                st32(oa, v);
+                                    o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                                st32(oa, o);
                             }
                             wait_st();
                         }
@@ -1124,19 +1131,29 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                         ok = false;
                         break;
                     }
-                    float rsv[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) rsv[e] = 0.f;
+                    // P = exp2(s * scale - mu): pairs by one f32x2 FMA, two ex2,
+                    // one f32x2 add and one pack
+                    const uint64_t sc2 = pair(sc, sc), nmu2 = pair(-mu, -mu);
+                    uint64_t rs2[2] = {pair(0.f, 0.f), pair(0.f, 0.f)};
                     uint32_t w[32];
 #pragma unroll
                     for (int e = 0; e < kTile / 2; ++e) {
-                        const float p0 = fast_exp2(x[2 * e] - mu);
-                        const float p1 = fast_exp2(x[2 * e + 1] - mu);
-                        rsv[e & 7] += p0 + p1;
+                        const int h = e / 16, f = 2 * (e % 16);
+                        float t0, t1;
+                        unpair(fma2(pair(__uint_as_float(v[h][f]), __uint_as_float(v[h][f + 1])),
+                                    sc2, nmu2),
+                               t0, t1);
+                        const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+                        rs2[e & 1] = add2(rs2[e & 1], pair(p0, p1));
                         w[e] = pack_bf16(p0, p1);
                     }
                     st32(tmem + lane_base + kColP + (uint32_t)(k & 1) * (kTile / 2), w);
-                    l += ((rsv[0] + rsv[1]) + (rsv[2] + rsv[3])) + ((rsv[4] + rsv[5]) + (rsv[6] + rsv[7]));
+                    {
+                        float r0, r1, r2, r3;
+                        unpair(rs2[0], r0, r1);
+                        unpair(rs2[1], r2, r3);
+                        l += (r0 + r1) + (r2 + r3);
+                    }
                 }
                 if (ti.nvalid < kTile) {
                     // V rows past the valid count hold whatever the copy left
