@@ -29,6 +29,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "attn_tc.cuh"
@@ -1311,16 +1312,11 @@ __global__ void check_seq_len_kernel(const __grid_constant__ TcParams P) {
 
 // 2-D bf16 map over [rows][d] with a (64 x box_rows) box, 128-byte swizzle.
 bool make_map(CUtensorMap *map, const void *base, long long rows, int d, int box_rows) {
-    auto fn = tensor_map_encoder();
-    if (!fn) return false;
     if (rows < 1) rows = 1;
-    cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)d * 2};
-    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1u, 1u};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    return encode_bf16_map(map, base, 2, dims, strides, box);
 }
 
 // Kernel shape chosen per problem shape.
@@ -1473,4 +1469,58 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
+
+namespace {
+
+// Arguments of one bf16 map encoding; zero-filled so that keys compare
+// bytewise.
+struct MapKey {
+    const void *base;
+    int rank;
+    cuuint64_t dims[5];
+    cuuint64_t strides[4];
+    cuuint32_t box[5];
+};
+
+constexpr int kMapCache = 64;
+std::mutex g_map_mu;
+MapKey g_map_keys[kMapCache];
+CUtensorMap g_map_vals[kMapCache];
+int g_map_used = 0, g_map_next = 0;
+
+}  // namespace
+
+bool encode_bf16_map(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
+                     const cuuint64_t *strides, const cuuint32_t *box) {
+    if (rank < 1 || rank > 5) return false;
+    MapKey key;
+    memset(&key, 0, sizeof(key));
+    key.base = base;
+    key.rank = rank;
+    for (int i = 0; i < rank; ++i) {
+        key.dims[i] = dims[i];
+        key.box[i] = box[i];
+        if (i + 1 < rank) key.strides[i] = strides[i];
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        for (int i = 0; i < g_map_used; ++i)
+            if (memcmp(&g_map_keys[i], &key, sizeof(key)) == 0) {
+                *map = g_map_vals[i];
+                return true;
+            }
+    }
+    auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    const cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+    if (fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base),
+           dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    const int slot = g_map_used < kMapCache ? g_map_used++ : (g_map_next++ % kMapCache);
+    g_map_keys[slot] = key;
+    g_map_vals[slot] = *map;
+    return true;
+}
 }  // namespace sv

@@ -499,16 +499,12 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
 // 128-position x 64-element block of one head, 128-byte swizzle.  Positions
 // past L read as zeros.
 bool make_map_4d(CUtensorMap *map, const void *base, int H, int L, int B) {
-    auto fn = tensor_map_encoder();
-    if (!fn) return false;
     constexpr int D = lap::kD;
-    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)L, (cuuint64_t)B};
-    cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)L * H * D * 2};
-    cuuint32_t box[4] = {64u, 1u, (cuuint32_t)lap::kM, 1u};
-    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
-              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)L, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2,
+                                   (cuuint64_t)L * H * D * 2};
+    const cuuint32_t box[4] = {64u, 1u, (cuuint32_t)lap::kM, 1u};
+    return encode_bf16_map(map, base, 4, dims, strides, box);
 }
 
 }  // namespace

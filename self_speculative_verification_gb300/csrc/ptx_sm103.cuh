@@ -129,6 +129,14 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
 // driver does not provide it.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
+// A bf16 tiled tensor map (128-byte swizzle, out-of-range elements read as
+// zero) over `rank` dimensions (dims innermost first, strides in bytes of
+// dims 1..rank-1, box in elements).  Encodings are cached by their
+// arguments, so a call repeating an earlier one costs a lookup.  Returns
+// false if the driver rejects the arguments.
+bool encode_bf16_map(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
+                     const cuuint64_t *strides, const cuuint32_t *box);
+
 // ------------------------------------------------------------- tcgen05
 namespace tc5 {
 
