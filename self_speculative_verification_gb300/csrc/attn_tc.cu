@@ -1270,18 +1270,19 @@ __global__ void __launch_bounds__(128) attn_tc_combine_kernel(const __grid_const
 
 // tcgen05 path: a segment wholly inside one CTA's range already holds its
 // final output; a split segment contains at least one boundary between
-// consecutive CTA ranges.  CTA i here takes the boundary between attention
-// CTAs i and i + 1 and merges the segment across it when that boundary is
-// the segment's first, so only split segments cost work (at most
-// n_ctas - 1 of them).
-constexpr int kUmmaCombineThreads = 512;
+// consecutive CTA ranges.  CTAs (i, y) here take the boundary between
+// attention CTAs i and i + 1 and merge the segment across it when that
+// boundary is the segment's first (CTA y takes every kUmmaCombineSplit-th
+// group of 8 rows), so only split segments cost work (at most n_ctas - 1).
+constexpr int kUmmaCombineThreads = 256;
+constexpr int kUmmaCombineSplit = 8;     // CTAs per boundary (row slices of the segment)
 
 template <int D>
 __global__ void __launch_bounds__(kUmmaCombineThreads)
 attn_umma_combine_kernel(const __grid_constant__ TcParams P) {
     const AttnParams &A = P.a;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (blockIdx.x == 0)
+    if (blockIdx.x == 0 && blockIdx.y == 0)
         for (int b = threadIdx.x; b < A.B; b += kUmmaCombineThreads) check_seq_len(A, b);
     const long long T = warp_total_tiles(P);
     const long long tb = range_lo(T, blockIdx.x + 1, P.n_ctas);
@@ -1299,7 +1300,9 @@ attn_umma_combine_kernel(const __grid_constant__ TcParams P) {
     const int h = segi / A.n_rb, rb = segi % A.n_rb;
     const int seg = (b * A.Hkv + h) * A.n_rb + rb;
     const int p_hi = min(A.M, (rb + 1) * A.rb_rows);
-    for (int p = rb * A.rb_rows + warp; p < p_hi; p += kUmmaCombineThreads / 32)
+    constexpr int kWarps = kUmmaCombineThreads / 32;
+    for (int p = rb * A.rb_rows + blockIdx.y * kWarps + warp; p < p_hi;
+         p += kUmmaCombineSplit * kWarps)
         merge_row<D>(P, 1, T, b, h, seg, s0, s1, first, last, p, lane);
 }
 
@@ -1376,7 +1379,8 @@ spec_status_t launch_umma(const TcParams &P, const CUtensorMap *maps, cudaStream
     spec_status_t st = launch_status();
     if (st != SPEC_OK) return st;
     if (P.n_ctas > 1)
-        attn_umma_combine_kernel<D><<<P.n_ctas - 1, kUmmaCombineThreads, 0, s>>>(P);
+        attn_umma_combine_kernel<D><<<dim3(P.n_ctas - 1, kUmmaCombineSplit),
+                                       kUmmaCombineThreads, 0, s>>>(P);
     else
         check_seq_len_kernel<<<1, 32, 0, s>>>(P);
     return launch_status();
