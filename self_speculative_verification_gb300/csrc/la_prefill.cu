@@ -229,15 +229,26 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
             if (lane == 0) {
                 const uint32_t id_s = idesc(kM, kN, false, false);
                 const uint32_t id_pv = idesc(kM, kD, false, true);
-                long long ld = 0;              // K/V loads consumed
+                int slot = 0;                  // ring slot of the next K/V load to consume
+                uint32_t ph = 0;               // and the parity of its fill
                 int nu = 0;                    // units started
                 int np[2] = {0, 0};            // P hand-offs taken, per tile
                 int nact[2] = {0, 0};          // units in which the tile took part
                 bool ok = true;
                 const uint64_t qd[2] = {smem_desc(smem_u32(qbuf), 16, 1024),
                                         smem_desc(smem_u32(qbuf + kTileBytes), 16, 1024)};
-                auto issue_s = [&](int x, int kslot) {
-                    const uint64_t kd = smem_desc(smem_u32(ring + kslot * kTileBytes), 16, 1024);
+                // descriptors of ring slot 0 (K: K-major, V: MN-major); a slot is
+                // kTileBytes further, i.e. kTileBytes >> 4 in the address field
+                const uint64_t kd0 = smem_desc(smem_u32(ring), 16, 1024);
+                const uint64_t vd0 = smem_desc(smem_u32(ring), kHalf, 1024);
+                auto advance = [&]() {
+                    if (++slot == kSlots) {
+                        slot = 0;
+                        ph ^= 1u;
+                    }
+                };
+                auto issue_s = [&](int x, int ks_slot) {
+                    const uint64_t kd = kd0 + (uint64_t)(ks_slot * (kTileBytes >> 4));
     #pragma unroll
                     for (int ks = 0; ks < kD / 16; ++ks) {
                         const uint64_t off = (uint64_t)((((ks >> 2) * kHalf) + (ks & 3) * 32) >> 4);
@@ -247,14 +258,14 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
                 };
                 // O_x += P_x V(j); the tile's first PV of a unit overwrites O_x,
                 // after the previous unit's epilogue of that tile read it
-                auto issue_pv = [&](int x, int vslot, bool first) -> bool {
+                auto issue_pv = [&](int x, int v_slot, bool first) -> bool {
                     if (!mbar_wait(&sh.p_full[x], (uint32_t)(np[x] & 1))) return false;
                     ++np[x];
                     if (first && nact[x] > 0 &&
                         !mbar_wait(&sh.o_free[x], (uint32_t)((nact[x] - 1) & 1)))
                         return false;
                     fence_after();
-                    const uint64_t vd = smem_desc(smem_u32(ring + vslot * kTileBytes), kHalf, 1024);
+                    const uint64_t vd = vd0 + (uint64_t)(v_slot * (kTileBytes >> 4));
     #pragma unroll
                     for (int ks = 0; ks < kN / 16; ++ks)
                         mma(tmem + col_o(x), tmem + col_s(x) + ks * 8,
@@ -265,60 +276,60 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
                     Unit u[2];
                     const int nus = units_of(P, w, u);
                     for (int s = 0; s < nus && ok; ++s, ++nu) {
-                        const int m[2] = {last_tile(P, u[s].t, 0), last_tile(P, u[s].t, 1)};
-                        const int jmax = m[1] >= 0 ? m[1] : m[0];
-                        if (*abort || !mbar_wait(&sh.q_full, (uint32_t)(nu & 1))) {
+                        // tile A always exists (2t < NM); tile B may not
+                        const int mA = last_tile(P, u[s].t, 0), mB = last_tile(P, u[s].t, 1);
+                        const int jmax = mB >= 0 ? mB : mA;
+                        if (*abort || !mbar_wait(&sh.q_full, (uint32_t)(nu & 1)) ||
+                            !mbar_wait(&sh.full[slot], ph)) {
                             ok = false;
                             break;
                         }
                         // S(0) of both tiles
-                        int kslot = (int)(ld % kSlots);
-                        if (!mbar_wait(&sh.full[kslot], (uint32_t)((ld / kSlots) & 1))) {
-                            ok = false;
-                            break;
-                        }
-                        fence_after();
-                        for (int x = 0; x < 2; ++x)
-                            if (m[x] >= 0) issue_s(x, kslot);
-                        commit(&sh.empty[kslot]);
+                        issue_s(0, slot);
+                        if (mB >= 0) issue_s(1, slot);
+                        commit(&sh.empty[slot]);
                         if (jmax == 0) commit(&sh.q_empty);
-                        ++ld;
-                        for (int j = 0; j <= jmax && ok; ++j) {
-                            const int vslot = (int)(ld % kSlots);
-                            if (!mbar_wait(&sh.full[vslot], (uint32_t)((ld / kSlots) & 1))) {
+                        advance();
+                        for (int j = 0; j <= jmax; ++j) {
+                            const int vslot = slot;
+                            if (!mbar_wait(&sh.full[vslot], ph)) {
                                 ok = false;
                                 break;
                             }
-                            ++ld;
-                            const bool next = j + 1 <= jmax;
-                            if (next) {
-                                kslot = (int)(ld % kSlots);
-                                if (!mbar_wait(&sh.full[kslot], (uint32_t)((ld / kSlots) & 1))) {
+                            advance();
+                            const bool next = j < jmax;
+                            const int kslot = slot;
+                            if (next && !mbar_wait(&sh.full[kslot], ph)) {
+                                ok = false;
+                                break;
+                            }
+                            if (j <= mA) {
+                                if (!issue_pv(0, vslot, j == 0)) {
                                     ok = false;
                                     break;
                                 }
+                                if (j == mA) commit(&sh.o_done[0]);
+                                if (j < mA) issue_s(0, kslot);
                             }
-                            fence_after();
-                            for (int x = 0; x < 2 && ok; ++x) {
-                                if (m[x] < 0 || j > m[x]) continue;
-                                if (!issue_pv(x, vslot, j == 0)) {
+                            if (mB >= 0) {     // j <= mB == jmax
+                                if (!issue_pv(1, vslot, j == 0)) {
                                     ok = false;
                                     break;
                                 }
-                                if (j == m[x]) commit(&sh.o_done[x]);
-                                if (x == 1) commit(&sh.empty[vslot]);
-                                if (next && j + 1 <= m[x]) issue_s(x, kslot);
+                                if (j == mB) commit(&sh.o_done[1]);
+                                commit(&sh.empty[vslot]);
+                                if (next) issue_s(1, kslot);
+                            } else {
+                                commit(&sh.empty[vslot]);
                             }
-                            if (!ok) break;
-                            if (m[1] < 0 || j > m[1]) commit(&sh.empty[vslot]);
                             if (next) {
                                 commit(&sh.empty[kslot]);
                                 if (j + 1 == jmax) commit(&sh.q_empty);
-                                ++ld;
+                                advance();
                             }
                         }
-                        for (int x = 0; x < 2; ++x)
-                            if (m[x] >= 0) ++nact[x];
+                        ++nact[0];
+                        if (mB >= 0) ++nact[1];
                     }
                 }
                 if (!ok) {
