@@ -33,7 +33,12 @@
 //   stops issuing work, waits (bounded) for its own copies and MMAs, frees
 //   its TMEM and returns.
 #include <algorithm>
+#include <functional>
+#include <map>
 #include <mutex>
+#include <queue>
+#include <tuple>
+#include <vector>
 
 #include "common.cuh"
 #include "ptx_sm103.cuh"
@@ -113,11 +118,58 @@ __device__ __forceinline__ int last_tile(const Params &P, int t, int X) {
     return m < P.NM ? m : -1;
 }
 
+// The units each CTA works on, in order: v[c] .. v[c + 1] index CTA c's run
+// of unit ids (b * Hq + hq) * NB + t stored from v[grid + 1] on.  Built on
+// the host (longest unit first onto the least-loaded CTA, a few heads at a
+// time) and passed by value with the launch; n == 0 means no table, and the
+// CTAs then take the paired items round-robin.
+constexpr int kSchedCap = 8192;
+struct Sched {
+    int n;
+    uint16_t v[kSchedCap];
+};
+
+struct Cursor {
+    int w, s, e, end;
+};
+
+__device__ __forceinline__ Cursor cursor_begin(const Sched &S) {
+    Cursor c{(int)blockIdx.x, 0, 0, 0};
+    if (S.n) {
+        c.e = S.v[blockIdx.x];
+        c.end = S.v[blockIdx.x + 1];
+    }
+    return c;
+}
+
+// the CTA's next unit; false when it has none left
+__device__ __forceinline__ bool next_unit(const Params &P, const Sched &S, Cursor &c, Unit &U) {
+    if (S.n) {
+        if (c.e >= c.end) return false;
+        const int id = S.v[gridDim.x + 1 + c.e++];
+        const int bh = id / P.NB;
+        U = Unit{bh / P.Hq, bh % P.Hq, id % P.NB};
+        return true;
+    }
+    while (c.w < P.n_items) {
+        Unit u[2];
+        const int nus = units_of(P, c.w, u);
+        if (c.s < nus) {
+            U = u[c.s++];
+            return true;
+        }
+        c.w += gridDim.x;
+        c.s = 0;
+    }
+    return false;
+}
+
 }  // namespace lap
 
 __global__ void __launch_bounds__(lap::kThreads, 1)
 la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__ CUtensorMap mq,
-                  const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv) {
+                  const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+                  const __grid_constant__ lap::Sched S) {
     using namespace lap;
     using namespace tc5;
     extern __shared__ uint8_t smem_raw[];
@@ -175,38 +227,35 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
                 long long ld = 0;          // K/V loads issued
                 int nu = 0;                // units (Q loads) issued
                 bool ok = true;
-                for (int w = blockIdx.x; w < P.n_items && ok; w += gridDim.x) {
-                    Unit u[2];
-                    const int nus = units_of(P, w, u);
-                    for (int s = 0; s < nus && ok; ++s) {
-                        const Unit &U = u[s];
-                        const int mA = last_tile(P, U.t, 0), mB = last_tile(P, U.t, 1);
-                        const int jmax = mB >= 0 ? mB : mA;
-                        if (*abort || !mbar_wait(&sh.q_empty, (uint32_t)((nu & 1) ^ 1))) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(&sh.q_full, (uint32_t)(mB >= 0 ? 2 : 1) * kTileBytes);
-                        for (int x = 0; x < (mB >= 0 ? 2 : 1); ++x)
-                            for (int hh = 0; hh < 2; ++hh)
-                                tma_load_4d(qbuf + x * kTileBytes + hh * kHalf, &mq, hh * 64, U.hq,
-                                            (2 * U.t + x) * kM, U.b, &sh.q_full, pol_q);
-                        ++nu;
-                        const int hk = U.hq / P.G;
-                        for (int j = 0; j <= jmax && ok; ++j) {
-                            for (int kv = 0; kv < 2; ++kv) {
-                                const int slot = (int)(ld % kSlots);
-                                if (*abort ||
-                                    !mbar_wait(&sh.empty[slot], (uint32_t)(((ld / kSlots) & 1) ^ 1))) {
-                                    ok = false;
-                                    break;
-                                }
-                                mbar_arrive_expect_tx(&sh.full[slot], (uint32_t)kTileBytes);
-                                for (int hh = 0; hh < 2; ++hh)
-                                    tma_load_4d(ring + slot * kTileBytes + hh * kHalf, kv ? &mv : &mk,
-                                                hh * 64, hk, j * kN, U.b, &sh.full[slot], pol_kv);
-                                ++ld;
+                Cursor cur = cursor_begin(S);
+                Unit U;
+                while (ok && next_unit(P, S, cur, U)) {
+                    const int mA = last_tile(P, U.t, 0), mB = last_tile(P, U.t, 1);
+                    const int jmax = mB >= 0 ? mB : mA;
+                    if (*abort || !mbar_wait(&sh.q_empty, (uint32_t)((nu & 1) ^ 1))) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&sh.q_full, (uint32_t)(mB >= 0 ? 2 : 1) * kTileBytes);
+                    for (int x = 0; x < (mB >= 0 ? 2 : 1); ++x)
+                        for (int hh = 0; hh < 2; ++hh)
+                            tma_load_4d(qbuf + x * kTileBytes + hh * kHalf, &mq, hh * 64, U.hq,
+                                        (2 * U.t + x) * kM, U.b, &sh.q_full, pol_q);
+                    ++nu;
+                    const int hk = U.hq / P.G;
+                    for (int j = 0; j <= jmax && ok; ++j) {
+                        for (int kv = 0; kv < 2; ++kv) {
+                            const int slot = (int)(ld % kSlots);
+                            if (*abort ||
+                                !mbar_wait(&sh.empty[slot], (uint32_t)(((ld / kSlots) & 1) ^ 1))) {
+                                ok = false;
+                                break;
                             }
+                            mbar_arrive_expect_tx(&sh.full[slot], (uint32_t)kTileBytes);
+                            for (int hh = 0; hh < 2; ++hh)
+                                tma_load_4d(ring + slot * kTileBytes + hh * kHalf, kv ? &mv : &mk,
+                                            hh * 64, hk, j * kN, U.b, &sh.full[slot], pol_kv);
+                            ++ld;
                         }
                     }
                 }
@@ -272,65 +321,64 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
                             vd + (uint64_t)((ks * 2048) >> 4), id_pv, (ks > 0 || !first) ? 1u : 0u);
                     return true;
                 };
-                for (int w = blockIdx.x; w < P.n_items && ok; w += gridDim.x) {
-                    Unit u[2];
-                    const int nus = units_of(P, w, u);
-                    for (int s = 0; s < nus && ok; ++s, ++nu) {
-                        // tile A always exists (2t < NM); tile B may not
-                        const int mA = last_tile(P, u[s].t, 0), mB = last_tile(P, u[s].t, 1);
-                        const int jmax = mB >= 0 ? mB : mA;
-                        if (*abort || !mbar_wait(&sh.q_full, (uint32_t)(nu & 1)) ||
-                            !mbar_wait(&sh.full[slot], ph)) {
+                Cursor cur = cursor_begin(S);
+                Unit U;
+                while (ok && next_unit(P, S, cur, U)) {
+                    // tile A always exists (2t < NM); tile B may not
+                    const int mA = last_tile(P, U.t, 0), mB = last_tile(P, U.t, 1);
+                    const int jmax = mB >= 0 ? mB : mA;
+                    if (*abort || !mbar_wait(&sh.q_full, (uint32_t)(nu & 1)) ||
+                        !mbar_wait(&sh.full[slot], ph)) {
+                        ok = false;
+                        break;
+                    }
+                    // S(0) of both tiles
+                    issue_s(0, slot);
+                    if (mB >= 0) issue_s(1, slot);
+                    commit(&sh.empty[slot]);
+                    if (jmax == 0) commit(&sh.q_empty);
+                    advance();
+                    for (int j = 0; j <= jmax; ++j) {
+                        const int vslot = slot;
+                        if (!mbar_wait(&sh.full[vslot], ph)) {
                             ok = false;
                             break;
                         }
-                        // S(0) of both tiles
-                        issue_s(0, slot);
-                        if (mB >= 0) issue_s(1, slot);
-                        commit(&sh.empty[slot]);
-                        if (jmax == 0) commit(&sh.q_empty);
                         advance();
-                        for (int j = 0; j <= jmax; ++j) {
-                            const int vslot = slot;
-                            if (!mbar_wait(&sh.full[vslot], ph)) {
-                                ok = false;
-                                break;
-                            }
-                            advance();
-                            const bool next = j < jmax;
-                            const int kslot = slot;
-                            if (next && !mbar_wait(&sh.full[kslot], ph)) {
-                                ok = false;
-                                break;
-                            }
-                            if (j <= mA) {
-                                if (!issue_pv(0, vslot, j == 0)) {
-                                    ok = false;
-                                    break;
-                                }
-                                if (j == mA) commit(&sh.o_done[0]);
-                                if (j < mA) issue_s(0, kslot);
-                            }
-                            if (mB >= 0) {     // j <= mB == jmax
-                                if (!issue_pv(1, vslot, j == 0)) {
-                                    ok = false;
-                                    break;
-                                }
-                                if (j == mB) commit(&sh.o_done[1]);
-                                commit(&sh.empty[vslot]);
-                                if (next) issue_s(1, kslot);
-                            } else {
-                                commit(&sh.empty[vslot]);
-                            }
-                            if (next) {
-                                commit(&sh.empty[kslot]);
-                                if (j + 1 == jmax) commit(&sh.q_empty);
-                                advance();
-                            }
+                        const bool next = j < jmax;
+                        const int kslot = slot;
+                        if (next && !mbar_wait(&sh.full[kslot], ph)) {
+                            ok = false;
+                            break;
                         }
-                        ++nact[0];
-                        if (mB >= 0) ++nact[1];
+                        if (j <= mA) {
+                            if (!issue_pv(0, vslot, j == 0)) {
+                                ok = false;
+                                break;
+                            }
+                            if (j == mA) commit(&sh.o_done[0]);
+                            if (j < mA) issue_s(0, kslot);
+                        }
+                        if (mB >= 0) {     // j <= mB == jmax
+                            if (!issue_pv(1, vslot, j == 0)) {
+                                ok = false;
+                                break;
+                            }
+                            if (j == mB) commit(&sh.o_done[1]);
+                            commit(&sh.empty[vslot]);
+                            if (next) issue_s(1, kslot);
+                        } else {
+                            commit(&sh.empty[vslot]);
+                        }
+                        if (next) {
+                            commit(&sh.empty[kslot]);
+                            if (j + 1 == jmax) commit(&sh.q_empty);
+                            advance();
+                        }
                     }
+                    ++nact[0];
+                    if (mB >= 0) ++nact[1];
+                    ++nu;
                 }
                 if (!ok) {
                     raise_status(P.status, SPEC_DEV_TIMEOUT);
@@ -351,147 +399,144 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
         const float sc = P.scale_log2;
         int ns = 0, nact = 0;      // S hand-offs taken; units this tile took part in
         bool ok = true;
-        for (int w = blockIdx.x; w < P.n_items && ok; w += gridDim.x) {
-            Unit u[2];
-            const int nus = units_of(P, w, u);
-            for (int s = 0; s < nus && ok; ++s) {
-                const Unit &U = u[s];
-                const int mX = last_tile(P, U.t, x);
-                if (mX < 0) continue;
-                const int i = mX * kM + r;               // this thread's position
-                float m_used = -INFINITY, l = 0.f;
-                for (int j = 0; j <= mX; ++j) {
-                    if (*abort || !mbar_wait(&sh.s_full[x], (uint32_t)(ns & 1))) {
-                        ok = false;
-                        break;
-                    }
-                    ++ns;
-                    fence_after();
-                    const bool masked = j == mX || (j + 1) * kN > P.n;
-                    const int c0 = j * kN;
-                    // visibility of keys lo .. lo + 31 for this row: key c is
-                    // visible iff c <= i and (c < n or c == i)
-                    auto vis_bits = [&](int lo) -> uint32_t {
-                        if (!masked) return 0xffffffffu;
-                        const int di = i - lo, dn = P.n - lo;
-                        const uint32_t le = di < 0 ? 0u : di >= 31 ? 0xffffffffu
-                                                                   : (2u << di) - 1u;
-                        const uint32_t lt = dn <= 0 ? 0u : dn >= 32 ? 0xffffffffu
-                                                                    : (1u << dn) - 1u;
-                        const uint32_t self = (di >= 0 && di < 32) ? (1u << di) : 0u;
-                        return (le & lt) | self;
-                    };
-                    // the S row: four TMEM loads in flight, one wait (each
-                    // wait_ld ties its registers; the later ones return at once)
-                    uint32_t v[kN / 32][32];
-#pragma unroll
-                    for (int c = 0; c < kN / 32; ++c) ld32(tS + c * 32, v[c]);
-#pragma unroll
-                    for (int c = 0; c < kN / 32; ++c) wait_ld(v[c]);
-                    // masked tiles: invisible scores become -inf in place
-                    if (masked) {
-#pragma unroll
-                        for (int c = 0; c < kN / 32; ++c) {
-                            const uint32_t vm = vis_bits(c0 + c * 32);
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                v[c][e] = ((vm >> e) & 1u) ? v[c][e] : 0xff800000u;
-                        }
-                    }
-                    // the row maximum (three-input max, four chains)
-                    float tmv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                    for (int c = 0; c < kN / 32; ++c)
-#pragma unroll
-                        for (int e = 0; e < 32; e += 8)
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                tmv[q] = max3(tmv[q], __uint_as_float(v[c][e + 2 * q]),
-                                              __uint_as_float(v[c][e + 2 * q + 1]));
-                    const float traw = fmaxf(fmaxf(tmv[0], tmv[1]), fmaxf(tmv[2], tmv[3]));
-                    const float tm = traw == -INFINITY ? -INFINITY : traw * sc;
-                    if (tm > m_used + kRescale || (m_used == -INFINITY && tm != -INFINITY)) {
-                        const float alpha = (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - tm);
-                        if (j > 0 && m_used != -INFINITY) {
-                            // O holds every earlier PV of this tile (issued
-                            // before the S just waited for): rescale it
-#pragma unroll 1
-                            for (int c = 0; c < kD / 32; ++c) {
-                                uint32_t o[32];
-                                ld32(tO + c * 32, o);
-                                wait_ld(o);
-#pragma unroll
-                                for (int e = 0; e < 32; ++e)
-                                    o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                                st32(tO + c * 32, o);
-                            }
-                        }
-                        l *= alpha;
-                        m_used = tm;
-                    }
-                    const float mu = m_used == -INFINITY ? 0.f : m_used;
-                    // P = exp2(s * scale - mu) (pairs: one f32x2 FMA, two ex2,
-                    // one f32x2 add, one pack) over the first 64 columns of S
-                    const uint64_t sc2 = pair(sc, sc), nmu2 = pair(-mu, -mu);
-                    uint64_t rs2[2] = {pair(0.f, 0.f), pair(0.f, 0.f)};
-#pragma unroll
-                    for (int c = 0; c < kN / 32; ++c) {
-                        uint32_t pw[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            float t0, t1;
-                            unpair(fma2(pair(__uint_as_float(v[c][2 * e]),
-                                             __uint_as_float(v[c][2 * e + 1])),
-                                        sc2, nmu2),
-                                   t0, t1);
-                            const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
-                            rs2[e & 1] = add2(rs2[e & 1], pair(p0, p1));
-                            pw[e] = pack_bf16(p0, p1);
-                        }
-                        st16(tS + c * 16, pw);
-                    }
-                    float rs[4];
-                    unpair(rs2[0], rs[0], rs[1]);
-                    unpair(rs2[1], rs[2], rs[3]);
-                    l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
-                    wait_st();
-                    fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&sh.p_full[x]);
-                }
-                if (!ok) break;
-                // epilogue: O / l (bf16) and the LSE of this row
-                if (!mbar_wait(&sh.o_done[x], (uint32_t)(nact & 1))) {
+        Cursor cur = cursor_begin(S);
+        Unit U;
+        while (ok && next_unit(P, S, cur, U)) {
+            const int mX = last_tile(P, U.t, x);
+            if (mX < 0) continue;
+            const int i = mX * kM + r;               // this thread's position
+            float m_used = -INFINITY, l = 0.f;
+            for (int j = 0; j <= mX; ++j) {
+                if (*abort || !mbar_wait(&sh.s_full[x], (uint32_t)(ns & 1))) {
                     ok = false;
                     break;
                 }
+                ++ns;
                 fence_after();
-                const bool row_ok = i < P.L;
-                const float inv = l > 0.f ? 1.f / l : 0.f;
-                uint4 *dst = reinterpret_cast<uint4 *>(
-                    P.o + (((size_t)U.b * P.L + (row_ok ? i : 0)) * P.Hq + U.hq) * kD);
-#pragma unroll 1
-                for (int c = 0; c < kD / 32; ++c) {
-                    uint32_t v[32];
-                    ld32(tO + c * 32, v);
-                    wait_ld(v);
-                    if (!row_ok) continue;
+                const bool masked = j == mX || (j + 1) * kN > P.n;
+                const int c0 = j * kN;
+                // visibility of keys lo .. lo + 31 for this row: key c is
+                // visible iff c <= i and (c < n or c == i)
+                auto vis_bits = [&](int lo) -> uint32_t {
+                    if (!masked) return 0xffffffffu;
+                    const int di = i - lo, dn = P.n - lo;
+                    const uint32_t le = di < 0 ? 0u : di >= 31 ? 0xffffffffu
+                                                               : (2u << di) - 1u;
+                    const uint32_t lt = dn <= 0 ? 0u : dn >= 32 ? 0xffffffffu
+                                                                : (1u << dn) - 1u;
+                    const uint32_t self = (di >= 0 && di < 32) ? (1u << di) : 0u;
+                    return (le & lt) | self;
+                };
+                // the S row: four TMEM loads in flight, one wait (each
+                // wait_ld ties its registers; the later ones return at once)
+                uint32_t v[kN / 32][32];
+#pragma unroll
+                for (int c = 0; c < kN / 32; ++c) ld32(tS + c * 32, v[c]);
+#pragma unroll
+                for (int c = 0; c < kN / 32; ++c) wait_ld(v[c]);
+                // masked tiles: invisible scores become -inf in place
+                if (masked) {
+#pragma unroll
+                    for (int c = 0; c < kN / 32; ++c) {
+                        const uint32_t vm = vis_bits(c0 + c * 32);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            v[c][e] = ((vm >> e) & 1u) ? v[c][e] : 0xff800000u;
+                    }
+                }
+                // the row maximum (three-input max, four chains)
+                float tmv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int c = 0; c < kN / 32; ++c)
 #pragma unroll
                     for (int e = 0; e < 32; e += 8)
-                        dst[(c * 32 + e) / 8] = make_uint4(
-                            pack_bf16(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv),
-                            pack_bf16(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv),
-                            pack_bf16(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv),
-                            pack_bf16(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv));
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            tmv[q] = max3(tmv[q], __uint_as_float(v[c][e + 2 * q]),
+                                          __uint_as_float(v[c][e + 2 * q + 1]));
+                const float traw = fmaxf(fmaxf(tmv[0], tmv[1]), fmaxf(tmv[2], tmv[3]));
+                const float tm = traw == -INFINITY ? -INFINITY : traw * sc;
+                if (tm > m_used + kRescale || (m_used == -INFINITY && tm != -INFINITY)) {
+                    const float alpha = (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - tm);
+                    if (j > 0 && m_used != -INFINITY) {
+                        // O holds every earlier PV of this tile (issued
+                        // before the S just waited for): rescale it
+#pragma unroll 1
+                        for (int c = 0; c < kD / 32; ++c) {
+                            uint32_t o[32];
+                            ld32(tO + c * 32, o);
+                            wait_ld(o);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            st32(tO + c * 32, o);
+                        }
+                    }
+                    l *= alpha;
+                    m_used = tm;
                 }
-                if (row_ok)
-                    P.lse[((size_t)U.b * P.Hq + U.hq) * P.L + i] =
-                        l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+                const float mu = m_used == -INFINITY ? 0.f : m_used;
+                // P = exp2(s * scale - mu) (pairs: one f32x2 FMA, two ex2,
+                // one f32x2 add, one pack) over the first 64 columns of S
+                const uint64_t sc2 = pair(sc, sc), nmu2 = pair(-mu, -mu);
+                uint64_t rs2[2] = {pair(0.f, 0.f), pair(0.f, 0.f)};
+#pragma unroll
+                for (int c = 0; c < kN / 32; ++c) {
+                    uint32_t pw[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float t0, t1;
+                        unpair(fma2(pair(__uint_as_float(v[c][2 * e]),
+                                         __uint_as_float(v[c][2 * e + 1])),
+                                    sc2, nmu2),
+                               t0, t1);
+                        const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+                        rs2[e & 1] = add2(rs2[e & 1], pair(p0, p1));
+                        pw[e] = pack_bf16(p0, p1);
+                    }
+                    st16(tS + c * 16, pw);
+                }
+                float rs[4];
+                unpair(rs2[0], rs[0], rs[1]);
+                unpair(rs2[1], rs[2], rs[3]);
+                l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+                wait_st();
                 fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.o_free[x]);
-                ++nact;
+                if (lane == 0) mbar_arrive(&sh.p_full[x]);
             }
+            if (!ok) break;
+            // epilogue: O / l (bf16) and the LSE of this row
+            if (!mbar_wait(&sh.o_done[x], (uint32_t)(nact & 1))) {
+                ok = false;
+                break;
+            }
+            fence_after();
+            const bool row_ok = i < P.L;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            uint4 *dst = reinterpret_cast<uint4 *>(
+                P.o + (((size_t)U.b * P.L + (row_ok ? i : 0)) * P.Hq + U.hq) * kD);
+#pragma unroll 1
+            for (int c = 0; c < kD / 32; ++c) {
+                uint32_t v[32];
+                ld32(tO + c * 32, v);
+                wait_ld(v);
+                if (!row_ok) continue;
+#pragma unroll
+                for (int e = 0; e < 32; e += 8)
+                    dst[(c * 32 + e) / 8] = make_uint4(
+                        pack_bf16(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv),
+                        pack_bf16(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv),
+                        pack_bf16(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv),
+                        pack_bf16(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv));
+            }
+            if (row_ok)
+                P.lse[((size_t)U.b * P.Hq + U.hq) * P.L + i] =
+                    l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.o_free[x]);
+            ++nact;
         }
         if (!ok) {
             raise_status(P.status, SPEC_DEV_TIMEOUT);
@@ -504,6 +549,56 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
     if (warp == kMmaWarp)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols));
+}
+
+// Unit schedule for `grid` CTAs: heads are taken kSchedHeads at a time (a
+// multiple of the KV group, so the CTAs at work share few K/V sets in L2),
+// and within such a window the longest unit goes first onto the CTA with the
+// least work so far (cost of a unit: its key tiles plus a fixed allowance
+// for the Q load and the epilogue).  Returns false when the table does not
+// fit; the result depends only on the arguments and is cached.
+constexpr int kSchedHeads = 8;
+constexpr int kUnitOverhead = 2;
+
+bool build_schedule(int BH, int G, int NB, int NM, int grid, lap::Sched &out) {
+    const long long n_units = (long long)BH * NB;
+    if (n_units >= 65536 || n_units + grid + 1 > lap::kSchedCap) return false;
+    using Key = std::tuple<int, int, int, int, int>;
+    static std::mutex mu;
+    static std::map<Key, std::vector<uint16_t>> cache;
+    const Key key{BH, G, NB, NM, grid};
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it == cache.end()) {
+        const int W = ((kSchedHeads + G - 1) / G) * G;
+        std::vector<std::vector<uint16_t>> lists(grid);
+        using Slot = std::pair<long long, int>;           // (work so far, CTA)
+        std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+        for (int c = 0; c < grid; ++c) heap.push({0, c});
+        for (int h0 = 0; h0 < BH; h0 += W) {
+            const int h1 = std::min(BH, h0 + W);
+            for (int t = NB - 1; t >= 0; --t) {
+                const int jmax = 2 * t + 1 < NM ? 2 * t + 1 : 2 * t;
+                for (int bh = h0; bh < h1; ++bh) {
+                    Slot sl = heap.top();
+                    heap.pop();
+                    lists[sl.second].push_back((uint16_t)(bh * NB + t));
+                    heap.push({sl.first + jmax + 1 + kUnitOverhead, sl.second});
+                }
+            }
+        }
+        std::vector<uint16_t> v(grid + 1 + n_units);
+        int e = 0;
+        for (int c = 0; c < grid; ++c) {
+            v[c] = (uint16_t)e;
+            for (uint16_t id : lists[c]) v[grid + 1 + e++] = id;
+        }
+        v[grid] = (uint16_t)e;
+        it = cache.emplace(key, std::move(v)).first;
+    }
+    out.n = (int)it->second.size();
+    std::copy(it->second.begin(), it->second.end(), out.v);
+    return true;
 }
 
 // 4-D bf16 map over [B][L][H][128] with a (64, 1, 128, 1) box: one
@@ -573,8 +668,14 @@ extern "C" spec_status_t spec_la_prefill_attn(const spec_prefill_desc *desc, con
                                         (int)lap::kSmemBytes);
     });
     if (attr_err != cudaSuccess) return SPEC_ERR_CUDA;
-    const int grid = (int)std::min<long long>(num_sms(), items);
+    const long long n_units = (long long)B * Hq * P.NB;
+    static thread_local lap::Sched sched;   // 16 KB: kept off the stack
+    int grid = (int)std::min<long long>(num_sms(), n_units);
+    if (!build_schedule(B * Hq, P.G, P.NB, P.NM, grid, sched)) {
+        sched.n = 0;
+        grid = (int)std::min<long long>(num_sms(), items);
+    }
     la_prefill_kernel<<<grid, lap::kThreads, lap::kSmemBytes, as_stream(stream)>>>(
-        P, maps[0], maps[1], maps[2]);
+        P, maps[0], maps[1], maps[2], sched);
     return launch_status();
 }

@@ -96,6 +96,15 @@ def test_prefill_many_items():
     check(wl, O, LSE, pairs=[(0, 0), (3, 5), (7, 15), (5, 8)])
 
 
+def test_prefill_without_unit_table():
+    """More (request, head, tile pair) units than the launch's unit table
+    holds: the CTAs fall back to taking the paired items round-robin."""
+    require_gpu()
+    wl = W.make_prefill(seed=13, B=64, n=5, k=3, Hq=128, Hkv=16)     # 8192 units
+    O, LSE = run_gpu(wl)
+    check(wl, O, LSE, pairs=[(b, h) for b in range(0, 64, 7) for h in range(0, 128, 5)])
+
+
 def test_prefill_full_size_slices():
     """The LLaMA-7B-shaped prefill workload, whole (request, head) slices."""
     require_gpu()
