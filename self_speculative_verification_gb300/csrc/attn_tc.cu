@@ -229,6 +229,15 @@ __device__ __forceinline__ size_t slot_row(const TcParams &P, int seg, int cta, 
 
 // ---------------------------------------------------------------- kernel
 
+// Optional per-segment query loads (tcgen05 kernel): the 128 packed rows of
+// a segment's row block, 128-byte-swizzled, into buffer n % 2 for the n-th
+// segment of the range, after its previous user released it (q_empty).
+struct QLoad {
+    const CUtensorMap *map;     // q viewed as [B * R][Hkv][G][D], box (64, G, 1, 128 / G)
+    uint8_t *buf;               // two buffers of 128 rows x D bf16
+    uint64_t *full, *empty;     // per buffer
+};
+
 // Producer warp: streams the K/V tiles of [t_begin, t_end) into the stage
 // ring.  The whole warp walks the tiles; lane i issues box i of a tile.
 template <int D, int NS>
@@ -236,7 +245,7 @@ __device__ __forceinline__ void run_producer(const TcParams &P, const CUtensorMa
                              const CUtensorMap &mkb, const CUtensorMap &mvb,
                              const CUtensorMap &msk, const CUtensorMap &msv, uint8_t *smem,
                              uint64_t *full, uint64_t *empty, long long t_begin,
-                             long long t_end) {
+                             long long t_end, const QLoad *ql = nullptr) {
     constexpr int NH = D / 64;
     constexpr int KV_BYTES = NH * kHalfBytes;
     constexpr int STAGE = 2 * KV_BYTES;
@@ -272,6 +281,7 @@ __device__ __forceinline__ void run_producer(const TcParams &P, const CUtensorMa
     };
 
     long long k = 0;
+    int nq = 0;                          // query blocks issued
     bool ok = true;
     int ids = load_ids(gc, t_begin);
     for (long long g0 = t_begin; g0 < t_end && ok; g0 += grp) {
@@ -296,7 +306,25 @@ __device__ __forceinline__ void run_producer(const TcParams &P, const CUtensorMa
             const int s = (int)(k % NS);
             const uint32_t ph = (uint32_t)((k / NS) & 1);
             bool got = true;
-            if (lane == 0) got = mbar_wait(&empty[s], ph ^ 1);
+            if (ql && (k == 0 || tc.tile == 0)) {
+                // the segment's query block, ahead of its first K/V tile
+                const int qb = nq & 1;
+                if (lane == 0) {
+                    got = mbar_wait(&ql->empty[qb], (uint32_t)(((nq >> 1) & 1) ^ 1));
+                    if (got) {
+                        constexpr uint32_t kQBytes = 128u * D * 2u;
+                        mbar_arrive_expect_tx(&ql->full[qb], kQBytes);
+                        const int G = A.G;
+                        for (int hh = 0; hh < NH; ++hh)
+                            tma_load_4d(ql->buf + qb * (128 * D * 2) + hh * (128 * 128), ql->map,
+                                        hh * 64, 0, tc.h, tc.b * A.R + tc.rb * (128 / G),
+                                        &ql->full[qb], pol_keep);
+                    }
+                }
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (got) ++nq;
+            }
+            if (got && lane == 0) got = mbar_wait(&empty[s], ph ^ 1);
             got = __shfl_sync(0xffffffffu, got, 0);
             if (!got) {
                 if (lane == 0) raise_status(A.status, SPEC_DEV_TIMEOUT);
@@ -365,6 +393,13 @@ __device__ __forceinline__ void run_producer(const TcParams &P, const CUtensorMa
                 break;
             }
         }
+        // and the query blocks issued last
+        if (ql)
+            for (int n = nq - 1; n >= 0 && n >= nq - 2; --n)
+                if (!mbar_wait(&ql->full[n & 1], (uint32_t)((n >> 1) & 1))) {
+                    raise_status(A.status, SPEC_DEV_TIMEOUT);
+                    break;
+                }
     }
 }
 
@@ -666,14 +701,18 @@ attn_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUten
 // partial slots and combine as attn_tc_kernel; the contraction runs on the
 // fifth-generation tensor cores:
 //   S = Q K^T  -> TMEM (fp32, lane = packed row, column = token), issued by
-//                 one thread as tcgen05.mma (bf16 x bf16 -> fp32), Q read from
-//                 TMEM (lane = row, two bf16 per column), K from the TMA tile;
+//                 one thread as tcgen05.mma (bf16 x bf16 -> fp32), Q and K
+//                 both from 128B-swizzled TMA copies in shared memory;
 //   softmax    -> one thread per row reads its S row from TMEM, masks,
 //                 scales, exponentiates in the exp2 domain and writes P (bf16)
 //                 back to TMEM;
 //   O += P V   -> TMEM (fp32, 128 columns = head_dim), P from TMEM, V read as
 //                 an MN-major operand straight from the TMA tile.
-// Shared memory therefore carries only K/V tiles (6 stages).
+// Shared memory carries 5 K/V stages and two query blocks: the producer warp
+// copies a segment's 128 packed query rows (a box of 128 / G rows x G
+// heads) ahead of its first K/V tile, into the buffer the segment before
+// the previous one released, so segment starts cost the softmax threads no
+// query traffic.
 // The running max is raised only when a row's tile max exceeds it by more
 // than 2^8 (then O and l are rescaled in place); below that, p <= 256 and
 // the fp32 accumulators absorb it.  S and P are double-buffered so S(t) is
@@ -687,11 +726,11 @@ constexpr int kSoftmaxWarps = 4;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kThreads = 6 * 32;
-constexpr int kNS = 6;                  // K/V stages
+constexpr int kNS = 5;                  // K/V stages
+constexpr int kQHalf = kRows * 128;     // one 64-element half of a query block
 constexpr int kTmemCols = 512;
 constexpr int kColO = 0;                // O: columns [0, 128)
 constexpr int kColS = 128;              // S buffer b: [128 + 64 b, 192 + 64 b)
-constexpr int kColQ = 256;              // Q buffer b: [256 + 128 b, 320 + 128 b), bf16 pairs
 constexpr int kColP = 320;              // P buffer b: [320 + 32 b, 352 + 32 b), bf16 pairs
 constexpr float kRescale = 8.f;         // log2 growth allowed before rescaling
 
@@ -706,7 +745,7 @@ __device__ __forceinline__ uint32_t row_off(int tok, int rbl) {
 struct Shared {
     uint64_t full[kNS], empty[kNS];
     uint64_t s_full[2], p_full[2], o_upd[2];
-    uint64_t q_ready[2];                // Q buffer b holds segment n (n % 2 == b)
+    uint64_t q_full[2], q_empty[2];     // Q buffer b holds segment n (n % 2 == b)
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -719,7 +758,7 @@ __global__ void __launch_bounds__(umma::kThreads, 1)
 attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUtensorMap mk,
                  const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mkb,
                  const __grid_constant__ CUtensorMap mvb, const __grid_constant__ CUtensorMap msk,
-                 const __grid_constant__ CUtensorMap msv) {
+                 const __grid_constant__ CUtensorMap msv, const __grid_constant__ CUtensorMap mq) {
     using namespace umma;
     static_assert(D == 128, "tcgen05 path is built for head_dim 128");
     constexpr int NH = D / 64;
@@ -728,14 +767,15 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Shared &sh = *reinterpret_cast<Shared *>(smem + kNS * STAGE + kRows * D * 2);
+    uint8_t *qbuf = smem + kNS * STAGE;          // two query blocks of kRows x D bf16
+    Shared &sh = *reinterpret_cast<Shared *>(qbuf + 2 * kRows * D * 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const AttnParams &A = P.a;
 
     if (threadIdx.x == kProducerWarp * 32) {
-        const CUtensorMap *maps[6] = {&mk, &mv, &mkb, &mvb, &msk, &msv};
-        for (int i = 0; i < 6; ++i)
+        const CUtensorMap *maps[7] = {&mk, &mv, &mkb, &mvb, &msk, &msv, &mq};
+        for (int i = 0; i < 7; ++i)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(maps[i]))
                          : "memory");
     }
@@ -749,8 +789,10 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
             mbar_init(&sh.p_full[b], kSoftmaxWarps);
             mbar_init(&sh.o_upd[b], 1);
         }
-        mbar_init(&sh.q_ready[0], kSoftmaxWarps);
-        mbar_init(&sh.q_ready[1], kSoftmaxWarps);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sh.q_full[b], 1);
+            mbar_init(&sh.q_empty[b], 1);
+        }
         mbar_init(&sh.drain, 1);
         sh.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -775,8 +817,9 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
 
     if (t_begin < t_end) {
         if (warp == kProducerWarp) {
+            const QLoad ql{&mq, qbuf, sh.q_full, sh.q_empty};
             run_producer<D, kNS>(P, mk, mv, mkb, mvb, msk, msv, smem, sh.full, sh.empty, t_begin,
-                                 t_end);
+                                 t_end, &ql);
         } else if (warp == kMmaWarp) {
             // --------------------------------------------------- MMA issuer
             Cursor c;
@@ -784,7 +827,7 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
             if (lane == 0) {
                 const uint32_t id_pv = idesc(kRows, D, false, true);
                 const uint32_t id_s64 = idesc(kRows, kTile, false, false);
-                uint32_t a_q = tmem + kColQ;
+                uint64_t qd = 0;               // query block of the current segment
                 int seg_n = 0;
                 int prev_rbl = 6, prev_stage = 0;
                 bool prev_first = true;
@@ -824,13 +867,14 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                         if (!ok) break;
                     }
                     if (new_seg) {
-                        if (!mbar_wait(&sh.q_ready[seg_n & 1], (uint32_t)((seg_n >> 1) & 1))) {
+                        // the previous segment's S MMAs were its last readers
+                        if (seg_n > 0) commit(&sh.q_empty[(seg_n - 1) & 1]);
+                        if (!mbar_wait(&sh.q_full[seg_n & 1], (uint32_t)((seg_n >> 1) & 1))) {
                             ok = false;
                             break;
                         }
-                        a_q = tmem + kColQ + (uint32_t)(seg_n & 1) * 128;
+                        qd = smem_desc(smem_u32(qbuf + (seg_n & 1) * (kRows * D * 2)), 16, 1024);
                         ++seg_n;
-                        fence_after();
                     }
                     if (!mbar_wait(&sh.full[stage], (uint32_t)((k / kNS) & 1))) { ok = false; break; }
                     // S(k) = Q K^T into S buffer k%2
@@ -840,9 +884,9 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                         const uint64_t kd = smem_desc(kb, 16, 1024);
 #pragma unroll
                         for (int ks = 0; ks < D / 16; ++ks)
-                            mma(s_col, a_q + ks * 8,
-                                kd + (uint64_t)((((ks >> 2) * kHalfBytes) + (ks & 3) * 32) >> 4),
-                                id_s64, ks > 0 ? 1u : 0u);
+                            mma_ss(s_col, qd + (uint64_t)((((ks >> 2) * kQHalf) + (ks & 3) * 32) >> 4),
+                                   kd + (uint64_t)((((ks >> 2) * kHalfBytes) + (ks & 3) * 32) >> 4),
+                                   id_s64, ks > 0 ? 1u : 0u);
                     } else {
                         // paged tile: one MMA per page block (its 8-row groups
                         // are contiguous only within the block)
@@ -853,8 +897,9 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                             for (int ks = 0; ks < D / 16; ++ks) {
                                 const int hh = ks >> 2, kk = ks & 3;
                                 const uint32_t boff = (uint32_t)((i * NH + hh) * blk) * 128u + kk * 32;
-                                mma(s_col + i * blk, a_q + ks * 8, smem_desc(kb + boff, 16, 1024),
-                                    id_s, ks > 0 ? 1u : 0u);
+                                mma_ss(s_col + i * blk,
+                                       qd + (uint64_t)(((hh * kQHalf) + kk * 32) >> 4),
+                                       smem_desc(kb + boff, 16, 1024), id_s, ks > 0 ? 1u : 0u);
                             }
                     }
                     commit(&sh.s_full[k & 1]);
@@ -880,7 +925,6 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
             // ------------------------------------------------------ softmax
             const int r = warp * 32 + lane;                 // row of the CTA tile
             const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-            uint8_t *qstage = smem + kNS * STAGE;           // [128 rows][D * 2 B]
             Cursor c;
             cursor_init(P, t_begin, c);
             float m_used = -INFINITY, l = 0.f;
@@ -892,57 +936,6 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
             long long k = 0;
             const float sc = A.scale_log2;
 
-            // this row's query for the segment at cursor cq (nullptr: padding)
-            auto q_row = [&](const Cursor &cq) -> const uint4 * {
-                const int p = cq.rb * kRows + r;
-                if (p >= A.M) return nullptr;
-                const int rr = p / A.G, hq = cq.h * A.G + p % A.G;
-                return reinterpret_cast<const uint4 *>(
-                    static_cast<const __nv_bfloat16 *>(A.q) + (((size_t)cq.b * A.R + rr) * A.Hq + hq) * D);
-            };
-            // start copying a query row into this thread's staging row
-            // (16-byte chunk v at chunk v ^ (r % 16): conflict-free reads)
-            auto stage_q = [&](const uint4 *src) {
-                if (src) {
-#pragma unroll
-                    for (int v = 0; v < D / 8; ++v) {
-                        const uint32_t dst = smem_u32(qstage + r * (D * 2) + ((v ^ (r & 15)) << 4));
-                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
-                                     "l"(src + v)
-                                     : "memory");
-                    }
-                }
-                asm volatile("cp.async.commit_group;" ::: "memory");
-            };
-            // query row -> TMEM Q buffer n % 2 (the bf16 pairs of a row, in
-            // order, are exactly the 32-bit columns the MMA reads); from
-            // global memory, or from this thread's staging row
-            auto put_q = [&](const uint4 *src, bool staged, int n) {
-                if (staged) asm volatile("cp.async.wait_all;" ::: "memory");
-#pragma unroll
-                for (int c32 = 0; c32 < D / 64; ++c32) {
-                    uint32_t w[32];
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        const int vi = c32 * 8 + v;
-                        uint4 x = make_uint4(0u, 0u, 0u, 0u);
-                        if (src) {
-                            x = staged ? *reinterpret_cast<const uint4 *>(
-                                             qstage + r * (D * 2) + ((vi ^ (r & 15)) << 4))
-                                       : src[vi];
-                        }
-                        w[4 * v] = x.x;
-                        w[4 * v + 1] = x.y;
-                        w[4 * v + 2] = x.z;
-                        w[4 * v + 3] = x.w;
-                    }
-                    st32(tmem + lane_base + kColQ + (uint32_t)(n & 1) * 128 + c32 * 32, w);
-                }
-                wait_st();
-                fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.q_ready[n & 1]);
-            };
             // end of this CTA's part of a segment (after PV(j)): a segment
             // wholly inside this CTA's range writes its final O (bf16) and
             // LSE; otherwise the (m, l, O) partial goes to the workspace
@@ -1010,29 +1003,6 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                     seg_id = (c.b * A.Hkv + c.h) * A.n_rb + c.rb;
                     const long long seg_lo = t - c.tile;
                     seg_whole = seg_lo >= t_begin && seg_lo + c.n_tiles <= t_end;
-                    // the next two segments of this range, if any
-                    const long long t_next = t + (c.n_tiles - c.tile);
-                    Cursor cn = c;
-                    cn.tile = cn.n_tiles - 1;
-                    cursor_next(P, cn);
-                    const bool has_next = t_next < t_end;
-                    const bool has_next2 = has_next && t_next + cn.n_tiles < t_end;
-                    Cursor cnn = cn;
-                    if (has_next2) {
-                        cnn.tile = cnn.n_tiles - 1;
-                        cursor_next(P, cnn);
-                    }
-                    // Q(seg_n) is in TMEM buffer seg_n % 2 already (except at
-                    // the first segment); Q(seg_n + 1) goes to the other
-                    // buffer now (its previous S MMAs finished: the epilogue
-                    // waited for the last PV); Q(seg_n + 2) starts staging.
-                    if (k == 0) {
-                        put_q(q_row(c), false, 0);
-                        if (has_next) put_q(q_row(cn), false, 1);
-                    } else if (has_next) {
-                        put_q(q_row(cn), true, seg_n + 1);
-                    }
-                    if (has_next2) stage_q(q_row(cnn));
                     // this row's flags for the segment
                     const int p = c.rb * kRows + r;
                     warp_rows = c.rb * kRows + warp * 32 < A.M;
@@ -1180,7 +1150,6 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                 cursor_next(P, c);
             }
             if (ok && k > 0) ok = epilogue(k - 1);
-            asm volatile("cp.async.wait_all;" ::: "memory");
             if (!ok) {
                 raise_status(A.status, SPEC_DEV_TIMEOUT);
                 *abort = 1;
@@ -1365,8 +1334,9 @@ spec_status_t launch_impl(const TcParams &P, const CUtensorMap *maps, cudaStream
 spec_status_t launch_umma(const TcParams &P, const CUtensorMap *maps, cudaStream_t s) {
     constexpr int D = 128;
     constexpr size_t smem = (size_t)umma::kNS * 2 * (D / 64) * kHalfBytes +   // K/V stages
-                            (size_t)umma::kRows * D * 2 +                    // query staging
+                            2 * (size_t)umma::kRows * D * 2 +                // query blocks
                             sizeof(umma::Shared) + 1024;
+    static_assert(smem <= 227 * 1024, "shared memory of the tcgen05 verify kernel");
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -1375,7 +1345,8 @@ spec_status_t launch_umma(const TcParams &P, const CUtensorMap *maps, cudaStream
     });
     if (attr_err != cudaSuccess) return SPEC_ERR_CUDA;
     attn_umma_kernel<D><<<P.n_ctas, umma::kThreads, smem, s>>>(P, maps[0], maps[1], maps[2],
-                                                                 maps[3], maps[4], maps[5]);
+                                                                 maps[3], maps[4], maps[5],
+                                                                 maps[6]);
     spec_status_t st = launch_status();
     if (st != SPEC_OK) return st;
     if (P.n_ctas > 1)
@@ -1396,8 +1367,10 @@ bool tc_supported(const AttnParams &P, int dtype) {
 }
 
 // The tcgen05 kernel takes 128-row blocks: worth it once a KV head carries
-// at least 64 packed rows (the contraction, not HBM, is then the bound).
-bool umma_selected(const AttnParams &P) { return P.d == 128 && P.M >= 64; }
+// at least 64 packed rows (the contraction, not HBM, is then the bound).  Its
+// query blocks are copied as (128 / G) speculative rows x G heads, so G must
+// divide 128.
+bool umma_selected(const AttnParams &P) { return P.d == 128 && P.M >= 64 && 128 % P.G == 0; }
 
 int tc_rows_per_block(const AttnParams &P) {
     if (umma_selected(P)) return umma::kRows;
@@ -1430,7 +1403,7 @@ spec_status_t launch_attn_tc(const AttnParams &A, cudaStream_t s) {
     P.tail = P.soft_tiles + ceil_div(A.R, kTile);
     P.box_rows = A.paged ? (A.d / 64) * A.page_size : kTile;
     P.page_log2 = A.page_size == 16 ? 4 : A.page_size == 32 ? 5 : 6;
-    CUtensorMap maps[6];
+    CUtensorMap maps[7];
     // paged caches: [page][head][d / 64][page_size][64] viewed as rows of 64
     // elements, one box = one (page, head); contiguous: rows of d elements
     const long long cache_rows = A.paged ? A.cache_rows * (A.d / 64) : A.cache_rows;
@@ -1446,6 +1419,16 @@ spec_status_t launch_attn_tc(const AttnParams &A, cudaStream_t s) {
     } else {
         maps[4] = maps[2];
         maps[5] = maps[3];
+    }
+    if (ok && use_umma) {
+        // q as [B * R][Hkv][G][d]: one box = the G heads of 128 / G rows, i.e.
+        // 128 packed rows (r * G + g) of one KV head, 64 elements wide
+        const cuuint64_t dims[4] = {(cuuint64_t)A.d, (cuuint64_t)A.G, (cuuint64_t)A.Hkv,
+                                    (cuuint64_t)A.B * A.R};
+        const cuuint64_t strides[3] = {(cuuint64_t)A.d * 2, (cuuint64_t)A.G * A.d * 2,
+                                       (cuuint64_t)A.Hq * A.d * 2};
+        const cuuint32_t box[4] = {64u, (cuuint32_t)A.G, 1u, (cuuint32_t)(umma::kRows / A.G)};
+        ok = encode_bf16_map(&maps[6], A.q, 4, dims, strides, box);
     }
     if (!ok) return SPEC_ERR_CUDA;
     if (use_umma) return launch_umma(P, maps, s);
