@@ -930,6 +930,18 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
             float m_used = -INFINITY, l = 0.f;
             bool rvalid = false, rsoft = false, warp_rows = false;
             int rrow = -1, seg_n = 0, vmask_j = -1;
+            // the next segment's row flags and block tile 0's mask words,
+            // loaded one segment ahead (unconditional loads of a clamped
+            // row, so nothing waits for them before their use)
+            uint32_t nx_fl = 0, nx_w0 = 0, nx_w1 = 0;
+            auto fetch_row = [&](const Cursor &cq) {
+                const int p = min(cq.rb * kRows + r, A.M - 1);
+                const size_t ri = (size_t)cq.b * A.R + p / A.G;
+                nx_fl = A.row_flags[ri];
+                const uint32_t *vr = A.vis + ri * A.W;
+                nx_w0 = vr[0];
+                nx_w1 = vr[A.W > 1 ? 1 : 0];
+            };
             int seg_b = 0, seg_h = 0, seg_rb = 0, seg_id = 0;
             uint64_t vmask = 0;
             bool first = true, seg_whole = false;
@@ -1003,21 +1015,29 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                     seg_id = (c.b * A.Hkv + c.h) * A.n_rb + c.rb;
                     const long long seg_lo = t - c.tile;
                     seg_whole = seg_lo >= t_begin && seg_lo + c.n_tiles <= t_end;
-                    // this row's flags for the segment
+                    // this row's flags for the segment (fetched one segment
+                    // ahead, except at the range's first)
                     const int p = c.rb * kRows + r;
                     warp_rows = c.rb * kRows + warp * 32 < A.M;
-                    rvalid = rsoft = false;
-                    rrow = -1;
-                    if (p < A.M) {
-                        rrow = p / A.G;
-                        const uint8_t fl = A.row_flags[(size_t)c.b * A.R + rrow];
-                        rvalid = (fl & SPEC_ROW_VALID) != 0;
-                        rsoft = rvalid && (fl & SPEC_ROW_SEES_SOFT) != 0;
+                    if (k == 0) fetch_row(c);
+                    rrow = p < A.M ? p / A.G : -1;
+                    rvalid = rrow >= 0 && (nx_fl & SPEC_ROW_VALID) != 0;
+                    rsoft = rvalid && (nx_fl & SPEC_ROW_SEES_SOFT) != 0;
+                    vmask = rvalid ? ((uint64_t)nx_w0 | (A.W > 1 ? (uint64_t)nx_w1 << 32 : 0ull))
+                                   : 0ull;
+                    vmask_j = 0;
+                    {
+                        const long long t_next = t + (c.n_tiles - c.tile);
+                        if (t_next < t_end) {
+                            Cursor cn = c;
+                            cn.tile = cn.n_tiles - 1;
+                            cursor_next(P, cn);
+                            fetch_row(cn);
+                        }
                     }
                     ++seg_n;
                     m_used = -INFINITY;
                     l = 0.f;
-                    vmask_j = -1;
                     first = true;
                 }
                 if (ti.kind == kBlock && vmask_j != ti.j) {
