@@ -281,6 +281,8 @@ __device__ __forceinline__ void run_producer(const TcParams &P, const CUtensorMa
     };
 
     long long k = 0;
+    int stage = 0;                       // stage of tile k, and its fill parity
+    uint32_t sphase = 0;
     int nq = 0;                          // query blocks issued
     bool ok = true;
     int ids = load_ids(gc, t_begin);
@@ -303,8 +305,12 @@ __device__ __forceinline__ void run_producer(const TcParams &P, const CUtensorMa
                     }
                 }
             }
-            const int s = (int)(k % NS);
-            const uint32_t ph = (uint32_t)((k / NS) & 1);
+            const int s = stage;
+            const uint32_t ph = sphase;
+            if (++stage == NS) {
+                stage = 0;
+                sphase ^= 1u;
+            }
             bool got = true;
             if (ql && (k == 0 || tc.tile == 0)) {
                 // the segment's query block, ahead of its first K/V tile
@@ -833,8 +839,8 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                 bool prev_first = true;
                 bool ok = true;
                 // O += P(j) V(j): A = P buffer j%2 (TMEM), B = V (MN-major smem)
-                auto issue_pv = [&](long long j, int rbl, int stage, bool first) -> bool {
-                    const int b = (int)(j & 1);
+                auto issue_pv = [&](int j, int rbl, int stage, bool first) -> bool {
+                    const int b = j & 1;
                     if (!mbar_wait(&sh.p_full[b], (uint32_t)((j >> 1) & 1))) return false;
                     fence_after();
                     const uint32_t vb = smem_u32(smem + stage * STAGE + KV_BYTES);
@@ -856,11 +862,12 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                     commit(&sh.empty[stage]);
                     return true;
                 };
-                long long k = 0;
+                int k = 0;                     // tiles of this range so far
+                int stage = 0;                 // their K/V stage, and its fill parity
+                uint32_t sph = 0;
                 for (long long t = t_begin; t < t_end && ok; ++t, ++k) {
                     const TileInfo ti = tile_info(P, c);
                     const bool new_seg = (k == 0) || (c.tile == 0);
-                    const int stage = (int)(k % kNS);
                     const int rbl = (ti.kind == kPrefix && A.paged) ? P.page_log2 : 6;
                     if (new_seg && k > 0) {
                         ok = issue_pv(k - 1, prev_rbl, prev_stage, prev_first);
@@ -876,7 +883,7 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                         qd = smem_desc(smem_u32(qbuf + (seg_n & 1) * (kRows * D * 2)), 16, 1024);
                         ++seg_n;
                     }
-                    if (!mbar_wait(&sh.full[stage], (uint32_t)((k / kNS) & 1))) { ok = false; break; }
+                    if (!mbar_wait(&sh.full[stage], sph)) { ok = false; break; }
                     // S(k) = Q K^T into S buffer k%2
                     const uint32_t kb = smem_u32(smem + stage * STAGE);
                     const uint32_t s_col = tmem + kColS + (uint32_t)(k & 1) * kTile;
@@ -910,6 +917,10 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                     prev_rbl = rbl;
                     prev_stage = stage;
                     prev_first = new_seg;
+                    if (++stage == kNS) {
+                        stage = 0;
+                        sph ^= 1u;
+                    }
                     cursor_next(P, c);
                 }
                 if (ok && k > 0) ok = issue_pv(k - 1, prev_rbl, prev_stage, prev_first);
