@@ -738,6 +738,7 @@ constexpr int kTmemCols = 512;
 constexpr int kColO = 0;                // O: columns [0, 128)
 constexpr int kColS = 128;              // S buffer b: [128 + 64 b, 192 + 64 b)
 constexpr int kColP = 320;              // P buffer b: [320 + 32 b, 352 + 32 b), bf16 pairs
+constexpr int kColQ = 384;              // Q buffer b: [384 + 64 b, 448 + 64 b), bf16 pairs
 constexpr float kRescale = 8.f;         // log2 growth allowed before rescaling
 
 // Byte offset, inside a K or V tile, of token `tok`'s first 128-byte row
@@ -752,6 +753,7 @@ struct Shared {
     uint64_t full[kNS], empty[kNS];
     uint64_t s_full[2], p_full[2], o_upd[2];
     uint64_t q_full[2], q_empty[2];     // Q buffer b holds segment n (n % 2 == b)
+    uint64_t q_tfree[2];                // TMEM Q buffer b: its segment's S MMAs done
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -798,6 +800,7 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sh.q_full[b], 1);
             mbar_init(&sh.q_empty[b], 1);
+            mbar_init(&sh.q_tfree[b], 1);
         }
         mbar_init(&sh.drain, 1);
         sh.abort = 0;
@@ -833,7 +836,7 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
             if (lane == 0) {
                 const uint32_t id_pv = idesc(kRows, D, false, true);
                 const uint32_t id_s64 = idesc(kRows, kTile, false, false);
-                uint64_t qd = 0;               // query block of the current segment
+                uint32_t a_q = 0;              // TMEM query block of the current segment
                 int seg_n = 0;
                 int prev_rbl = 6, prev_stage = 0;
                 bool prev_first = true;
@@ -874,13 +877,25 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                         if (!ok) break;
                     }
                     if (new_seg) {
-                        // the previous segment's S MMAs were its last readers
-                        if (seg_n > 0) commit(&sh.q_empty[(seg_n - 1) & 1]);
-                        if (!mbar_wait(&sh.q_full[seg_n & 1], (uint32_t)((seg_n >> 1) & 1))) {
+                        // the segment's query block: shared memory -> TMEM
+                        // buffer seg_n % 2 (tcgen05.cp, ordered before the
+                        // MMAs that read it), once the segment two back has
+                        // finished its S MMAs on that buffer; the copy's
+                        // completion frees the shared-memory block
+                        const int qb = seg_n & 1;
+                        if ((seg_n >= 2 &&
+                             !mbar_wait(&sh.q_tfree[qb], (uint32_t)(((seg_n - 2) >> 1) & 1))) ||
+                            !mbar_wait(&sh.q_full[qb], (uint32_t)((seg_n >> 1) & 1))) {
                             ok = false;
                             break;
                         }
-                        qd = smem_desc(smem_u32(qbuf + (seg_n & 1) * (kRows * D * 2)), 16, 1024);
+                        a_q = tmem + kColQ + (uint32_t)qb * 64;
+                        const uint64_t qd = smem_desc(smem_u32(qbuf + qb * (kRows * D * 2)), 16, 1024);
+#pragma unroll
+                        for (int i = 0; i < D / 16; ++i)
+                            tc_cp_128x256b(a_q + i * 8,
+                                           qd + (uint64_t)((((i >> 2) * kQHalf) + (i & 3) * 32) >> 4));
+                        commit(&sh.q_empty[qb]);
                         ++seg_n;
                     }
                     if (!mbar_wait(&sh.full[stage], sph)) { ok = false; break; }
@@ -891,9 +906,9 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                         const uint64_t kd = smem_desc(kb, 16, 1024);
 #pragma unroll
                         for (int ks = 0; ks < D / 16; ++ks)
-                            mma_ss(s_col, qd + (uint64_t)((((ks >> 2) * kQHalf) + (ks & 3) * 32) >> 4),
-                                   kd + (uint64_t)((((ks >> 2) * kHalfBytes) + (ks & 3) * 32) >> 4),
-                                   id_s64, ks > 0 ? 1u : 0u);
+                            mma(s_col, a_q + ks * 8,
+                                kd + (uint64_t)((((ks >> 2) * kHalfBytes) + (ks & 3) * 32) >> 4),
+                                id_s64, ks > 0 ? 1u : 0u);
                     } else {
                         // paged tile: one MMA per page block (its 8-row groups
                         // are contiguous only within the block)
@@ -904,12 +919,14 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                             for (int ks = 0; ks < D / 16; ++ks) {
                                 const int hh = ks >> 2, kk = ks & 3;
                                 const uint32_t boff = (uint32_t)((i * NH + hh) * blk) * 128u + kk * 32;
-                                mma_ss(s_col + i * blk,
-                                       qd + (uint64_t)(((hh * kQHalf) + kk * 32) >> 4),
-                                       smem_desc(kb + boff, 16, 1024), id_s, ks > 0 ? 1u : 0u);
+                                mma(s_col + i * blk, a_q + ks * 8, smem_desc(kb + boff, 16, 1024),
+                                    id_s, ks > 0 ? 1u : 0u);
                             }
                     }
                     commit(&sh.s_full[k & 1]);
+                    // last S of the segment in this range: its TMEM query
+                    // buffer may be refilled two segments on
+                    if (c.tile == c.n_tiles - 1 || t == t_end - 1) commit(&sh.q_tfree[(seg_n - 1) & 1]);
                     if (!new_seg && k > 0) {
                         ok = issue_pv(k - 1, prev_rbl, prev_stage, prev_first);
                         if (!ok) break;

@@ -176,6 +176,14 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, 
         "l"(a), "l"(b), "r"(id), "r"(accumulate));
 }
 
+// TMEM <- shared memory: 128 rows x 256 bits (16 bf16 per row) of a
+// matrix-descriptor-described operand tile into lanes 0..127, 8 32-bit
+// columns from taddr (lane = row, the row's bits in order).  Asynchronous;
+// ordered before this thread's later tcgen05.mma.
+__device__ __forceinline__ void tc_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc));
+}
+
 // Arrive on `bar` once every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void commit(uint64_t *bar) {
