@@ -729,9 +729,12 @@ using namespace tc5;
 
 constexpr int kRows = 128;              // rows per CTA tile (MMA M)
 constexpr int kSoftmaxWarps = 4;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kThreads = 6 * 32;
+// The producer and the MMA issuer sit on SM sub-partitions 3 and 2, whose
+// softmax warps are the idle ones when a block has at most 64 rows (warps
+// 4 and 5 only complete the warp count).
+constexpr int kProducerWarp = 7;
+constexpr int kMmaWarp = 6;
+constexpr int kThreads = 8 * 32;
 constexpr int kNS = 5;                  // K/V stages
 constexpr int kQHalf = kRows * 128;     // one 64-element half of a query block
 constexpr int kTmemCols = 512;
@@ -949,7 +952,7 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                 commit(&sh.drain);
                 if (!mbar_wait(&sh.drain, 0)) raise_status(A.status, SPEC_DEV_TIMEOUT);
             }
-        } else {
+        } else if (warp < kSoftmaxWarps) {
             // ------------------------------------------------------ softmax
             const int r = warp * 32 + lane;                 // row of the CTA tile
             const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
