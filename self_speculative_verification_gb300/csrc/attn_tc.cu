@@ -48,6 +48,9 @@ struct TcParams {
     int tail;            // soft_tiles + ceil(R / 64)
     int box_rows;        // rows per cache box: 64 (contiguous) or NH * page_size
     int page_log2;       // log2(page_size) (paged)
+    int seg_cost;        // what a segment start costs, in tiles, for the split
+    long long *bounds;   // first tile of each CTA's range, [n_ctas + 1] (workspace),
+                         // written by the attention kernel for the combine
 };
 
 // -------------------------------------------- mma.sync helpers
@@ -153,13 +156,92 @@ __device__ void warp_locate(const TcParams &P, long long t, int *b_out, long lon
     *start_out = acc;
 }
 
-// First tile of CTA i's range.
-__device__ __forceinline__ long long range_lo(long long T, int i, int n) { return T * i / n; }
+// The split.  CTAs take equal parts of a cost space in which every segment
+// counts its tiles plus P.seg_cost for its start (epilogue, query block,
+// row flags), so a CTA whose range holds many short segments gets fewer
+// tiles.  Segment s of request b occupies costs [Cb + s u, Cb + (s + 1) u),
+// u = tiles + seg_cost; the first seg_cost + 1 of them map to its first tile.
+// A CTA's range is the tiles its part of the cost space maps to.
 
-// CTA whose range holds tile t.
-__device__ __forceinline__ int cta_of(long long T, long long t, int n) {
-    long long i = ((t + 1) * n - 1) / T;
-    return (int)(i < n - 1 ? i : n - 1);
+__device__ __forceinline__ long long req_cost(const TcParams &P, int b) {
+    return (long long)(seg_tiles(P, req_seq(P, b)) + P.seg_cost) * P.a.Hkv * P.a.n_rb;
+}
+
+// Total cost over all requests (every lane gets it).
+__device__ long long warp_total_cost(const TcParams &P) {
+    const int lane = threadIdx.x & 31;
+    long long s = 0;
+    for (int b = lane; b < P.a.B; b += 32) s += req_cost(P, b);
+    return warp_sum_ll(s);
+}
+
+// Request containing cost position c (< total), with the costs and tiles of
+// the requests before it (every lane gets them).
+__device__ void warp_locate_cost(const TcParams &P, long long c, int *b_out, long long *cost0,
+                                 long long *tile0) {
+    const int lane = threadIdx.x & 31;
+    const int B = P.a.B;
+    const int per = ceil_div(B, 32);
+    const int lo = min(B, lane * per), hi = min(B, lo + per);
+    long long sc = 0, st = 0;
+    for (int b = lo; b < hi; ++b) {
+        sc += req_cost(P, b);
+        st += req_tiles(P, b);
+    }
+    long long ic = sc, it = st;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long vc = __shfl_up_sync(0xffffffffu, ic, o);
+        const long long vt = __shfl_up_sync(0xffffffffu, it, o);
+        if (lane >= o) {
+            ic += vc;
+            it += vt;
+        }
+    }
+    const long long ec = ic - sc, et = it - st;
+    const unsigned m = __ballot_sync(0xffffffffu, lo < hi && c >= ec && c < ic);
+    const int src = m ? __ffs(m) - 1 : 0;
+    long long ac = __shfl_sync(0xffffffffu, ec, src);
+    long long at = __shfl_sync(0xffffffffu, et, src);
+    int b = src * per;
+    while (b < B - 1) {
+        const long long n = req_cost(P, b);
+        if (c < ac + n) break;
+        ac += n;
+        at += req_tiles(P, b);
+        ++b;
+    }
+    *b_out = b;
+    *cost0 = ac;
+    *tile0 = at;
+}
+
+// First tile of CTA i's range (C, T: total cost and tiles; warp-collective).
+__device__ long long warp_range_lo(const TcParams &P, long long C, long long T, int i) {
+    if (i <= 0) return 0;
+    if (i >= P.n_ctas) return T;
+    if (P.seg_cost == 0) return T * i / P.n_ctas;    // plain tile split
+    const long long c = C * i / P.n_ctas;
+    int b;
+    long long c0, t0;
+    warp_locate_cost(P, c, &b, &c0, &t0);
+    const int nt = seg_tiles(P, req_seq(P, b));
+    const long long u = nt + P.seg_cost;
+    const long long seg = (c - c0) / u, off = (c - c0) % u;
+    return t0 + seg * nt + (off > P.seg_cost ? off - P.seg_cost : 0);
+}
+
+// CTA whose range holds tile t, from the bounds the attention kernel wrote:
+// the last CTA whose range starts at or before t (empty ranges share their
+// start with the next one).
+__device__ __forceinline__ int cta_holding(const TcParams &P, long long t) {
+    int lo = 0, hi = P.n_ctas - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (P.bounds[mid] <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
 }
 
 struct Cursor {
@@ -454,8 +536,13 @@ attn_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUten
 
     const long long T = warp_total_tiles(P);
     const int cta = blockIdx.x;
-    const long long t_begin = range_lo(T, cta, P.n_ctas);
-    const long long t_end = range_lo(T, cta + 1, P.n_ctas);
+    const long long C = warp_total_cost(P);
+    const long long t_begin = warp_range_lo(P, C, T, cta);
+    const long long t_end = warp_range_lo(P, C, T, cta + 1);
+    if (threadIdx.x == 0) {
+        P.bounds[cta] = t_begin;
+        if (cta == P.n_ctas - 1) P.bounds[P.n_ctas] = T;
+    }
     if (t_begin >= t_end) return;
 
     if (warp == NCW) {
@@ -823,8 +910,13 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
 
     const long long T = warp_total_tiles(P);
     const int cta = blockIdx.x;
-    const long long t_begin = range_lo(T, cta, P.n_ctas);
-    const long long t_end = range_lo(T, cta + 1, P.n_ctas);
+    const long long C = warp_total_cost(P);
+    const long long t_begin = warp_range_lo(P, C, T, cta);
+    const long long t_end = warp_range_lo(P, C, T, cta + 1);
+    if (threadIdx.x == 0) {
+        P.bounds[cta] = t_begin;
+        if (cta == P.n_ctas - 1) P.bounds[P.n_ctas] = T;
+    }
     volatile int *abort = &sh.abort;
 
     if (t_begin < t_end) {
@@ -1219,13 +1311,13 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
 // partials from CTAs first..last, wcn per CTA) into the final O and LSE.
 // One warp.
 template <int D>
-__device__ void merge_row(const TcParams &P, int wcn, long long T, int b, int h, int seg,
+__device__ void merge_row(const TcParams &P, int wcn, int b, int h, int seg,
                           long long s0, long long s1, int first, int last, int p, int lane) {
     const AttnParams &A = P.a;
     const int rr = p % A.rb_rows;
     float mstar = -INFINITY;
     for (int i = first; i <= last; ++i) {
-        const long long lo = range_lo(T, i, P.n_ctas), hi = range_lo(T, i + 1, P.n_ctas);
+        const long long lo = P.bounds[i], hi = P.bounds[i + 1];
         if (max(lo, s0) >= min(hi, s1)) continue;
         for (int w = 0; w < wcn; ++w)
             mstar = fmaxf(mstar, A.part_ml[slot_row(P, seg, i, w, wcn, rr) * 2]);
@@ -1239,7 +1331,7 @@ __device__ void merge_row(const TcParams &P, int wcn, long long T, int b, int h,
     if (mstar != -INFINITY) {
         float L = 0.f;
         for (int i = first; i <= last; ++i) {
-            const long long lo = range_lo(T, i, P.n_ctas), hi = range_lo(T, i + 1, P.n_ctas);
+            const long long lo = P.bounds[i], hi = P.bounds[i + 1];
             if (max(lo, s0) >= min(hi, s1)) continue;
             for (int w = 0; w < wcn; ++w) {
                 const size_t row = slot_row(P, seg, i, w, wcn, rr);
@@ -1278,14 +1370,12 @@ __global__ void __launch_bounds__(128) attn_tc_combine_kernel(const __grid_const
     const int h = blockIdx.y, b = blockIdx.z;
     if (p >= A.M) return;
     if (p == 0 && h == 0 && lane == 0) check_seq_len(A, b);
-    const long long T = warp_total_tiles(P);
     const int rb = p / A.rb_rows;
     const int nt = seg_tiles(P, req_seq(P, b));
     const long long s0 = warp_tiles_before(P, b) + (long long)(h * A.n_rb + rb) * nt;
     const long long s1 = s0 + nt;
     const int seg = (b * A.Hkv + h) * A.n_rb + rb;
-    merge_row<D>(P, wcn, T, b, h, seg, s0, s1, cta_of(T, s0, P.n_ctas),
-                 cta_of(T, s1 - 1, P.n_ctas), p, lane);
+    merge_row<D>(P, wcn, b, h, seg, s0, s1, cta_holding(P, s0), cta_holding(P, s1 - 1), p, lane);
 }
 
 // tcgen05 path: a segment wholly inside one CTA's range already holds its
@@ -1304,9 +1394,8 @@ attn_umma_combine_kernel(const __grid_constant__ TcParams P) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (blockIdx.x == 0 && blockIdx.y == 0)
         for (int b = threadIdx.x; b < A.B; b += kUmmaCombineThreads) check_seq_len(A, b);
-    const long long T = warp_total_tiles(P);
-    const long long tb = range_lo(T, blockIdx.x + 1, P.n_ctas);
-    if (tb <= 0 || tb >= T) return;
+    const long long tb = P.bounds[blockIdx.x + 1];
+    if (tb <= 0 || tb >= P.bounds[P.n_ctas]) return;
     int b;
     long long start;
     warp_locate(P, tb, &b, &start);
@@ -1314,16 +1403,16 @@ attn_umma_combine_kernel(const __grid_constant__ TcParams P) {
     const int segi = (int)((tb - start) / nt);
     const long long s0 = start + (long long)segi * nt, s1 = s0 + nt;
     if (s0 == tb) return;                       // the boundary starts a segment
-    const int first = cta_of(T, s0, P.n_ctas);
+    const int first = cta_holding(P, s0);
     if (first != (int)blockIdx.x) return;        // not this segment's first boundary
-    const int last = cta_of(T, s1 - 1, P.n_ctas);
+    const int last = cta_holding(P, s1 - 1);
     const int h = segi / A.n_rb, rb = segi % A.n_rb;
     const int seg = (b * A.Hkv + h) * A.n_rb + rb;
     const int p_hi = min(A.M, (rb + 1) * A.rb_rows);
     constexpr int kWarps = kUmmaCombineThreads / 32;
     for (int p = rb * A.rb_rows + blockIdx.y * kWarps + warp; p < p_hi;
          p += kUmmaCombineSplit * kWarps)
-        merge_row<D>(P, 1, T, b, h, seg, s0, s1, first, last, p, lane);
+        merge_row<D>(P, 1, b, h, seg, s0, s1, first, last, p, lane);
 }
 
 // Single-CTA launches have no boundary: only the seq_len check remains.
@@ -1440,8 +1529,10 @@ size_t tc_workspace_bytes(const AttnParams &P, size_t *off_ml) {
     const size_t segs = (size_t)P.B * P.Hkv * P.n_rb;
     const size_t rows = (segs + (size_t)ctas) * wc * P.rb_rows;
     const size_t o_bytes = (rows * P.d * sizeof(float) + 255) & ~size_t(255);
+    const size_t ml_bytes = (rows * 2 * sizeof(float) + 255) & ~size_t(255);
     *off_ml = o_bytes;
-    return o_bytes + ((rows * 2 * sizeof(float) + 255) & ~size_t(255));
+    // then the split's CTA bounds
+    return o_bytes + ml_bytes + (((size_t)ctas + 1) * sizeof(long long) + 255) / 256 * 256;
 }
 
 spec_status_t launch_attn_tc(const AttnParams &A, cudaStream_t s) {
@@ -1450,6 +1541,18 @@ spec_status_t launch_attn_tc(const AttnParams &A, cudaStream_t s) {
     const bool use_umma = umma_selected(A);
     const TcConfig cfg = use_umma ? TcConfig{8, 4, 0, 1} : choose(A);
     P.n_ctas = num_sms() * cfg.minb;
+    // a segment start costs the tcgen05 kernel about three tiles (epilogue,
+    // query block, row flags); the mma.sync kernel's segments (decode-shaped:
+    // long prefixes, few rows) are split by tiles alone
+    P.seg_cost = use_umma ? 3 : 0;
+    {
+        // the bounds follow the partials (same sizes as tc_workspace_bytes)
+        const int wc = use_umma ? 1 : cfg.ncw / cfg.wr;
+        const size_t segs = (size_t)A.B * A.Hkv * A.n_rb;
+        const size_t rows = (segs + (size_t)P.n_ctas) * wc * A.rb_rows;
+        P.bounds = reinterpret_cast<long long *>(
+            reinterpret_cast<char *>(A.part_ml) + ((rows * 2 * sizeof(float) + 255) & ~size_t(255)));
+    }
     P.soft_tiles = ceil_div(A.n_soft, kTile);
     P.tail = P.soft_tiles + ceil_div(A.R, kTile);
     P.box_rows = A.paged ? (A.d / 64) * A.page_size : kTile;
