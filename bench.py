@@ -417,8 +417,14 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
     assert bn.spec_get_status() == 0, "device status set during warm-up"
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_st + 1)]
-           for _ in range(args.steps)]
+    # The timed steps carry no events between their calls (an event between
+    # two kernels would stop the next one from being scheduled while the
+    # previous drains); with the L2 flushed between steps each step is timed
+    # by its own pair of events, the flush outside them.  The per-call
+    # breakdown comes from a separate pass of the same steps with events
+    # between the calls.
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
     region = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     if world > 1:
         dist.barrier()
@@ -426,7 +432,9 @@ def run_gpu(args):
     with ClockSampler(local) as clk:
         region[0].record(stream)
         for i in range(args.steps):
-            step(evs[i])
+            step_ev[i][0].record(stream)
+            step()
+            step_ev[i][1].record(stream)
             if flush:
                 flush_buf.random_()
         region[1].record(stream)
@@ -434,13 +442,22 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     status = bn.spec_get_status()
-
-    per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(n_st)]
-                    for i in range(args.steps)])          # ms per stage
-    step_ms = per.sum(axis=1)
+    step_ms = np.array([a.elapsed_time(b) for a, b in step_ev])
     region_ms = region[0].elapsed_time(region[1])
     total_ms = float(step_ms.sum()) if flush else region_ms
     total_ms = max_over_ranks(total_ms, dev)
+
+    # per-call breakdown (not part of the timed region)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_st + 1)]
+           for _ in range(args.steps)]
+    for i in range(args.steps):
+        step(evs[i])
+        if flush:
+            flush_buf.random_()
+    torch.cuda.synchronize(dev)
+    status |= bn.spec_get_status()
+    per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(n_st)]
+                    for i in range(args.steps)])          # ms per stage
 
     tokens = wl.verified_tokens()
     value = job_throughput(tokens, args.steps, world, total_ms)

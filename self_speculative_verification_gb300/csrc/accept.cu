@@ -68,6 +68,8 @@ __global__ void __launch_bounds__(kReduceThreads)
 vocab_reduce_kernel(const T *__restrict__ logits, int V, const int32_t *__restrict__ proposal,
                     int32_t *__restrict__ argmax, float *__restrict__ lse,
                     float *__restrict__ zprop, float inv_t) {
+    pdl_wait();
+    pdl_trigger();
     const float c2 = kLog2e * inv_t;
     cg::cluster_group cluster = cg::this_cluster();
     const int nc = (int)cluster.num_blocks();
@@ -175,6 +177,8 @@ struct AcceptParams {
 
 // One warp per request.
 __global__ void __launch_bounds__(128) accept_kernel(AcceptParams P) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.x * 4 + (threadIdx.x >> 5);
     if (b >= P.B) return;
@@ -296,13 +300,15 @@ spec_status_t launch_vocab_cluster(const void *logits, int n_rows, int V, int nc
     cfg.blockDim = dim3(kReduceThreads, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = nc;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, vocab_reduce_kernel<T>,
                                              static_cast<const T *>(logits), V, proposal, argmax,
                                              lse, zprop, inv_t);
@@ -358,6 +364,8 @@ __device__ __forceinline__ float prob_at(const T *row, int v, float lse, float i
 // token (tile sums, a scan over tiles, a scan inside the tile).
 template <typename T>
 __global__ void __launch_bounds__(kSoftThreads) soft_accept_kernel(SoftParams P) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float s_tile[kMaxSoftTiles];
     __shared__ int s_par[SPEC_MAX_ROWS];
     __shared__ uint8_t s_acc[SPEC_MAX_ROWS];
@@ -657,7 +665,8 @@ extern "C" spec_status_t spec_accept(const spec_accept_desc *d, const void *logi
     P.last_node = last_node;
     P.status = sv::status_ptr();
     if (!P.status) return SPEC_ERR_CUDA;
-    sv::accept_kernel<<<sv::ceil_div(P.B, 4), 128, 0, s>>>(P);
+    if (sv::launch(sv::accept_kernel, dim3(sv::ceil_div(P.B, 4)), dim3(128), 0, s, P) != SPEC_OK)
+        return SPEC_ERR_CUDA;
     return sv::launch_status();
 }
 
@@ -722,9 +731,10 @@ extern "C" spec_status_t spec_accept_soft(const spec_soft_desc *d, const void *l
     P.last_node = last_node;
     P.status = status_ptr();
     if (!P.status) return SPEC_ERR_CUDA;
-    if (d->logit_dtype == SPEC_BF16)
-        soft_accept_kernel<__nv_bfloat16><<<P.B, kSoftThreads, 0, s>>>(P);
-    else
-        soft_accept_kernel<float><<<P.B, kSoftThreads, 0, s>>>(P);
+    const spec_status_t ls =
+        d->logit_dtype == SPEC_BF16
+            ? launch(soft_accept_kernel<__nv_bfloat16>, dim3(P.B), dim3(kSoftThreads), 0, s, P)
+            : launch(soft_accept_kernel<float>, dim3(P.B), dim3(kSoftThreads), 0, s, P);
+    if (ls != SPEC_OK) return ls;
     return launch_status();
 }

@@ -499,6 +499,8 @@ attn_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUten
                const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mkb,
                const __grid_constant__ CUtensorMap mvb, const __grid_constant__ CUtensorMap msk,
                const __grid_constant__ CUtensorMap msv) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int NH = D / 64;                       // 128-byte halves per row
     constexpr int KV_BYTES = NH * kHalfBytes;        // K (or V) of one tile
     constexpr int STAGE = 2 * KV_BYTES;
@@ -857,6 +859,8 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                  const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mkb,
                  const __grid_constant__ CUtensorMap mvb, const __grid_constant__ CUtensorMap msk,
                  const __grid_constant__ CUtensorMap msv, const __grid_constant__ CUtensorMap mq) {
+    pdl_wait();
+    pdl_trigger();
     using namespace umma;
     static_assert(D == 128, "tcgen05 path is built for head_dim 128");
     constexpr int NH = D / 64;
@@ -1364,6 +1368,8 @@ __device__ __forceinline__ void check_seq_len(const AttnParams &A, int b) {
 template <int D>
 __global__ void __launch_bounds__(128) attn_tc_combine_kernel(const __grid_constant__ TcParams P,
                                                                int wcn) {
+    pdl_wait();
+    pdl_trigger();
     const AttnParams &A = P.a;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int p = blockIdx.x * 4 + warp;
@@ -1390,6 +1396,8 @@ constexpr int kUmmaCombineSplit = 8;     // CTAs per boundary (row slices of the
 template <int D>
 __global__ void __launch_bounds__(kUmmaCombineThreads)
 attn_umma_combine_kernel(const __grid_constant__ TcParams P) {
+    pdl_wait();
+    pdl_trigger();
     const AttnParams &A = P.a;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (blockIdx.x == 0 && blockIdx.y == 0)
@@ -1417,6 +1425,8 @@ attn_umma_combine_kernel(const __grid_constant__ TcParams P) {
 
 // Single-CTA launches have no boundary: only the seq_len check remains.
 __global__ void check_seq_len_kernel(const __grid_constant__ TcParams P) {
+    pdl_wait();
+    pdl_trigger();
     for (int b = threadIdx.x; b < P.a.B; b += blockDim.x) check_seq_len(P.a, b);
 }
 
@@ -1462,12 +1472,14 @@ spec_status_t launch_impl(const TcParams &P, const CUtensorMap *maps, cudaStream
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     });
     if (attr_err != cudaSuccess) return SPEC_ERR_CUDA;
-    attn_tc_kernel<D, WR, NCW, NS, MINB><<<P.n_ctas, (NCW + 1) * 32, smem, s>>>(
-        P, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5]);
+    if (launch(attn_tc_kernel<D, WR, NCW, NS, MINB>, dim3(P.n_ctas), dim3((NCW + 1) * 32), smem, s,
+               P, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5]) != SPEC_OK)
+        return SPEC_ERR_CUDA;
     spec_status_t st = launch_status();
     if (st != SPEC_OK) return st;
     dim3 grid(ceil_div(P.a.M, 4), P.a.Hkv, P.a.B);
-    attn_tc_combine_kernel<D><<<grid, 128, 0, s>>>(P, NCW / WR);
+    if (launch(attn_tc_combine_kernel<D>, dim3(grid), dim3(128), 0, s, P, NCW / WR) != SPEC_OK)
+        return SPEC_ERR_CUDA;
     return launch_status();
 }
 
@@ -1484,16 +1496,16 @@ spec_status_t launch_umma(const TcParams &P, const CUtensorMap *maps, cudaStream
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     });
     if (attr_err != cudaSuccess) return SPEC_ERR_CUDA;
-    attn_umma_kernel<D><<<P.n_ctas, umma::kThreads, smem, s>>>(P, maps[0], maps[1], maps[2],
-                                                                 maps[3], maps[4], maps[5],
-                                                                 maps[6]);
+    if (launch(attn_umma_kernel<D>, dim3(P.n_ctas), dim3(umma::kThreads), smem, s, P, maps[0],
+               maps[1], maps[2], maps[3], maps[4], maps[5], maps[6]) != SPEC_OK)
+        return SPEC_ERR_CUDA;
     spec_status_t st = launch_status();
     if (st != SPEC_OK) return st;
-    if (P.n_ctas > 1)
-        attn_umma_combine_kernel<D><<<dim3(P.n_ctas - 1, kUmmaCombineSplit),
-                                       kUmmaCombineThreads, 0, s>>>(P);
-    else
-        check_seq_len_kernel<<<1, 32, 0, s>>>(P);
+    const spec_status_t ls =
+        P.n_ctas > 1 ? launch(attn_umma_combine_kernel<D>, dim3(P.n_ctas - 1, kUmmaCombineSplit),
+                              dim3(kUmmaCombineThreads), 0, s, P)
+                     : launch(check_seq_len_kernel, dim3(1), dim3(32), 0, s, P);
+    if (ls != SPEC_OK) return ls;
     return launch_status();
 }
 

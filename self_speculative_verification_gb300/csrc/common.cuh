@@ -23,6 +23,36 @@ inline spec_status_t launch_status() {
     return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialisation, so it may be scheduled while the
+// kernel before it in the stream is still running; it first waits
+// (pdl_wait) until that kernel has completed and its writes are visible,
+// then lets the next one be scheduled (pdl_trigger).  Launch latency and
+// block scheduling thus overlap the previous kernel's tail.  Both are no-ops
+// for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+// kernel<<<grid, block, smem, stream>>>(args...) with the attribute above;
+// returns the launch's status.
+template <typename... KArgs, typename... Args>
+inline spec_status_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t s, Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...) == cudaSuccess
+               ? SPEC_OK
+               : SPEC_ERR_CUDA;
+}
+
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 __host__ __device__ inline long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
 

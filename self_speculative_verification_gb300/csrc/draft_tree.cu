@@ -77,6 +77,8 @@ constexpr int kMaxCand = 2048;
 // previous pick" over the whole row decide instead.
 template <typename T>
 __global__ void __launch_bounds__(kDraftThreads) draft_tree_kernel(DraftParams P) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float s_max[kDraftThreads];
     __shared__ float s_cv[kMaxCand];
     __shared__ int s_ci[kMaxCand];
@@ -280,6 +282,8 @@ __device__ __forceinline__ int clamp_nodes(const PruneParams &P, int b, bool rep
 // (keep[c] = 1 / 0; the root's entry is left to the compaction).
 template <typename T>
 __global__ void __launch_bounds__(kThreads) prune_edge_kernel(PruneParams P) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int s_kids[kMaxPruneNodes];
     __shared__ int s_nk;
     __shared__ float s_m[kThreads / 32], s_s[kThreads / 32];
@@ -381,6 +385,8 @@ __global__ void __launch_bounds__(kThreads) prune_edge_kernel(PruneParams P) {
 // chains in shared memory (parents precede children, so a chain ends), then
 // a block scan numbers the survivors.
 __global__ void __launch_bounds__(kThreads) prune_compact_kernel(PruneParams P) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int kPer = kMaxPruneNodes / kThreads;
     __shared__ int s_par[kMaxPruneNodes], s_idx[kMaxPruneNodes];
     __shared__ uint8_t s_edge[kMaxPruneNodes];
@@ -518,10 +524,11 @@ extern "C" spec_status_t spec_draft_tree(const spec_draft_desc *d, const void *s
     if (!P.status) return SPEC_ERR_CUDA;
     dim3 grid(d->gamma, d->batch);
     cudaStream_t s = as_stream(stream);
-    if (d->logit_dtype == SPEC_BF16)
-        draft_tree_kernel<__nv_bfloat16><<<grid, kDraftThreads, 0, s>>>(P);
-    else
-        draft_tree_kernel<float><<<grid, kDraftThreads, 0, s>>>(P);
+    const spec_status_t ls =
+        d->logit_dtype == SPEC_BF16
+            ? launch(draft_tree_kernel<__nv_bfloat16>, grid, dim3(kDraftThreads), 0, s, P)
+            : launch(draft_tree_kernel<float>, grid, dim3(kDraftThreads), 0, s, P);
+    if (ls != SPEC_OK) return ls;
     return launch_status();
 }
 
@@ -563,12 +570,14 @@ extern "C" spec_status_t spec_prune_tree(const spec_prune_desc *d, const int32_t
     if (!P.status) return SPEC_ERR_CUDA;
     cudaStream_t s = as_stream(stream);
     dim3 grid(d->max_nodes, d->batch);
-    if (d->logit_dtype == SPEC_BF16)
-        prune_edge_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(P);
-    else
-        prune_edge_kernel<float><<<grid, kThreads, 0, s>>>(P);
+    const spec_status_t ls =
+        d->logit_dtype == SPEC_BF16
+            ? launch(prune_edge_kernel<__nv_bfloat16>, grid, dim3(kThreads), 0, s, P)
+            : launch(prune_edge_kernel<float>, grid, dim3(kThreads), 0, s, P);
+    if (ls != SPEC_OK) return ls;
     spec_status_t st = launch_status();
     if (st != SPEC_OK) return st;
-    prune_compact_kernel<<<d->batch, kThreads, 0, s>>>(P);
+    if (launch(prune_compact_kernel, dim3(d->batch), dim3(kThreads), 0, s, P) != SPEC_OK)
+        return SPEC_ERR_CUDA;
     return launch_status();
 }

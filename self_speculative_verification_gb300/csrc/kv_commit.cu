@@ -92,6 +92,8 @@ __device__ void page_prefix(const CommitParams &P, int b, int *before, int *tota
 
 // One CTA per (request, KV head): copies every accepted row, K and V.
 __global__ void __launch_bounds__(128) kv_commit_copy_kernel(CommitParams P) {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x / P.Hkv, h = blockIdx.x % P.Hkv;
     int before = 0, total = 0;
     int head = 0;
@@ -147,6 +149,8 @@ __global__ void __launch_bounds__(128) kv_commit_copy_kernel(CommitParams P) {
 
 // One CTA: new page-table entries, seq_len += accepted, free_head += taken.
 __global__ void __launch_bounds__(256) kv_commit_finalize_kernel(CommitParams P) {
+    pdl_wait();
+    pdl_trigger();
     int head = 0, total = 0;
     if (P.paged) {
         int dummy = 0;
@@ -249,9 +253,11 @@ extern "C" spec_status_t kv_commit(const spec_kv_desc *cache, int batch, int n_r
     P.status = sv::status_ptr();
     if (!P.status) return SPEC_ERR_CUDA;
     cudaStream_t s = sv::as_stream(stream);
-    sv::kv_commit_copy_kernel<<<batch * P.Hkv, 128, 0, s>>>(P);
+    if (sv::launch(sv::kv_commit_copy_kernel, dim3(batch * P.Hkv), dim3(128), 0, s, P) != SPEC_OK)
+        return SPEC_ERR_CUDA;
     spec_status_t st = sv::launch_status();
     if (st != SPEC_OK) return st;
-    sv::kv_commit_finalize_kernel<<<1, 256, 0, s>>>(P);
+    if (sv::launch(sv::kv_commit_finalize_kernel, dim3(1), dim3(256), 0, s, P) != SPEC_OK)
+        return SPEC_ERR_CUDA;
     return sv::launch_status();
 }

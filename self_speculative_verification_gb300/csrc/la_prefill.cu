@@ -170,6 +170,8 @@ __global__ void __launch_bounds__(lap::kThreads, 1)
 la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__ CUtensorMap mq,
                   const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                   const __grid_constant__ lap::Sched S) {
+    pdl_wait();
+    pdl_trigger();
     using namespace lap;
     using namespace tc5;
     extern __shared__ uint8_t smem_raw[];
@@ -675,7 +677,8 @@ extern "C" spec_status_t spec_la_prefill_attn(const spec_prefill_desc *desc, con
         sched.n = 0;
         grid = (int)std::min<long long>(num_sms(), items);
     }
-    la_prefill_kernel<<<grid, lap::kThreads, lap::kSmemBytes, as_stream(stream)>>>(
-        P, maps[0], maps[1], maps[2], sched);
+    if (launch(la_prefill_kernel, dim3(grid), dim3(lap::kThreads), lap::kSmemBytes,
+               as_stream(stream), P, maps[0], maps[1], maps[2], sched) != SPEC_OK)
+        return SPEC_ERR_CUDA;
     return launch_status();
 }

@@ -18,6 +18,8 @@ __global__ void mask_build_kernel(const int32_t *__restrict__ vparent,
                                   const uint8_t *__restrict__ soft_flags, int R, int W,
                                   uint32_t *__restrict__ vis, uint8_t *__restrict__ row_flags,
                                   int *status) {
+    sv::pdl_wait();
+    sv::pdl_trigger();
     __shared__ int32_t svp[SPEC_MAX_ROWS];
     const int b = blockIdx.x;
     for (int r = threadIdx.x; r < R; r += blockDim.x) svp[r] = vparent[(size_t)b * R + r];
@@ -75,7 +77,8 @@ extern "C" spec_status_t spec_mask_build(const int32_t *vparent, const uint8_t *
     if (!st) return SPEC_ERR_CUDA;
     const int W = sv::ceil_div(n_rows, 32);
     const int threads = n_rows <= 128 ? 128 : 256;
-    mask_build_kernel<<<batch, threads, 0, sv::as_stream(stream)>>>(vparent, soft_flags, n_rows,
-                                                                   W, vis, row_flags, st);
+    if (sv::launch(mask_build_kernel, dim3(batch), dim3(threads), 0, sv::as_stream(stream), vparent,
+               soft_flags, n_rows, W, vis, row_flags, st) != SPEC_OK)
+        return SPEC_ERR_CUDA;
     return sv::launch_status();
 }

@@ -63,6 +63,8 @@ __device__ __forceinline__ void st8(float *p, const float (&x)[8]) {
 // one stream row per step; cos / sin of eps * s are computed once per CTA.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) rotate_kernel(RotateParams P) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float s_cos[kMaxGamma], s_sin[kMaxGamma];
     const int b = blockIdx.x / P.Hkv, h = blockIdx.x % P.Hkv;
     const int T_b = P.n_nodes[b];
@@ -100,6 +102,8 @@ struct GatherParams {
 };
 
 __global__ void __launch_bounds__(kThreads) gather_kernel(GatherParams P) {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x;
     const int ln = P.last_node[b];
     const int row = P.row_offset + ln;
@@ -142,10 +146,11 @@ extern "C" spec_status_t spec_stream_rotate_values(const spec_rotate_desc *d,
     P.status = status_ptr();
     if (!P.status) return SPEC_ERR_CUDA;
     const int grid = d->batch * d->n_kv_heads;
-    if (d->dtype == SPEC_BF16)
-        rotate_kernel<__nv_bfloat16><<<grid, kThreads, 0, as_stream(stream)>>>(P);
-    else
-        rotate_kernel<float><<<grid, kThreads, 0, as_stream(stream)>>>(P);
+    const spec_status_t ls =
+        d->dtype == SPEC_BF16
+            ? launch(rotate_kernel<__nv_bfloat16>, dim3(grid), dim3(kThreads), 0, as_stream(stream), P)
+            : launch(rotate_kernel<float>, dim3(grid), dim3(kThreads), 0, as_stream(stream), P);
+    if (ls != SPEC_OK) return ls;
     return launch_status();
 }
 
@@ -171,6 +176,7 @@ extern "C" spec_status_t spec_future_gather(int batch, int n_rows, int row_elems
     P.out = static_cast<uint8_t *>(out);
     P.status = status_ptr();
     if (!P.status) return SPEC_ERR_CUDA;
-    gather_kernel<<<batch, kThreads, 0, as_stream(stream)>>>(P);
+    if (launch(gather_kernel, dim3(batch), dim3(kThreads), 0, as_stream(stream), P) != SPEC_OK)
+        return SPEC_ERR_CUDA;
     return launch_status();
 }

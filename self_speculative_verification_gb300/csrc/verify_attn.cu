@@ -44,6 +44,8 @@ enum { kColPrefix = 0, kColSoft = 1, kColBlock = 2 };
 
 template <typename T, int D>
 __global__ void __launch_bounds__(128) attn_simt_kernel(AttnParams P) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float sq[kSimtRows][D];
     __shared__ float sk[kSimtCols][D + 1];
     __shared__ float sv_[kSimtCols][D];
@@ -205,6 +207,8 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnParams P) {
 // packed row.  O = sum_s 2^(m_s - m*) o_s / sum_s 2^(m_s - m*) l_s.
 template <typename T, int D>
 __global__ void __launch_bounds__(128) attn_combine_kernel(AttnParams P) {
+    pdl_wait();
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int p = blockIdx.x * 4 + warp;
     const int h = blockIdx.y, b = blockIdx.z;
@@ -338,16 +342,18 @@ spec_status_t make_plan(const spec_attn_desc *a, const spec_kv_desc *c, Plan *ou
 template <typename T>
 spec_status_t launch_simt(const AttnParams &P, cudaStream_t s) {
     dim3 grid(P.max_splits, P.Hkv * P.n_rb, P.B);
-    if (P.d == 64) attn_simt_kernel<T, 64><<<grid, 128, 0, s>>>(P);
-    else attn_simt_kernel<T, 128><<<grid, 128, 0, s>>>(P);
+    const spec_status_t ls = P.d == 64 ? launch(attn_simt_kernel<T, 64>, grid, dim3(128), 0, s, P)
+                                       : launch(attn_simt_kernel<T, 128>, grid, dim3(128), 0, s, P);
+    if (ls != SPEC_OK) return ls;
     return launch_status();
 }
 
 template <typename T>
 spec_status_t launch_combine(const AttnParams &P, cudaStream_t s) {
     dim3 grid(ceil_div(P.M, 4), P.Hkv, P.B);
-    if (P.d == 64) attn_combine_kernel<T, 64><<<grid, 128, 0, s>>>(P);
-    else attn_combine_kernel<T, 128><<<grid, 128, 0, s>>>(P);
+    const spec_status_t ls = P.d == 64 ? launch(attn_combine_kernel<T, 64>, grid, dim3(128), 0, s, P)
+                                       : launch(attn_combine_kernel<T, 128>, grid, dim3(128), 0, s, P);
+    if (ls != SPEC_OK) return ls;
     return launch_status();
 }
 
