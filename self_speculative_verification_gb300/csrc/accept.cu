@@ -69,7 +69,6 @@ vocab_reduce_kernel(const T *__restrict__ logits, int V, const int32_t *__restri
                     int32_t *__restrict__ argmax, float *__restrict__ lse,
                     float *__restrict__ zprop, float inv_t) {
     pdl_wait();
-    pdl_trigger();
     const float c2 = kLog2e * inv_t;
     cg::cluster_group cluster = cg::this_cluster();
     const int nc = (int)cluster.num_blocks();
@@ -178,7 +177,6 @@ struct AcceptParams {
 // One warp per request.
 __global__ void __launch_bounds__(128) accept_kernel(AcceptParams P) {
     pdl_wait();
-    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.x * 4 + (threadIdx.x >> 5);
     if (b >= P.B) return;
@@ -365,7 +363,6 @@ __device__ __forceinline__ float prob_at(const T *row, int v, float lse, float i
 template <typename T>
 __global__ void __launch_bounds__(kSoftThreads) soft_accept_kernel(SoftParams P) {
     pdl_wait();
-    pdl_trigger();
     __shared__ float s_tile[kMaxSoftTiles];
     __shared__ int s_par[SPEC_MAX_ROWS];
     __shared__ uint8_t s_acc[SPEC_MAX_ROWS];

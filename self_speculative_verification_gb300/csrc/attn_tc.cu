@@ -500,7 +500,6 @@ attn_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUten
                const __grid_constant__ CUtensorMap mvb, const __grid_constant__ CUtensorMap msk,
                const __grid_constant__ CUtensorMap msv) {
     pdl_wait();
-    pdl_trigger();
     constexpr int NH = D / 64;                       // 128-byte halves per row
     constexpr int KV_BYTES = NH * kHalfBytes;        // K (or V) of one tile
     constexpr int STAGE = 2 * KV_BYTES;
@@ -860,7 +859,6 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                  const __grid_constant__ CUtensorMap mvb, const __grid_constant__ CUtensorMap msk,
                  const __grid_constant__ CUtensorMap msv, const __grid_constant__ CUtensorMap mq) {
     pdl_wait();
-    pdl_trigger();
     using namespace umma;
     static_assert(D == 128, "tcgen05 path is built for head_dim 128");
     constexpr int NH = D / 64;
@@ -1369,7 +1367,6 @@ template <int D>
 __global__ void __launch_bounds__(128) attn_tc_combine_kernel(const __grid_constant__ TcParams P,
                                                                int wcn) {
     pdl_wait();
-    pdl_trigger();
     const AttnParams &A = P.a;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int p = blockIdx.x * 4 + warp;
@@ -1397,7 +1394,6 @@ template <int D>
 __global__ void __launch_bounds__(kUmmaCombineThreads)
 attn_umma_combine_kernel(const __grid_constant__ TcParams P) {
     pdl_wait();
-    pdl_trigger();
     const AttnParams &A = P.a;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (blockIdx.x == 0 && blockIdx.y == 0)
@@ -1426,7 +1422,6 @@ attn_umma_combine_kernel(const __grid_constant__ TcParams P) {
 // Single-CTA launches have no boundary: only the seq_len check remains.
 __global__ void check_seq_len_kernel(const __grid_constant__ TcParams P) {
     pdl_wait();
-    pdl_trigger();
     for (int b = threadIdx.x; b < P.a.B; b += blockDim.x) check_seq_len(P.a, b);
 }
 

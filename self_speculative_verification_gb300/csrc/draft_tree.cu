@@ -78,7 +78,6 @@ constexpr int kMaxCand = 2048;
 template <typename T>
 __global__ void __launch_bounds__(kDraftThreads) draft_tree_kernel(DraftParams P) {
     pdl_wait();
-    pdl_trigger();
     __shared__ float s_max[kDraftThreads];
     __shared__ float s_cv[kMaxCand];
     __shared__ int s_ci[kMaxCand];
@@ -283,7 +282,6 @@ __device__ __forceinline__ int clamp_nodes(const PruneParams &P, int b, bool rep
 template <typename T>
 __global__ void __launch_bounds__(kThreads) prune_edge_kernel(PruneParams P) {
     pdl_wait();
-    pdl_trigger();
     __shared__ int s_kids[kMaxPruneNodes];
     __shared__ int s_nk;
     __shared__ float s_m[kThreads / 32], s_s[kThreads / 32];
@@ -386,7 +384,6 @@ __global__ void __launch_bounds__(kThreads) prune_edge_kernel(PruneParams P) {
 // a block scan numbers the survivors.
 __global__ void __launch_bounds__(kThreads) prune_compact_kernel(PruneParams P) {
     pdl_wait();
-    pdl_trigger();
     constexpr int kPer = kMaxPruneNodes / kThreads;
     __shared__ int s_par[kMaxPruneNodes], s_idx[kMaxPruneNodes];
     __shared__ uint8_t s_edge[kMaxPruneNodes];

@@ -93,7 +93,6 @@ __device__ void page_prefix(const CommitParams &P, int b, int *before, int *tota
 // One CTA per (request, KV head): copies every accepted row, K and V.
 __global__ void __launch_bounds__(128) kv_commit_copy_kernel(CommitParams P) {
     pdl_wait();
-    pdl_trigger();
     const int b = blockIdx.x / P.Hkv, h = blockIdx.x % P.Hkv;
     int before = 0, total = 0;
     int head = 0;
@@ -150,7 +149,6 @@ __global__ void __launch_bounds__(128) kv_commit_copy_kernel(CommitParams P) {
 // One CTA: new page-table entries, seq_len += accepted, free_head += taken.
 __global__ void __launch_bounds__(256) kv_commit_finalize_kernel(CommitParams P) {
     pdl_wait();
-    pdl_trigger();
     int head = 0, total = 0;
     if (P.paged) {
         int dummy = 0;

@@ -171,7 +171,6 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
                   const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                   const __grid_constant__ lap::Sched S) {
     pdl_wait();
-    pdl_trigger();
     using namespace lap;
     using namespace tc5;
     extern __shared__ uint8_t smem_raw[];

@@ -19,7 +19,6 @@ __global__ void mask_build_kernel(const int32_t *__restrict__ vparent,
                                   uint32_t *__restrict__ vis, uint8_t *__restrict__ row_flags,
                                   int *status) {
     sv::pdl_wait();
-    sv::pdl_trigger();
     __shared__ int32_t svp[SPEC_MAX_ROWS];
     const int b = blockIdx.x;
     for (int r = threadIdx.x; r < R; r += blockDim.x) svp[r] = vparent[(size_t)b * R + r];

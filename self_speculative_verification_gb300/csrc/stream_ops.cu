@@ -64,7 +64,6 @@ __device__ __forceinline__ void st8(float *p, const float (&x)[8]) {
 template <typename T>
 __global__ void __launch_bounds__(kThreads) rotate_kernel(RotateParams P) {
     pdl_wait();
-    pdl_trigger();
     __shared__ float s_cos[kMaxGamma], s_sin[kMaxGamma];
     const int b = blockIdx.x / P.Hkv, h = blockIdx.x % P.Hkv;
     const int T_b = P.n_nodes[b];
@@ -103,7 +102,6 @@ struct GatherParams {
 
 __global__ void __launch_bounds__(kThreads) gather_kernel(GatherParams P) {
     pdl_wait();
-    pdl_trigger();
     const int b = blockIdx.x;
     const int ln = P.last_node[b];
     const int row = P.row_offset + ln;

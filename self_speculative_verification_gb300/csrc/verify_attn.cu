@@ -45,7 +45,6 @@ enum { kColPrefix = 0, kColSoft = 1, kColBlock = 2 };
 template <typename T, int D>
 __global__ void __launch_bounds__(128) attn_simt_kernel(AttnParams P) {
     pdl_wait();
-    pdl_trigger();
     __shared__ float sq[kSimtRows][D];
     __shared__ float sk[kSimtCols][D + 1];
     __shared__ float sv_[kSimtCols][D];
@@ -208,7 +207,6 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnParams P) {
 template <typename T, int D>
 __global__ void __launch_bounds__(128) attn_combine_kernel(AttnParams P) {
     pdl_wait();
-    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int p = blockIdx.x * 4 + warp;
     const int h = blockIdx.y, b = blockIdx.z;
