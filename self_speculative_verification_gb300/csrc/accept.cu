@@ -15,6 +15,7 @@
 
 #include "common.cuh"
 #include "logits.cuh"
+#include "ptx_sm103.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -60,7 +61,67 @@ __device__ __forceinline__ Best best_merge(Best a, Best b, float inv_t) {
 // increasing order, so an equal later value never wins a tie); then one
 // FFMA + one ex2 per element.  Rank 0 merges the CTAs' results through
 // distributed shared memory.
+// bf16 batches without a ragged end take packed arithmetic: the batch max
+// on bf16 pairs (exact: a max selects one of its inputs), the exponent
+// arguments and the sums on fp32 pairs, so per element about one ex2 and
+// three other instructions issue.
 constexpr int kUnroll = 4;
+
+struct Bf16Batch {
+    uint32_t w[kUnroll][4];     // kUnroll x 8 bf16, pairs in 32-bit words
+};
+
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Running (max, index, sum) over one full batch of kUnroll 8-element
+// vectors; vector u starts at element (i0 + u * kReduceThreads) * 8.
+__device__ __forceinline__ void push_bf16_batch(Best &best, const Bf16Batch &x, int i0, float c2) {
+    uint32_t m2 = x.w[0][0];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) m2 = bf16x2_max(m2, x.w[u][q]);
+    const float bm = fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xffff0000u));
+    if (bm > best.m) {
+        int bi = INT_MAX;
+#pragma unroll
+        for (int u = kUnroll - 1; u >= 0; --u)
+#pragma unroll
+            for (int j = 7; j >= 0; --j) {
+                const uint32_t wq = x.w[u][j >> 1];
+                const float v = __uint_as_float((j & 1) ? (wq & 0xffff0000u) : (wq << 16));
+                if (v == bm) bi = (i0 + u * kReduceThreads) * 8 + j;
+            }
+        best.s *= ex2((best.m - bm) * c2);
+        best.m = bm;
+        best.idx = bi;
+    }
+    const uint64_t c22 = pair(c2, c2);
+    const float nmb = -best.m * c2;
+    const uint64_t nmb2 = pair(nmb, nmb);
+    uint64_t acc[4] = {pair(0.f, 0.f), pair(0.f, 0.f), pair(0.f, 0.f), pair(0.f, 0.f)};
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t wq = x.w[u][q];
+            float t0, t1;
+            unpair(fma2(pair(__uint_as_float(wq << 16), __uint_as_float(wq & 0xffff0000u)), c22,
+                        nmb2),
+                   t0, t1);
+            acc[q] = add2(acc[q], pair(ex2(t0), ex2(t1)));
+        }
+    float a0, a1, a2, a3, a4, a5, a6, a7;
+    unpair(acc[0], a0, a1);
+    unpair(acc[1], a2, a3);
+    unpair(acc[2], a4, a5);
+    unpair(acc[3], a6, a7);
+    best.s += ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7));
+}
 
 
 template <typename T>
@@ -80,7 +141,25 @@ vocab_reduce_kernel(const T *__restrict__ logits, int V, const int32_t *__restri
     if ((reinterpret_cast<uintptr_t>(z) & 15) == 0) {
         const int nv = V / N;
         const int lo = (int)((long long)nv * rank / nc), hi = (int)((long long)nv * (rank + 1) / nc);
-        for (int i0 = lo + threadIdx.x; i0 < hi; i0 += kReduceThreads * kUnroll) {
+        int i0 = lo + threadIdx.x;
+        if constexpr (N == 8) {
+            // full batches
+            const uint4 *zv = reinterpret_cast<const uint4 *>(z);
+            for (; i0 + (kUnroll - 1) * kReduceThreads < hi; i0 += kReduceThreads * kUnroll) {
+                Bf16Batch x;
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const uint4 v = zv[i0 + u * kReduceThreads];
+                    x.w[u][0] = v.x;
+                    x.w[u][1] = v.y;
+                    x.w[u][2] = v.z;
+                    x.w[u][3] = v.w;
+                }
+                push_bf16_batch(best, x, i0, c2);
+            }
+        }
+        // the ragged last batch (all batches for fp32)
+        for (; i0 < hi; i0 += kReduceThreads * kUnroll) {
             float x[kUnroll][N];
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {

@@ -59,3 +59,22 @@ def test_many_rows_on_paged_cache(name, page_size):
                          page_size=page_size)
     gh.run_and_check(wl)
     gh.run_and_check(wl, split_tokens=64)
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_split_row_layout_gqa(paged):
+    """64 packed rows with G = 4 (a ConFu tree of 8 nodes: 16 rows x 4
+    heads) take the tcgen05 kernel's split layout: each row in two TMEM
+    lanes, one per column half, query boxes of 4 rows x 4 heads."""
+    wl = W.make_workload("confu", 26, B=3, T=8, seq=("uniform", 150, 900), V=2000,
+                         paged=paged)
+    gh.run_and_check(wl)
+    gh.run_and_check(wl, split_tokens=64)
+
+
+def test_partial_row_block():
+    """96 packed rows (a ConFu tree of 12 nodes, G = 4): one tcgen05 row
+    block, its last 32 lanes empty."""
+    wl = W.make_workload("confu", 27, B=3, T=12, seq=("uniform", 150, 900), V=2000)
+    gh.run_and_check(wl)
+    gh.run_and_check(wl, split_tokens=64)
