@@ -250,7 +250,8 @@ spec_status_t spec_mask_build(const int32_t *vparent, const uint8_t *soft_flags,
  * (split partials: per request, KV head and split, the packed rows'
  * running max, sum and unnormalised output in fp32; on the tensor-core
  * paths also the first tile of each CTA's range, which the attention
- * kernel writes and the combine reads).
+ * kernel writes and the combine reads, and for the tcgen05 kernel a record
+ * per CTA of the split segment its range starts inside of).
  */
 spec_status_t spec_verify_attn_workspace_size(const spec_attn_desc *attn,
                                               const spec_kv_desc *cache,

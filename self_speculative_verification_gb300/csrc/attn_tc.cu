@@ -41,6 +41,16 @@ namespace {
 constexpr int kTile = 64;                 // tokens per tile
 constexpr int kHalfBytes = kTile * 128;   // one 64-token x 64-element bf16 box
 
+// A split segment, as the CTA holding its first boundary between CTA
+// ranges records it (tcgen05 attention kernel) for the combine; seg < 0 in
+// every other CTA's record.
+struct BoundaryRec {
+    long long s0, s1;    // the segment's tiles
+    int seg;             // (b * Hkv + h) * n_rb + rb
+    int first, last;     // CTAs whose ranges meet [s0, s1)
+    uint32_t parts;      // bit j: CTA first + j holds a part (when last - first < 32)
+};
+
 struct TcParams {
     AttnParams a;
     int n_ctas;
@@ -51,6 +61,8 @@ struct TcParams {
     int seg_cost;        // what a segment start costs, in tiles, for the split
     long long *bounds;   // first tile of each CTA's range, [n_ctas + 1] (workspace),
                          // written by the attention kernel for the combine
+    BoundaryRec *recs;   // tcgen05 kernel: per CTA, the split segment it merges
+                         // (workspace, [n_ctas])
 };
 
 // -------------------------------------------- mma.sync helpers
@@ -921,6 +933,45 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
     }
     volatile int *abort = &sh.abort;
 
+    if (warp == 5) {
+        // A warp with no other role: when this CTA's range starts inside a
+        // segment and the ranges between the segment's first CTA and this
+        // one are empty (this is the segment's first boundary), record the
+        // segment and the CTAs sharing it for the combine.
+        BoundaryRec rec{0, 0, -1, 0, 0, 0};
+        if (t_begin < t_end) {
+            Cursor c;
+            cursor_init(P, t_begin, c);
+            if (c.tile > 0) {
+                rec.s0 = t_begin - c.tile;
+                rec.s1 = rec.s0 + c.n_tiles;
+                bool first_boundary = true;
+                int f = cta - 1, l = cta;
+                for (;; --f) {
+                    const long long lo = warp_range_lo(P, C, T, f);
+                    if (lo <= rec.s0 || f == 0) break;
+                    if (lo < t_begin) first_boundary = false;   // a part starts in between
+                }
+                while (l + 1 < P.n_ctas && warp_range_lo(P, C, T, l + 1) < rec.s1) ++l;
+                if (first_boundary) {
+                    rec.seg = (c.b * A.Hkv + c.h) * A.n_rb + c.rb;
+                    rec.first = f;
+                    rec.last = l;
+                    // which of them hold a part (ranges between may be empty)
+                    if (l - f < 32) {
+                        long long lo = warp_range_lo(P, C, T, f);
+                        for (int j = f; j <= l; ++j) {
+                            const long long hi = warp_range_lo(P, C, T, j + 1);
+                            if (max(lo, rec.s0) < min(hi, rec.s1)) rec.parts |= 1u << (j - f);
+                            lo = hi;
+                        }
+                    }
+                }
+            }
+        }
+        if (lane == 0) P.recs[cta] = rec;
+    }
+
     if (t_begin < t_end) {
         if (warp == kProducerWarp) {
             const QLoad ql{&mq, qbuf, sh.q_full, sh.q_empty};
@@ -1381,6 +1432,58 @@ __global__ void __launch_bounds__(128) attn_tc_combine_kernel(const __grid_const
     merge_row<D>(P, wcn, b, h, seg, s0, s1, cta_holding(P, s0), cta_holding(P, s1 - 1), p, lane);
 }
 
+// merge_row for the tcgen05 path, from a boundary record: with at most
+// four contributing CTAs every partial's (m, l) and then every O slice are
+// loaded together (two dependent round trips per row); otherwise merge_row.
+template <int D>
+__device__ void merge_row_rec(const TcParams &P, const BoundaryRec &rec, int b, int h, int p,
+                              int lane) {
+    const AttnParams &A = P.a;
+    constexpr int kMaxParts = 4;
+    if (rec.last - rec.first >= kMaxParts) {
+        merge_row<D>(P, 1, b, h, rec.seg, rec.s0, rec.s1, rec.first, rec.last, p, lane);
+        return;
+    }
+    const int rr = p % A.rb_rows;
+    size_t row[kMaxParts];
+    float ms[kMaxParts], ls[kMaxParts];
+#pragma unroll
+    for (int j = 0; j < kMaxParts; ++j) {
+        const bool part = rec.first + j <= rec.last && ((rec.parts >> j) & 1u);
+        row[j] = part ? slot_row(P, rec.seg, rec.first + j, 0, 1, rr) : 0;
+        ms[j] = part ? A.part_ml[row[j] * 2] : -INFINITY;
+        ls[j] = part ? A.part_ml[row[j] * 2 + 1] : 0.f;
+    }
+    float mstar = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kMaxParts; ++j) mstar = fmaxf(mstar, ms[j]);
+    float wgt[kMaxParts], L = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxParts; ++j) {
+        wgt[j] = ms[j] == -INFINITY ? 0.f : exp2f(ms[j] - mstar);
+        L = fmaf(wgt[j], ls[j], L);
+    }
+    float x[kMaxParts][D / 32];
+#pragma unroll
+    for (int j = 0; j < kMaxParts; ++j)
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+            x[j][c] = wgt[j] != 0.f ? A.part_o[row[j] * D + lane + 32 * c] : 0.f;
+    const int r = p / A.G, hq = h * A.G + p % A.G;
+    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(A.o) + (((size_t)b * A.R + r) * A.Hq + hq) * D;
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < kMaxParts; ++j) acc = fmaf(wgt[j], x[j][c], acc);
+        o[lane + 32 * c] = __float2bfloat16_rn(acc * inv);
+    }
+    if (lane == 0)
+        A.lse[((size_t)b * A.Hq + hq) * A.R + r] =
+            L > 0.f ? (mstar + log2f(L)) * kLn2 : -INFINITY;
+}
+
 // tcgen05 path: a segment wholly inside one CTA's range already holds its
 // final output; a split segment contains at least one boundary between
 // consecutive CTA ranges.  CTAs (i, y) here take the boundary between
@@ -1398,25 +1501,16 @@ attn_umma_combine_kernel(const __grid_constant__ TcParams P) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (blockIdx.x == 0 && blockIdx.y == 0)
         for (int b = threadIdx.x; b < A.B; b += kUmmaCombineThreads) check_seq_len(A, b);
-    const long long tb = P.bounds[blockIdx.x + 1];
-    if (tb <= 0 || tb >= P.bounds[P.n_ctas]) return;
-    int b;
-    long long start;
-    warp_locate(P, tb, &b, &start);
-    const int nt = seg_tiles(P, req_seq(P, b));
-    const int segi = (int)((tb - start) / nt);
-    const long long s0 = start + (long long)segi * nt, s1 = s0 + nt;
-    if (s0 == tb) return;                       // the boundary starts a segment
-    const int first = cta_holding(P, s0);
-    if (first != (int)blockIdx.x) return;        // not this segment's first boundary
-    const int last = cta_holding(P, s1 - 1);
-    const int h = segi / A.n_rb, rb = segi % A.n_rb;
-    const int seg = (b * A.Hkv + h) * A.n_rb + rb;
+    // the boundary between CTAs i - 1 and i
+    const int i = blockIdx.x + 1;
+    const BoundaryRec rec = P.recs[i];
+    if (rec.seg < 0) return;         // no segment's first boundary
+    const int rb = rec.seg % A.n_rb, h = (rec.seg / A.n_rb) % A.Hkv, b = rec.seg / (A.n_rb * A.Hkv);
     const int p_hi = min(A.M, (rb + 1) * A.rb_rows);
     constexpr int kWarps = kUmmaCombineThreads / 32;
     for (int p = rb * A.rb_rows + blockIdx.y * kWarps + warp; p < p_hi;
          p += kUmmaCombineSplit * kWarps)
-        merge_row<D>(P, 1, b, h, seg, s0, s1, first, last, p, lane);
+        merge_row_rec<D>(P, rec, b, h, p, lane);
 }
 
 // Single-CTA launches have no boundary: only the seq_len check remains.
@@ -1538,8 +1632,9 @@ size_t tc_workspace_bytes(const AttnParams &P, size_t *off_ml) {
     const size_t o_bytes = (rows * P.d * sizeof(float) + 255) & ~size_t(255);
     const size_t ml_bytes = (rows * 2 * sizeof(float) + 255) & ~size_t(255);
     *off_ml = o_bytes;
-    // then the split's CTA bounds
-    return o_bytes + ml_bytes + (((size_t)ctas + 1) * sizeof(long long) + 255) / 256 * 256;
+    // then the split's CTA bounds and boundary records
+    return o_bytes + ml_bytes + (((size_t)ctas + 1) * sizeof(long long) + 255) / 256 * 256 +
+           ((size_t)ctas * sizeof(BoundaryRec) + 255) / 256 * 256;
 }
 
 spec_status_t launch_attn_tc(const AttnParams &A, cudaStream_t s) {
@@ -1559,6 +1654,9 @@ spec_status_t launch_attn_tc(const AttnParams &A, cudaStream_t s) {
         const size_t rows = (segs + (size_t)P.n_ctas) * wc * A.rb_rows;
         P.bounds = reinterpret_cast<long long *>(
             reinterpret_cast<char *>(A.part_ml) + ((rows * 2 * sizeof(float) + 255) & ~size_t(255)));
+        P.recs = reinterpret_cast<BoundaryRec *>(
+            reinterpret_cast<char *>(P.bounds) +
+            ((((size_t)P.n_ctas + 1) * sizeof(long long) + 255) & ~size_t(255)));
     }
     P.soft_tiles = ceil_div(A.n_soft, kTile);
     P.tail = P.soft_tiles + ceil_div(A.R, kTile);
