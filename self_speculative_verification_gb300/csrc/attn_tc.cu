@@ -1542,6 +1542,10 @@ TcConfig choose(const AttnParams &P) {
     const int wr = P.rb_rows / 16;
     // Up to 32 rows: two CTAs per SM, i.e. two independent TMA pipelines
     // (measured on GB300: 74% vs 38% of HBM for the long paged workload).
+    // One 16-row group at d = 128 takes two consumer warps, 32 keys of each
+    // tile apiece (measured on the LLaMA-7B-shaped step: 141 -> 138 us; one
+    // warp: 168 us; two warps with three CTAs per SM: 139 us).
+    if (wr == 1 && P.d == 128) return {1, 2, 3, 2};
     if (wr <= 2) return {wr, 4, P.d == 128 ? 3 : 6, 2};
     return {wr, 8, P.d == 128 ? 5 : 8, 1};
 }
@@ -1692,7 +1696,7 @@ spec_status_t launch_attn_tc(const AttnParams &A, cudaStream_t s) {
     if (!ok) return SPEC_ERR_CUDA;
     if (use_umma) return launch_umma(P, maps, s);
     if (A.d == 128) {
-        if (cfg.wr == 1) return launch_impl<128, 1, 4, 3, 2>(P, maps, s);
+        if (cfg.wr == 1) return launch_impl<128, 1, 2, 3, 2>(P, maps, s);
         if (cfg.wr == 2) return launch_impl<128, 2, 4, 3, 2>(P, maps, s);
         return launch_impl<128, 4, 8, 5, 1>(P, maps, s);
     }
