@@ -476,6 +476,7 @@ def run_gpu(args):
             dist.destroy_process_group()
         return
     ms_step = total_ms / args.steps
+    accepted_tps = accepted_rows * args.steps * world / (total_ms / 1e3)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -500,6 +501,7 @@ def run_gpu(args):
             "algorithmic_bytes_per_call": attn_bytes,
             "traffic": recorded_traffic(args.config),
         },
+        "accepted_tokens_per_s": accepted_tps,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": ds.launches_per_step * args.steps,
@@ -523,7 +525,8 @@ def run_e2e(ds, steps, stream):
                          "logits", "tokens", "tree_parent", "n_nodes", "draft_logits",
                          "child_draft_row", "u_accept", "u_sample")
              if getattr(ds, n, None) is not None]
-    outputs = [ds.acc_len, ds.path, ds.next_token, ds.last_node]
+    # the step's results: acceptance, and the attention outputs O and LSE
+    outputs = [ds.acc_len, ds.path, ds.next_token, ds.last_node, ds.o, ds.lse]
     if ds.future is not None:
         outputs.append(ds.future)
     h_in = [getattr(ds, n).cpu().pin_memory() for n in names]
@@ -579,7 +582,8 @@ def run_e2e(ds, steps, stream):
             "d2h_bytes_per_step": bo, "ms_per_step": 1e3 * dt / steps,
             "timing": "host wall clock over the steps; each step's inputs copied in from "
                       "pinned host memory on a copy stream (overlapping the previous step's "
-                      "compute) and its results copied out and waited for by the host"}
+                      "compute) and its results (acceptance outputs, attention O and LSE) "
+                      "copied out and waited for by the host"}
 
 
 # ------------------------------------------------------ prefill-form LA

@@ -474,9 +474,15 @@ spec_status_t spec_la_prefill_attn(const spec_prefill_desc *desc, const void *q,
  *     needs more scratch than that (spec_verify_attn_workspace_size tells);
  *     such shapes must use spec_verify_attn.
  *   - Calls no allocating routine (no cudaMalloc, cudaFree or the like).
- *   - The first call on each device resolves the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; it is looked up again
+ *     only when the device's context has changed (e.g. after
+ *     cudaDeviceReset).  Under lazy module loading (the CUDA default) that
+ *     first lookup loads the library module holding the array, and that
+ *     load is when the 64 MiB are taken from the device.  So make the first
+ *     call on each device (any arguments: the lookup comes before every
+ *     check) before reserving the rest of the device's memory, and before
+ *     any stream capture.
  *   - Every call on a device shares the one array, which keeps the previous
  *     call's contents (nothing needs to start at zero: the kernels write each
  *     partial before reading it).  Calls that can overlap on the GPU (other
@@ -568,6 +574,21 @@ spec_status_t kv_commit(const spec_kv_desc *cache, int batch, int n_rows,
                         const int32_t *path, const int32_t *acc_len,
                         int32_t *seq_len, const int32_t *free_pages,
                         int n_free, int32_t *free_head, void *stream);
+
+/*
+ * spec_set_wait_limit -- limit, in SM clock cycles, of the internal pipeline
+ * waits of the kernels launched from now on (verify attention, prefill
+ * attention), process-wide.  The pages have no counterpart: this is the
+ * library's guard against a hang.  A wait that runs out sets
+ * SPEC_DEV_TIMEOUT; the kernel then stops issuing work, waits (with the
+ * default limit) for its own copies and tensor-core operations, frees its
+ * tensor memory and returns, and the context stays usable.  cycles < 0
+ * restores the default (2e9 cycles, about one second); 0 makes any wait
+ * whose condition is not already met fail at once, which is how the tests
+ * exercise this path.  Returns the previous limit.  Not for use while other
+ * threads launch work of this library.
+ */
+long long spec_set_wait_limit(long long cycles);
 
 /*
  * spec_get_status -- synchronise `stream`, then read and clear the current

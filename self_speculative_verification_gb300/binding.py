@@ -38,12 +38,14 @@ SPEC_DEV_BAD_PAGE = 0x02
 SPEC_DEV_SEQ_OVERFLOW = 0x04
 SPEC_DEV_CAPACITY = 0x08
 SPEC_DEV_BAD_INDEX = 0x10
+SPEC_DEV_TIMEOUT = 0x20
 
 EXPORTS = ("spec_version", "spec_status_string", "spec_mask_build",
            "spec_verify_attn_workspace_size", "spec_verify_attn",
            "spec_verify_attn_noalloc", "spec_vocab_reduce", "spec_accept", "kv_commit",
            "spec_get_status", "spec_la_prefill_attn", "spec_accept_soft", "spec_draft_tree",
-           "spec_prune_tree", "spec_stream_rotate_values", "spec_future_gather")
+           "spec_prune_tree", "spec_stream_rotate_values", "spec_future_gather",
+           "spec_set_wait_limit")
 SPEC_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -136,6 +138,7 @@ def load_library():
         "kv_commit": ([POINTER(KvDesc), c_int, c_int, vp, vp, c_int, vp, vp, vp, vp,
                        c_int, vp, vp], c_int),
         "spec_get_status": ([vp, POINTER(ctypes.c_int32)], c_int),
+        "spec_set_wait_limit": ([ctypes.c_longlong], ctypes.c_longlong),
         "spec_la_prefill_attn": ([POINTER(PrefillDesc), vp, vp, vp, vp, vp, vp], c_int),
         "spec_accept_soft": ([POINTER(SoftDesc)] + [vp] * 16, c_int),
         "spec_draft_tree": ([POINTER(DraftDesc)] + [vp] * 8, c_int),
@@ -335,6 +338,12 @@ def spec_get_status(stream=None) -> int:
     if code not in (SPEC_OK, SPEC_ERR_DEVICE):
         _check("spec_get_status", code)
     return out.value
+
+
+def spec_set_wait_limit(cycles: int) -> int:
+    """Limit (SM cycles) of the kernels' pipeline waits from now on; a
+    negative value restores the default.  Returns the previous limit."""
+    return load_library().spec_set_wait_limit(int(cycles))
 
 
 def spec_la_prefill_attn(desc: PrefillDesc, q, k, v, o, lse, stream=None):

@@ -63,6 +63,7 @@ struct TcParams {
                          // written by the attention kernel for the combine
     BoundaryRec *recs;   // tcgen05 kernel: per CTA, the split segment it merges
                          // (workspace, [n_ctas])
+    long long wait;      // limit of every pipeline wait, in SM cycles
 };
 
 // -------------------------------------------- mma.sync helpers
@@ -410,7 +411,7 @@ __device__ __forceinline__ void run_producer(const TcParams &P, const CUtensorMa
                 // the segment's query block, ahead of its first K/V tile
                 const int qb = nq & 1;
                 if (lane == 0) {
-                    got = mbar_wait(&ql->empty[qb], (uint32_t)(((nq >> 1) & 1) ^ 1));
+                    got = mbar_wait(&ql->empty[qb], (uint32_t)(((nq >> 1) & 1) ^ 1), P.wait);
                     if (got) {
                         constexpr uint32_t kQBytes = 128u * D * 2u;
                         mbar_arrive_expect_tx(&ql->full[qb], kQBytes);
@@ -424,7 +425,7 @@ __device__ __forceinline__ void run_producer(const TcParams &P, const CUtensorMa
                 got = __shfl_sync(0xffffffffu, got, 0);
                 if (got) ++nq;
             }
-            if (got && lane == 0) got = mbar_wait(&empty[s], ph ^ 1);
+            if (got && lane == 0) got = mbar_wait(&empty[s], ph ^ 1, P.wait);
             got = __shfl_sync(0xffffffffu, got, 0);
             if (!got) {
                 if (lane == 0) raise_status(A.status, SPEC_DEV_TIMEOUT);
@@ -627,7 +628,7 @@ attn_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUten
 
         const int s = (int)(k % NS);
         const uint32_t ph = (uint32_t)((k / NS) & 1);
-        if (!mbar_wait(&full[s], ph)) {
+        if (!mbar_wait(&full[s], ph, P.wait)) {
             raise_status(A.status, SPEC_DEV_TIMEOUT);
             break;
         }
@@ -992,7 +993,7 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                 // O += P(j) V(j): A = P buffer j%2 (TMEM), B = V (MN-major smem)
                 auto issue_pv = [&](int j, int rbl, int stage, bool first) -> bool {
                     const int b = j & 1;
-                    if (!mbar_wait(&sh.p_full[b], (uint32_t)((j >> 1) & 1))) return false;
+                    if (!mbar_wait(&sh.p_full[b], (uint32_t)((j >> 1) & 1), P.wait)) return false;
                     fence_after();
                     const uint32_t vb = smem_u32(smem + stage * STAGE + KV_BYTES);
                     const uint32_t a_p = tmem + kColP + (uint32_t)b * (kTile / 2);
@@ -1032,8 +1033,8 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                         // completion frees the shared-memory block
                         const int qb = seg_n & 1;
                         if ((seg_n >= 2 &&
-                             !mbar_wait(&sh.q_tfree[qb], (uint32_t)(((seg_n - 2) >> 1) & 1))) ||
-                            !mbar_wait(&sh.q_full[qb], (uint32_t)((seg_n >> 1) & 1))) {
+                             !mbar_wait(&sh.q_tfree[qb], (uint32_t)(((seg_n - 2) >> 1) & 1), P.wait)) ||
+                            !mbar_wait(&sh.q_full[qb], (uint32_t)((seg_n >> 1) & 1), P.wait)) {
                             ok = false;
                             break;
                         }
@@ -1046,7 +1047,7 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                         commit(&sh.q_empty[qb]);
                         ++seg_n;
                     }
-                    if (!mbar_wait(&sh.full[stage], sph)) { ok = false; break; }
+                    if (!mbar_wait(&sh.full[stage], sph, P.wait)) { ok = false; break; }
                     // S(k) = Q K^T into S buffer k%2
                     const uint32_t kb = smem_u32(smem + stage * STAGE);
                     const uint32_t s_col = tmem + kColS + (uint32_t)(k & 1) * kTile;
@@ -1128,7 +1129,7 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
             // wholly inside this CTA's range writes its final O (bf16) and
             // LSE; otherwise the (m, l, O) partial goes to the workspace
             auto epilogue = [&](long long j) -> bool {
-                if (!mbar_wait(&sh.o_upd[j & 1], (uint32_t)((j >> 1) & 1))) return false;
+                if (!mbar_wait(&sh.o_upd[j & 1], (uint32_t)((j >> 1) & 1), P.wait)) return false;
                 fence_after();
                 // tcgen05.ld is warp-collective: a warp with any real row
                 // loads, and only its real rows store
@@ -1226,7 +1227,7 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                     vmask = w;
                     vmask_j = ti.j;
                 }
-                if (!mbar_wait(&sh.s_full[k & 1], (uint32_t)((k >> 1) & 1))) { ok = false; break; }
+                if (!mbar_wait(&sh.s_full[k & 1], (uint32_t)((k >> 1) & 1), P.wait)) { ok = false; break; }
                 fence_after();
                 if (warp_rows) {
                     // the S row: both TMEM loads in flight, one wait
@@ -1271,7 +1272,7 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                         const float alpha = (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - tm);
                         if (!first && m_used != -INFINITY) {
                             // O holds PV(k-1): wait for it, then scale this row in place
-                            if (!mbar_wait(&sh.o_upd[(k - 1) & 1], (uint32_t)(((k - 1) >> 1) & 1))) {
+                            if (!mbar_wait(&sh.o_upd[(k - 1) & 1], (uint32_t)(((k - 1) >> 1) & 1), P.wait)) {
                                 ok = false;
                                 break;
                             }
@@ -1294,7 +1295,7 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                     }
                     const float mu = m_used == -INFINITY ? 0.f : m_used;
                     // P buffer k%2 was last read by PV(k-2)
-                    if (k >= 2 && !mbar_wait(&sh.o_upd[k & 1], (uint32_t)(((k - 2) >> 1) & 1))) {
+                    if (k >= 2 && !mbar_wait(&sh.o_upd[k & 1], (uint32_t)(((k - 2) >> 1) & 1), P.wait)) {
                         ok = false;
                         break;
                     }
@@ -1557,14 +1558,10 @@ size_t smem_bytes(int d, int ns) {
 
 template <int D, int WR, int NCW, int NS, int MINB>
 spec_status_t launch_impl(const TcParams &P, const CUtensorMap *maps, cudaStream_t s) {
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
     const size_t smem = smem_bytes(D, NS);
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(attn_tc_kernel<D, WR, NCW, NS, MINB>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    });
-    if (attr_err != cudaSuccess) return SPEC_ERR_CUDA;
+    if (set_smem_limit(reinterpret_cast<const void *>(attn_tc_kernel<D, WR, NCW, NS, MINB>),
+                       smem) != SPEC_OK)
+        return SPEC_ERR_CUDA;
     if (launch(attn_tc_kernel<D, WR, NCW, NS, MINB>, dim3(P.n_ctas), dim3((NCW + 1) * 32), smem, s,
                P, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5]) != SPEC_OK)
         return SPEC_ERR_CUDA;
@@ -1582,13 +1579,8 @@ spec_status_t launch_umma(const TcParams &P, const CUtensorMap *maps, cudaStream
                             2 * (size_t)umma::kRows * D * 2 +                // query blocks
                             sizeof(umma::Shared) + 1024;
     static_assert(smem <= 227 * 1024, "shared memory of the tcgen05 verify kernel");
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(attn_umma_kernel<D>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    });
-    if (attr_err != cudaSuccess) return SPEC_ERR_CUDA;
+    if (set_smem_limit(reinterpret_cast<const void *>(attn_umma_kernel<D>), smem) != SPEC_OK)
+        return SPEC_ERR_CUDA;
     if (launch(attn_umma_kernel<D>, dim3(P.n_ctas), dim3(umma::kThreads), smem, s, P, maps[0],
                maps[1], maps[2], maps[3], maps[4], maps[5], maps[6]) != SPEC_OK)
         return SPEC_ERR_CUDA;
@@ -1644,6 +1636,7 @@ size_t tc_workspace_bytes(const AttnParams &P, size_t *off_ml) {
 spec_status_t launch_attn_tc(const AttnParams &A, cudaStream_t s) {
     TcParams P{};
     P.a = A;
+    P.wait = wait_limit();
     const bool use_umma = umma_selected(A);
     const TcConfig cfg = use_umma ? TcConfig{8, 4, 0, 1} : choose(A);
     P.n_ctas = num_sms() * cfg.minb;

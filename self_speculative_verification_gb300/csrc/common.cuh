@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "specverify.h"
 
 namespace sv {
@@ -12,6 +14,30 @@ namespace sv {
 // Device address of the per-device status word (SPEC_DEV_* bits) for the
 // current device; nullptr if it cannot be resolved.
 int *status_ptr();
+
+// The current CUDA context (driver handle), or nullptr.
+void *current_context();
+
+// Device addresses of one __device__ symbol, per device and context: host
+// code sees only a stand-in for such a symbol, and the address it has on a
+// device is looked up (cudaGetSymbolAddress) with that device current.  A
+// new context on a device (after cudaDeviceReset, say) is looked up again.
+struct DeviceSymbolCache {
+    static constexpr int kDevices = 64;
+    std::mutex mu;
+    void *addr[kDevices] = {};
+    void *ctx[kDevices] = {};
+};
+spec_status_t symbol_address(DeviceSymbolCache &cache, const void *symbol, void **out);
+
+// Limit, in SM cycles, that kernel launches give their pipeline waits
+// (spec_set_wait_limit; default ~1 s).
+long long wait_limit();
+
+// Raise `func`'s dynamic shared-memory limit to `bytes` on the current
+// device (once per device and context: the attribute applies to the device
+// current when it is set).
+spec_status_t set_smem_limit(const void *func, size_t bytes);
 
 // Number of SMs of the current device (cached per device).
 int num_sms();

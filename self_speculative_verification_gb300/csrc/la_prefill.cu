@@ -85,6 +85,7 @@ struct Params {
     __nv_bfloat16 *o;
     float *lse;
     int *status;
+    long long wait;       // limit of every pipeline wait, in SM cycles
 };
 
 struct Shared {
@@ -233,7 +234,7 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
                 while (ok && next_unit(P, S, cur, U)) {
                     const int mA = last_tile(P, U.t, 0), mB = last_tile(P, U.t, 1);
                     const int jmax = mB >= 0 ? mB : mA;
-                    if (*abort || !mbar_wait(&sh.q_empty, (uint32_t)((nu & 1) ^ 1))) {
+                    if (*abort || !mbar_wait(&sh.q_empty, (uint32_t)((nu & 1) ^ 1), P.wait)) {
                         ok = false;
                         break;
                     }
@@ -248,7 +249,7 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
                         for (int kv = 0; kv < 2; ++kv) {
                             const int slot = (int)(ld % kSlots);
                             if (*abort ||
-                                !mbar_wait(&sh.empty[slot], (uint32_t)(((ld / kSlots) & 1) ^ 1))) {
+                                !mbar_wait(&sh.empty[slot], (uint32_t)(((ld / kSlots) & 1) ^ 1), P.wait)) {
                                 ok = false;
                                 break;
                             }
@@ -309,10 +310,10 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
                 // O_x += P_x V(j); the tile's first PV of a unit overwrites O_x,
                 // after the previous unit's epilogue of that tile read it
                 auto issue_pv = [&](int x, int v_slot, bool first) -> bool {
-                    if (!mbar_wait(&sh.p_full[x], (uint32_t)(np[x] & 1))) return false;
+                    if (!mbar_wait(&sh.p_full[x], (uint32_t)(np[x] & 1), P.wait)) return false;
                     ++np[x];
                     if (first && nact[x] > 0 &&
-                        !mbar_wait(&sh.o_free[x], (uint32_t)((nact[x] - 1) & 1)))
+                        !mbar_wait(&sh.o_free[x], (uint32_t)((nact[x] - 1) & 1), P.wait))
                         return false;
                     fence_after();
                     const uint64_t vd = vd0 + (uint64_t)(v_slot * (kTileBytes >> 4));
@@ -328,8 +329,8 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
                     // tile A always exists (2t < NM); tile B may not
                     const int mA = last_tile(P, U.t, 0), mB = last_tile(P, U.t, 1);
                     const int jmax = mB >= 0 ? mB : mA;
-                    if (*abort || !mbar_wait(&sh.q_full, (uint32_t)(nu & 1)) ||
-                        !mbar_wait(&sh.full[slot], ph)) {
+                    if (*abort || !mbar_wait(&sh.q_full, (uint32_t)(nu & 1), P.wait) ||
+                        !mbar_wait(&sh.full[slot], ph, P.wait)) {
                         ok = false;
                         break;
                     }
@@ -341,14 +342,14 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
                     advance();
                     for (int j = 0; j <= jmax; ++j) {
                         const int vslot = slot;
-                        if (!mbar_wait(&sh.full[vslot], ph)) {
+                        if (!mbar_wait(&sh.full[vslot], ph, P.wait)) {
                             ok = false;
                             break;
                         }
                         advance();
                         const bool next = j < jmax;
                         const int kslot = slot;
-                        if (next && !mbar_wait(&sh.full[kslot], ph)) {
+                        if (next && !mbar_wait(&sh.full[kslot], ph, P.wait)) {
                             ok = false;
                             break;
                         }
@@ -408,7 +409,7 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
             const int i = mX * kM + r;               // this thread's position
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; j <= mX; ++j) {
-                if (*abort || !mbar_wait(&sh.s_full[x], (uint32_t)(ns & 1))) {
+                if (*abort || !mbar_wait(&sh.s_full[x], (uint32_t)(ns & 1), P.wait)) {
                     ok = false;
                     break;
                 }
@@ -508,7 +509,7 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
             }
             if (!ok) break;
             // epilogue: O / l (bf16) and the LSE of this row
-            if (!mbar_wait(&sh.o_done[x], (uint32_t)(nact & 1))) {
+            if (!mbar_wait(&sh.o_done[x], (uint32_t)(nact & 1), P.wait)) {
                 ok = false;
                 break;
             }
@@ -656,19 +657,16 @@ extern "C" spec_status_t spec_la_prefill_attn(const spec_prefill_desc *desc, con
     P.o = static_cast<__nv_bfloat16 *>(o);
     P.lse = lse;
     P.status = st;
+    P.wait = wait_limit();
 
     CUtensorMap maps[3];
     if (!make_map_4d(&maps[0], q, Hq, (int)L, B) || !make_map_4d(&maps[1], k, Hkv, (int)L, B) ||
         !make_map_4d(&maps[2], v, Hkv, (int)L, B))
         return SPEC_ERR_CUDA;
 
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(la_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)lap::kSmemBytes);
-    });
-    if (attr_err != cudaSuccess) return SPEC_ERR_CUDA;
+    if (set_smem_limit(reinterpret_cast<const void *>(la_prefill_kernel), lap::kSmemBytes) !=
+        SPEC_OK)
+        return SPEC_ERR_CUDA;
     const long long n_units = (long long)B * Hq * P.NB;
     static thread_local lap::Sched sched;   // 16 KB: kept off the stack
     int grid = (int)std::min<long long>(num_sms(), n_units);

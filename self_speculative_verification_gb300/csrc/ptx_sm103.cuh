@@ -12,8 +12,11 @@
 
 namespace sv {
 
-// Upper bound, in SM clock cycles (~1 s), of every wait in these kernels;
-// past it the waiting kernel reports SPEC_DEV_TIMEOUT instead of hanging.
+// Default upper bound, in SM clock cycles (~1 s), of every wait in these
+// kernels; past it the waiting kernel reports SPEC_DEV_TIMEOUT instead of
+// hanging.  The pipeline waits take the limit their launch carries
+// (spec_set_wait_limit); the waits with which a stopping CTA drains its own
+// copies and MMAs always take this one.
 constexpr long long kTimeoutCycles = 2000000000ll;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -46,13 +49,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Non-blocking test of the same condition.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete, for at most `limit`
+// cycles after a first non-blocking test; false when the limit ran out.
+// (With limit 0 any phase still open at the first test fails at once.)
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long long limit) {
+    if (mbar_test_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity))
-        if (clock64() - t0 > kTimeoutCycles) return false;
-    return true;
+    while (clock64() - t0 < limit)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// The same with the default limit: for the drain at the end of a CTA's work.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    return mbar_wait(bar, parity, kTimeoutCycles);
 }
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,

@@ -211,42 +211,61 @@ def block_bits(x: np.ndarray, dtype: str) -> np.ndarray:
 
 
 def check_commit(ds: DeviceStep, before_k, before_v, paths):
-    """The cache after the step equals the cache before it, except the new
-    slots, which hold the accepted rows' K/V bits; bookkeeping matches."""
+    """The cache after the step equals the oracle's commit (kv_commit_contiguous
+    / kv_commit_paged) applied to the cache's bits before it and the block's
+    bits; page table, seq_len and free_head equal the oracle's."""
     wl = ds.wl
     after_k = cache_bits(ds.k_cache)
     after_v = cache_bits(ds.v_cache)
     kb_bits = block_bits(wl.kb, wl.dtype)
     vb_bits = block_bits(wl.vb, wl.dtype)
-    exp_k = before_k.copy()
-    exp_v = before_v.copy()
-    seq = wl.seq_len.astype(np.int64)
     if wl.paged:
-        pt, seq2, head = wl.page_table.copy(), seq.copy(), 0
-        ps = wl.page_size
-        for b, path in enumerate(paths):
-            for i, row in enumerate(path):
-                pos = int(seq[b]) + i
-                j = pos // ps
-                if pos % ps == 0:
-                    pt[b, j] = wl.free_pages[head]
-                    head += 1
-                nb = wl.d // 64
-                exp_k[pt[b, j], :, :, pos % ps] = kb_bits[b, :, row].reshape(wl.Hkv, nb, 64)
-                exp_v[pt[b, j], :, :, pos % ps] = vb_bits[b, :, row].reshape(wl.Hkv, nb, 64)
-            seq2[b] += len(path)
+        exp_k, exp_v, pt, seq2, head = oracle.kv_commit_paged(
+            before_k, before_v, wl.page_table, wl.seq_len, wl.free_pages, 0,
+            kb_bits, vb_bits, paths, wl.page_size)
         assert np.array_equal(ds.page_table.cpu().numpy(), pt)
         assert int(ds.free_head.item()) == head
     else:
-        seq2 = seq.copy()
-        for b, path in enumerate(paths):
-            for i, row in enumerate(path):
-                exp_k[b, :, int(seq[b]) + i] = kb_bits[b, :, row]
-                exp_v[b, :, int(seq[b]) + i] = vb_bits[b, :, row]
-            seq2[b] += len(path)
+        exp_k, exp_v, seq2 = oracle.kv_commit_contiguous(before_k, before_v, wl.seq_len,
+                                                         kb_bits, vb_bits, paths)
     assert np.array_equal(after_k, exp_k)
     assert np.array_equal(after_v, exp_v)
     assert ds.seq_len.cpu().numpy().tolist() == seq2.tolist()
+
+
+def commit_expected_on_device(ds: DeviceStep, k0, v0, paths):
+    """Expected cache after the commit of a full-size workload, without a
+    host copy of the cache: the oracle's commit is applied to index arrays
+    (one entry per cache slot, holding 1 + b * R + row of the block row the
+    slot receives, 0 for untouched slots), which gives every slot's source;
+    the device snapshot k0 / v0 then receives those rows.  Returns (k, v,
+    page_table, seq_len, free_head) as the oracle computes them."""
+    wl = ds.wl
+    R = wl.R
+    src = (1 + np.arange(wl.B)[:, None] * R + np.arange(R)[None, :]).astype(np.int64)
+    blk = src[:, None, :, None]                      # [B][1][R][1]
+    ek, ev = k0.clone(), v0.clone()
+    if wl.paged:
+        n_pages = ds.k_cache.shape[0]
+        idx = np.zeros((n_pages, 1, 1, wl.page_size, 1), dtype=np.int64)
+        idx, _, pt, seq2, head = oracle.kv_commit_paged(
+            idx, idx, wl.page_table, wl.seq_len, wl.free_pages, 0, blk, blk, paths,
+            wl.page_size)
+        pages, slots = np.nonzero(idx[:, 0, 0, :, 0])
+        nb = wl.d // 64
+        for p, t in zip(pages.tolist(), slots.tolist()):
+            b, row = divmod(int(idx[p, 0, 0, t, 0]) - 1, R)
+            ek[p, :, :, t] = ds.kb[b, :, row].view(wl.Hkv, nb, 64)
+            ev[p, :, :, t] = ds.vb[b, :, row].view(wl.Hkv, nb, 64)
+        return ek, ev, pt, seq2, head
+    idx = np.zeros((wl.B, 1, ds.k_cache.shape[2], 1), dtype=np.int64)
+    idx, _, seq2 = oracle.kv_commit_contiguous(idx, idx, wl.seq_len, blk, blk, paths)
+    reqs, poss = np.nonzero(idx[:, 0, :, 0])
+    for bb, t in zip(reqs.tolist(), poss.tolist()):
+        b, row = divmod(int(idx[bb, 0, t, 0]) - 1, R)
+        ek[bb, :, t] = ds.kb[b, :, row]
+        ev[bb, :, t] = ds.vb[b, :, row]
+    return ek, ev, None, seq2, None
 
 
 def run_and_check(wl, split_tokens=0, requests=None, heads=None):

@@ -18,7 +18,7 @@ HEADER = os.path.join(_build.INCLUDE, "specverify.h")
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = re.findall(r"^\s*(?:const\s+)?(?:spec_status_t|int|char)\s*\*?\s*(\w+)\s*\(",
+    names = re.findall(r"^\s*(?:const\s+)?(?:spec_status_t|int|char|long long)\s*\*?\s*(\w+)\s*\(",
                        text, flags=re.M)
     return sorted(set(names))
 
@@ -137,3 +137,16 @@ int main(void) {
             if key.startswith(struct + "."):
                 field = key.split(".")[1]
                 assert getattr(cls, field).offset == int(val), key
+
+
+def test_wait_limit_setter_round_trips_without_gpu():
+    """spec_set_wait_limit only stores the limit later launches carry."""
+    lib = binding.load_library()
+    prev = binding.spec_set_wait_limit(12345)
+    try:
+        assert binding.spec_set_wait_limit(0) == 12345
+        assert binding.spec_set_wait_limit(-1) == 0
+        assert binding.spec_set_wait_limit(-1) == 2000000000   # the default restored
+    finally:
+        binding.spec_set_wait_limit(prev)
+    assert lib is binding.load_library()

@@ -15,26 +15,6 @@ from self_speculative_verification_gb300.device import DeviceStep
 pytestmark = pytest.mark.gpu
 
 
-def _commit_expected_on_device(ds, k0, v0, paths):
-    """Expected cache after the commit, built on the device from the
-    snapshot, the oracle's paths and the page rule (pages from the table)."""
-    wl = ds.wl
-    ek, ev = k0.clone(), v0.clone()
-    pt = ds.page_table.cpu().numpy() if wl.paged else None
-    for b, path in enumerate(paths):
-        for i, row in enumerate(path):
-            pos = int(wl.seq_len[b]) + i
-            if wl.paged:
-                page, slot = int(pt[b, pos // wl.page_size]), pos % wl.page_size
-                nb = wl.d // 64
-                ek[page, :, :, slot] = ds.kb[b, :, row].view(wl.Hkv, nb, 64)
-                ev[page, :, :, slot] = ds.vb[b, :, row].view(wl.Hkv, nb, 64)
-            else:
-                ek[b, :, pos] = ds.kb[b, :, row]
-                ev[b, :, pos] = ds.vb[b, :, row]
-    return ek, ev
-
-
 @pytest.mark.parametrize("name", ["la7b", "confu", "ss", "long_paged"])
 def test_full_size_sampled(name):
     gh.require_gpu()
@@ -50,20 +30,12 @@ def test_full_size_sampled(name):
     O_ref, L_ref = gh.oracle_attention(wl, vis, valid, sees, requests=reqs, heads=heads)
     gh.check_attention(ds, O_ref, L_ref, requests=reqs, heads=heads)
     acc, paths = gh.check_accept(ds)
-    # commit: whole cache compared bit for bit on the device
+    # commit: the oracle's commit gives every slot's source row; the whole
+    # cache is then compared bit for bit on the device
+    ek, ev, pt, seq2, head = gh.commit_expected_on_device(ds, k0, v0, paths)
     if wl.paged:
-        head = 0
-        pt = wl.page_table.copy()
-        for b, path in enumerate(paths):
-            S = int(wl.seq_len[b])
-            for i in range(len(path)):
-                pos = S + i
-                if pos % wl.page_size == 0:
-                    pt[b, pos // wl.page_size] = wl.free_pages[head]
-                    head += 1
         assert np.array_equal(ds.page_table.cpu().numpy(), pt)
         assert int(ds.free_head.item()) == head
-    ek, ev = _commit_expected_on_device(ds, k0, v0, paths)
     assert torch.equal(ds.k_cache.view(torch.int16), ek.view(torch.int16))
     assert torch.equal(ds.v_cache.view(torch.int16), ev.view(torch.int16))
-    assert ds.seq_len.cpu().numpy().tolist() == (wl.seq_len + acc).tolist()
+    assert ds.seq_len.cpu().numpy().tolist() == seq2.tolist()
