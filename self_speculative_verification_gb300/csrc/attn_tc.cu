@@ -64,6 +64,17 @@ struct TcParams {
     BoundaryRec *recs;   // tcgen05 kernel: per CTA, the split segment it merges
                          // (workspace, [n_ctas])
     long long wait;      // limit of every pipeline wait, in SM cycles
+    // segments of a request: seg_h x seg_rb, numbered h * seg_rb + rb (the
+    // mma.sync kernel: KV heads x row blocks; the tcgen05 kernel: its units,
+    // see umma::Mode)
+    int seg_h, seg_rb;
+    // tcgen05 kernel: um_merged: a unit is two KV heads, their rows in one
+    // query block (the second at lanes 64..127), else one row block;
+    // um_act[x]: softmax warps of sub-tile x that take part (bit q: lane
+    // quarter q)
+    int um_merged;
+    unsigned um_act[2];
+    int pair_steps;      // a schedule step covers two 64-token tiles (tcgen05 rows mode)
 };
 
 // -------------------------------------------- mma.sync helpers
@@ -110,12 +121,15 @@ __device__ __forceinline__ int req_seq(const TcParams &P, int b) {
     return S < 0 ? 0 : (S > P.a.capacity ? P.a.capacity : S);
 }
 
+// Schedule steps of a segment with prefix S: its 64-token tiles (prefix,
+// soft prompt, block), or pairs of them.
 __device__ __forceinline__ int seg_tiles(const TcParams &P, int S) {
-    return ceil_div(S, kTile) + P.tail;
+    const int n = ceil_div(S, kTile) + P.tail;
+    return P.pair_steps ? (n + 1) >> 1 : n;
 }
 
 __device__ __forceinline__ long long req_tiles(const TcParams &P, int b) {
-    return (long long)seg_tiles(P, req_seq(P, b)) * P.a.Hkv * P.a.n_rb;
+    return (long long)seg_tiles(P, req_seq(P, b)) * P.seg_h * P.seg_rb;
 }
 
 __device__ __forceinline__ long long warp_sum_ll(long long x) {
@@ -177,7 +191,7 @@ __device__ void warp_locate(const TcParams &P, long long t, int *b_out, long lon
 // A CTA's range is the tiles its part of the cost space maps to.
 
 __device__ __forceinline__ long long req_cost(const TcParams &P, int b) {
-    return (long long)(seg_tiles(P, req_seq(P, b)) + P.seg_cost) * P.a.Hkv * P.a.n_rb;
+    return (long long)(seg_tiles(P, req_seq(P, b)) + P.seg_cost) * P.seg_h * P.seg_rb;
 }
 
 // Total cost over all requests (every lane gets it).
@@ -259,8 +273,8 @@ __device__ __forceinline__ int cta_holding(const TcParams &P, long long t) {
 
 struct Cursor {
     int b, h, rb;
-    int S, n_prefix, n_tiles;
-    int tile;
+    int S, n_prefix, n_tiles;   // prefix tokens, its 64-token tiles, the segment's steps
+    int tile;                   // step within the segment
 };
 
 __device__ void cursor_init(const TcParams &P, long long t, Cursor &c) {
@@ -268,25 +282,25 @@ __device__ void cursor_init(const TcParams &P, long long t, Cursor &c) {
     warp_locate(P, t, &c.b, &start);
     c.S = req_seq(P, c.b);
     c.n_prefix = ceil_div(c.S, kTile);
-    c.n_tiles = c.n_prefix + P.tail;
+    c.n_tiles = seg_tiles(P, c.S);
     const long long local = t - start;
     const int seg = (int)(local / c.n_tiles);
     c.tile = (int)(local % c.n_tiles);
-    c.h = seg / P.a.n_rb;
-    c.rb = seg % P.a.n_rb;
+    c.h = seg / P.seg_rb;
+    c.rb = seg % P.seg_rb;
 }
 
 __device__ __forceinline__ void cursor_next(const TcParams &P, Cursor &c) {
     if (++c.tile < c.n_tiles) return;
     c.tile = 0;
-    if (++c.rb < P.a.n_rb) return;
+    if (++c.rb < P.seg_rb) return;
     c.rb = 0;
-    if (++c.h < P.a.Hkv) return;
+    if (++c.h < P.seg_h) return;
     c.h = 0;
     if (++c.b < P.a.B) {
         c.S = req_seq(P, c.b);
         c.n_prefix = ceil_div(c.S, kTile);
-        c.n_tiles = c.n_prefix + P.tail;
+        c.n_tiles = seg_tiles(P, c.S);
     }
 }
 
@@ -296,25 +310,31 @@ struct TileInfo {
     int kind, base, nvalid, j;
 };
 
-__device__ __forceinline__ TileInfo tile_info(const TcParams &P, const Cursor &c) {
+// 64-token tile t of the cursor's segment (0 <= t < n_prefix + tail).
+__device__ __forceinline__ TileInfo tile_at(const TcParams &P, const Cursor &c, int t) {
     TileInfo ti;
-    if (c.tile < c.n_prefix) {
+    if (t < c.n_prefix) {
         ti.kind = kPrefix;
-        ti.j = c.tile;
-        ti.base = c.tile * kTile;
+        ti.j = t;
+        ti.base = t * kTile;
         ti.nvalid = min(kTile, c.S - ti.base);
-    } else if (c.tile - c.n_prefix < P.soft_tiles) {
+    } else if (t - c.n_prefix < P.soft_tiles) {
         ti.kind = kSoft;
-        ti.j = c.tile - c.n_prefix;
+        ti.j = t - c.n_prefix;
         ti.base = ti.j * kTile;
         ti.nvalid = min(kTile, P.a.n_soft - ti.base);
     } else {
         ti.kind = kBlock;
-        ti.j = c.tile - c.n_prefix - P.soft_tiles;
+        ti.j = t - c.n_prefix - P.soft_tiles;
         ti.base = ti.j * kTile;
         ti.nvalid = min(kTile, P.a.R - ti.base);
     }
     return ti;
+}
+
+// The tile of the cursor's step (segments of one tile per step).
+__device__ __forceinline__ TileInfo tile_info(const TcParams &P, const Cursor &c) {
+    return tile_at(P, c, c.tile);
 }
 
 __device__ __forceinline__ size_t slot_row(const TcParams &P, int seg, int cta, int wc, int wcn,
@@ -628,7 +648,7 @@ attn_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUten
 
         const int s = (int)(k % NS);
         const uint32_t ph = (uint32_t)((k / NS) & 1);
-        if (!mbar_wait(&full[s], ph, P.wait)) {
+        if (!mbar_wait_warp(&full[s], ph, P.wait)) {
             raise_status(A.status, SPEC_DEV_TIMEOUT);
             break;
         }
@@ -803,65 +823,251 @@ attn_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUten
 
 // ===================================================== tcgen05 / TMEM variant
 //
-// For row blocks of up to 128 packed rows (the compute-bound shapes: many
-// speculative rows x GQA heads per KV head).  Same schedule, producer,
-// partial slots and combine as attn_tc_kernel; the contraction runs on the
-// fifth-generation tensor cores:
-//   S = Q K^T  -> TMEM (fp32, lane = packed row, column = token), issued by
-//                 one thread as tcgen05.mma (bf16 x bf16 -> fp32), Q and K
-//                 both from 128B-swizzled TMA copies in shared memory;
-//   softmax    -> one thread per row reads its S row from TMEM, masks,
-//                 scales, exponentiates in the exp2 domain and writes P (bf16)
-//                 back to TMEM;
-//   O += P V   -> TMEM (fp32, 128 columns = head_dim), P from TMEM, V read as
-//                 an MN-major operand straight from the TMA tile.
-// Shared memory carries 5 K/V stages and two query blocks: the producer warp
-// copies a segment's 128 packed query rows (a box of 128 / G rows x G
-// heads) ahead of its first K/V tile, into the buffer the segment before
-// the previous one released, so segment starts cost the softmax threads no
-// query traffic.
-// The running max is raised only when a row's tile max exceeds it by more
-// than 2^8 (then O and l are rescaled in place); below that, p <= 256 and
-// the fp32 accumulators absorb it.  S and P are double-buffered so S(t) is
-// computed while the softmax works on tile t-1.
+// For blocks of at least 64 packed rows per KV head (SS, ConFu: shapes whose
+// tile time the softmax and the tensor cores set, not HBM).  Same linear
+// schedule, split and partial slots as attn_tc_kernel; its segments are
+// units of one 128-lane row tile, and every step of a unit feeds the tile
+// 128 keys: two 64-token sub-tiles, side by side in shared memory, so that
+// S takes one N = 128 MMA per 16 head dimensions and PV one M = 128 /
+// N = 128 MMA per 16 keys (few, large MMAs: the issuing thread shares its SM
+// sub-partition with softmax warps, and small MMAs cost more to issue than
+// to run).
+//   * rows mode: a unit is row block rb of KV head h (128 packed rows); a
+//     step is the segment's tiles 2j and 2j + 1 (prefix, soft-prompt and
+//     block tiles in that order), both seen by every row;
+//   * merged mode (at most 64 packed rows per KV head): a unit is KV heads
+//     2u and 2u + 1 of one request, their rows in TMEM lanes 0..63 and
+//     64..127 of one query block; a step is tile j of both heads, sub-tile
+//     x holding head 2u + x's keys, and each row sees its own head's
+//     sub-tile only (P is block-diagonal: zero on the other head's keys).
+// The contraction runs on the fifth-generation tensor cores:
+//   S = Q K^T -> TMEM (fp32, lane = row, column = key), one thread issues
+//                tcgen05.mma with Q from TMEM (copied there by tcgen05.cp from
+//                a TMA-loaded shared-memory block) and K (both sub-tiles, one
+//                128-row K-major operand) from shared memory;
+//   softmax   -> warp w handles TMEM lane quarter w % 4 and sub-tile w / 4:
+//                each thread reads its 64 scores, masks, scales, exponentiates
+//                (exp2 domain) and writes P (bf16) over the first 32 columns
+//                of its sub-tile's 64; in rows mode the two threads of a row
+//                (warps w and w + 4) first exchange their maxima through
+//                shared memory, so both use one reference max;
+//   O += P V  -> TMEM (fp32, 128 columns), V (MN-major) from shared memory.
+// S is double-buffered, so S(k + 1) runs on the tensor cores while the
+// softmax works on step k.  The running max is raised only when a row's step
+// max exceeds it by more than 2^8 (then O and l are rescaled in place, after
+// the previous PV); below that, p <= 256 and the fp32 accumulators absorb it.
+// Warps: 0-7 softmax, 8 TMA producer, 9 MMA issuer, 10 the boundary record
+// for the combine, 11 completes the third warpgroup (setmaxnreg works per
+// warpgroup).
 namespace umma {
 
 using namespace tc5;
 
-constexpr int kRows = 128;              // rows per CTA tile (MMA M)
-constexpr int kSoftmaxWarps = 4;
-// The producer and the MMA issuer sit on SM sub-partitions 3 and 2, whose
-// softmax warps are the idle ones when a block has at most 64 rows (warps
-// 4 and 5 only complete the warp count).
-constexpr int kProducerWarp = 7;
-constexpr int kMmaWarp = 6;
-constexpr int kThreads = 8 * 32;
-constexpr int kNS = 5;                  // K/V stages
+constexpr int kRows = 128;              // rows per tile (MMA M)
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kRecWarp = 10;
+constexpr int kThreads = 12 * 32;
+// Registers a thread, split by setmaxnreg: the launch gives every thread
+// kLaunchRegs (the most a 384-thread CTA can have); the softmax warpgroups
+// raise theirs to kSoftmaxRegs and the third lowers to kOtherRegs.  The
+// split must fit the launch allocation, or the raise would wait forever.
+constexpr int kLaunchRegs = 168;
+constexpr int kSoftmaxRegs = 176;
+constexpr int kOtherRegs = 152;
+static_assert(8 * 32 * kSoftmaxRegs + 4 * 32 * kOtherRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
+// A slot holds the K (or V) of one step: two 64-token sub-tiles x 128 head
+// dimensions, as two 64-element halves hh, each 128 rows of 128 bytes
+// (sub-tile x at rows 64 x ..), 128-byte swizzled: token t of sub-tile x,
+// elements 64 hh .. 64 hh + 63 at byte hh * kHalf + (64 x + t) * 128.
+constexpr int kHalf = 2 * 64 * 128;
+constexpr int kSlotBytes = 2 * kHalf;   // 32 KB
+constexpr int kSlots = 5;               // ring: K and V of a step in consecutive slots
 constexpr int kQHalf = kRows * 128;     // one 64-element half of a query block
+constexpr int kQBytes = 2 * kQHalf;     // one query block: 128 rows x 128
 constexpr int kTmemCols = 512;
-constexpr int kColO = 0;                // O: columns [0, 128)
-constexpr int kColS = 128;              // S buffer b: [128 + 64 b, 192 + 64 b)
-constexpr int kColP = 320;              // P buffer b: [320 + 32 b, 352 + 32 b), bf16 pairs
-constexpr int kColQ = 384;              // Q buffer b: [384 + 64 b, 448 + 64 b), bf16 pairs
+// TMEM columns: O at [0, 128); S buffer b at [128 + 128 b, 256 + 128 b), its
+// sub-tile x scores at + 64 x, P (bf16 pairs) of sub-tile x over the first 32
+// of those; query buffer b at [384 + 64 b, 448 + 64 b)
+constexpr uint32_t kColO = 0;
+__device__ __forceinline__ uint32_t col_s(int b) { return 128u + 128u * (uint32_t)b; }
+__device__ __forceinline__ uint32_t col_q(int b) { return 384u + 64u * (uint32_t)b; }
 constexpr float kRescale = 8.f;         // log2 growth allowed before rescaling
 
-// Byte offset, inside a K or V tile, of token `tok`'s first 128-byte row
-// (half 0); tiles are blocks of 2^rbl tokens, each block NH halves of
-// 2^rbl rows of 128 bytes (see tile_addr).
-template <int NH>
-__device__ __forceinline__ uint32_t row_off(int tok, int rbl) {
-    return (uint32_t)((((tok >> rbl) * NH) << rbl) + (tok & ((1 << rbl) - 1))) * 128u;
-}
-
 struct Shared {
-    uint64_t full[kNS], empty[kNS];
+    uint64_t full[kSlots], empty[kSlots];
+    uint64_t q_full, q_empty;           // the query staging block (shared memory)
+    uint64_t q_tfree[2];                // TMEM query buffer b: its last S MMA done
     uint64_t s_full[2], p_full[2], o_upd[2];
-    uint64_t q_full[2], q_empty[2];     // Q buffer b holds segment n (n % 2 == b)
-    uint64_t q_tfree[2];                // TMEM Q buffer b: its segment's S MMAs done
     uint64_t drain;
+    // rows mode: the two threads of a row swap a value (step maxima, the
+    // sums at the epilogue) through xval[n % 2][sub-tile][lane], the n-th
+    // swap of lane quarter q completing xbar[q][n % 2] (one arrival per warp)
+    uint64_t xbar[4][2];
+    float xval[2][2][kRows];
     uint32_t tmem_base;
     int abort;
 };
+
+constexpr size_t kSmemBytes =
+    (size_t)kSlots * kSlotBytes + (size_t)kQBytes + sizeof(Shared) + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory of the tcgen05 verify kernel");
+
+// One sub-tile of a step: the KV head whose keys it holds and its 64-token
+// tile, or absent (merged: an odd last head; rows mode: past the last tile).
+struct Sub {
+    int head;
+    TileInfo ti;
+    bool present;
+};
+
+// Sub-tile x of the cursor's step.
+__device__ __forceinline__ Sub sub_tile(const TcParams &P, const Cursor &c, int x) {
+    Sub u;
+    if (P.um_merged) {
+        u.head = 2 * c.h + x;
+        u.present = u.head < P.a.Hkv;
+        u.ti = tile_at(P, c, c.tile);
+    } else {
+        u.head = c.h;
+        const int t = 2 * c.tile + x;
+        u.present = t < c.n_prefix + P.tail;
+        u.ti = tile_at(P, c, u.present ? t : 0);
+    }
+    return u;
+}
+
+// Producer warp: for each step of [t_begin, t_end), its K and V (both
+// sub-tiles) into consecutive ring slots, and each unit's query block ahead
+// of its first step.  Every lane owns one box of a step -- lane
+// 16 kv + 8 x + 2 i + hh: K (kv = 0) or V, sub-tile x, page i (paged prefix
+// tiles: boxes of page_size rows; other tiles: i = 0, boxes of 64 rows),
+// half hh -- so that one warp-wide TMA instruction issues the whole step and
+// every sub-tile has the same layout.
+__device__ void run_umma_producer(const TcParams &P, const CUtensorMap &mk, const CUtensorMap &mv,
+                                  const CUtensorMap &mkb, const CUtensorMap &mvb,
+                                  const CUtensorMap &msk, const CUtensorMap &msv,
+                                  const CUtensorMap &mq, uint8_t *ring, uint8_t *qbuf,
+                                  Shared &sh, long long t_begin, long long t_end) {
+    constexpr int NH = 2;
+    const AttnParams &A = P.a;
+    const int lane = threadIdx.x & 31;
+    const int kv = lane >> 4, x = (lane >> 3) & 1, pi = (lane >> 1) & 3, hh = lane & 1;
+    const uint64_t pol_keep = policy_evict_last();
+    // a prefix is read by one unit unless several row blocks share its head
+    const uint64_t pol_stream =
+        (P.um_merged || A.n_rb == 1) ? policy_evict_first() : pol_keep;
+    const int ps = A.paged ? A.page_size : kTile;
+    const int ppt = kTile / ps;          // pages per 64-token tile (paged)
+
+    long long ld = 0;                    // slot loads issued
+    int nq = 0;                          // query blocks issued
+    bool ok = true;
+    Cursor c;
+    cursor_init(P, t_begin, c);          // warp-collective
+    for (long long t = t_begin; t < t_end; ++t) {
+        if (t == t_begin || c.tile == 0) {
+            // the unit's query block (once the previous unit's block has been
+            // copied to TMEM): 128 packed rows of one head, lane hh issuing
+            // half hh; or 64 of each of the unit's two heads (merged), lane
+            // 2 x + hh issuing head 2u + x's half hh
+            bool got = true;
+            if (lane == 0) got = nq == 0 || mbar_wait(&sh.q_empty, (uint32_t)((nq - 1) & 1), P.wait);
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) {
+                ok = false;
+                break;
+            }
+            const int nh = P.um_merged ? (2 * c.h + 1 < A.Hkv ? 2 : 1) : 1;
+            if (lane == 0)
+                mbar_arrive_expect_tx(&sh.q_full, (uint32_t)nh * (P.um_merged ? kQBytes / 2 : kQBytes));
+            __syncwarp();
+            if (P.um_merged) {
+                if (lane < 2 * nh)
+                    tma_load_4d(qbuf + (lane & 1) * kQHalf + (lane >> 1) * (kQHalf / 2), &mq,
+                                (lane & 1) * 64, 0, 2 * c.h + (lane >> 1), c.b * A.R, &sh.q_full,
+                                pol_keep);
+            } else if (lane < NH) {
+                tma_load_4d(qbuf + lane * kQHalf, &mq, lane * 64, 0, c.h,
+                            c.b * A.R + c.rb * (kRows / A.G), &sh.q_full, pol_keep);
+            }
+            ++nq;
+        }
+        // this lane's box of the step
+        const Sub u = sub_tile(P, c, x);
+        const CUtensorMap *map = nullptr;
+        int bx = 0, by = 0;
+        uint32_t bytes = 0;
+        uint64_t pol = pol_keep;
+        if (u.present) {
+            const TileInfo &ti = u.ti;
+            if (ti.kind == kPrefix && A.paged) {
+                const int tok = ti.base + pi * ps;
+                if (pi < ppt && tok < c.S) {
+                    const int pg = A.page_table[(size_t)c.b * A.max_pages + tok / ps];
+                    if (pg < 0 || pg >= A.n_pages) {
+                        raise_status(A.status, SPEC_DEV_BAD_PAGE);
+                    } else {
+                        map = kv ? &mv : &mk;
+                        by = ((pg * A.Hkv + u.head) * NH + hh) * ps;
+                        bytes = (uint32_t)ps * 128u;
+                        pol = pol_stream;
+                    }
+                }
+            } else if (pi == 0) {
+                bx = hh * 64;
+                bytes = (uint32_t)kTile * 128u;
+                if (ti.kind == kPrefix) {
+                    map = kv ? &mv : &mk;
+                    by = (c.b * A.Hkv + u.head) * A.max_seq + ti.base;
+                    pol = pol_stream;
+                } else if (ti.kind == kSoft) {
+                    map = kv ? &msv : &msk;
+                    by = u.head * A.n_soft + ti.base;
+                } else {
+                    map = kv ? &mvb : &mkb;
+                    by = (c.b * A.Hkv + u.head) * A.R + ti.base;
+                }
+            }
+        }
+        const uint32_t bytes_k = __reduce_add_sync(0xffffffffu, kv == 0 ? bytes : 0u);
+        const uint32_t bytes_v = __reduce_add_sync(0xffffffffu, kv == 1 ? bytes : 0u);
+        const int ks = (int)(ld % kSlots), vs = (int)((ld + 1) % kSlots);
+        bool got = true;
+        if (lane == 0)
+            got = mbar_wait(&sh.empty[ks], (uint32_t)(((ld / kSlots) & 1) ^ 1), P.wait) &&
+                  mbar_wait(&sh.empty[vs], (uint32_t)((((ld + 1) / kSlots) & 1) ^ 1), P.wait);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+            ok = false;
+            break;
+        }
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&sh.full[ks], bytes_k);
+            mbar_arrive_expect_tx(&sh.full[vs], bytes_v);
+        }
+        __syncwarp();
+        const int slot = kv ? vs : ks;
+        if (bytes)
+            tma_load_2d(ring + slot * kSlotBytes + hh * kHalf + (x * kTile + pi * ps) * 128, map, bx,
+                        by, &sh.full[slot], pol);
+        ld += 2;
+        cursor_next(P, c);
+    }
+    if (lane == 0) {
+        if (!ok) raise_status(A.status, SPEC_DEV_TIMEOUT);
+        // do not leave while copies into this CTA's shared memory are in
+        // flight (the default limit: these copies were issued and complete)
+        for (long long i = ld - 1; i >= 0 && i >= ld - kSlots; --i)
+            if (!mbar_wait(&sh.full[i % kSlots], (uint32_t)((i / kSlots) & 1))) {
+                raise_status(A.status, SPEC_DEV_TIMEOUT);
+                break;
+            }
+        if (nq > 0 && !mbar_wait(&sh.q_full, (uint32_t)((nq - 1) & 1)))
+            raise_status(A.status, SPEC_DEV_TIMEOUT);
+    }
+}
 
 }  // namespace umma
 
@@ -874,14 +1080,12 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
     pdl_wait();
     using namespace umma;
     static_assert(D == 128, "tcgen05 path is built for head_dim 128");
-    constexpr int NH = D / 64;
-    constexpr int KV_BYTES = NH * kHalfBytes;
-    constexpr int STAGE = 2 * KV_BYTES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *qbuf = smem + kNS * STAGE;          // two query blocks of kRows x D bf16
-    Shared &sh = *reinterpret_cast<Shared *>(qbuf + 2 * kRows * D * 2);
+    uint8_t *ring = smem;                                  // kSlots K / V slots
+    uint8_t *qbuf = smem + kSlots * kSlotBytes;            // the query staging block
+    Shared &sh = *reinterpret_cast<Shared *>(qbuf + kQBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const AttnParams &A = P.a;
@@ -893,21 +1097,22 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                          : "memory");
     }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kNS; ++s) {
+        for (int s = 0; s < kSlots; ++s) {
             mbar_init(&sh.full[s], 1);
             mbar_init(&sh.empty[s], 1);
         }
+        const int nw = __popc(P.um_act[0]) + __popc(P.um_act[1]);
+        mbar_init(&sh.q_full, 1);
+        mbar_init(&sh.q_empty, 1);
         for (int b = 0; b < 2; ++b) {
+            mbar_init(&sh.q_tfree[b], 1);
             mbar_init(&sh.s_full[b], 1);
-            mbar_init(&sh.p_full[b], kSoftmaxWarps);
+            mbar_init(&sh.p_full[b], nw);
             mbar_init(&sh.o_upd[b], 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&sh.q_full[b], 1);
-            mbar_init(&sh.q_empty[b], 1);
-            mbar_init(&sh.q_tfree[b], 1);
-        }
         mbar_init(&sh.drain, 1);
+        for (int q = 0; q < 4; ++q)
+            for (int b = 0; b < 2; ++b) mbar_init(&sh.xbar[q][b], 2);
         sh.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -922,6 +1127,7 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
     __syncthreads();
     fence_after();
     const uint32_t tmem = sh.tmem_base;
+    volatile int *abort = &sh.abort;
 
     const long long T = warp_total_tiles(P);
     const int cta = blockIdx.x;
@@ -932,378 +1138,382 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
         P.bounds[cta] = t_begin;
         if (cta == P.n_ctas - 1) P.bounds[P.n_ctas] = T;
     }
-    volatile int *abort = &sh.abort;
 
-    if (warp == 5) {
-        // A warp with no other role: when this CTA's range starts inside a
-        // segment and the ranges between the segment's first CTA and this
-        // one are empty (this is the segment's first boundary), record the
-        // segment and the CTAs sharing it for the combine.
-        BoundaryRec rec{0, 0, -1, 0, 0, 0};
-        if (t_begin < t_end) {
-            Cursor c;
-            cursor_init(P, t_begin, c);
-            if (c.tile > 0) {
-                rec.s0 = t_begin - c.tile;
-                rec.s1 = rec.s0 + c.n_tiles;
-                bool first_boundary = true;
-                int f = cta - 1, l = cta;
-                for (;; --f) {
-                    const long long lo = warp_range_lo(P, C, T, f);
-                    if (lo <= rec.s0 || f == 0) break;
-                    if (lo < t_begin) first_boundary = false;   // a part starts in between
-                }
-                while (l + 1 < P.n_ctas && warp_range_lo(P, C, T, l + 1) < rec.s1) ++l;
-                if (first_boundary) {
-                    rec.seg = (c.b * A.Hkv + c.h) * A.n_rb + c.rb;
-                    rec.first = f;
-                    rec.last = l;
-                    // which of them hold a part (ranges between may be empty)
-                    if (l - f < 32) {
-                        long long lo = warp_range_lo(P, C, T, f);
-                        for (int j = f; j <= l; ++j) {
-                            const long long hi = warp_range_lo(P, C, T, j + 1);
-                            if (max(lo, rec.s0) < min(hi, rec.s1)) rec.parts |= 1u << (j - f);
-                            lo = hi;
+    if (warp >= kProducerWarp) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
+        if (warp == kRecWarp) {
+            // When this CTA's range starts inside a unit and the ranges
+            // between the unit's first CTA and this one are empty (this is
+            // the unit's first boundary), record the unit and the CTAs
+            // sharing it for the combine.
+            BoundaryRec rec{0, 0, -1, 0, 0, 0};
+            if (t_begin < t_end) {
+                Cursor c;
+                cursor_init(P, t_begin, c);
+                if (c.tile > 0) {
+                    rec.s0 = t_begin - c.tile;
+                    rec.s1 = rec.s0 + c.n_tiles;
+                    bool first_boundary = true;
+                    int f = cta - 1, l = cta;
+                    for (;; --f) {
+                        const long long lo = warp_range_lo(P, C, T, f);
+                        if (lo <= rec.s0 || f == 0) break;
+                        if (lo < t_begin) first_boundary = false;   // a part starts in between
+                    }
+                    while (l + 1 < P.n_ctas && warp_range_lo(P, C, T, l + 1) < rec.s1) ++l;
+                    if (first_boundary) {
+                        rec.seg = (c.b * P.seg_h + c.h) * P.seg_rb + c.rb;
+                        rec.first = f;
+                        rec.last = l;
+                        if (l - f < 32) {
+                            long long lo = warp_range_lo(P, C, T, f);
+                            for (int j = f; j <= l; ++j) {
+                                const long long hi = warp_range_lo(P, C, T, j + 1);
+                                if (max(lo, rec.s0) < min(hi, rec.s1)) rec.parts |= 1u << (j - f);
+                                lo = hi;
+                            }
                         }
                     }
                 }
             }
-        }
-        if (lane == 0) P.recs[cta] = rec;
-    }
-
-    if (t_begin < t_end) {
-        if (warp == kProducerWarp) {
-            const QLoad ql{&mq, qbuf, sh.q_full, sh.q_empty};
-            run_producer<D, kNS>(P, mk, mv, mkb, mvb, msk, msv, smem, sh.full, sh.empty, t_begin,
-                                 t_end, &ql);
-        } else if (warp == kMmaWarp) {
+            if (lane == 0) P.recs[cta] = rec;
+        } else if (t_begin < t_end && warp == kProducerWarp) {
+            run_umma_producer(P, mk, mv, mkb, mvb, msk, msv, mq, ring, qbuf, sh, t_begin, t_end);
+        } else if (t_begin < t_end && warp == kMmaWarp) {
             // --------------------------------------------------- MMA issuer
+            // (the cursor's set-up is warp-collective: the whole warp)
             Cursor c;
             cursor_init(P, t_begin, c);
             if (lane == 0) {
                 const uint32_t id_pv = idesc(kRows, D, false, true);
+                const uint32_t id_s128 = idesc(kRows, 2 * kTile, false, false);
                 const uint32_t id_s64 = idesc(kRows, kTile, false, false);
-                uint32_t a_q = 0;              // TMEM query block of the current segment
-                int seg_n = 0;
-                int prev_rbl = 6, prev_stage = 0;
-                bool prev_first = true;
+                // descriptors of ring slot 0 (K: K-major over 128 rows; V:
+                // MN-major, halves kHalf apart); slot i is i * kSlotBytes
+                // further, i.e. (i * kSlotBytes) >> 4 in the address field
+                const uint64_t kd0 = smem_desc(smem_u32(ring), 16, 1024);
+                const uint64_t vd0 = smem_desc(smem_u32(ring), kHalf, 1024);
+                int nq = 0;                    // query blocks (units) started
                 bool ok = true;
-                // O += P(j) V(j): A = P buffer j%2 (TMEM), B = V (MN-major smem)
-                auto issue_pv = [&](int j, int rbl, int stage, bool first) -> bool {
-                    const int b = j & 1;
+                // previous step: its V slot, whether it has sub-tile 1, and
+                // whether it was its unit's first in this range
+                int pv_slot = 0;
+                bool pv_two = false, pv_first = true;
+                // O (+)= P(j) V(j): A = P of S buffer j % 2 (TMEM, sub-tile x
+                // at column 64 x), B = V (both sub-tiles, MN-major)
+                auto issue_pv = [&](long long j) -> bool {
+                    const int b = (int)(j & 1);
                     if (!mbar_wait(&sh.p_full[b], (uint32_t)((j >> 1) & 1), P.wait)) return false;
+                    if (!mbar_wait(&sh.full[pv_slot], (uint32_t)(((2 * j + 1) / kSlots) & 1), P.wait))
+                        return false;
                     fence_after();
-                    const uint32_t vb = smem_u32(smem + stage * STAGE + KV_BYTES);
-                    const uint32_t a_p = tmem + kColP + (uint32_t)b * (kTile / 2);
-                    if (rbl == 6) {
-                        const uint64_t vd = smem_desc(vb, kHalfBytes, 1024);
+                    const uint64_t vd = vd0 + (uint64_t)((pv_slot * kSlotBytes) >> 4);
+                    const int nks = pv_two ? 8 : 4;
 #pragma unroll
-                        for (int ks = 0; ks < kTile / 16; ++ks)
-                            mma(tmem + kColO, a_p + ks * 8, vd + (uint64_t)((ks * 2048) >> 4),
-                                id_pv, (ks > 0 || !first) ? 1u : 0u);
-                    } else {
-#pragma unroll
-                        for (int ks = 0; ks < kTile / 16; ++ks)
-                            mma(tmem + kColO, a_p + ks * 8,
-                                smem_desc(vb + row_off<NH>(ks * 16, rbl), (1u << rbl) * 128u, 1024),
-                                id_pv, (ks > 0 || !first) ? 1u : 0u);
+                    for (int ks = 0; ks < 8; ++ks) {
+                        if (ks >= nks) break;
+                        mma(tmem + kColO, tmem + col_s(b) + (uint32_t)((ks >> 2) * 64 + (ks & 3) * 8),
+                            vd + (uint64_t)((ks * 16 * 128) >> 4), id_pv,
+                            (ks > 0 || !pv_first) ? 1u : 0u);
                     }
                     commit(&sh.o_upd[b]);
-                    commit(&sh.empty[stage]);
+                    commit(&sh.empty[pv_slot]);
                     return true;
                 };
-                int k = 0;                     // tiles of this range so far
-                int stage = 0;                 // their K/V stage, and its fill parity
-                uint32_t sph = 0;
+                long long k = 0;               // steps of this range so far
                 for (long long t = t_begin; t < t_end && ok; ++t, ++k) {
-                    const TileInfo ti = tile_info(P, c);
-                    const bool new_seg = (k == 0) || (c.tile == 0);
-                    const int rbl = (ti.kind == kPrefix && A.paged) ? P.page_log2 : 6;
-                    if (new_seg && k > 0) {
-                        ok = issue_pv(k - 1, prev_rbl, prev_stage, prev_first);
-                        if (!ok) break;
+                    const bool new_unit = k == 0 || c.tile == 0;
+                    const bool last_of_unit = c.tile == c.n_tiles - 1 || t == t_end - 1;
+                    if (new_unit && k > 0) {
+                        if (!(ok = issue_pv(k - 1))) break;
                     }
-                    if (new_seg) {
-                        // the segment's query block: shared memory -> TMEM
-                        // buffer seg_n % 2 (tcgen05.cp, ordered before the
-                        // MMAs that read it), once the segment two back has
-                        // finished its S MMAs on that buffer; the copy's
-                        // completion frees the shared-memory block
-                        const int qb = seg_n & 1;
-                        if ((seg_n >= 2 &&
-                             !mbar_wait(&sh.q_tfree[qb], (uint32_t)(((seg_n - 2) >> 1) & 1), P.wait)) ||
-                            !mbar_wait(&sh.q_full[qb], (uint32_t)((seg_n >> 1) & 1), P.wait)) {
+                    if (new_unit) {
+                        // the unit's query block: shared memory -> TMEM buffer
+                        // nq % 2 (tcgen05.cp, ordered before the MMAs that
+                        // read it), once the unit two back has finished its S
+                        // MMAs there; the copy's completion frees the block
+                        const int qb = nq & 1;
+                        if ((nq >= 2 &&
+                             !mbar_wait(&sh.q_tfree[qb], (uint32_t)(((nq - 2) >> 1) & 1), P.wait)) ||
+                            !mbar_wait(&sh.q_full, (uint32_t)(nq & 1), P.wait)) {
                             ok = false;
                             break;
                         }
-                        a_q = tmem + kColQ + (uint32_t)qb * 64;
-                        const uint64_t qd = smem_desc(smem_u32(qbuf + qb * (kRows * D * 2)), 16, 1024);
+                        const uint64_t qd = smem_desc(smem_u32(qbuf), 16, 1024);
 #pragma unroll
                         for (int i = 0; i < D / 16; ++i)
-                            tc_cp_128x256b(a_q + i * 8,
+                            tc_cp_128x256b(tmem + col_q(qb) + i * 8,
                                            qd + (uint64_t)((((i >> 2) * kQHalf) + (i & 3) * 32) >> 4));
-                        commit(&sh.q_empty[qb]);
-                        ++seg_n;
+                        commit(&sh.q_empty);
+                        ++nq;
                     }
-                    if (!mbar_wait(&sh.full[stage], sph, P.wait)) { ok = false; break; }
-                    // S(k) = Q K^T into S buffer k%2
-                    const uint32_t kb = smem_u32(smem + stage * STAGE);
-                    const uint32_t s_col = tmem + kColS + (uint32_t)(k & 1) * kTile;
-                    if (rbl == 6) {
-                        const uint64_t kd = smem_desc(kb, 16, 1024);
-#pragma unroll
-                        for (int ks = 0; ks < D / 16; ++ks)
-                            mma(s_col, a_q + ks * 8,
-                                kd + (uint64_t)((((ks >> 2) * kHalfBytes) + (ks & 3) * 32) >> 4),
-                                id_s64, ks > 0 ? 1u : 0u);
-                    } else {
-                        // paged tile: one MMA per page block (its 8-row groups
-                        // are contiguous only within the block)
-                        const int blk = 1 << rbl;
-                        const uint32_t id_s = idesc(kRows, blk, false, false);
-                        for (int i = 0; i < kTile / blk; ++i)
-#pragma unroll
-                            for (int ks = 0; ks < D / 16; ++ks) {
-                                const int hh = ks >> 2, kk = ks & 3;
-                                const uint32_t boff = (uint32_t)((i * NH + hh) * blk) * 128u + kk * 32;
-                                mma(s_col + i * blk, a_q + ks * 8, smem_desc(kb + boff, 16, 1024),
-                                    id_s, ks > 0 ? 1u : 0u);
-                            }
+                    // S(k) into S buffer k % 2: one N = 128 MMA per 16 head
+                    // dimensions over both sub-tiles (N = 64 when sub-tile 1 is
+                    // absent)
+                    const int kslot = (int)((2 * k) % kSlots);
+                    if (!mbar_wait(&sh.full[kslot], (uint32_t)(((2 * k) / kSlots) & 1), P.wait)) {
+                        ok = false;
+                        break;
                     }
+                    const bool two = sub_tile(P, c, 1).present;
+                    const uint32_t a_q = tmem + col_q((nq - 1) & 1);
+                    const uint64_t kd = kd0 + (uint64_t)((kslot * kSlotBytes) >> 4);
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        mma(tmem + col_s((int)(k & 1)), a_q + ks * 8,
+                            kd + (uint64_t)((((ks >> 2) * kHalf) + (ks & 3) * 32) >> 4),
+                            two ? id_s128 : id_s64, ks > 0 ? 1u : 0u);
                     commit(&sh.s_full[k & 1]);
-                    // last S of the segment in this range: its TMEM query
-                    // buffer may be refilled two segments on
-                    if (c.tile == c.n_tiles - 1 || t == t_end - 1) commit(&sh.q_tfree[(seg_n - 1) & 1]);
-                    if (!new_seg && k > 0) {
-                        ok = issue_pv(k - 1, prev_rbl, prev_stage, prev_first);
-                        if (!ok) break;
+                    commit(&sh.empty[kslot]);
+                    // the unit's last S in this range: its TMEM query buffer
+                    // may be refilled two units on
+                    if (last_of_unit) commit(&sh.q_tfree[(nq - 1) & 1]);
+                    if (!new_unit) {
+                        if (!(ok = issue_pv(k - 1))) break;
                     }
-                    prev_rbl = rbl;
-                    prev_stage = stage;
-                    prev_first = new_seg;
-                    if (++stage == kNS) {
-                        stage = 0;
-                        sph ^= 1u;
-                    }
+                    pv_slot = (int)((2 * k + 1) % kSlots);
+                    pv_two = two;
+                    pv_first = new_unit;
                     cursor_next(P, c);
                 }
-                if (ok && k > 0) ok = issue_pv(k - 1, prev_rbl, prev_stage, prev_first);
+                if (ok && k > 0) ok = issue_pv(k - 1);
                 if (!ok) {
                     raise_status(A.status, SPEC_DEV_TIMEOUT);
                     *abort = 1;
                 }
-                // every MMA issued above has completed before TMEM is released
+                // every MMA and copy issued above has completed before TMEM
+                // is released (the default limit)
                 commit(&sh.drain);
                 if (!mbar_wait(&sh.drain, 0)) raise_status(A.status, SPEC_DEV_TIMEOUT);
             }
-        } else if (warp < kSoftmaxWarps) {
-            // ------------------------------------------------------ softmax
-            const int r = warp * 32 + lane;                 // row of the CTA tile
-            const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-            Cursor c;
-            cursor_init(P, t_begin, c);
-            float m_used = -INFINITY, l = 0.f;
-            bool rvalid = false, rsoft = false, warp_rows = false;
-            int rrow = -1, seg_n = 0, vmask_j = -1;
-            // the next segment's row flags and block tile 0's mask words,
-            // loaded one segment ahead (unconditional loads of a clamped
-            // row, so nothing waits for them before their use)
-            uint32_t nx_fl = 0, nx_w0 = 0, nx_w1 = 0;
-            auto fetch_row = [&](const Cursor &cq) {
-                const int p = min(cq.rb * kRows + r, A.M - 1);
-                const size_t ri = (size_t)cq.b * A.R + p / A.G;
-                nx_fl = A.row_flags[ri];
-                const uint32_t *vr = A.vis + ri * A.W;
-                nx_w0 = vr[0];
-                nx_w1 = vr[A.W > 1 ? 1 : 0];
-            };
-            int seg_b = 0, seg_h = 0, seg_rb = 0, seg_id = 0;
-            uint64_t vmask = 0;
-            bool first = true, seg_whole = false;
-            long long k = 0;
-            const float sc = A.scale_log2;
+        }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
+        // ------------------------------------------------------ softmax
+        const int q = warp & 3, x = warp >> 2;         // lane quarter, sub-tile
+        const int r = q * 32 + lane;                    // TMEM lane of this row
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        const bool active = ((P.um_act[x] >> q) & 1) != 0;
+        // merged: sub-tile x's rows are lanes 64 x .. 64 x + 63 (packed row
+        // r - 64 x of head 2u + x); rows mode: packed row rb * 128 + r, and
+        // the two threads of a row (sub-tiles 0 and 1) share every step
+        const bool merged = P.um_merged != 0;
+        const float sc = A.scale_log2;
+        // threads of this sub-tile that clear ragged V rows
+        const int nsan = __popc(P.um_act[x]) * 32;
+        const int isan = __popc(P.um_act[x] & ((1u << q) - 1u)) * 32 + lane;
+        Cursor c;
+        cursor_init(P, t_begin, c);
+        float m_used = -INFINITY, l = 0.f;
+        bool rvalid = false, rsoft = false, warp_rows = false, row_ok = false, seg_whole = false;
+        int rrow = -1, seg_b = 0, head = 0, p = 0, seg_id = 0;
+        uint64_t vmask = 0;
+        int vmask_j = -1;
+        long long k = 0;
+        bool ok = true;
+        int nx = 0;                    // swaps with the other thread of the row
+        // rows mode: give v to the other thread of this row, take its value
+        // (bounded: if the other warp has stopped, this one stops too)
+        auto swap = [&](float v, float &other) -> bool {
+            const int b = nx & 1;
+            sh.xval[b][x][r] = v;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.xbar[q][b]);
+            const bool got = mbar_wait_warp(&sh.xbar[q][b], (uint32_t)((nx >> 1) & 1), P.wait);
+            other = sh.xval[b][x ^ 1][r];
+            ++nx;
+            return got;
+        };
 
-            // end of this CTA's part of a segment (after PV(j)): a segment
-            // wholly inside this CTA's range writes its final O (bf16) and
-            // LSE; otherwise the (m, l, O) partial goes to the workspace
-            auto epilogue = [&](long long j) -> bool {
-                if (!mbar_wait(&sh.o_upd[j & 1], (uint32_t)((j >> 1) & 1), P.wait)) return false;
-                fence_after();
-                // tcgen05.ld is warp-collective: a warp with any real row
-                // loads, and only its real rows store
-                if (!warp_rows) return true;
-                const int p = seg_rb * kRows + r;
-                const bool row_ok = p < A.M;
-                if (seg_whole) {
-                    const int rr = p / A.G, hq = seg_h * A.G + p % A.G;
-                    const float inv = l > 0.f ? 1.f / l : 0.f;
-                    uint4 *dst = reinterpret_cast<uint4 *>(
-                        static_cast<__nv_bfloat16 *>(A.o) + (((size_t)seg_b * A.R + rr) * A.Hq + hq) * D);
+        // end of this CTA's part of a unit (after PV(j)): a unit wholly inside
+        // this CTA's range writes its final O (bf16) and LSE; otherwise the
+        // (m, l, O) partial goes to the workspace.  Rows mode: each thread of
+        // the pair writes half of the row's columns, with the pair's sum.
+        auto epilogue = [&](long long j) -> bool {
+            if (!mbar_wait_warp(&sh.o_upd[j & 1], (uint32_t)((j >> 1) & 1), P.wait)) return false;
+            fence_after();
+            float lt = l;
+            if (!merged) {
+                float lo = 0.f;
+                if (!swap(l, lo)) return false;
+                lt = l + lo;
+            }
+            if (!warp_rows) return true;
+            const int c_lo = merged ? 0 : 2 * x, c_hi = merged ? D / 32 : 2 * x + 2;
+            if (seg_whole) {
+                const int rr = row_ok ? p / A.G : 0, hq = head * A.G + (row_ok ? p % A.G : 0);
+                const float inv = lt > 0.f ? 1.f / lt : 0.f;
+                uint4 *dst = reinterpret_cast<uint4 *>(
+                    static_cast<__nv_bfloat16 *>(A.o) + (((size_t)seg_b * A.R + rr) * A.Hq + hq) * D);
+#pragma unroll 1
+                for (int c32 = c_lo; c32 < c_hi; ++c32) {
+                    uint32_t v[32];
+                    ld32(tmem + lane_base + kColO + c32 * 32, v);
+                    wait_ld(v);
+                    if (!row_ok) continue;
 #pragma unroll
-                    for (int c32 = 0; c32 < D / 32; ++c32) {
-                        uint32_t v[32];
-                        ld32(tmem + lane_base + kColO + c32 * 32, v);
-                        wait_ld();
-                        if (!row_ok) continue;
+                    for (int e = 0; e < 32; e += 8)
+                        dst[(c32 * 32 + e) / 8] = make_uint4(
+                            pack_bf16(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv),
+                            pack_bf16(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv),
+                            pack_bf16(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv),
+                            pack_bf16(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv));
+                }
+                if (row_ok && x == (merged ? x : 0))
+                    A.lse[((size_t)seg_b * A.Hq + hq) * A.R + rr] =
+                        lt > 0.f ? (m_used + log2f(lt)) * kLn2 : -INFINITY;
+            } else {
+                // partial slots hold a unit's 128 lanes
+                const size_t row = slot_row(P, seg_id, cta, 0, 1, r);
+                float *po = A.part_o + row * D;
+#pragma unroll 1
+                for (int c32 = c_lo; c32 < c_hi; ++c32) {
+                    uint32_t v[32];
+                    ld32(tmem + lane_base + kColO + c32 * 32, v);
+                    wait_ld(v);
+                    if (!row_ok) continue;
 #pragma unroll
-                        for (int e = 0; e < 32; e += 8)
-                            dst[(c32 * 32 + e) / 8] = make_uint4(
-                                pack_bf16(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv),
-                                pack_bf16(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv),
-                                pack_bf16(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv),
-                                pack_bf16(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv));
-                    }
-                    if (row_ok)
-                        A.lse[((size_t)seg_b * A.Hq + hq) * A.R + rr] =
-                            l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
-                } else {
-                    // partial slots hold all kRows rows of a segment
-                    const size_t row = slot_row(P, seg_id, cta, 0, 1, r);
-                    float *po = A.part_o + row * D;
-#pragma unroll
-                    for (int c32 = 0; c32 < D / 32; ++c32) {
-                        uint32_t v[32];
-                        ld32(tmem + lane_base + kColO + c32 * 32, v);
-                        wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; e += 4)
-                            *reinterpret_cast<float4 *>(po + c32 * 32 + e) =
-                                make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                                            __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-                    }
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4 *>(po + c32 * 32 + e) =
+                            make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                                        __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+                }
+                if (row_ok && x == (merged ? x : 0)) {
                     A.part_ml[row * 2] = m_used;
-                    A.part_ml[row * 2 + 1] = l;
+                    A.part_ml[row * 2 + 1] = lt;
                 }
-                return true;
-            };
+            }
+            return true;
+        };
 
-            bool ok = true;
-            for (long long t = t_begin; t < t_end; ++t, ++k) {
-                if (*abort) { ok = false; break; }
-                const TileInfo ti = tile_info(P, c);
-                const bool new_seg = (k == 0) || (c.tile == 0);
-                if (new_seg) {
-                    if (k > 0 && !(ok = epilogue(k - 1))) break;
-                    seg_b = c.b;
-                    seg_h = c.h;
-                    seg_rb = c.rb;
-                    seg_id = (c.b * A.Hkv + c.h) * A.n_rb + c.rb;
-                    const long long seg_lo = t - c.tile;
-                    seg_whole = seg_lo >= t_begin && seg_lo + c.n_tiles <= t_end;
-                    // this row's flags for the segment (fetched one segment
-                    // ahead, except at the range's first)
-                    const int p = c.rb * kRows + r;
-                    warp_rows = c.rb * kRows + warp * 32 < A.M;
-                    if (k == 0) fetch_row(c);
-                    rrow = p < A.M ? p / A.G : -1;
-                    rvalid = rrow >= 0 && (nx_fl & SPEC_ROW_VALID) != 0;
-                    rsoft = rvalid && (nx_fl & SPEC_ROW_SEES_SOFT) != 0;
-                    vmask = rvalid ? ((uint64_t)nx_w0 | (A.W > 1 ? (uint64_t)nx_w1 << 32 : 0ull))
-                                   : 0ull;
-                    vmask_j = 0;
-                    {
-                        const long long t_next = t + (c.n_tiles - c.tile);
-                        if (t_next < t_end) {
-                            Cursor cn = c;
-                            cn.tile = cn.n_tiles - 1;
-                            cursor_next(P, cn);
-                            fetch_row(cn);
-                        }
-                    }
-                    ++seg_n;
-                    m_used = -INFINITY;
-                    l = 0.f;
-                    first = true;
+        for (long long t = t_begin; active && t < t_end; ++t, ++k) {
+            if (__any_sync(0xffffffffu, *abort != 0)) { ok = false; break; }
+            const bool new_unit = k == 0 || c.tile == 0;
+            if (new_unit) {
+                if (k > 0 && !(ok = epilogue(k - 1))) break;
+                seg_b = c.b;
+                seg_id = (c.b * P.seg_h + c.h) * P.seg_rb + c.rb;
+                const long long seg_lo = t - c.tile;
+                seg_whole = seg_lo >= t_begin && seg_lo + c.n_tiles <= t_end;
+                if (merged) {
+                    head = 2 * c.h + x;
+                    p = r - 64 * x;
+                    row_ok = head < A.Hkv && p >= 0 && p < 64 && p < A.M;
+                } else {
+                    head = c.h;
+                    p = c.rb * kRows + r;
+                    row_ok = p < A.M;
                 }
-                if (ti.kind == kBlock && vmask_j != ti.j) {
-                    uint64_t w = 0;
-                    if (rrow >= 0 && rvalid) {
-                        const uint32_t *vr = A.vis + ((size_t)c.b * A.R + rrow) * A.W;
-                        w = vr[2 * ti.j];
-                        if (2 * ti.j + 1 < A.W) w |= (uint64_t)vr[2 * ti.j + 1] << 32;
-                    }
-                    vmask = w;
-                    vmask_j = ti.j;
+                warp_rows = __any_sync(0xffffffffu, row_ok);
+                rrow = row_ok ? p / A.G : -1;
+                rvalid = rsoft = false;
+                if (row_ok) {
+                    const uint8_t fl = A.row_flags[(size_t)seg_b * A.R + rrow];
+                    rvalid = (fl & SPEC_ROW_VALID) != 0;
+                    rsoft = rvalid && (fl & SPEC_ROW_SEES_SOFT) != 0;
                 }
-                if (!mbar_wait(&sh.s_full[k & 1], (uint32_t)((k >> 1) & 1), P.wait)) { ok = false; break; }
+                vmask_j = -1;
+                m_used = -INFINITY;
+                l = 0.f;
+            }
+            const Sub su = sub_tile(P, c, x);
+            const TileInfo &ti = su.ti;
+            if (su.present && ti.kind == kBlock && vmask_j != ti.j) {
+                uint64_t w = 0;
+                if (rvalid) {
+                    const uint32_t *vr = A.vis + ((size_t)seg_b * A.R + rrow) * A.W;
+                    w = vr[2 * ti.j];
+                    if (2 * ti.j + 1 < A.W) w |= (uint64_t)vr[2 * ti.j + 1] << 32;
+                }
+                vmask = w;
+                vmask_j = ti.j;
+            }
+            if (!(ok = mbar_wait_warp(&sh.s_full[k & 1], (uint32_t)((k >> 1) & 1), P.wait))) break;
+            fence_after();
+            const uint32_t tS = tmem + lane_base + col_s((int)(k & 1)) + 64u * x;
+            uint32_t v[2][32];
+            float pm = -INFINITY;          // this thread's raw score maximum
+            if (warp_rows && su.present) {
+                // the 64 scores of this row and sub-tile: both TMEM loads in
+                // flight, one wait
+                ld32(tS, v[0]);
+                ld32(tS + 32, v[1]);
+                wait_ld(v[0]);
+                wait_ld(v[1]);
+                // columns this row sees, as one 64-bit mask; the others
+                // become -inf in place
+                const uint64_t valid_cols =
+                    ti.nvalid >= kTile ? ~0ull : ((1ull << ti.nvalid) - 1ull);
+                uint64_t vm;
+                if (ti.kind == kPrefix) vm = rvalid ? valid_cols : 0ull;
+                else if (ti.kind == kSoft) vm = rsoft ? valid_cols : 0ull;
+                else vm = vmask & valid_cols;
+                if (vm != ~0ull) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t hm = (uint32_t)(vm >> (32 * h));
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            v[h][e] = ((hm >> e) & 1u) ? v[h][e] : 0xff800000u;
+                    }
+                }
+                float tmv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            tmv[i] = max3(tmv[i], __uint_as_float(v[h][e + 2 * i]),
+                                          __uint_as_float(v[h][e + 2 * i + 1]));
+                pm = fmaxf(fmaxf(tmv[0], tmv[1]), fmaxf(tmv[2], tmv[3]));
+            }
+            if (!merged) {
+                // one reference max for both threads of the row
+                float po = -INFINITY;
+                if (!(ok = swap(pm, po))) break;
+                pm = fmaxf(pm, po);
+            }
+            const float tm = pm == -INFINITY ? -INFINITY : pm * sc;
+            // raise the reference max only when it grew by more than 2^8
+            const bool raise = tm > m_used + kRescale || (m_used == -INFINITY && tm != -INFINITY);
+            const float alpha = !raise ? 1.f : (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - tm);
+            // O holds the PVs before PV(k - 1): wait for that one, then
+            // rescale the rows that raised their max (TMEM loads and stores
+            // are warp-collective: the whole warp takes part, the other rows
+            // scaled by exactly 1); rows mode: each thread of the pair takes
+            // half of the row's columns
+            const bool scale_o = raise && !new_unit && m_used != -INFINITY;
+            if (warp_rows && __any_sync(0xffffffffu, scale_o)) {
+                if (!(ok = mbar_wait_warp(&sh.o_upd[(k - 1) & 1], (uint32_t)(((k - 1) >> 1) & 1),
+                                          P.wait)))
+                    break;
                 fence_after();
-                if (warp_rows) {
-                    // the S row: both TMEM loads in flight, one wait
-                    uint32_t v[2][32];
-                    {
-                        const uint32_t sa = tmem + lane_base + kColS + (uint32_t)(k & 1) * kTile;
-                        ld32(sa, v[0]);
-                        ld32(sa + 32, v[1]);
-                        wait_ld(v[0]);
-                        wait_ld(v[1]);
-                    }
-                    // columns this row sees in this tile, as one 64-bit mask;
-                    // the others become -inf in place
-                    const uint64_t valid_cols =
-                        ti.nvalid >= kTile ? ~0ull : ((1ull << ti.nvalid) - 1ull);
-                    uint64_t vm;
-                    if (ti.kind == kPrefix) vm = rvalid ? valid_cols : 0ull;
-                    else if (ti.kind == kSoft) vm = rsoft ? valid_cols : 0ull;
-                    else vm = vmask & valid_cols;
-                    if (vm != ~0ull) {
+                const float a = scale_o ? alpha : 1.f;
+                const int c_lo = merged ? 0 : 2 * x, c_hi = merged ? D / 32 : 2 * x + 2;
+#pragma unroll 1
+                for (int c32 = c_lo; c32 < c_hi; ++c32) {
+                    uint32_t o[32];
+                    const uint32_t oa = tmem + lane_base + kColO + c32 * 32;
+                    ld32(oa, o);
+                    wait_ld(o);
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const uint32_t hm = (uint32_t)(vm >> (32 * h));
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                v[h][e] = ((hm >> e) & 1u) ? v[h][e] : 0xff800000u;
-                        }
-                    }
-                    float tmv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-#pragma unroll
-                        for (int e = 0; e < 32; e += 8)
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                tmv[q] = max3(tmv[q], __uint_as_float(v[h][e + 2 * q]),
-                                              __uint_as_float(v[h][e + 2 * q + 1]));
-                    const float traw = fmaxf(fmaxf(tmv[0], tmv[1]), fmaxf(tmv[2], tmv[3]));
-                    const float tm = traw == -INFINITY ? -INFINITY : traw * sc;
-                    // raise the reference max only when it grew by more than 2^8
-                    if (tm > m_used + kRescale || (m_used == -INFINITY && tm != -INFINITY)) {
-                        const float alpha = (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - tm);
-                        if (!first && m_used != -INFINITY) {
-                            // O holds PV(k-1): wait for it, then scale this row in place
-                            if (!mbar_wait(&sh.o_upd[(k - 1) & 1], (uint32_t)(((k - 1) >> 1) & 1), P.wait)) {
-                                ok = false;
-                                break;
-                            }
-                            fence_after();
-#pragma unroll
-                            for (int c32 = 0; c32 < D / 32; ++c32) {
-                                uint32_t o[32];
-                                const uint32_t oa = tmem + lane_base + kColO + c32 * 32;
-                                ld32(oa, o);
-                                wait_ld(o);
-#pragma unroll
-                                for (int e = 0; e < 32; ++e)
-                                    o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                                st32(oa, o);
-                            }
-                            wait_st();
-                        }
-                        l *= alpha;
-                        m_used = tm;
-                    }
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
+                    st32(oa, o);
+                }
+            }
+            if (raise) {
+                l *= alpha;
+                m_used = tm;
+            }
+            if (warp_rows) {
+                uint32_t w[32];
+                if (su.present) {
+                    // P = exp2(s * scale - mu): pairs by one f32x2 FMA, two
+                    // ex2, one f32x2 add and one pack
                     const float mu = m_used == -INFINITY ? 0.f : m_used;
-                    // P buffer k%2 was last read by PV(k-2)
-                    if (k >= 2 && !mbar_wait(&sh.o_upd[k & 1], (uint32_t)(((k - 2) >> 1) & 1), P.wait)) {
-                        ok = false;
-                        break;
-                    }
-                    // P = exp2(s * scale - mu): pairs by one f32x2 FMA, two ex2,
-                    // one f32x2 add and one pack
                     const uint64_t sc2 = pair(sc, sc), nmu2 = pair(-mu, -mu);
                     uint64_t rs2[2] = {pair(0.f, 0.f), pair(0.f, 0.f)};
-                    uint32_t w[32];
 #pragma unroll
                     for (int e = 0; e < kTile / 2; ++e) {
                         const int h = e / 16, f = 2 * (e % 16);
@@ -1315,42 +1525,51 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                         rs2[e & 1] = add2(rs2[e & 1], pair(p0, p1));
                         w[e] = pack_bf16(p0, p1);
                     }
-                    st32(tmem + lane_base + kColP + (uint32_t)(k & 1) * (kTile / 2), w);
-                    {
-                        float r0, r1, r2, r3;
-                        unpair(rs2[0], r0, r1);
-                        unpair(rs2[1], r2, r3);
-                        l += (r0 + r1) + (r2 + r3);
-                    }
+                    float r0, r1, r2, r3;
+                    unpair(rs2[0], r0, r1);
+                    unpair(rs2[1], r2, r3);
+                    l += (r0 + r1) + (r2 + r3);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) w[e] = 0u;
                 }
-                if (ti.nvalid < kTile) {
-                    // V rows past the valid count hold whatever the copy left
-                    // (stale or unwritten shared memory, cache slots past S_b):
-                    // P is 0 there, but 0 x NaN is NaN, so clear them
-                    const int rbl = (ti.kind == kPrefix && A.paged) ? P.page_log2 : 6;
-                    uint8_t *vt = smem + (int)(k % kNS) * STAGE + KV_BYTES;
-                    const int nchunk = (kTile - ti.nvalid) * NH * 8;
-                    for (int i = r; i < nchunk; i += kSoftmaxWarps * 32) {
-                        const int tok = ti.nvalid + i / (NH * 8), rem = i % (NH * 8);
-                        const int hh = rem >> 3, ch = rem & 7;
-                        *reinterpret_cast<uint4 *>(vt + row_off<NH>(tok, rbl) +
-                                                   hh * ((1 << rbl) * 128) + ch * 16) =
-                            make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                st32(tS, w);
+                if (merged) {
+                    // the other head's keys: P = 0 in this row
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) w[e] = 0u;
+                    st32(tmem + lane_base + col_s((int)(k & 1)) + 64u * (x ^ 1), w);
                 }
-                wait_st();
-                fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.p_full[k & 1]);
-                first = false;
-                cursor_next(P, c);
             }
-            if (ok && k > 0) ok = epilogue(k - 1);
-            if (!ok) {
-                raise_status(A.status, SPEC_DEV_TIMEOUT);
-                *abort = 1;
+            if (su.present && ti.nvalid < kTile) {
+                // V rows past the valid count hold whatever the copy left
+                // (stale or unwritten shared memory, cache slots past S_b):
+                // P is 0 there, but 0 x NaN is NaN, so clear them, once the V
+                // copy has landed
+                const long long vn = 2 * k + 1;
+                if (!(ok = mbar_wait_warp(&sh.full[vn % kSlots], (uint32_t)((vn / kSlots) & 1),
+                                          P.wait)))
+                    break;
+                uint8_t *vt = ring + (int)(vn % kSlots) * kSlotBytes + x * kTile * 128;
+                const int nchunk = (kTile - ti.nvalid) * 2 * 8;
+                for (int i = isan; i < nchunk; i += nsan) {
+                    const int tok = ti.nvalid + i / 16, rem = i % 16;
+                    const int hh = rem >> 3, ch = rem & 7;
+                    *reinterpret_cast<uint4 *>(vt + hh * kHalf + tok * 128 + ch * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
+            wait_st();
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.p_full[k & 1]);
+            cursor_next(P, c);
+        }
+        if (ok && active && k > 0) ok = epilogue(k - 1);
+        if (!ok) {
+            raise_status(A.status, SPEC_DEV_TIMEOUT);
+            *abort = 1;
         }
     }
     fence_before();
@@ -1433,66 +1652,90 @@ __global__ void __launch_bounds__(128) attn_tc_combine_kernel(const __grid_const
     merge_row<D>(P, wcn, b, h, seg, s0, s1, cta_holding(P, s0), cta_holding(P, s1 - 1), p, lane);
 }
 
-// merge_row for the tcgen05 path, from a boundary record: with at most
-// four contributing CTAs every partial's (m, l) and then every O slice are
-// loaded together (two dependent round trips per row); otherwise merge_row.
+// tcgen05 path: merge one row of a split unit -- TMEM lane lane_t of the
+// unit's tile, output row p of KV head h of request b -- over the CTAs
+// first..last whose ranges meet the unit's steps [s0, s1).  With at most
+// four such CTAs every part's (m, l) and then every O slice are loaded
+// together (two dependent round trips); otherwise they are visited one by
+// one.  One warp.
 template <int D>
-__device__ void merge_row_rec(const TcParams &P, const BoundaryRec &rec, int b, int h, int p,
-                              int lane) {
+__device__ void merge_unit_row(const TcParams &P, const BoundaryRec &rec, int lane_t, int b,
+                               int h, int p, int lane) {
     const AttnParams &A = P.a;
     constexpr int kMaxParts = 4;
-    if (rec.last - rec.first >= kMaxParts) {
-        merge_row<D>(P, 1, b, h, rec.seg, rec.s0, rec.s1, rec.first, rec.last, p, lane);
-        return;
-    }
-    const int rr = p % A.rb_rows;
-    size_t row[kMaxParts];
-    float ms[kMaxParts], ls[kMaxParts];
-#pragma unroll
-    for (int j = 0; j < kMaxParts; ++j) {
-        const bool part = rec.first + j <= rec.last && ((rec.parts >> j) & 1u);
-        row[j] = part ? slot_row(P, rec.seg, rec.first + j, 0, 1, rr) : 0;
-        ms[j] = part ? A.part_ml[row[j] * 2] : -INFINITY;
-        ls[j] = part ? A.part_ml[row[j] * 2 + 1] : 0.f;
-    }
-    float mstar = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kMaxParts; ++j) mstar = fmaxf(mstar, ms[j]);
-    float wgt[kMaxParts], L = 0.f;
-#pragma unroll
-    for (int j = 0; j < kMaxParts; ++j) {
-        wgt[j] = ms[j] == -INFINITY ? 0.f : exp2f(ms[j] - mstar);
-        L = fmaf(wgt[j], ls[j], L);
-    }
-    float x[kMaxParts][D / 32];
-#pragma unroll
-    for (int j = 0; j < kMaxParts; ++j)
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c)
-            x[j][c] = wgt[j] != 0.f ? A.part_o[row[j] * D + lane + 32 * c] : 0.f;
     const int r = p / A.G, hq = h * A.G + p % A.G;
     __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(A.o) + (((size_t)b * A.R + r) * A.Hq + hq) * D;
+    float mstar = -INFINITY, L = 0.f;
+    float out[D / 32];
+    if (rec.last - rec.first < kMaxParts) {
+        size_t row[kMaxParts];
+        float ms[kMaxParts], ls[kMaxParts];
+#pragma unroll
+        for (int j = 0; j < kMaxParts; ++j) {
+            const bool part = rec.first + j <= rec.last && ((rec.parts >> j) & 1u);
+            row[j] = part ? slot_row(P, rec.seg, rec.first + j, 0, 1, lane_t) : 0;
+            ms[j] = part ? A.part_ml[row[j] * 2] : -INFINITY;
+            ls[j] = part ? A.part_ml[row[j] * 2 + 1] : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxParts; ++j) mstar = fmaxf(mstar, ms[j]);
+        float wgt[kMaxParts];
+#pragma unroll
+        for (int j = 0; j < kMaxParts; ++j) {
+            wgt[j] = ms[j] == -INFINITY ? 0.f : exp2f(ms[j] - mstar);
+            L = fmaf(wgt[j], ls[j], L);
+        }
+        float xs[kMaxParts][D / 32];
+#pragma unroll
+        for (int j = 0; j < kMaxParts; ++j)
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c)
+                xs[j][c] = wgt[j] != 0.f ? A.part_o[row[j] * D + lane + 32 * c] : 0.f;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < kMaxParts; ++j) acc = fmaf(wgt[j], xs[j][c], acc);
+            out[c] = acc;
+        }
+    } else {
+        auto has_part = [&](int i) {
+            const long long lo = P.bounds[i], hi = P.bounds[i + 1];
+            return max(lo, rec.s0) < min(hi, rec.s1);
+        };
+        for (int i = rec.first; i <= rec.last; ++i)
+            if (has_part(i)) mstar = fmaxf(mstar, A.part_ml[slot_row(P, rec.seg, i, 0, 1, lane_t) * 2]);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) out[c] = 0.f;
+        if (mstar != -INFINITY) {
+            for (int i = rec.first; i <= rec.last; ++i) {
+                if (!has_part(i)) continue;
+                const size_t row = slot_row(P, rec.seg, i, 0, 1, lane_t);
+                const float ms = A.part_ml[row * 2];
+                if (ms == -INFINITY) continue;
+                const float wgt = exp2f(ms - mstar);
+                L = fmaf(wgt, A.part_ml[row * 2 + 1], L);
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c)
+                    out[c] = fmaf(wgt, A.part_o[row * D + lane + 32 * c], out[c]);
+            }
+        }
+    }
     const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-        float acc = 0.f;
-#pragma unroll
-        for (int j = 0; j < kMaxParts; ++j) acc = fmaf(wgt[j], x[j][c], acc);
-        o[lane + 32 * c] = __float2bfloat16_rn(acc * inv);
-    }
+    for (int c = 0; c < D / 32; ++c) o[lane + 32 * c] = __float2bfloat16_rn(out[c] * inv);
     if (lane == 0)
-        A.lse[((size_t)b * A.Hq + hq) * A.R + r] =
-            L > 0.f ? (mstar + log2f(L)) * kLn2 : -INFINITY;
+        A.lse[((size_t)b * A.Hq + hq) * A.R + r] = L > 0.f ? (mstar + log2f(L)) * kLn2 : -INFINITY;
 }
 
-// tcgen05 path: a segment wholly inside one CTA's range already holds its
-// final output; a split segment contains at least one boundary between
+// tcgen05 path: a unit wholly inside one CTA's range already holds its
+// final output; a split unit contains at least one boundary between
 // consecutive CTA ranges.  CTAs (i, y) here take the boundary between
-// attention CTAs i and i + 1 and merge the segment across it when that
-// boundary is the segment's first (CTA y takes every kUmmaCombineSplit-th
-// group of 8 rows), so only split segments cost work (at most n_ctas - 1).
+// attention CTAs i and i + 1 and merge the unit across it when that boundary
+// is the unit's first (CTA y takes every kUmmaCombineSplit-th group of 8 of
+// its rows), so only split units cost work (at most n_ctas - 1).
 constexpr int kUmmaCombineThreads = 256;
-constexpr int kUmmaCombineSplit = 8;     // CTAs per boundary (row slices of the segment)
+constexpr int kUmmaCombineSplit = 8;     // CTAs per boundary (row slices of the unit)
 
 template <int D>
 __global__ void __launch_bounds__(kUmmaCombineThreads)
@@ -1505,13 +1748,29 @@ attn_umma_combine_kernel(const __grid_constant__ TcParams P) {
     // the boundary between CTAs i - 1 and i
     const int i = blockIdx.x + 1;
     const BoundaryRec rec = P.recs[i];
-    if (rec.seg < 0) return;         // no segment's first boundary
-    const int rb = rec.seg % A.n_rb, h = (rec.seg / A.n_rb) % A.Hkv, b = rec.seg / (A.n_rb * A.Hkv);
-    const int p_hi = min(A.M, (rb + 1) * A.rb_rows);
+    if (rec.seg < 0) return;         // no unit's first boundary
+    const int rb = rec.seg % P.seg_rb, hu = (rec.seg / P.seg_rb) % P.seg_h;
+    const int b = rec.seg / (P.seg_rb * P.seg_h);
+    // the unit's rows: merged, M of each of its heads (2 hu at lanes 0..63,
+    // 2 hu + 1 at 64..127); rows mode, those of row block rb
+    int nrows[2];
+    if (P.um_merged) {
+        nrows[0] = A.M;
+        nrows[1] = 2 * hu + 1 < A.Hkv ? A.M : 0;
+    } else {
+        nrows[0] = min(umma::kRows, A.M - rb * umma::kRows);
+        nrows[1] = 0;
+    }
     constexpr int kWarps = kUmmaCombineThreads / 32;
-    for (int p = rb * A.rb_rows + blockIdx.y * kWarps + warp; p < p_hi;
-         p += kUmmaCombineSplit * kWarps)
-        merge_row_rec<D>(P, rec, b, h, p, lane);
+    for (int q = blockIdx.y * kWarps + warp; q < nrows[0] + nrows[1];
+         q += kUmmaCombineSplit * kWarps) {
+        const int x = q < nrows[0] ? 0 : 1;
+        const int rl = q - (x ? nrows[0] : 0);
+        if (P.um_merged)
+            merge_unit_row<D>(P, rec, 64 * x + rl, b, 2 * hu + x, rl, lane);
+        else
+            merge_unit_row<D>(P, rec, rl, b, hu, rb * umma::kRows + rl, lane);
+    }
 }
 
 // Single-CTA launches have no boundary: only the seq_len check remains.
@@ -1575,14 +1834,11 @@ spec_status_t launch_impl(const TcParams &P, const CUtensorMap *maps, cudaStream
 
 spec_status_t launch_umma(const TcParams &P, const CUtensorMap *maps, cudaStream_t s) {
     constexpr int D = 128;
-    constexpr size_t smem = (size_t)umma::kNS * 2 * (D / 64) * kHalfBytes +   // K/V stages
-                            2 * (size_t)umma::kRows * D * 2 +                // query blocks
-                            sizeof(umma::Shared) + 1024;
-    static_assert(smem <= 227 * 1024, "shared memory of the tcgen05 verify kernel");
-    if (set_smem_limit(reinterpret_cast<const void *>(attn_umma_kernel<D>), smem) != SPEC_OK)
+    if (set_smem_limit(reinterpret_cast<const void *>(attn_umma_kernel<D>), umma::kSmemBytes) !=
+        SPEC_OK)
         return SPEC_ERR_CUDA;
-    if (launch(attn_umma_kernel<D>, dim3(P.n_ctas), dim3(umma::kThreads), smem, s, P, maps[0],
-               maps[1], maps[2], maps[3], maps[4], maps[5], maps[6]) != SPEC_OK)
+    if (launch(attn_umma_kernel<D>, dim3(P.n_ctas), dim3(umma::kThreads), umma::kSmemBytes, s, P,
+               maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6]) != SPEC_OK)
         return SPEC_ERR_CUDA;
     spec_status_t st = launch_status();
     if (st != SPEC_OK) return st;
@@ -1592,6 +1848,34 @@ spec_status_t launch_umma(const TcParams &P, const CUtensorMap *maps, cudaStream
                      : launch(check_seq_len_kernel, dim3(1), dim3(32), 0, s, P);
     if (ls != SPEC_OK) return ls;
     return launch_status();
+}
+
+// Units of the tcgen05 kernel for this shape: merged (two KV heads' rows in
+// one 128-lane tile) when a KV head has at most 64 packed rows, else row
+// blocks of 128 with steps of two 64-token tiles.
+struct UmmaPlan {
+    int merged, seg_h, seg_rb;
+    unsigned act[2];
+};
+
+UmmaPlan umma_plan(const AttnParams &A) {
+    UmmaPlan u{};
+    if (A.M > 64) {
+        u.seg_h = A.Hkv;
+        u.seg_rb = ceil_div(A.M, umma::kRows);
+        u.act[0] = u.act[1] = 0xFu;
+        return u;
+    }
+    u.merged = 1;
+    u.seg_h = (A.Hkv + 1) / 2;
+    u.seg_rb = 1;
+    // softmax warps of sub-tile x: the lane quarters holding head 2u + x's rows
+    for (int x = 0; x < 2; ++x) {
+        const int lo = 64 * x, hi = lo + A.M;
+        for (int w = 0; w < 4; ++w)
+            if (32 * w < hi && 32 * w + 32 > lo) u.act[x] |= 1u << w;
+    }
+    return u;
 }
 
 }  // namespace
@@ -1616,15 +1900,23 @@ int tc_rows_per_block(const AttnParams &P) {
     return 64;
 }
 
-size_t tc_workspace_bytes(const AttnParams &P, size_t *off_ml) {
-    int wc = 1, ctas = num_sms();
-    if (!umma_selected(P)) {
-        const TcConfig cfg = choose(P);
-        wc = cfg.ncw / cfg.wr;
-        ctas = num_sms() * cfg.minb;
+// Partial-slot rows of the workspace: (segments + CTAs) x slots a segment
+// takes per CTA (mma.sync: one per warp splitting the tile tokens; tcgen05:
+// one per row tile of a unit) x rows of a slot.
+size_t tc_slot_rows(const AttnParams &P, int *n_ctas) {
+    if (umma_selected(P)) {
+        const UmmaPlan u = umma_plan(P);
+        *n_ctas = num_sms();
+        return ((size_t)P.B * u.seg_h * u.seg_rb + (size_t)*n_ctas) * umma::kRows;
     }
-    const size_t segs = (size_t)P.B * P.Hkv * P.n_rb;
-    const size_t rows = (segs + (size_t)ctas) * wc * P.rb_rows;
+    const TcConfig cfg = choose(P);
+    *n_ctas = num_sms() * cfg.minb;
+    return ((size_t)P.B * P.Hkv * P.n_rb + (size_t)*n_ctas) * (cfg.ncw / cfg.wr) * P.rb_rows;
+}
+
+size_t tc_workspace_bytes(const AttnParams &P, size_t *off_ml) {
+    int ctas = 0;
+    const size_t rows = tc_slot_rows(P, &ctas);
     const size_t o_bytes = (rows * P.d * sizeof(float) + 255) & ~size_t(255);
     const size_t ml_bytes = (rows * 2 * sizeof(float) + 255) & ~size_t(255);
     *off_ml = o_bytes;
@@ -1639,25 +1931,35 @@ spec_status_t launch_attn_tc(const AttnParams &A, cudaStream_t s) {
     P.wait = wait_limit();
     const bool use_umma = umma_selected(A);
     const TcConfig cfg = use_umma ? TcConfig{8, 4, 0, 1} : choose(A);
-    P.n_ctas = num_sms() * cfg.minb;
-    // a segment start costs the tcgen05 kernel about three tiles (epilogue,
-    // query block, row flags); the mma.sync kernel's segments (decode-shaped:
-    // long prefixes, few rows) are split by tiles alone
-    P.seg_cost = use_umma ? 3 : 0;
     {
         // the bounds follow the partials (same sizes as tc_workspace_bytes)
-        const int wc = use_umma ? 1 : cfg.ncw / cfg.wr;
-        const size_t segs = (size_t)A.B * A.Hkv * A.n_rb;
-        const size_t rows = (segs + (size_t)P.n_ctas) * wc * A.rb_rows;
+        const size_t rows = tc_slot_rows(A, &P.n_ctas);
         P.bounds = reinterpret_cast<long long *>(
             reinterpret_cast<char *>(A.part_ml) + ((rows * 2 * sizeof(float) + 255) & ~size_t(255)));
         P.recs = reinterpret_cast<BoundaryRec *>(
             reinterpret_cast<char *>(P.bounds) +
             ((((size_t)P.n_ctas + 1) * sizeof(long long) + 255) & ~size_t(255)));
     }
+    // a unit start costs the tcgen05 kernel about three steps (epilogue,
+    // query block, row flags); the mma.sync kernel's segments (decode-shaped:
+    // long prefixes, few rows) are split by tiles alone
+    P.seg_cost = use_umma ? 3 : 0;
+    P.seg_h = A.Hkv;
+    P.seg_rb = A.n_rb;
+    if (use_umma) {
+        const UmmaPlan u = umma_plan(A);
+        P.seg_h = u.seg_h;
+        P.seg_rb = u.seg_rb;
+        P.um_merged = u.merged;
+        P.um_act[0] = u.act[0];
+        P.um_act[1] = u.act[1];
+        P.pair_steps = !u.merged;
+    }
     P.soft_tiles = ceil_div(A.n_soft, kTile);
     P.tail = P.soft_tiles + ceil_div(A.R, kTile);
-    P.box_rows = A.paged ? (A.d / 64) * A.page_size : kTile;
+    // paged boxes: one (page, head), both halves (mma.sync kernel), or one
+    // half of it (tcgen05 kernel, whose sub-tiles keep the halves apart)
+    P.box_rows = A.paged ? (use_umma ? 1 : A.d / 64) * A.page_size : kTile;
     P.page_log2 = A.page_size == 16 ? 4 : A.page_size == 32 ? 5 : 6;
     CUtensorMap maps[7];
     // paged caches: [page][head][d / 64][page_size][64] viewed as rows of 64
@@ -1677,13 +1979,15 @@ spec_status_t launch_attn_tc(const AttnParams &A, cudaStream_t s) {
         maps[5] = maps[3];
     }
     if (ok && use_umma) {
-        // q as [B * R][Hkv][G][d]: one box = the G heads of 128 / G rows, i.e.
-        // 128 packed rows (r * G + g) of one KV head, 64 elements wide
+        // q as [B * R][Hkv][G][d]: one box = the G heads of n / G rows, i.e.
+        // n packed rows (r * G + g) of one KV head, 64 elements wide; n = 128
+        // (a tile's query block), or 64 when two heads share one block
+        const int box_packed = P.um_merged ? 64 : umma::kRows;
         const cuuint64_t dims[4] = {(cuuint64_t)A.d, (cuuint64_t)A.G, (cuuint64_t)A.Hkv,
                                     (cuuint64_t)A.B * A.R};
         const cuuint64_t strides[3] = {(cuuint64_t)A.d * 2, (cuuint64_t)A.G * A.d * 2,
                                        (cuuint64_t)A.Hq * A.d * 2};
-        const cuuint32_t box[4] = {64u, (cuuint32_t)A.G, 1u, (cuuint32_t)(umma::kRows / A.G)};
+        const cuuint32_t box[4] = {64u, (cuuint32_t)A.G, 1u, (cuuint32_t)(box_packed / A.G)};
         ok = encode_bf16_map(&maps[6], A.q, 4, dims, strides, box);
     }
     if (!ok) return SPEC_ERR_CUDA;

@@ -409,7 +409,8 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
             const int i = mX * kM + r;               // this thread's position
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; j <= mX; ++j) {
-                if (*abort || !mbar_wait(&sh.s_full[x], (uint32_t)(ns & 1), P.wait)) {
+                if (__any_sync(0xffffffffu, *abort != 0) ||
+                    !mbar_wait_warp(&sh.s_full[x], (uint32_t)(ns & 1), P.wait)) {
                     ok = false;
                     break;
                 }
@@ -458,22 +459,28 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
                                           __uint_as_float(v[c][e + 2 * q + 1]));
                 const float traw = fmaxf(fmaxf(tmv[0], tmv[1]), fmaxf(tmv[2], tmv[3]));
                 const float tm = traw == -INFINITY ? -INFINITY : traw * sc;
-                if (tm > m_used + kRescale || (m_used == -INFINITY && tm != -INFINITY)) {
-                    const float alpha = (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - tm);
-                    if (j > 0 && m_used != -INFINITY) {
-                        // O holds every earlier PV of this tile (issued
-                        // before the S just waited for): rescale it
+                const bool raise = tm > m_used + kRescale || (m_used == -INFINITY && tm != -INFINITY);
+                const float alpha =
+                    !raise ? 1.f : (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - tm);
+                // O holds every earlier PV of this tile (issued before the S
+                // just waited for): rescale the rows that raised their max
+                // (TMEM loads and stores are warp-collective: the whole warp
+                // takes part, the other rows scaled by exactly 1)
+                const bool scale_o = raise && j > 0 && m_used != -INFINITY;
+                if (__any_sync(0xffffffffu, scale_o)) {
+                    const float a = scale_o ? alpha : 1.f;
 #pragma unroll 1
-                        for (int c = 0; c < kD / 32; ++c) {
-                            uint32_t o[32];
-                            ld32(tO + c * 32, o);
-                            wait_ld(o);
+                    for (int c = 0; c < kD / 32; ++c) {
+                        uint32_t o[32];
+                        ld32(tO + c * 32, o);
+                        wait_ld(o);
 #pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                            st32(tO + c * 32, o);
-                        }
+                        for (int e = 0; e < 32; ++e)
+                            o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
+                        st32(tO + c * 32, o);
                     }
+                }
+                if (raise) {
                     l *= alpha;
                     m_used = tm;
                 }
@@ -509,7 +516,7 @@ la_prefill_kernel(const __grid_constant__ lap::Params P, const __grid_constant__
             }
             if (!ok) break;
             // epilogue: O / l (bf16) and the LSE of this row
-            if (!mbar_wait(&sh.o_done[x], (uint32_t)(nact & 1), P.wait)) {
+            if (!mbar_wait_warp(&sh.o_done[x], (uint32_t)(nact & 1), P.wait)) {
                 ok = false;
                 break;
             }

@@ -78,6 +78,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     return mbar_wait(bar, parity, kTimeoutCycles);
 }
 
+// A bounded wait by every lane of a warp with one result for all of them
+// (if any lane's wait ran out, the warp fails together), so that the warp's
+// collective instructions after it are reached by all lanes or by none.
+// Call with the whole warp.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, long long limit) {
+    const bool ok = mbar_wait(bar, parity, limit);
+    return __all_sync(0xffffffffu, ok);
+}
+
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
                                             uint64_t *bar, uint64_t policy) {
     asm volatile(

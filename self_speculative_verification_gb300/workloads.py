@@ -440,9 +440,13 @@ def make_workload(name: str, seed: int = 0, *, B=None, seq=None, V=None,
                   q_scale: float = 1.0, T=None, k_choices=None,
                   paged=None, n_soft=None, slack_pages=None,
                   page_order: str = "shuffled", d=None, page_size=None,
-                  dtype=None) -> Workload:
+                  dtype=None, Hq=None, Hkv=None) -> Workload:
     """Build one seeded workload; keyword overrides shrink it for tests."""
     cfg = dict(CONFIGS[name])
+    if Hq is not None:
+        cfg["Hq"] = Hq
+    if Hkv is not None:
+        cfg["Hkv"] = Hkv
     if B is not None:
         cfg["B"] = B
     if seq is not None:

@@ -64,8 +64,9 @@ def test_many_rows_on_paged_cache(name, page_size):
 @pytest.mark.parametrize("paged", [False, True])
 def test_split_row_layout_gqa(paged):
     """64 packed rows with G = 4 (a ConFu tree of 8 nodes: 16 rows x 4
-    heads) take the tcgen05 kernel's split layout: each row in two TMEM
-    lanes, one per column half, query boxes of 4 rows x 4 heads."""
+    heads): the tcgen05 kernel's heads mode with two KV heads' rows in one
+    query block (query boxes of 16 rows x 4 heads, the second head's rows in
+    TMEM lanes 64..127)."""
     wl = W.make_workload("confu", 26, B=3, T=8, seq=("uniform", 150, 900), V=2000,
                          paged=paged)
     gh.run_and_check(wl)
@@ -76,5 +77,27 @@ def test_partial_row_block():
     """96 packed rows (a ConFu tree of 12 nodes, G = 4): one tcgen05 row
     block, its last 32 lanes empty."""
     wl = W.make_workload("confu", 27, B=3, T=12, seq=("uniform", 150, 900), V=2000)
+    gh.run_and_check(wl)
+    gh.run_and_check(wl, split_tokens=64)
+
+
+@pytest.mark.parametrize("T", [20, 40])
+def test_row_block_pairs(T):
+    """The tcgen05 kernel's rows mode: 160 packed rows (two row blocks, one
+    unit) and 320 (three row blocks: a unit of two, then a unit whose second
+    tile is absent), on ConFu trees of 20 and 40 nodes (G = 4)."""
+    wl = W.make_workload("confu", 28, B=3, T=T, seq=("uniform", 150, 900), V=2000)
+    gh.run_and_check(wl)
+    gh.run_and_check(wl, split_tokens=64)
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("ss", dict(Hq=5, Hkv=5)),              # 64 packed rows, heads share a query block
+    ("confu", dict(T=12, Hq=12, Hkv=3)),    # 96 packed rows, a block per head
+])
+def test_odd_kv_heads(name, kw):
+    """The tcgen05 kernel's heads mode with an odd number of KV heads: the
+    last unit holds one head."""
+    wl = W.make_workload(name, 29, B=3, seq=("uniform", 150, 700), V=2000, **kw)
     gh.run_and_check(wl)
     gh.run_and_check(wl, split_tokens=64)
