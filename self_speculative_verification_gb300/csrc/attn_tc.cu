@@ -33,49 +33,11 @@
 #include <mutex>
 
 #include "attn_tc.cuh"
+#include "attn_tc_sched.cuh"
 #include "ptx_sm103.cuh"
 
 namespace sv {
 namespace {
-
-constexpr int kTile = 64;                 // tokens per tile
-constexpr int kHalfBytes = kTile * 128;   // one 64-token x 64-element bf16 box
-
-// A split segment, as the CTA holding its first boundary between CTA
-// ranges records it (tcgen05 attention kernel) for the combine; seg < 0 in
-// every other CTA's record.
-struct BoundaryRec {
-    long long s0, s1;    // the segment's tiles
-    int seg;             // (b * Hkv + h) * n_rb + rb
-    int first, last;     // CTAs whose ranges meet [s0, s1)
-    uint32_t parts;      // bit j: CTA first + j holds a part (when last - first < 32)
-};
-
-struct TcParams {
-    AttnParams a;
-    int n_ctas;
-    int soft_tiles;      // ceil(n_soft / 64)
-    int tail;            // soft_tiles + ceil(R / 64)
-    int box_rows;        // rows per cache box: 64 (contiguous) or NH * page_size
-    int page_log2;       // log2(page_size) (paged)
-    int seg_cost;        // what a segment start costs, in tiles, for the split
-    long long *bounds;   // first tile of each CTA's range, [n_ctas + 1] (workspace),
-                         // written by the attention kernel for the combine
-    BoundaryRec *recs;   // tcgen05 kernel: per CTA, the split segment it merges
-                         // (workspace, [n_ctas])
-    long long wait;      // limit of every pipeline wait, in SM cycles
-    // segments of a request: seg_h x seg_rb, numbered h * seg_rb + rb (the
-    // mma.sync kernel: KV heads x row blocks; the tcgen05 kernel: its units,
-    // see umma::Mode)
-    int seg_h, seg_rb;
-    // tcgen05 kernel: um_merged: a unit is two KV heads, their rows in one
-    // query block (the second at lanes 64..127), else one row block;
-    // um_act[x]: softmax warps of sub-tile x that take part (bit q: lane
-    // quarter q)
-    int um_merged;
-    unsigned um_act[2];
-    int pair_steps;      // a schedule step covers two 64-token tiles (tcgen05 rows mode)
-};
 
 // -------------------------------------------- mma.sync helpers
 
@@ -112,234 +74,6 @@ template <int NH>
 __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int tok, int hh, int chunk, int rbl) {
     const int row = ((((tok >> rbl) * NH + hh) << rbl) | (tok & ((1 << rbl) - 1)));
     return base + row * 128 + ((chunk ^ (tok & 7)) << 4);
-}
-
-// -------------------------------------------------------------- schedule
-
-__device__ __forceinline__ int req_seq(const TcParams &P, int b) {
-    int S = P.a.seq_len[b];
-    return S < 0 ? 0 : (S > P.a.capacity ? P.a.capacity : S);
-}
-
-// Schedule steps of a segment with prefix S: its 64-token tiles (prefix,
-// soft prompt, block), or pairs of them.
-__device__ __forceinline__ int seg_tiles(const TcParams &P, int S) {
-    const int n = ceil_div(S, kTile) + P.tail;
-    return P.pair_steps ? (n + 1) >> 1 : n;
-}
-
-__device__ __forceinline__ long long req_tiles(const TcParams &P, int b) {
-    return (long long)seg_tiles(P, req_seq(P, b)) * P.seg_h * P.seg_rb;
-}
-
-__device__ __forceinline__ long long warp_sum_ll(long long x) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
-}
-
-// Total tiles over all requests (every lane gets it).
-__device__ long long warp_total_tiles(const TcParams &P) {
-    const int lane = threadIdx.x & 31;
-    long long s = 0;
-    for (int b = lane; b < P.a.B; b += 32) s += req_tiles(P, b);
-    return warp_sum_ll(s);
-}
-
-// Tiles of requests before b (every lane gets it).
-__device__ long long warp_tiles_before(const TcParams &P, int b) {
-    const int lane = threadIdx.x & 31;
-    long long s = 0;
-    for (int i = lane; i < b; i += 32) s += req_tiles(P, i);
-    return warp_sum_ll(s);
-}
-
-// Request containing linear tile t (< total), and its first tile.
-__device__ void warp_locate(const TcParams &P, long long t, int *b_out, long long *start_out) {
-    const int lane = threadIdx.x & 31;
-    const int B = P.a.B;
-    const int per = ceil_div(B, 32);
-    const int lo = min(B, lane * per), hi = min(B, lo + per);
-    long long sum = 0;
-    for (int b = lo; b < hi; ++b) sum += req_tiles(P, b);
-    long long incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const long long v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    const long long excl = incl - sum;
-    const unsigned m = __ballot_sync(0xffffffffu, lo < hi && t >= excl && t < incl);
-    const int src = m ? __ffs(m) - 1 : 0;
-    long long acc = __shfl_sync(0xffffffffu, excl, src);
-    int b = src * per;
-    while (b < B - 1) {
-        const long long n = req_tiles(P, b);
-        if (t < acc + n) break;
-        acc += n;
-        ++b;
-    }
-    *b_out = b;
-    *start_out = acc;
-}
-
-// The split.  CTAs take equal parts of a cost space in which every segment
-// counts its tiles plus P.seg_cost for its start (epilogue, query block,
-// row flags), so a CTA whose range holds many short segments gets fewer
-// tiles.  Segment s of request b occupies costs [Cb + s u, Cb + (s + 1) u),
-// u = tiles + seg_cost; the first seg_cost + 1 of them map to its first tile.
-// A CTA's range is the tiles its part of the cost space maps to.
-
-__device__ __forceinline__ long long req_cost(const TcParams &P, int b) {
-    return (long long)(seg_tiles(P, req_seq(P, b)) + P.seg_cost) * P.seg_h * P.seg_rb;
-}
-
-// Total cost over all requests (every lane gets it).
-__device__ long long warp_total_cost(const TcParams &P) {
-    const int lane = threadIdx.x & 31;
-    long long s = 0;
-    for (int b = lane; b < P.a.B; b += 32) s += req_cost(P, b);
-    return warp_sum_ll(s);
-}
-
-// Request containing cost position c (< total), with the costs and tiles of
-// the requests before it (every lane gets them).
-__device__ void warp_locate_cost(const TcParams &P, long long c, int *b_out, long long *cost0,
-                                 long long *tile0) {
-    const int lane = threadIdx.x & 31;
-    const int B = P.a.B;
-    const int per = ceil_div(B, 32);
-    const int lo = min(B, lane * per), hi = min(B, lo + per);
-    long long sc = 0, st = 0;
-    for (int b = lo; b < hi; ++b) {
-        sc += req_cost(P, b);
-        st += req_tiles(P, b);
-    }
-    long long ic = sc, it = st;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const long long vc = __shfl_up_sync(0xffffffffu, ic, o);
-        const long long vt = __shfl_up_sync(0xffffffffu, it, o);
-        if (lane >= o) {
-            ic += vc;
-            it += vt;
-        }
-    }
-    const long long ec = ic - sc, et = it - st;
-    const unsigned m = __ballot_sync(0xffffffffu, lo < hi && c >= ec && c < ic);
-    const int src = m ? __ffs(m) - 1 : 0;
-    long long ac = __shfl_sync(0xffffffffu, ec, src);
-    long long at = __shfl_sync(0xffffffffu, et, src);
-    int b = src * per;
-    while (b < B - 1) {
-        const long long n = req_cost(P, b);
-        if (c < ac + n) break;
-        ac += n;
-        at += req_tiles(P, b);
-        ++b;
-    }
-    *b_out = b;
-    *cost0 = ac;
-    *tile0 = at;
-}
-
-// First tile of CTA i's range (C, T: total cost and tiles; warp-collective).
-__device__ long long warp_range_lo(const TcParams &P, long long C, long long T, int i) {
-    if (i <= 0) return 0;
-    if (i >= P.n_ctas) return T;
-    if (P.seg_cost == 0) return T * i / P.n_ctas;    // plain tile split
-    const long long c = C * i / P.n_ctas;
-    int b;
-    long long c0, t0;
-    warp_locate_cost(P, c, &b, &c0, &t0);
-    const int nt = seg_tiles(P, req_seq(P, b));
-    const long long u = nt + P.seg_cost;
-    const long long seg = (c - c0) / u, off = (c - c0) % u;
-    return t0 + seg * nt + (off > P.seg_cost ? off - P.seg_cost : 0);
-}
-
-// CTA whose range holds tile t, from the bounds the attention kernel wrote:
-// the last CTA whose range starts at or before t (empty ranges share their
-// start with the next one).
-__device__ __forceinline__ int cta_holding(const TcParams &P, long long t) {
-    int lo = 0, hi = P.n_ctas - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (P.bounds[mid] <= t) lo = mid;
-        else hi = mid - 1;
-    }
-    return lo;
-}
-
-struct Cursor {
-    int b, h, rb;
-    int S, n_prefix, n_tiles;   // prefix tokens, its 64-token tiles, the segment's steps
-    int tile;                   // step within the segment
-};
-
-__device__ void cursor_init(const TcParams &P, long long t, Cursor &c) {
-    long long start;
-    warp_locate(P, t, &c.b, &start);
-    c.S = req_seq(P, c.b);
-    c.n_prefix = ceil_div(c.S, kTile);
-    c.n_tiles = seg_tiles(P, c.S);
-    const long long local = t - start;
-    const int seg = (int)(local / c.n_tiles);
-    c.tile = (int)(local % c.n_tiles);
-    c.h = seg / P.seg_rb;
-    c.rb = seg % P.seg_rb;
-}
-
-__device__ __forceinline__ void cursor_next(const TcParams &P, Cursor &c) {
-    if (++c.tile < c.n_tiles) return;
-    c.tile = 0;
-    if (++c.rb < P.seg_rb) return;
-    c.rb = 0;
-    if (++c.h < P.seg_h) return;
-    c.h = 0;
-    if (++c.b < P.a.B) {
-        c.S = req_seq(P, c.b);
-        c.n_prefix = ceil_div(c.S, kTile);
-        c.n_tiles = seg_tiles(P, c.S);
-    }
-}
-
-enum { kPrefix = 0, kSoft = 1, kBlock = 2 };
-
-struct TileInfo {
-    int kind, base, nvalid, j;
-};
-
-// 64-token tile t of the cursor's segment (0 <= t < n_prefix + tail).
-__device__ __forceinline__ TileInfo tile_at(const TcParams &P, const Cursor &c, int t) {
-    TileInfo ti;
-    if (t < c.n_prefix) {
-        ti.kind = kPrefix;
-        ti.j = t;
-        ti.base = t * kTile;
-        ti.nvalid = min(kTile, c.S - ti.base);
-    } else if (t - c.n_prefix < P.soft_tiles) {
-        ti.kind = kSoft;
-        ti.j = t - c.n_prefix;
-        ti.base = ti.j * kTile;
-        ti.nvalid = min(kTile, P.a.n_soft - ti.base);
-    } else {
-        ti.kind = kBlock;
-        ti.j = t - c.n_prefix - P.soft_tiles;
-        ti.base = ti.j * kTile;
-        ti.nvalid = min(kTile, P.a.R - ti.base);
-    }
-    return ti;
-}
-
-// The tile of the cursor's step (segments of one tile per step).
-__device__ __forceinline__ TileInfo tile_info(const TcParams &P, const Cursor &c) {
-    return tile_at(P, c, c.tile);
-}
-
-__device__ __forceinline__ size_t slot_row(const TcParams &P, int seg, int cta, int wc, int wcn,
-                                           int row) {
-    return ((size_t)(seg + cta) * wcn + wc) * P.a.rb_rows + row;
 }
 
 // ---------------------------------------------------------------- kernel
@@ -862,8 +596,8 @@ attn_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUten
 namespace umma {
 
 using namespace tc5;
+using namespace tcs;
 
-constexpr int kRows = 128;              // rows per tile (MMA M)
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kRecWarp = 10;
@@ -877,15 +611,6 @@ constexpr int kSoftmaxRegs = 176;
 constexpr int kOtherRegs = 152;
 static_assert(8 * 32 * kSoftmaxRegs + 4 * 32 * kOtherRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
-// A slot holds the K (or V) of one step: two 64-token sub-tiles x 128 head
-// dimensions, as two 64-element halves hh, each 128 rows of 128 bytes
-// (sub-tile x at rows 64 x ..), 128-byte swizzled: token t of sub-tile x,
-// elements 64 hh .. 64 hh + 63 at byte hh * kHalf + (64 x + t) * 128.
-constexpr int kHalf = 2 * 64 * 128;
-constexpr int kSlotBytes = 2 * kHalf;   // 32 KB
-constexpr int kSlots = 5;               // ring: K and V of a step in consecutive slots
-constexpr int kQHalf = kRows * 128;     // one 64-element half of a query block
-constexpr int kQBytes = 2 * kQHalf;     // one query block: 128 rows x 128
 constexpr int kTmemCols = 512;
 // TMEM columns: O at [0, 128); S buffer b at [128 + 128 b, 256 + 128 b), its
 // sub-tile x scores at + 64 x, P (bf16 pairs) of sub-tile x over the first 32
@@ -913,161 +638,6 @@ struct Shared {
 constexpr size_t kSmemBytes =
     (size_t)kSlots * kSlotBytes + (size_t)kQBytes + sizeof(Shared) + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory of the tcgen05 verify kernel");
-
-// One sub-tile of a step: the KV head whose keys it holds and its 64-token
-// tile, or absent (merged: an odd last head; rows mode: past the last tile).
-struct Sub {
-    int head;
-    TileInfo ti;
-    bool present;
-};
-
-// Sub-tile x of the cursor's step.
-__device__ __forceinline__ Sub sub_tile(const TcParams &P, const Cursor &c, int x) {
-    Sub u;
-    if (P.um_merged) {
-        u.head = 2 * c.h + x;
-        u.present = u.head < P.a.Hkv;
-        u.ti = tile_at(P, c, c.tile);
-    } else {
-        u.head = c.h;
-        const int t = 2 * c.tile + x;
-        u.present = t < c.n_prefix + P.tail;
-        u.ti = tile_at(P, c, u.present ? t : 0);
-    }
-    return u;
-}
-
-// Producer warp: for each step of [t_begin, t_end), its K and V (both
-// sub-tiles) into consecutive ring slots, and each unit's query block ahead
-// of its first step.  Every lane owns one box of a step -- lane
-// 16 kv + 8 x + 2 i + hh: K (kv = 0) or V, sub-tile x, page i (paged prefix
-// tiles: boxes of page_size rows; other tiles: i = 0, boxes of 64 rows),
-// half hh -- so that one warp-wide TMA instruction issues the whole step and
-// every sub-tile has the same layout.
-__device__ void run_umma_producer(const TcParams &P, const CUtensorMap &mk, const CUtensorMap &mv,
-                                  const CUtensorMap &mkb, const CUtensorMap &mvb,
-                                  const CUtensorMap &msk, const CUtensorMap &msv,
-                                  const CUtensorMap &mq, uint8_t *ring, uint8_t *qbuf,
-                                  Shared &sh, long long t_begin, long long t_end) {
-    constexpr int NH = 2;
-    const AttnParams &A = P.a;
-    const int lane = threadIdx.x & 31;
-    const int kv = lane >> 4, x = (lane >> 3) & 1, pi = (lane >> 1) & 3, hh = lane & 1;
-    const uint64_t pol_keep = policy_evict_last();
-    // a prefix is read by one unit unless several row blocks share its head
-    const uint64_t pol_stream =
-        (P.um_merged || A.n_rb == 1) ? policy_evict_first() : pol_keep;
-    const int ps = A.paged ? A.page_size : kTile;
-    const int ppt = kTile / ps;          // pages per 64-token tile (paged)
-
-    long long ld = 0;                    // slot loads issued
-    int nq = 0;                          // query blocks issued
-    bool ok = true;
-    Cursor c;
-    cursor_init(P, t_begin, c);          // warp-collective
-    for (long long t = t_begin; t < t_end; ++t) {
-        if (t == t_begin || c.tile == 0) {
-            // the unit's query block (once the previous unit's block has been
-            // copied to TMEM): 128 packed rows of one head, lane hh issuing
-            // half hh; or 64 of each of the unit's two heads (merged), lane
-            // 2 x + hh issuing head 2u + x's half hh
-            bool got = true;
-            if (lane == 0) got = nq == 0 || mbar_wait(&sh.q_empty, (uint32_t)((nq - 1) & 1), P.wait);
-            got = __shfl_sync(0xffffffffu, got, 0);
-            if (!got) {
-                ok = false;
-                break;
-            }
-            const int nh = P.um_merged ? (2 * c.h + 1 < A.Hkv ? 2 : 1) : 1;
-            if (lane == 0)
-                mbar_arrive_expect_tx(&sh.q_full, (uint32_t)nh * (P.um_merged ? kQBytes / 2 : kQBytes));
-            __syncwarp();
-            if (P.um_merged) {
-                if (lane < 2 * nh)
-                    tma_load_4d(qbuf + (lane & 1) * kQHalf + (lane >> 1) * (kQHalf / 2), &mq,
-                                (lane & 1) * 64, 0, 2 * c.h + (lane >> 1), c.b * A.R, &sh.q_full,
-                                pol_keep);
-            } else if (lane < NH) {
-                tma_load_4d(qbuf + lane * kQHalf, &mq, lane * 64, 0, c.h,
-                            c.b * A.R + c.rb * (kRows / A.G), &sh.q_full, pol_keep);
-            }
-            ++nq;
-        }
-        // this lane's box of the step
-        const Sub u = sub_tile(P, c, x);
-        const CUtensorMap *map = nullptr;
-        int bx = 0, by = 0;
-        uint32_t bytes = 0;
-        uint64_t pol = pol_keep;
-        if (u.present) {
-            const TileInfo &ti = u.ti;
-            if (ti.kind == kPrefix && A.paged) {
-                const int tok = ti.base + pi * ps;
-                if (pi < ppt && tok < c.S) {
-                    const int pg = A.page_table[(size_t)c.b * A.max_pages + tok / ps];
-                    if (pg < 0 || pg >= A.n_pages) {
-                        raise_status(A.status, SPEC_DEV_BAD_PAGE);
-                    } else {
-                        map = kv ? &mv : &mk;
-                        by = ((pg * A.Hkv + u.head) * NH + hh) * ps;
-                        bytes = (uint32_t)ps * 128u;
-                        pol = pol_stream;
-                    }
-                }
-            } else if (pi == 0) {
-                bx = hh * 64;
-                bytes = (uint32_t)kTile * 128u;
-                if (ti.kind == kPrefix) {
-                    map = kv ? &mv : &mk;
-                    by = (c.b * A.Hkv + u.head) * A.max_seq + ti.base;
-                    pol = pol_stream;
-                } else if (ti.kind == kSoft) {
-                    map = kv ? &msv : &msk;
-                    by = u.head * A.n_soft + ti.base;
-                } else {
-                    map = kv ? &mvb : &mkb;
-                    by = (c.b * A.Hkv + u.head) * A.R + ti.base;
-                }
-            }
-        }
-        const uint32_t bytes_k = __reduce_add_sync(0xffffffffu, kv == 0 ? bytes : 0u);
-        const uint32_t bytes_v = __reduce_add_sync(0xffffffffu, kv == 1 ? bytes : 0u);
-        const int ks = (int)(ld % kSlots), vs = (int)((ld + 1) % kSlots);
-        bool got = true;
-        if (lane == 0)
-            got = mbar_wait(&sh.empty[ks], (uint32_t)(((ld / kSlots) & 1) ^ 1), P.wait) &&
-                  mbar_wait(&sh.empty[vs], (uint32_t)((((ld + 1) / kSlots) & 1) ^ 1), P.wait);
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
-            ok = false;
-            break;
-        }
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&sh.full[ks], bytes_k);
-            mbar_arrive_expect_tx(&sh.full[vs], bytes_v);
-        }
-        __syncwarp();
-        const int slot = kv ? vs : ks;
-        if (bytes)
-            tma_load_2d(ring + slot * kSlotBytes + hh * kHalf + (x * kTile + pi * ps) * 128, map, bx,
-                        by, &sh.full[slot], pol);
-        ld += 2;
-        cursor_next(P, c);
-    }
-    if (lane == 0) {
-        if (!ok) raise_status(A.status, SPEC_DEV_TIMEOUT);
-        // do not leave while copies into this CTA's shared memory are in
-        // flight (the default limit: these copies were issued and complete)
-        for (long long i = ld - 1; i >= 0 && i >= ld - kSlots; --i)
-            if (!mbar_wait(&sh.full[i % kSlots], (uint32_t)((i / kSlots) & 1))) {
-                raise_status(A.status, SPEC_DEV_TIMEOUT);
-                break;
-            }
-        if (nq > 0 && !mbar_wait(&sh.q_full, (uint32_t)((nq - 1) & 1)))
-            raise_status(A.status, SPEC_DEV_TIMEOUT);
-    }
-}
 
 }  // namespace umma
 
@@ -1142,43 +712,12 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
     if (warp >= kProducerWarp) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
         if (warp == kRecWarp) {
-            // When this CTA's range starts inside a unit and the ranges
-            // between the unit's first CTA and this one are empty (this is
-            // the unit's first boundary), record the unit and the CTAs
-            // sharing it for the combine.
-            BoundaryRec rec{0, 0, -1, 0, 0, 0};
-            if (t_begin < t_end) {
-                Cursor c;
-                cursor_init(P, t_begin, c);
-                if (c.tile > 0) {
-                    rec.s0 = t_begin - c.tile;
-                    rec.s1 = rec.s0 + c.n_tiles;
-                    bool first_boundary = true;
-                    int f = cta - 1, l = cta;
-                    for (;; --f) {
-                        const long long lo = warp_range_lo(P, C, T, f);
-                        if (lo <= rec.s0 || f == 0) break;
-                        if (lo < t_begin) first_boundary = false;   // a part starts in between
-                    }
-                    while (l + 1 < P.n_ctas && warp_range_lo(P, C, T, l + 1) < rec.s1) ++l;
-                    if (first_boundary) {
-                        rec.seg = (c.b * P.seg_h + c.h) * P.seg_rb + c.rb;
-                        rec.first = f;
-                        rec.last = l;
-                        if (l - f < 32) {
-                            long long lo = warp_range_lo(P, C, T, f);
-                            for (int j = f; j <= l; ++j) {
-                                const long long hi = warp_range_lo(P, C, T, j + 1);
-                                if (max(lo, rec.s0) < min(hi, rec.s1)) rec.parts |= 1u << (j - f);
-                                lo = hi;
-                            }
-                        }
-                    }
-                }
-            }
+            const BoundaryRec rec = warp_boundary_record(P, C, T, cta, t_begin, t_end);
             if (lane == 0) P.recs[cta] = rec;
         } else if (t_begin < t_end && warp == kProducerWarp) {
-            run_umma_producer(P, mk, mv, mkb, mvb, msk, msv, mq, ring, qbuf, sh, t_begin, t_end);
+            run_step_producer(P, mk, mv, mkb, mvb, msk, msv, mq,
+                              ProducerIO{ring, qbuf, sh.full, sh.empty, &sh.q_full, &sh.q_empty},
+                              t_begin, t_end);
         } else if (t_begin < t_end && warp == kMmaWarp) {
             // --------------------------------------------------- MMA issuer
             // (the cursor's set-up is warp-collective: the whole warp)
@@ -1627,11 +1166,6 @@ __device__ void merge_row(const TcParams &P, int wcn, int b, int h, int seg,
     if (lane == 0) A.lse[((size_t)b * A.Hq + hq) * A.R + r] = lse;
 }
 
-__device__ __forceinline__ void check_seq_len(const AttnParams &A, int b) {
-    const int S_raw = A.seq_len[b];
-    if (S_raw < 0 || S_raw > A.capacity) raise_status(A.status, SPEC_DEV_SEQ_OVERFLOW);
-}
-
 // mma.sync path: every segment has partials.  One warp per (request, KV
 // head, packed row).
 template <int D>
@@ -1652,61 +1186,85 @@ __global__ void __launch_bounds__(128) attn_tc_combine_kernel(const __grid_const
     merge_row<D>(P, wcn, b, h, seg, s0, s1, cta_holding(P, s0), cta_holding(P, s1 - 1), p, lane);
 }
 
-// tcgen05 path: merge one row of a split unit -- TMEM lane lane_t of the
-// unit's tile, output row p of KV head h of request b -- over the CTAs
-// first..last whose ranges meet the unit's steps [s0, s1).  With at most
-// four such CTAs every part's (m, l) and then every O slice are loaded
-// together (two dependent round trips); otherwise they are visited one by
-// one.  One warp.
+// tcgen05 path: a unit wholly inside one CTA's range already holds its
+// final output; a split unit contains at least one boundary between
+// consecutive CTA ranges.  CTA i here takes the boundary between attention
+// CTAs i and i + 1 and merges the unit across it when that boundary is the
+// unit's first, so only split units cost work (at most n_ctas - 1).  Thread
+// t takes TMEM lane t / 4 of the unit's tile and 32 of its 128 columns; with
+// at most two parts it loads both parts' (m, l) and O slices at once (one
+// round trip after the record), with more it visits them one by one.
+constexpr int kUmmaCombineThreads = 4 * tcs::kRows;
+
 template <int D>
-__device__ void merge_unit_row(const TcParams &P, const BoundaryRec &rec, int lane_t, int b,
-                               int h, int p, int lane) {
+__global__ void __launch_bounds__(kUmmaCombineThreads)
+attn_umma_combine_kernel(const __grid_constant__ TcParams P) {
+    static_assert(D == 128, "one 32-column slice per thread and quarter of a row");
+    pdl_wait();
     const AttnParams &A = P.a;
-    constexpr int kMaxParts = 4;
-    const int r = p / A.G, hq = h * A.G + p % A.G;
-    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(A.o) + (((size_t)b * A.R + r) * A.Hq + hq) * D;
+    if (blockIdx.x == 0)
+        for (int b = threadIdx.x; b < A.B; b += kUmmaCombineThreads) check_seq_len(A, b);
+    // the boundary between CTAs i - 1 and i
+    const BoundaryRec rec = P.recs[blockIdx.x + 1];
+    if (rec.seg < 0) return;         // no unit's first boundary
+    const int rb = rec.seg % P.seg_rb, hu = (rec.seg / P.seg_rb) % P.seg_h;
+    const int b = rec.seg / (P.seg_rb * P.seg_h);
+    const int lane_t = threadIdx.x >> 2, c0 = (threadIdx.x & 3) * 32;
+    // this lane's output row: merged, head 2 hu at lanes 0..63 and 2 hu + 1
+    // at 64..127; rows mode, packed row rb * 128 + lane of KV head hu
+    int h, p;
+    bool valid;
+    if (P.um_merged) {
+        h = 2 * hu + (lane_t >> 6);
+        p = lane_t & 63;
+        valid = h < A.Hkv && p < A.M;
+    } else {
+        h = hu;
+        p = rb * tcs::kRows + lane_t;
+        valid = p < A.M;
+    }
+    if (!valid) return;
     float mstar = -INFINITY, L = 0.f;
-    float out[D / 32];
-    if (rec.last - rec.first < kMaxParts) {
-        size_t row[kMaxParts];
-        float ms[kMaxParts], ls[kMaxParts];
+    float out[32];
+    const int nparts = rec.last - rec.first + 1;
+    if (nparts <= 2) {
+        size_t row[2];
+        float ms[2], ls[2];
+        float4 xo[2][8];
 #pragma unroll
-        for (int j = 0; j < kMaxParts; ++j) {
-            const bool part = rec.first + j <= rec.last && ((rec.parts >> j) & 1u);
+        for (int j = 0; j < 2; ++j) {
+            const bool part = j < nparts && ((rec.parts >> j) & 1u);
             row[j] = part ? slot_row(P, rec.seg, rec.first + j, 0, 1, lane_t) : 0;
             ms[j] = part ? A.part_ml[row[j] * 2] : -INFINITY;
             ls[j] = part ? A.part_ml[row[j] * 2 + 1] : 0.f;
+            const float4 *po = reinterpret_cast<const float4 *>(A.part_o + row[j] * D + c0);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xo[j][e] = part ? po[e] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        mstar = fmaxf(ms[0], ms[1]);
+        float wgt[2];
 #pragma unroll
-        for (int j = 0; j < kMaxParts; ++j) mstar = fmaxf(mstar, ms[j]);
-        float wgt[kMaxParts];
-#pragma unroll
-        for (int j = 0; j < kMaxParts; ++j) {
+        for (int j = 0; j < 2; ++j) {
             wgt[j] = ms[j] == -INFINITY ? 0.f : exp2f(ms[j] - mstar);
             L = fmaf(wgt[j], ls[j], L);
         }
-        float xs[kMaxParts][D / 32];
 #pragma unroll
-        for (int j = 0; j < kMaxParts; ++j)
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c)
-                xs[j][c] = wgt[j] != 0.f ? A.part_o[row[j] * D + lane + 32 * c] : 0.f;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-            float acc = 0.f;
-#pragma unroll
-            for (int j = 0; j < kMaxParts; ++j) acc = fmaf(wgt[j], xs[j][c], acc);
-            out[c] = acc;
+        for (int e = 0; e < 8; ++e) {
+            out[4 * e] = wgt[0] * xo[0][e].x + wgt[1] * xo[1][e].x;
+            out[4 * e + 1] = wgt[0] * xo[0][e].y + wgt[1] * xo[1][e].y;
+            out[4 * e + 2] = wgt[0] * xo[0][e].z + wgt[1] * xo[1][e].z;
+            out[4 * e + 3] = wgt[0] * xo[0][e].w + wgt[1] * xo[1][e].w;
         }
     } else {
         auto has_part = [&](int i) {
+            if (rec.last - rec.first < 32) return ((rec.parts >> (i - rec.first)) & 1u) != 0;
             const long long lo = P.bounds[i], hi = P.bounds[i + 1];
             return max(lo, rec.s0) < min(hi, rec.s1);
         };
         for (int i = rec.first; i <= rec.last; ++i)
             if (has_part(i)) mstar = fmaxf(mstar, A.part_ml[slot_row(P, rec.seg, i, 0, 1, lane_t) * 2]);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) out[c] = 0.f;
+        for (int e = 0; e < 32; ++e) out[e] = 0.f;
         if (mstar != -INFINITY) {
             for (int i = rec.first; i <= rec.last; ++i) {
                 if (!has_part(i)) continue;
@@ -1715,62 +1273,30 @@ __device__ void merge_unit_row(const TcParams &P, const BoundaryRec &rec, int la
                 if (ms == -INFINITY) continue;
                 const float wgt = exp2f(ms - mstar);
                 L = fmaf(wgt, A.part_ml[row * 2 + 1], L);
+                const float4 *po = reinterpret_cast<const float4 *>(A.part_o + row * D + c0);
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c)
-                    out[c] = fmaf(wgt, A.part_o[row * D + lane + 32 * c], out[c]);
+                for (int e = 0; e < 8; ++e) {
+                    const float4 v = po[e];
+                    out[4 * e] = fmaf(wgt, v.x, out[4 * e]);
+                    out[4 * e + 1] = fmaf(wgt, v.y, out[4 * e + 1]);
+                    out[4 * e + 2] = fmaf(wgt, v.z, out[4 * e + 2]);
+                    out[4 * e + 3] = fmaf(wgt, v.w, out[4 * e + 3]);
+                }
             }
         }
     }
+    const int r = p / A.G, hq = h * A.G + p % A.G;
     const float inv = L > 0.f ? 1.f / L : 0.f;
+    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(A.o) +
+                                           (((size_t)b * A.R + r) * A.Hq + hq) * D + c0);
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) o[lane + 32 * c] = __float2bfloat16_rn(out[c] * inv);
-    if (lane == 0)
+    for (int e = 0; e < 32; e += 8)
+        dst[e / 8] = make_uint4(pack_bf16(out[e] * inv, out[e + 1] * inv),
+                                pack_bf16(out[e + 2] * inv, out[e + 3] * inv),
+                                pack_bf16(out[e + 4] * inv, out[e + 5] * inv),
+                                pack_bf16(out[e + 6] * inv, out[e + 7] * inv));
+    if (c0 == 0)
         A.lse[((size_t)b * A.Hq + hq) * A.R + r] = L > 0.f ? (mstar + log2f(L)) * kLn2 : -INFINITY;
-}
-
-// tcgen05 path: a unit wholly inside one CTA's range already holds its
-// final output; a split unit contains at least one boundary between
-// consecutive CTA ranges.  CTAs (i, y) here take the boundary between
-// attention CTAs i and i + 1 and merge the unit across it when that boundary
-// is the unit's first (CTA y takes every kUmmaCombineSplit-th group of 8 of
-// its rows), so only split units cost work (at most n_ctas - 1).
-constexpr int kUmmaCombineThreads = 256;
-constexpr int kUmmaCombineSplit = 8;     // CTAs per boundary (row slices of the unit)
-
-template <int D>
-__global__ void __launch_bounds__(kUmmaCombineThreads)
-attn_umma_combine_kernel(const __grid_constant__ TcParams P) {
-    pdl_wait();
-    const AttnParams &A = P.a;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (blockIdx.x == 0 && blockIdx.y == 0)
-        for (int b = threadIdx.x; b < A.B; b += kUmmaCombineThreads) check_seq_len(A, b);
-    // the boundary between CTAs i - 1 and i
-    const int i = blockIdx.x + 1;
-    const BoundaryRec rec = P.recs[i];
-    if (rec.seg < 0) return;         // no unit's first boundary
-    const int rb = rec.seg % P.seg_rb, hu = (rec.seg / P.seg_rb) % P.seg_h;
-    const int b = rec.seg / (P.seg_rb * P.seg_h);
-    // the unit's rows: merged, M of each of its heads (2 hu at lanes 0..63,
-    // 2 hu + 1 at 64..127); rows mode, those of row block rb
-    int nrows[2];
-    if (P.um_merged) {
-        nrows[0] = A.M;
-        nrows[1] = 2 * hu + 1 < A.Hkv ? A.M : 0;
-    } else {
-        nrows[0] = min(umma::kRows, A.M - rb * umma::kRows);
-        nrows[1] = 0;
-    }
-    constexpr int kWarps = kUmmaCombineThreads / 32;
-    for (int q = blockIdx.y * kWarps + warp; q < nrows[0] + nrows[1];
-         q += kUmmaCombineSplit * kWarps) {
-        const int x = q < nrows[0] ? 0 : 1;
-        const int rl = q - (x ? nrows[0] : 0);
-        if (P.um_merged)
-            merge_unit_row<D>(P, rec, 64 * x + rl, b, 2 * hu + x, rl, lane);
-        else
-            merge_unit_row<D>(P, rec, rl, b, hu, rb * umma::kRows + rl, lane);
-    }
 }
 
 // Single-CTA launches have no boundary: only the seq_len check remains.
@@ -1843,16 +1369,17 @@ spec_status_t launch_umma(const TcParams &P, const CUtensorMap *maps, cudaStream
     spec_status_t st = launch_status();
     if (st != SPEC_OK) return st;
     const spec_status_t ls =
-        P.n_ctas > 1 ? launch(attn_umma_combine_kernel<D>, dim3(P.n_ctas - 1, kUmmaCombineSplit),
+        P.n_ctas > 1 ? launch(attn_umma_combine_kernel<D>, dim3(P.n_ctas - 1),
                               dim3(kUmmaCombineThreads), 0, s, P)
                      : launch(check_seq_len_kernel, dim3(1), dim3(32), 0, s, P);
     if (ls != SPEC_OK) return ls;
     return launch_status();
 }
 
-// Units of the tcgen05 kernel for this shape: merged (two KV heads' rows in
-// one 128-lane tile) when a KV head has at most 64 packed rows, else row
-// blocks of 128 with steps of two 64-token tiles.
+// Units of the tcgen05 kernel for this shape: row blocks of 128 packed rows
+// (a 128-lane tile, steps of two 64-token tiles) when a KV head has more
+// than 64 packed rows; two KV heads' rows in one tile (merged, steps of one
+// 64-token tile of each head) when it has at most 64.
 struct UmmaPlan {
     int merged, seg_h, seg_rb;
     unsigned act[2];
@@ -1862,7 +1389,7 @@ UmmaPlan umma_plan(const AttnParams &A) {
     UmmaPlan u{};
     if (A.M > 64) {
         u.seg_h = A.Hkv;
-        u.seg_rb = ceil_div(A.M, umma::kRows);
+        u.seg_rb = ceil_div(A.M, tcs::kRows);
         u.act[0] = u.act[1] = 0xFu;
         return u;
     }
@@ -1894,7 +1421,7 @@ bool tc_supported(const AttnParams &P, int dtype) {
 bool umma_selected(const AttnParams &P) { return P.d == 128 && P.M >= 64 && 128 % P.G == 0; }
 
 int tc_rows_per_block(const AttnParams &P) {
-    if (umma_selected(P)) return umma::kRows;
+    if (umma_selected(P)) return tcs::kRows;
     if (P.M <= 16) return 16;
     if (P.M <= 32) return 32;
     return 64;
@@ -1907,7 +1434,7 @@ size_t tc_slot_rows(const AttnParams &P, int *n_ctas) {
     if (umma_selected(P)) {
         const UmmaPlan u = umma_plan(P);
         *n_ctas = num_sms();
-        return ((size_t)P.B * u.seg_h * u.seg_rb + (size_t)*n_ctas) * umma::kRows;
+        return ((size_t)P.B * u.seg_h * u.seg_rb + (size_t)*n_ctas) * tcs::kRows;
     }
     const TcConfig cfg = choose(P);
     *n_ctas = num_sms() * cfg.minb;
@@ -1982,7 +1509,7 @@ spec_status_t launch_attn_tc(const AttnParams &A, cudaStream_t s) {
         // q as [B * R][Hkv][G][d]: one box = the G heads of n / G rows, i.e.
         // n packed rows (r * G + g) of one KV head, 64 elements wide; n = 128
         // (a tile's query block), or 64 when two heads share one block
-        const int box_packed = P.um_merged ? 64 : umma::kRows;
+        const int box_packed = P.um_merged ? 64 : tcs::kRows;
         const cuuint64_t dims[4] = {(cuuint64_t)A.d, (cuuint64_t)A.G, (cuuint64_t)A.Hkv,
                                     (cuuint64_t)A.B * A.R};
         const cuuint64_t strides[3] = {(cuuint64_t)A.d * 2, (cuuint64_t)A.G * A.d * 2,
