@@ -9,6 +9,7 @@
 // Accept: the LA threshold longest prefix, or the greedy walk down the draft
 // tree ("Speculative Streaming", verification step; "ConFu" tree verify);
 // spec_accept_soft: the soft-matching walk and the residual draw.
+#include <atomic>
 #include <cooperative_groups.h>
 #include <limits.h>
 #include <math.h>
@@ -78,7 +79,8 @@ __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
 }
 
 // Running (max, index, sum) over one full batch of kUnroll 8-element
-// vectors; vector u starts at element (i0 + u * kReduceThreads) * 8.
+// vectors; vector u starts at element (i0 + u * kStride) * 8.
+template <int kStride = kReduceThreads>
 __device__ __forceinline__ void push_bf16_batch(Best &best, const Bf16Batch &x, int i0, float c2) {
     uint32_t m2 = x.w[0][0];
 #pragma unroll
@@ -94,7 +96,7 @@ __device__ __forceinline__ void push_bf16_batch(Best &best, const Bf16Batch &x, 
             for (int j = 7; j >= 0; --j) {
                 const uint32_t wq = x.w[u][j >> 1];
                 const float v = __uint_as_float((j & 1) ? (wq & 0xffff0000u) : (wq << 16));
-                if (v == bm) bi = (i0 + u * kReduceThreads) * 8 + j;
+                if (v == bm) bi = (i0 + u * kStride) * 8 + j;
             }
         best.s *= ex2((best.m - bm) * c2);
         best.m = bm;
@@ -242,6 +244,195 @@ vocab_reduce_kernel(const T *__restrict__ logits, int V, const int32_t *__restri
     cluster.sync();     // peers' shared memory stays alive until rank 0 has read it
 }
 
+// The same reduction for bf16 rows whose start is 16-byte aligned, with the
+// row slice streamed through shared memory: thread 0 issues bulk copies
+// (cp.async.bulk) of kBulkChunk-element chunks into a ring of kBulkStages
+// buffers ahead of the consumers, so about kBulkStages chunks per CTA are in
+// flight instead of one batch of loads per thread.  Every thread then reduces
+// its kUnroll 16-byte vectors of a chunk from shared memory with the packed
+// arithmetic of the kernel above.  CTAs are small (kBulkThreads threads,
+// kBulkStages x 8 KB of shared memory) so that many fit on an SM: the host
+// picks the CTAs per row so that every CTA is resident at once and the SMs'
+// shares of the bytes are even (bulk_cluster_size).  A copy that has not
+// landed within the bounded wait sets SPEC_DEV_TIMEOUT; the CTA then waits
+// for its other copies and writes nothing.
+constexpr int kBulkThreads = 128;
+constexpr int kBulkChunk = kBulkThreads * kUnroll * 8;     // elements (8 KB of bf16)
+constexpr int kBulkStages = 3;
+constexpr int kBulkSmem = kBulkStages * kBulkChunk * 2;
+
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                          uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__global__ void __launch_bounds__(kBulkThreads)
+vocab_reduce_bulk_kernel(const __nv_bfloat16 *__restrict__ logits, int V,
+                         const int32_t *__restrict__ proposal, int32_t *__restrict__ argmax,
+                         float *__restrict__ lse, float *__restrict__ zprop, float inv_t,
+                         int *status, long long wait) {
+    pdl_wait();
+    const float c2 = kLog2e * inv_t;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int nc = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    const int row = blockIdx.x / nc;
+    const __nv_bfloat16 *z = logits + (size_t)row * V;
+    extern __shared__ __align__(128) uint8_t stage[];
+    __shared__ uint64_t full[kBulkStages];
+    Best best{-INFINITY, INT_MAX, 0.f};
+    // this CTA's slice: 8-element vectors [lo, hi) of the row
+    const int nv = V / 8;
+    const int lo = (int)((long long)nv * rank / nc), hi = (int)((long long)nv * (rank + 1) / nc);
+    const int n_el = (hi - lo) * 8;
+    const int n_chunks = (n_el + kBulkChunk - 1) / kBulkChunk;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kBulkStages; ++i) mbar_init(&full[i], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+    const uint64_t pol = policy_evict_first();
+    auto issue = [&](int ch) {        // thread 0: chunk ch into its stage
+        const int b = ch % kBulkStages;
+        const uint32_t bytes = (uint32_t)min(kBulkChunk, n_el - ch * kBulkChunk) * 2u;
+        mbar_arrive_expect_tx(&full[b], bytes);
+        bulk_load(stage + b * (kBulkChunk * 2), z + (size_t)lo * 8 + (size_t)ch * kBulkChunk, bytes,
+                  &full[b], pol);
+    };
+    if (threadIdx.x == 0)
+        for (int ch = 0; ch < n_chunks && ch < kBulkStages; ++ch) issue(ch);
+    int ch = 0;
+    bool failed = false;
+    for (; ch < n_chunks; ++ch) {
+        const int b = ch % kBulkStages;
+        const uint32_t parity = (uint32_t)((ch / kBulkStages) & 1);
+        // Thread 0 alone polls; the others sleep in the block barrier rather
+        // than spin (spinning threads took the issue slots of the reducing
+        // warps).  After the barrier every thread tests the completed phase
+        // once, which also gives each its own acquire of the copied bytes.
+        const bool got = threadIdx.x != 0 || mbar_wait(&full[b], parity, wait);
+        if (__syncthreads_or(!got)) {
+            failed = true;
+            break;
+        }
+        (void)mbar_test_wait(&full[b], parity);
+        const uint4 *sv = reinterpret_cast<const uint4 *>(stage + b * (kBulkChunk * 2));
+        const int i0 = lo + ch * (kBulkChunk / 8) + (int)threadIdx.x;   // vector index in the row
+        const int nvec = min(kBulkChunk, n_el - ch * kBulkChunk) / 8;
+        if ((int)threadIdx.x + (kUnroll - 1) * kBulkThreads < nvec) {
+            Bf16Batch x;
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const uint4 v = sv[threadIdx.x + u * kBulkThreads];
+                x.w[u][0] = v.x;
+                x.w[u][1] = v.y;
+                x.w[u][2] = v.z;
+                x.w[u][3] = v.w;
+            }
+            push_bf16_batch<kBulkThreads>(best, x, i0, c2);
+        } else if ((int)threadIdx.x < nvec) {
+            // a batch that runs past the end of the slice
+            float xs[kUnroll][8];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int iv = (int)threadIdx.x + u * kBulkThreads;
+                if (iv < nvec) {
+                    const uint4 v = sv[iv];
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        xs[u][2 * j] = __uint_as_float(w[j] << 16);
+                        xs[u][2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) xs[u][j] = -INFINITY;
+                }
+            }
+            float bm = xs[0][0];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) bm = fmaxf(bm, xs[u][j]);
+            if (bm > best.m) {
+                int bi = INT_MAX;
+#pragma unroll
+                for (int u = kUnroll - 1; u >= 0; --u)
+#pragma unroll
+                    for (int j = 7; j >= 0; --j)
+                        if (xs[u][j] == bm) bi = (i0 + u * kBulkThreads) * 8 + j;
+                best.s *= ex2((best.m - bm) * c2);
+                best.m = bm;
+                best.idx = bi;
+            }
+            const float mb = best.m * c2;
+            float acc[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] += ex2(fmaf(xs[u][j], c2, -mb));
+#pragma unroll
+            for (int j = 1; j < 8; ++j) acc[0] += acc[j];
+            best.s += acc[0];
+        }
+        __syncthreads();                 // every thread is done with this stage
+        if (threadIdx.x == 0 && ch + kBulkStages < n_chunks) issue(ch + kBulkStages);
+    }
+    if (failed) {
+        if (threadIdx.x == 0) {
+            raise_status(status, SPEC_DEV_TIMEOUT);
+            // do not leave while copies into this CTA's shared memory are in
+            // flight
+            for (int c = ch; c < n_chunks && c < ch + kBulkStages; ++c)
+                if (!mbar_wait(&full[c % kBulkStages], (uint32_t)((c / kBulkStages) & 1))) break;
+        }
+        __syncthreads();
+    }
+    if (rank == nc - 1)
+        for (int i = nv * 8 + threadIdx.x; i < V; i += kBulkThreads)
+            best_push(best, load_f(z + i), i, inv_t);
+
+    // block reduction: warps, then across warps
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        Best other;
+        other.m = __shfl_xor_sync(0xffffffffu, best.m, o);
+        other.idx = __shfl_xor_sync(0xffffffffu, best.idx, o);
+        other.s = __shfl_xor_sync(0xffffffffu, best.s, o);
+        best = best_merge(best, other, inv_t);
+    }
+    __shared__ Best sb[kBulkThreads / 32];
+    __shared__ Best cta_best;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) sb[warp] = best;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        Best r = sb[0];
+        for (int w = 1; w < kBulkThreads / 32; ++w) r = best_merge(r, sb[w], inv_t);
+        cta_best = r;
+    }
+    cluster.sync();
+    if (rank == 0 && threadIdx.x == 0 && !failed) {
+        Best r = cta_best;
+        for (int i = 1; i < nc; ++i)
+            r = best_merge(r, *cluster.map_shared_rank(&cta_best, i), inv_t);
+        if (argmax) argmax[row] = r.idx == INT_MAX ? 0 : r.idx;
+        lse[row] = r.m * inv_t + logf(r.s);
+        if (proposal && zprop) {
+            const int pidx = proposal[row];
+            zprop[row] = (pidx >= 0 && pidx < V) ? load_f(z + pidx) : NAN;
+        }
+    }
+    cluster.sync();     // peers' shared memory stays alive until rank 0 has read it
+}
+
 struct AcceptParams {
     int mode;
     float log_tau;
@@ -368,14 +559,71 @@ int cluster_size(int n_rows, int V, int dtype) {
     return nc;
 }
 
+// Resident bulk-kernel CTAs per SM on the current device (cached).
+int bulk_ctas_per_sm() {
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    const int slot = dev & 63;
+    int n = cached[slot].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    if (set_smem_limit(reinterpret_cast<const void *>(vocab_reduce_bulk_kernel), kBulkSmem) !=
+            SPEC_OK ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, vocab_reduce_bulk_kernel, kBulkThreads,
+                                                      kBulkSmem) != cudaSuccess ||
+        n < 1) {
+        (void)cudaGetLastError();
+        return 1;
+    }
+    cached[slot].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+// CTAs per row for the bulk kernel: among the cluster sizes 1, 2, 4, 8 whose
+// CTAs are all resident at once (rows x nc <= resident CTAs per SM x SMs;
+// slices of at least 16 KB), the one whose busiest SM streams the fewest
+// bytes, ceil(rows x nc / SMs) slices of row/nc bytes each; the smaller on
+// ties.  With one CTA per row, 480 rows on 152 SMs leave 24 SMs four rows
+// and the rest three: the last quarter of the kernel ran on those 24 alone.
+int bulk_cluster_size(int n_rows, int V) {
+    const long long row_bytes = 2ll * V;
+    const long long sms = num_sms();
+    const long long slots = sms * bulk_ctas_per_sm();
+    int best = 1;
+    long long best_busy = ceil_div_ll(n_rows, sms);     // slices on the busiest SM, nc = 1
+    for (int nc = 2; nc <= 8; nc *= 2) {
+        if (row_bytes / nc < 16384 || (long long)n_rows * nc > slots) break;
+        const long long busy = ceil_div_ll((long long)n_rows * nc, sms);
+        if (busy * best < best_busy * nc) {      // busy / nc < best_busy / best
+            best = nc;
+            best_busy = busy;
+        }
+    }
+    return best;
+}
+
 template <typename T>
 spec_status_t launch_vocab_cluster(const void *logits, int n_rows, int V, int nc,
                                    const int32_t *proposal, int32_t *argmax, float *lse,
                                    float *zprop, float inv_t, cudaStream_t s) {
+    // bf16 rows that start on 16-byte boundaries stream through shared
+    // memory (vocab_reduce_bulk_kernel)
+    const bool bulk = sizeof(T) == 2 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0 &&
+                      (V % 8) == 0;
+    int *status = nullptr;
+    if (bulk) {
+        status = status_ptr();
+        if (!status) return SPEC_ERR_CUDA;
+        if (set_smem_limit(reinterpret_cast<const void *>(vocab_reduce_bulk_kernel), kBulkSmem) !=
+            SPEC_OK)
+            return SPEC_ERR_CUDA;
+        nc = bulk_cluster_size(n_rows, V);
+    }
+    if ((long long)n_rows * nc > 2147483647ll) return SPEC_ERR_UNSUPPORTED;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)((long long)n_rows * nc), 1, 1);
-    cfg.blockDim = dim3(kReduceThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.blockDim = dim3(bulk ? kBulkThreads : kReduceThreads, 1, 1);
+    cfg.dynamicSmemBytes = bulk ? kBulkSmem : 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -386,9 +634,12 @@ spec_status_t launch_vocab_cluster(const void *logits, int n_rows, int V, int nc
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, vocab_reduce_kernel<T>,
-                                             static_cast<const T *>(logits), V, proposal, argmax,
-                                             lse, zprop, inv_t);
+    const cudaError_t e =
+        bulk ? cudaLaunchKernelEx(&cfg, vocab_reduce_bulk_kernel,
+                                  static_cast<const __nv_bfloat16 *>(logits), V, proposal, argmax,
+                                  lse, zprop, inv_t, status, wait_limit())
+             : cudaLaunchKernelEx(&cfg, vocab_reduce_kernel<T>, static_cast<const T *>(logits), V,
+                                  proposal, argmax, lse, zprop, inv_t);
     return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
