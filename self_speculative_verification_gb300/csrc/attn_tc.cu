@@ -93,8 +93,8 @@ template <int D, int NS>
 __device__ __forceinline__ void run_producer(const TcParams &P, const CUtensorMap &mk, const CUtensorMap &mv,
                              const CUtensorMap &mkb, const CUtensorMap &mvb,
                              const CUtensorMap &msk, const CUtensorMap &msv, uint8_t *smem,
-                             uint64_t *full, uint64_t *empty, long long t_begin,
-                             long long t_end, const QLoad *ql = nullptr) {
+                             uint64_t *full, uint64_t *empty, const WarpSched &w,
+                             long long t_begin, long long t_end, const QLoad *ql = nullptr) {
     constexpr int NH = D / 64;
     constexpr int KV_BYTES = NH * kHalfBytes;
     constexpr int STAGE = 2 * KV_BYTES;
@@ -105,7 +105,7 @@ __device__ __forceinline__ void run_producer(const TcParams &P, const CUtensorMa
     // (one id per lane) one group ahead, so no page-table load sits
     // between two tile issues.
     Cursor gc;
-    cursor_init(P, t_begin, gc);         // warp-collective
+    cursor_init(P, w, t_begin, gc);      // warp-collective
     const uint64_t pol_keep = policy_evict_last();
     // the prefix is read once unless several row blocks share it
     const uint64_t pol_stream = A.n_rb == 1 ? policy_evict_first() : pol_keep;
@@ -302,19 +302,18 @@ attn_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUten
     }
     __syncthreads();
 
-    const long long T = warp_total_tiles(P);
+    const WarpSched ws = warp_sched(P);
     const int cta = blockIdx.x;
-    const long long C = warp_total_cost(P);
-    const long long t_begin = warp_range_lo(P, C, T, cta);
-    const long long t_end = warp_range_lo(P, C, T, cta + 1);
+    const long long t_begin = sched_range_lo(P, ws, cta);
+    const long long t_end = sched_range_lo(P, ws, cta + 1);
     if (threadIdx.x == 0) {
         P.bounds[cta] = t_begin;
-        if (cta == P.n_ctas - 1) P.bounds[P.n_ctas] = T;
+        if (cta == P.n_ctas - 1) P.bounds[P.n_ctas] = ws.T;
     }
     if (t_begin >= t_end) return;
 
     if (warp == NCW) {
-        run_producer<D, NS>(P, mk, mv, mkb, mvb, msk, msv, smem, full, empty, t_begin, t_end);
+        run_producer<D, NS>(P, mk, mv, mkb, mvb, msk, msv, smem, full, empty, ws, t_begin, t_end);
         return;
     }
 
@@ -333,7 +332,7 @@ attn_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUten
     int vmask_j = -1;
 
     Cursor c;
-    cursor_init(P, t_begin, c);
+    cursor_init(P, ws, t_begin, c);
     bool seg_open = false;
     long long k = 0;
     for (long long t = t_begin; t < t_end; ++t, ++k) {
@@ -699,30 +698,29 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
     const uint32_t tmem = sh.tmem_base;
     volatile int *abort = &sh.abort;
 
-    const long long T = warp_total_tiles(P);
+    const WarpSched ws = warp_sched(P);
     const int cta = blockIdx.x;
-    const long long C = warp_total_cost(P);
-    const long long t_begin = warp_range_lo(P, C, T, cta);
-    const long long t_end = warp_range_lo(P, C, T, cta + 1);
+    const long long t_begin = sched_range_lo(P, ws, cta);
+    const long long t_end = sched_range_lo(P, ws, cta + 1);
     if (threadIdx.x == 0) {
         P.bounds[cta] = t_begin;
-        if (cta == P.n_ctas - 1) P.bounds[P.n_ctas] = T;
+        if (cta == P.n_ctas - 1) P.bounds[P.n_ctas] = ws.T;
     }
 
     if (warp >= kProducerWarp) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
         if (warp == kRecWarp) {
-            const BoundaryRec rec = warp_boundary_record(P, C, T, cta, t_begin, t_end);
+            const BoundaryRec rec = warp_boundary_record(P, ws, cta, t_begin, t_end);
             if (lane == 0) P.recs[cta] = rec;
         } else if (t_begin < t_end && warp == kProducerWarp) {
             run_step_producer(P, mk, mv, mkb, mvb, msk, msv, mq,
                               ProducerIO{ring, qbuf, sh.full, sh.empty, &sh.q_full, &sh.q_empty},
-                              t_begin, t_end);
+                              ws, t_begin, t_end);
         } else if (t_begin < t_end && warp == kMmaWarp) {
             // --------------------------------------------------- MMA issuer
             // (the cursor's set-up is warp-collective: the whole warp)
             Cursor c;
-            cursor_init(P, t_begin, c);
+            cursor_init(P, ws, t_begin, c);
             if (lane == 0) {
                 const uint32_t id_pv = idesc(kRows, D, false, true);
                 const uint32_t id_s128 = idesc(kRows, 2 * kTile, false, false);
@@ -842,7 +840,7 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
         const int nsan = __popc(P.um_act[x]) * 32;
         const int isan = __popc(P.um_act[x] & ((1u << q) - 1u)) * 32 + lane;
         Cursor c;
-        cursor_init(P, t_begin, c);
+        cursor_init(P, ws, t_begin, c);
         float m_used = -INFINITY, l = 0.f;
         bool rvalid = false, rsoft = false, warp_rows = false, row_ok = false, seg_whole = false;
         int rrow = -1, seg_b = 0, head = 0, p = 0, seg_id = 0;

@@ -85,14 +85,6 @@ __device__ __forceinline__ long long warp_sum_ll(long long x) {
     return x;
 }
 
-// Total tiles over all requests (every lane gets it).
-__device__ long long warp_total_tiles(const TcParams &P) {
-    const int lane = threadIdx.x & 31;
-    long long s = 0;
-    for (int b = lane; b < P.a.B; b += 32) s += req_tiles(P, b);
-    return warp_sum_ll(s);
-}
-
 // Tiles of requests before b (every lane gets it).
 __device__ long long warp_tiles_before(const TcParams &P, int b) {
     const int lane = threadIdx.x & 31;
@@ -101,105 +93,93 @@ __device__ long long warp_tiles_before(const TcParams &P, int b) {
     return warp_sum_ll(s);
 }
 
-// Request containing linear tile t (< total), and its first tile.
-__device__ void warp_locate(const TcParams &P, long long t, int *b_out, long long *start_out) {
-    const int lane = threadIdx.x & 31;
-    const int B = P.a.B;
-    const int per = ceil_div(B, 32);
-    const int lo = min(B, lane * per), hi = min(B, lo + per);
-    long long sum = 0;
-    for (int b = lo; b < hi; ++b) sum += req_tiles(P, b);
-    long long incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const long long v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    const long long excl = incl - sum;
-    const unsigned m = __ballot_sync(0xffffffffu, lo < hi && t >= excl && t < incl);
-    const int src = m ? __ffs(m) - 1 : 0;
-    long long acc = __shfl_sync(0xffffffffu, excl, src);
-    int b = src * per;
-    while (b < B - 1) {
-        const long long n = req_tiles(P, b);
-        if (t < acc + n) break;
-        acc += n;
-        ++b;
-    }
-    *b_out = b;
-    *start_out = acc;
-}
-
 // The split.  CTAs take equal parts of a cost space in which every segment
 // counts its tiles plus P.seg_cost for its start (epilogue, query block,
 // row flags), so a CTA whose range holds many short segments gets fewer
 // tiles.  Segment s of request b occupies costs [Cb + s u, Cb + (s + 1) u),
 // u = tiles + seg_cost; the first seg_cost + 1 of them map to its first tile.
 // A CTA's range is the tiles its part of the cost space maps to.
+//
+// A warp reads the prefix lengths once (WarpSched): lane l holds requests
+// [lo, hi), ceil(B / 32) of them, with their tile and cost sums and the
+// exclusive prefix sums of both over the lanes before it.  Every lookup
+// below is then a ballot and a few shuffles (and, with more than 32
+// requests, a walk over one lane's requests).
+struct WarpSched {
+    long long T, C;          // total tiles and cost
+    long long et, ec;        // tiles and cost of the requests before lo
+    long long st, sc;        // tiles and cost of requests lo .. hi - 1
+    int lo, hi;
+    int s_lo;                // prefix length of request lo (lo < hi)
+};
 
-__device__ __forceinline__ long long req_cost(const TcParams &P, int b) {
-    return (long long)(seg_tiles(P, req_seq(P, b)) + P.seg_cost) * P.seg_h * P.seg_rb;
-}
-
-// Total cost over all requests (every lane gets it).
-__device__ long long warp_total_cost(const TcParams &P) {
+__device__ WarpSched warp_sched(const TcParams &P) {
     const int lane = threadIdx.x & 31;
-    long long s = 0;
-    for (int b = lane; b < P.a.B; b += 32) s += req_cost(P, b);
-    return warp_sum_ll(s);
-}
-
-// Request containing cost position c (< total), with the costs and tiles of
-// the requests before it (every lane gets them).
-__device__ void warp_locate_cost(const TcParams &P, long long c, int *b_out, long long *cost0,
-                                 long long *tile0) {
-    const int lane = threadIdx.x & 31;
-    const int B = P.a.B;
-    const int per = ceil_div(B, 32);
-    const int lo = min(B, lane * per), hi = min(B, lo + per);
-    long long sc = 0, st = 0;
-    for (int b = lo; b < hi; ++b) {
-        sc += req_cost(P, b);
-        st += req_tiles(P, b);
+    const int B = P.a.B, per = ceil_div(B, 32);
+    const long long units = (long long)P.seg_h * P.seg_rb;
+    WarpSched w;
+    w.lo = min(B, lane * per);
+    w.hi = min(B, w.lo + per);
+    w.st = w.sc = 0;
+    w.s_lo = 0;
+    for (int b = w.lo; b < w.hi; ++b) {
+        const int S = req_seq(P, b);
+        if (b == w.lo) w.s_lo = S;
+        const long long n = (long long)seg_tiles(P, S) * units;
+        w.st += n;
+        w.sc += n + (long long)P.seg_cost * units;
     }
-    long long ic = sc, it = st;
+    long long it = w.st, ic = w.sc;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const long long vc = __shfl_up_sync(0xffffffffu, ic, o);
         const long long vt = __shfl_up_sync(0xffffffffu, it, o);
+        const long long vc = __shfl_up_sync(0xffffffffu, ic, o);
         if (lane >= o) {
-            ic += vc;
             it += vt;
+            ic += vc;
         }
     }
-    const long long ec = ic - sc, et = it - st;
-    const unsigned m = __ballot_sync(0xffffffffu, lo < hi && c >= ec && c < ic);
-    const int src = m ? __ffs(m) - 1 : 0;
-    long long ac = __shfl_sync(0xffffffffu, ec, src);
-    long long at = __shfl_sync(0xffffffffu, et, src);
-    int b = src * per;
-    while (b < B - 1) {
-        const long long n = req_cost(P, b);
-        if (c < ac + n) break;
-        ac += n;
-        at += req_tiles(P, b);
-        ++b;
-    }
-    *b_out = b;
-    *cost0 = ac;
-    *tile0 = at;
+    w.et = it - w.st;
+    w.ec = ic - w.sc;
+    w.T = __shfl_sync(0xffffffffu, it, 31);
+    w.C = __shfl_sync(0xffffffffu, ic, 31);
+    return w;
 }
 
-// First tile of CTA i's range (C, T: total cost and tiles; warp-collective).
-__device__ long long warp_range_lo(const TcParams &P, long long C, long long T, int i) {
+// Request b holding position x (< the total) of the tile space (by_cost =
+// false) or of the cost space (true), with the tiles and cost of the
+// requests before it and its prefix length (warp-collective).
+__device__ void sched_locate(const TcParams &P, const WarpSched &w, long long x, bool by_cost,
+                             int &b, long long &t0, long long &c0, int &S) {
+    const long long e = by_cost ? w.ec : w.et, n = by_cost ? w.sc : w.st;
+    const unsigned m = __ballot_sync(0xffffffffu, w.lo < w.hi && x >= e && x < e + n);
+    const int src = m ? __ffs(m) - 1 : 0;
+    b = __shfl_sync(0xffffffffu, w.lo, src);
+    const int hi = __shfl_sync(0xffffffffu, w.hi, src);
+    t0 = __shfl_sync(0xffffffffu, w.et, src);
+    c0 = __shfl_sync(0xffffffffu, w.ec, src);
+    S = __shfl_sync(0xffffffffu, w.s_lo, src);
+    const long long units = (long long)P.seg_h * P.seg_rb;
+    while (b < hi - 1) {            // more than 32 requests: walk the lane's
+        const long long nt = (long long)seg_tiles(P, S) * units;
+        const long long nc = nt + (long long)P.seg_cost * units;
+        if (x < (by_cost ? c0 + nc : t0 + nt)) break;
+        t0 += nt;
+        c0 += nc;
+        S = req_seq(P, ++b);
+    }
+}
+
+// First tile of CTA i's range (warp-collective).
+__device__ long long sched_range_lo(const TcParams &P, const WarpSched &w, int i) {
     if (i <= 0) return 0;
-    if (i >= P.n_ctas) return T;
-    if (P.seg_cost == 0) return T * i / P.n_ctas;    // plain tile split
-    const long long c = C * i / P.n_ctas;
-    int b;
-    long long c0, t0;
-    warp_locate_cost(P, c, &b, &c0, &t0);
-    const int nt = seg_tiles(P, req_seq(P, b));
+    if (i >= P.n_ctas) return w.T;
+    if (P.seg_cost == 0) return w.T * i / P.n_ctas;    // plain tile split
+    const long long c = w.C * i / P.n_ctas;
+    int b, S;
+    long long t0, c0;
+    sched_locate(P, w, c, true, b, t0, c0, S);
+    const int nt = seg_tiles(P, S);
     const long long u = nt + P.seg_cost;
     const long long seg = (c - c0) / u, off = (c - c0) % u;
     return t0 + seg * nt + (off > P.seg_cost ? off - P.seg_cost : 0);
@@ -224,10 +204,10 @@ struct Cursor {
     int tile;                   // step within the segment
 };
 
-__device__ void cursor_init(const TcParams &P, long long t, Cursor &c) {
-    long long start;
-    warp_locate(P, t, &c.b, &start);
-    c.S = req_seq(P, c.b);
+// The cursor at tile t (< the total; warp-collective).
+__device__ void cursor_init(const TcParams &P, const WarpSched &w, long long t, Cursor &c) {
+    long long start, c0;
+    sched_locate(P, w, t, false, c.b, start, c0, c.S);
     c.n_prefix = ceil_div(c.S, kTile);
     c.n_tiles = seg_tiles(P, c.S);
     const long long local = t - start;
@@ -298,31 +278,31 @@ __device__ __forceinline__ void check_seq_len(const AttnParams &A, int b) {
 // range starts inside a unit and the ranges between the unit's first CTA
 // and this one are empty (this is the unit's first boundary), the unit and
 // the CTAs sharing it; otherwise seg = -1.
-__device__ BoundaryRec warp_boundary_record(const TcParams &P, long long C, long long T, int cta,
+__device__ BoundaryRec warp_boundary_record(const TcParams &P, const WarpSched &w, int cta,
                                             long long t_begin, long long t_end) {
     BoundaryRec rec{0, 0, -1, 0, 0, 0};
     if (t_begin >= t_end) return rec;
     Cursor c;
-    cursor_init(P, t_begin, c);
+    cursor_init(P, w, t_begin, c);
     if (c.tile == 0) return rec;
     rec.s0 = t_begin - c.tile;
     rec.s1 = rec.s0 + c.n_tiles;
     bool first_boundary = true;
     int f = cta - 1, l = cta;
     for (;; --f) {
-        const long long lo = warp_range_lo(P, C, T, f);
+        const long long lo = sched_range_lo(P, w, f);
         if (lo <= rec.s0 || f == 0) break;
         if (lo < t_begin) first_boundary = false;   // a part starts in between
     }
-    while (l + 1 < P.n_ctas && warp_range_lo(P, C, T, l + 1) < rec.s1) ++l;
+    while (l + 1 < P.n_ctas && sched_range_lo(P, w, l + 1) < rec.s1) ++l;
     if (!first_boundary) return rec;
     rec.seg = (c.b * P.seg_h + c.h) * P.seg_rb + c.rb;
     rec.first = f;
     rec.last = l;
     if (l - f < 32) {
-        long long lo = warp_range_lo(P, C, T, f);
+        long long lo = sched_range_lo(P, w, f);
         for (int j = f; j <= l; ++j) {
-            const long long hi = warp_range_lo(P, C, T, j + 1);
+            const long long hi = sched_range_lo(P, w, j + 1);
             if (max(lo, rec.s0) < min(hi, rec.s1)) rec.parts |= 1u << (j - f);
             lo = hi;
         }
@@ -392,8 +372,8 @@ __device__ __forceinline__ Sub sub_tile(const TcParams &P, const Cursor &c, int 
 __device__ void run_step_producer(const TcParams &P, const CUtensorMap &mk, const CUtensorMap &mv,
                                   const CUtensorMap &mkb, const CUtensorMap &mvb,
                                   const CUtensorMap &msk, const CUtensorMap &msv,
-                                  const CUtensorMap &mq, const ProducerIO &io, long long t_begin,
-                                  long long t_end) {
+                                  const CUtensorMap &mq, const ProducerIO &io,
+                                  const WarpSched &w, long long t_begin, long long t_end) {
     uint8_t *ring = io.ring, *qbuf = io.qbuf;
     constexpr int NH = 2;
     const AttnParams &A = P.a;
@@ -410,7 +390,7 @@ __device__ void run_step_producer(const TcParams &P, const CUtensorMap &mk, cons
     int nq = 0;                          // query blocks issued
     bool ok = true;
     Cursor c;
-    cursor_init(P, t_begin, c);          // warp-collective
+    cursor_init(P, w, t_begin, c);       // warp-collective
     for (long long t = t_begin; t < t_end; ++t) {
         if (t == t_begin || c.tile == 0) {
             // the unit's query block, once the previous unit's block has
