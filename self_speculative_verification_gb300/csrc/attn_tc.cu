@@ -1117,55 +1117,95 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                      "r"(kTmemCols));
 }
 
-// Merge packed row p of segment seg (request b, KV head h; tiles [s0, s1),
-// partials from CTAs first..last, wcn per CTA) into the final O and LSE.
-// One warp.
+// Merge packed row p of segment seg (request b, KV head h; tiles [s0, s1))
+// into the final O and LSE, from the partials of the CTAs whose ranges meet
+// it (the split is by tiles: CTA i's range is [T i / n, T (i + 1) / n)),
+// wcn per CTA.  One warp; lane l takes columns l + 32 j.  Up to kMergeParts
+// partials are loaded in one round (their (m, l) and O slices together);
+// more are visited one by one.
+constexpr int kMergeParts = 8;
+
 template <int D>
-__device__ void merge_row(const TcParams &P, int wcn, int b, int h, int seg,
-                          long long s0, long long s1, int first, int last, int p, int lane) {
+__device__ void merge_row(const TcParams &P, long long T, int wcn, int b, int h, int seg,
+                          long long s0, long long s1, int p, int lane) {
     const AttnParams &A = P.a;
+    const int n = P.n_ctas;
+    const int first = tile_split_cta(T, n, s0), last = tile_split_cta(T, n, s1 - 1);
     const int rr = p % A.rb_rows;
-    float mstar = -INFINITY;
-    for (int i = first; i <= last; ++i) {
-        const long long lo = P.bounds[i], hi = P.bounds[i + 1];
-        if (max(lo, s0) >= min(hi, s1)) continue;
-        for (int w = 0; w < wcn; ++w)
-            mstar = fmaxf(mstar, A.part_ml[slot_row(P, seg, i, w, wcn, rr) * 2]);
-    }
-    const int r = p / A.G, hq = h * A.G + p % A.G;
-    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(A.o) + (((size_t)b * A.R + r) * A.Hq + hq) * D;
+    // CTA i's range meets the segment: every CTA from first to last when no
+    // range is empty (T >= n)
+    auto holds = [&](int i) {
+        return T >= n || max(T * i / n, s0) < min(T * (i + 1) / n, s1);
+    };
+    auto holds_b = [&](int i) {     // the same from the bounds the kernel wrote
+        return max(P.bounds[i], s0) < min(P.bounds[i + 1], s1);
+    };
     float out[D / 32];
 #pragma unroll
     for (int j = 0; j < D / 32; ++j) out[j] = 0.f;
-    float lse = -INFINITY;
-    if (mstar != -INFINITY) {
-        float L = 0.f;
-        for (int i = first; i <= last; ++i) {
-            const long long lo = P.bounds[i], hi = P.bounds[i + 1];
-            if (max(lo, s0) >= min(hi, s1)) continue;
-            for (int w = 0; w < wcn; ++w) {
-                const size_t row = slot_row(P, seg, i, w, wcn, rr);
-                const float ms = A.part_ml[row * 2];
-                if (ms == -INFINITY) continue;
-                const float wgt = exp2f(ms - mstar);
-                L = fmaf(wgt, A.part_ml[row * 2 + 1], L);
-                const float *po = A.part_o + row * D;
+    float mstar = -INFINITY, L = 0.f;
+    if ((last - first + 1) * wcn <= kMergeParts) {
+        float ms[kMergeParts], ls[kMergeParts], po[kMergeParts][D / 32];
 #pragma unroll
-                for (int j = 0; j < D / 32; ++j) out[j] = fmaf(wgt, po[lane + 32 * j], out[j]);
+        for (int k = 0; k < kMergeParts; ++k) {
+            const int i = first + k / wcn, w = k % wcn;
+            const bool part = k < (last - first + 1) * wcn && holds(i);
+            const size_t row = part ? slot_row(P, seg, i, w, wcn, rr) : 0;
+            ms[k] = part ? A.part_ml[row * 2] : -INFINITY;
+            ls[k] = part ? A.part_ml[row * 2 + 1] : 0.f;
+#pragma unroll
+            for (int j = 0; j < D / 32; ++j) po[k][j] = part ? A.part_o[row * D + lane + 32 * j] : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kMergeParts; ++k) mstar = fmaxf(mstar, ms[k]);
+        if (mstar != -INFINITY) {
+#pragma unroll
+            for (int k = 0; k < kMergeParts; ++k) {
+                const float wgt = ms[k] == -INFINITY ? 0.f : exp2f(ms[k] - mstar);
+                L = fmaf(wgt, ls[k], L);
+#pragma unroll
+                for (int j = 0; j < D / 32; ++j) out[j] = fmaf(wgt, po[k][j], out[j]);
             }
         }
+    } else {
+        for (int i = first; i <= last; ++i) {
+            if (!holds_b(i)) continue;
+            for (int w = 0; w < wcn; ++w)
+                mstar = fmaxf(mstar, A.part_ml[slot_row(P, seg, i, w, wcn, rr) * 2]);
+        }
+        if (mstar != -INFINITY) {
+            for (int i = first; i <= last; ++i) {
+                if (!holds_b(i)) continue;
+                for (int w = 0; w < wcn; ++w) {
+                    const size_t row = slot_row(P, seg, i, w, wcn, rr);
+                    const float ms = A.part_ml[row * 2];
+                    if (ms == -INFINITY) continue;
+                    const float wgt = exp2f(ms - mstar);
+                    L = fmaf(wgt, A.part_ml[row * 2 + 1], L);
+                    const float *po = A.part_o + row * D;
+#pragma unroll
+                    for (int j = 0; j < D / 32; ++j) out[j] = fmaf(wgt, po[lane + 32 * j], out[j]);
+                }
+            }
+        }
+    }
+    float lse = -INFINITY;
+    if (mstar != -INFINITY) {
         const float inv = 1.f / L;
 #pragma unroll
         for (int j = 0; j < D / 32; ++j) out[j] *= inv;
         lse = (mstar + log2f(L)) * kLn2;
     }
+    const int r = p / A.G, hq = h * A.G + p % A.G;
+    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(A.o) + (((size_t)b * A.R + r) * A.Hq + hq) * D;
 #pragma unroll
     for (int j = 0; j < D / 32; ++j) o[lane + 32 * j] = __float2bfloat16_rn(out[j]);
     if (lane == 0) A.lse[((size_t)b * A.Hq + hq) * A.R + r] = lse;
 }
 
 // mma.sync path: every segment has partials.  One warp per (request, KV
-// head, packed row).
+// head, packed row); the split is recomputed from the prefix lengths (one
+// pass), not searched in the bounds.
 template <int D>
 __global__ void __launch_bounds__(128) attn_tc_combine_kernel(const __grid_constant__ TcParams P,
                                                                int wcn) {
@@ -1176,12 +1216,16 @@ __global__ void __launch_bounds__(128) attn_tc_combine_kernel(const __grid_const
     const int h = blockIdx.y, b = blockIdx.z;
     if (p >= A.M) return;
     if (p == 0 && h == 0 && lane == 0) check_seq_len(A, b);
+    const WarpSched ws = warp_sched(P);
+    int S;
+    long long t0;
+    sched_request(P, ws, b, S, t0);
     const int rb = p / A.rb_rows;
-    const int nt = seg_tiles(P, req_seq(P, b));
-    const long long s0 = warp_tiles_before(P, b) + (long long)(h * A.n_rb + rb) * nt;
-    const long long s1 = s0 + nt;
+    const int nt = seg_tiles(P, S);
+    const long long s0 = t0 + (long long)(h * A.n_rb + rb) * nt;
+    const long long s1 = s0 + nt;        // nt >= 1: every segment has block tiles
     const int seg = (b * A.Hkv + h) * A.n_rb + rb;
-    merge_row<D>(P, wcn, b, h, seg, s0, s1, cta_holding(P, s0), cta_holding(P, s1 - 1), p, lane);
+    merge_row<D>(P, ws.T, wcn, b, h, seg, s0, s1, p, lane);
 }
 
 // tcgen05 path: a unit wholly inside one CTA's range already holds its

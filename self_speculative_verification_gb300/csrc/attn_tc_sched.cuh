@@ -75,24 +75,6 @@ __device__ __forceinline__ int seg_tiles(const TcParams &P, int S) {
     return P.pair_steps ? (n + 1) >> 1 : n;
 }
 
-__device__ __forceinline__ long long req_tiles(const TcParams &P, int b) {
-    return (long long)seg_tiles(P, req_seq(P, b)) * P.seg_h * P.seg_rb;
-}
-
-__device__ __forceinline__ long long warp_sum_ll(long long x) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
-}
-
-// Tiles of requests before b (every lane gets it).
-__device__ long long warp_tiles_before(const TcParams &P, int b) {
-    const int lane = threadIdx.x & 31;
-    long long s = 0;
-    for (int i = lane; i < b; i += 32) s += req_tiles(P, i);
-    return warp_sum_ll(s);
-}
-
 // The split.  CTAs take equal parts of a cost space in which every segment
 // counts its tiles plus P.seg_cost for its start (epilogue, query block,
 // row flags), so a CTA whose range holds many short segments gets fewer
@@ -170,6 +152,20 @@ __device__ void sched_locate(const TcParams &P, const WarpSched &w, long long x,
     }
 }
 
+// Request b's prefix length and the tiles of the requests before it
+// (warp-collective).
+__device__ void sched_request(const TcParams &P, const WarpSched &w, int b, int &S,
+                              long long &t0) {
+    const int per = ceil_div(P.a.B, 32), src = b / per;
+    t0 = __shfl_sync(0xffffffffu, w.et, src);
+    S = __shfl_sync(0xffffffffu, w.s_lo, src);
+    const long long units = (long long)P.seg_h * P.seg_rb;
+    for (int i = src * per; i < b; ++i) {      // more than 32 requests
+        t0 += (long long)seg_tiles(P, S) * units;
+        S = req_seq(P, i + 1);
+    }
+}
+
 // First tile of CTA i's range (warp-collective).
 __device__ long long sched_range_lo(const TcParams &P, const WarpSched &w, int i) {
     if (i <= 0) return 0;
@@ -183,6 +179,14 @@ __device__ long long sched_range_lo(const TcParams &P, const WarpSched &w, int i
     const long long u = nt + P.seg_cost;
     const long long seg = (c - c0) / u, off = (c - c0) % u;
     return t0 + seg * nt + (off > P.seg_cost ? off - P.seg_cost : 0);
+}
+
+// CTA whose range holds tile t (< T) when the split is by tiles alone
+// (seg_cost 0, range i = [T i / n, T (i + 1) / n)): the last i with
+// T i / n <= t.
+__device__ __forceinline__ int tile_split_cta(long long T, int n, long long t) {
+    const long long i = ((long long)n * (t + 1) + T - 1) / T - 1;
+    return (int)(i < 0 ? 0 : (i >= n ? n - 1 : i));
 }
 
 // CTA whose range holds tile t, from the bounds the attention kernel wrote:
