@@ -640,7 +640,7 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory of the tcgen05 verify ker
 
 }  // namespace umma
 
-template <int D>
+template <int D, bool MERGED>
 __global__ void __launch_bounds__(umma::kThreads, 1)
 attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUtensorMap mk,
                  const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mkb,
@@ -827,18 +827,26 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
         // ------------------------------------------------------ softmax
-        const int q = warp & 3, x = warp >> 2;         // lane quarter, sub-tile
+        const int q = warp & 3, x = warp >> 2;         // lane quarter, half of the row
         const int r = q * 32 + lane;                    // TMEM lane of this row
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const bool active = ((P.um_act[x] >> q) & 1) != 0;
-        // merged: sub-tile x's rows are lanes 64 x .. 64 x + 63 (packed row
-        // r - 64 x of head 2u + x); rows mode: packed row rb * 128 + r, and
-        // the two threads of a row (sub-tiles 0 and 1) share every step
-        const bool merged = P.um_merged != 0;
+        // Every row is shared by two threads (warps q and q + 4), which swap
+        // their step maxima and, at the end, their sums.  Rows mode: packed
+        // row rb * 128 + r; thread x takes sub-tile x (64 keys, S columns
+        // 64 x .., P over the first 32 of them).  Merged: lanes 64 y .. 64 y
+        // + 63 hold head 2u + y's rows (packed row r - 64 y) and see sub-tile
+        // y only; thread x takes its keys 32 x .. 32 x + 31 (S columns 64 y
+        // + 32 x .., P at 64 y + 16 x .., zeros at 64 (1 - y) + 16 x ..).
+        constexpr bool merged = MERGED;
+        const int sub = merged ? q >> 1 : x;            // this thread's sub-tile
+        const uint32_t s_off = merged ? 64u * sub + 32u * x : 64u * x;
+        const uint32_t p_off = merged ? 64u * sub + 16u * x : 64u * x;
         const float sc = A.scale_log2;
-        // threads of this sub-tile that clear ragged V rows
-        const int nsan = __popc(P.um_act[x]) * 32;
-        const int isan = __popc(P.um_act[x] & ((1u << q) - 1u)) * 32 + lane;
+        // threads of this sub-tile that clear its ragged V rows
+        const unsigned sub_q = merged ? (P.um_act[0] & (3u << (2 * sub))) : P.um_act[x];
+        const int nsan = __popc(sub_q) * (merged ? 64 : 32);
+        const int isan = ((merged ? x * __popc(sub_q) : 0) + __popc(sub_q & ((1u << q) - 1u))) * 32 + lane;
         Cursor c;
         cursor_init(P, ws, t_begin, c);
         float m_used = -INFINITY, l = 0.f;
@@ -869,14 +877,11 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
         auto epilogue = [&](long long j) -> bool {
             if (!mbar_wait_warp(&sh.o_upd[j & 1], (uint32_t)((j >> 1) & 1), P.wait)) return false;
             fence_after();
-            float lt = l;
-            if (!merged) {
-                float lo = 0.f;
-                if (!swap(l, lo)) return false;
-                lt = l + lo;
-            }
+            float lo = 0.f;
+            if (!swap(l, lo)) return false;
+            const float lt = l + lo;
             if (!warp_rows) return true;
-            const int c_lo = merged ? 0 : 2 * x, c_hi = merged ? D / 32 : 2 * x + 2;
+            const int c_lo = 2 * x, c_hi = 2 * x + 2;   // this thread's half of O
             if (seg_whole) {
                 const int rr = row_ok ? p / A.G : 0, hq = head * A.G + (row_ok ? p % A.G : 0);
                 const float inv = lt > 0.f ? 1.f / lt : 0.f;
@@ -896,7 +901,7 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                             pack_bf16(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv),
                             pack_bf16(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv));
                 }
-                if (row_ok && x == (merged ? x : 0))
+                if (row_ok && x == 0)
                     A.lse[((size_t)seg_b * A.Hq + hq) * A.R + rr] =
                         lt > 0.f ? (m_used + log2f(lt)) * kLn2 : -INFINITY;
             } else {
@@ -915,7 +920,7 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                             make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
                                         __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
                 }
-                if (row_ok && x == (merged ? x : 0)) {
+                if (row_ok && x == 0) {
                     A.part_ml[row * 2] = m_used;
                     A.part_ml[row * 2 + 1] = lt;
                 }
@@ -933,9 +938,9 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                 const long long seg_lo = t - c.tile;
                 seg_whole = seg_lo >= t_begin && seg_lo + c.n_tiles <= t_end;
                 if (merged) {
-                    head = 2 * c.h + x;
-                    p = r - 64 * x;
-                    row_ok = head < A.Hkv && p >= 0 && p < 64 && p < A.M;
+                    head = 2 * c.h + sub;
+                    p = r - 64 * sub;
+                    row_ok = head < A.Hkv && p < A.M;
                 } else {
                     head = c.h;
                     p = c.rb * kRows + r;
@@ -953,7 +958,7 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                 m_used = -INFINITY;
                 l = 0.f;
             }
-            const Sub su = sub_tile(P, c, x);
+            const Sub su = sub_tile(P, c, sub);
             const TileInfo &ti = su.ti;
             if (su.present && ti.kind == kBlock && vmask_j != ti.j) {
                 uint64_t w = 0;
@@ -967,28 +972,31 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
             }
             if (!(ok = mbar_wait_warp(&sh.s_full[k & 1], (uint32_t)((k >> 1) & 1), P.wait))) break;
             fence_after();
-            const uint32_t tS = tmem + lane_base + col_s((int)(k & 1)) + 64u * x;
+            const uint32_t tS = tmem + lane_base + col_s((int)(k & 1)) + s_off;
             uint32_t v[2][32];
             float pm = -INFINITY;          // this thread's raw score maximum
             if (warp_rows && su.present) {
-                // the 64 scores of this row and sub-tile: both TMEM loads in
-                // flight, one wait
+                // this thread's scores (64 or 32): the TMEM loads in flight,
+                // one wait
                 ld32(tS, v[0]);
-                ld32(tS + 32, v[1]);
+                if (!merged) ld32(tS + 32, v[1]);
                 wait_ld(v[0]);
-                wait_ld(v[1]);
-                // columns this row sees, as one 64-bit mask; the others
-                // become -inf in place
+                if (!merged) wait_ld(v[1]);
+                // columns this row sees, as one 64-bit mask over the
+                // sub-tile, shifted to this thread's keys; the others become
+                // -inf in place
                 const uint64_t valid_cols =
                     ti.nvalid >= kTile ? ~0ull : ((1ull << ti.nvalid) - 1ull);
                 uint64_t vm;
                 if (ti.kind == kPrefix) vm = rvalid ? valid_cols : 0ull;
                 else if (ti.kind == kSoft) vm = rsoft ? valid_cols : 0ull;
                 else vm = vmask & valid_cols;
+                vm = merged ? (vm >> (32 * x)) | 0xffffffff00000000ull : vm;
                 if (vm != ~0ull) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const uint32_t hm = (uint32_t)(vm >> (32 * h));
+                        if (h == 1 && merged) break;
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
                             v[h][e] = ((hm >> e) & 1u) ? v[h][e] : 0xff800000u;
@@ -996,17 +1004,21 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                 }
                 float tmv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
+                for (int h = 0; h < 2; ++h) {
+                    if (h == 1 && merged) break;
 #pragma unroll
                     for (int e = 0; e < 32; e += 8)
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
                             tmv[i] = max3(tmv[i], __uint_as_float(v[h][e + 2 * i]),
                                           __uint_as_float(v[h][e + 2 * i + 1]));
+                }
                 pm = fmaxf(fmaxf(tmv[0], tmv[1]), fmaxf(tmv[2], tmv[3]));
             }
-            if (!merged) {
-                // one reference max for both threads of the row
+            {
+                // one reference max for both threads of the row (the swap
+                // also orders both threads' score loads before either
+                // writes P over the row's S columns)
                 float po = -INFINITY;
                 if (!(ok = swap(pm, po))) break;
                 pm = fmaxf(pm, po);
@@ -1027,7 +1039,7 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                     break;
                 fence_after();
                 const float a = scale_o ? alpha : 1.f;
-                const int c_lo = merged ? 0 : 2 * x, c_hi = merged ? D / 32 : 2 * x + 2;
+                const int c_lo = 2 * x, c_hi = 2 * x + 2;   // this thread's half of O
 #pragma unroll 1
                 for (int c32 = c_lo; c32 < c_hi; ++c32) {
                     uint32_t o[32];
@@ -1053,6 +1065,7 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                     uint64_t rs2[2] = {pair(0.f, 0.f), pair(0.f, 0.f)};
 #pragma unroll
                     for (int e = 0; e < kTile / 2; ++e) {
+                        if (merged && e >= 16) break;      // 32 keys
                         const int h = e / 16, f = 2 * (e % 16);
                         float t0, t1;
                         unpair(fma2(pair(__uint_as_float(v[h][f]), __uint_as_float(v[h][f + 1])),
@@ -1070,12 +1083,18 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
 #pragma unroll
                     for (int e = 0; e < 32; ++e) w[e] = 0u;
                 }
-                st32(tS, w);
-                if (merged) {
+                const uint32_t tP = tmem + lane_base + col_s((int)(k & 1)) + p_off;
+                if (!merged) {
+                    st32(tP, w);
+                } else {
+                    uint32_t w16[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) w16[e] = w[e];
+                    st16(tP, w16);
                     // the other head's keys: P = 0 in this row
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) w[e] = 0u;
-                    st32(tmem + lane_base + col_s((int)(k & 1)) + 64u * (x ^ 1), w);
+                    for (int e = 0; e < 16; ++e) w16[e] = 0u;
+                    st16(tmem + lane_base + col_s((int)(k & 1)) + 64u * (1 - sub) + 16u * x, w16);
                 }
             }
             if (su.present && ti.nvalid < kTile) {
@@ -1087,7 +1106,7 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                 if (!(ok = mbar_wait_warp(&sh.full[vn % kSlots], (uint32_t)((vn / kSlots) & 1),
                                           P.wait)))
                     break;
-                uint8_t *vt = ring + (int)(vn % kSlots) * kSlotBytes + x * kTile * 128;
+                uint8_t *vt = ring + (int)(vn % kSlots) * kSlotBytes + sub * kTile * 128;
                 const int nchunk = (kTile - ti.nvalid) * 2 * 8;
                 for (int i = isan; i < nchunk; i += nsan) {
                     const int tok = ti.nvalid + i / 16, rem = i % 16;
@@ -1400,14 +1419,24 @@ spec_status_t launch_impl(const TcParams &P, const CUtensorMap *maps, cudaStream
     return launch_status();
 }
 
+template <bool MERGED>
+spec_status_t launch_umma_kernel(const TcParams &P, const CUtensorMap *maps, cudaStream_t s) {
+    constexpr int D = 128;
+    if (set_smem_limit(reinterpret_cast<const void *>(attn_umma_kernel<D, MERGED>),
+                       umma::kSmemBytes) != SPEC_OK)
+        return SPEC_ERR_CUDA;
+    if (launch(attn_umma_kernel<D, MERGED>, dim3(P.n_ctas), dim3(umma::kThreads),
+               umma::kSmemBytes, s, P, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
+               maps[6]) != SPEC_OK)
+        return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
 spec_status_t launch_umma(const TcParams &P, const CUtensorMap *maps, cudaStream_t s) {
     constexpr int D = 128;
-    if (set_smem_limit(reinterpret_cast<const void *>(attn_umma_kernel<D>), umma::kSmemBytes) !=
-        SPEC_OK)
-        return SPEC_ERR_CUDA;
-    if (launch(attn_umma_kernel<D>, dim3(P.n_ctas), dim3(umma::kThreads), umma::kSmemBytes, s, P,
-               maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6]) != SPEC_OK)
-        return SPEC_ERR_CUDA;
+    const spec_status_t lk = P.um_merged ? launch_umma_kernel<true>(P, maps, s)
+                                         : launch_umma_kernel<false>(P, maps, s);
+    if (lk != SPEC_OK) return lk;
     spec_status_t st = launch_status();
     if (st != SPEC_OK) return st;
     const spec_status_t ls =
@@ -1438,12 +1467,11 @@ UmmaPlan umma_plan(const AttnParams &A) {
     u.merged = 1;
     u.seg_h = (A.Hkv + 1) / 2;
     u.seg_rb = 1;
-    // softmax warps of sub-tile x: the lane quarters holding head 2u + x's rows
-    for (int x = 0; x < 2; ++x) {
-        const int lo = 64 * x, hi = lo + A.M;
-        for (int w = 0; w < 4; ++w)
-            if (32 * w < hi && 32 * w + 32 > lo) u.act[x] |= 1u << w;
-    }
+    // the lane quarters holding rows (head 2u + x's rows at lanes 64 x ..
+    // 64 x + M - 1), each with both of its warps (the two key halves)
+    for (int w = 0; w < 4; ++w)
+        if (32 * (w & 1) < A.M) u.act[0] |= 1u << w;
+    u.act[1] = u.act[0];
     return u;
 }
 
