@@ -1537,10 +1537,13 @@ spec_status_t launch_attn_tc(const AttnParams &A, cudaStream_t s) {
             reinterpret_cast<char *>(P.bounds) +
             ((((size_t)P.n_ctas + 1) * sizeof(long long) + 255) & ~size_t(255)));
     }
-    // a unit start costs the tcgen05 kernel about three steps (epilogue,
-    // query block, row flags); the mma.sync kernel's segments (decode-shaped:
-    // long prefixes, few rows) are split by tiles alone
-    P.seg_cost = use_umma ? 3 : 0;
+    // a unit start (epilogue, query block, row flags) costs the tcgen05
+    // kernel about two steps in rows mode and one in merged mode (GB300,
+    // per-CTA loop times fitted as a x steps + b x units: ConFu 1.47 us x
+    // steps + 2.77 us x units, SS 1.52 us x steps + 1.85 us x units); the
+    // mma.sync kernel's segments (decode-shaped: long prefixes, few rows)
+    // are split by tiles alone
+    P.seg_cost = use_umma ? (umma_plan(A).merged ? 1 : 2) : 0;
     P.seg_h = A.Hkv;
     P.seg_rb = A.n_rb;
     if (use_umma) {
