@@ -1136,27 +1136,20 @@ attn_umma_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUt
                      "r"(kTmemCols));
 }
 
-// Merge packed row p of segment seg (request b, KV head h; tiles [s0, s1))
-// into the final O and LSE, from the partials of the CTAs whose ranges meet
-// it (the split is by tiles: CTA i's range is [T i / n, T (i + 1) / n)),
-// wcn per CTA.  One warp; lane l takes columns l + 32 j.  Up to kMergeParts
+// Merge packed row p of segment seg (request b, KV head h; tiles [s0, s1),
+// held by CTAs first..last) into the final O and LSE, from the partials of
+// the CTAs whose ranges meet it (the bounds the attention kernel wrote), wcn
+// per CTA.  One warp; lane l takes columns l + 32 j.  Up to kMergeParts
 // partials are loaded in one round (their (m, l) and O slices together);
 // more are visited one by one.
 constexpr int kMergeParts = 8;
 
 template <int D>
-__device__ void merge_row(const TcParams &P, long long T, int wcn, int b, int h, int seg,
-                          long long s0, long long s1, int p, int lane) {
+__device__ void merge_row(const TcParams &P, int wcn, int b, int h, int seg, long long s0,
+                          long long s1, int first, int last, int p, int lane) {
     const AttnParams &A = P.a;
-    const int n = P.n_ctas;
-    const int first = tile_split_cta(T, n, s0), last = tile_split_cta(T, n, s1 - 1);
     const int rr = p % A.rb_rows;
-    // CTA i's range meets the segment: every CTA from first to last when no
-    // range is empty (T >= n)
-    auto holds = [&](int i) {
-        return T >= n || max(T * i / n, s0) < min(T * (i + 1) / n, s1);
-    };
-    auto holds_b = [&](int i) {     // the same from the bounds the kernel wrote
+    auto holds = [&](int i) {       // CTA i's range meets the segment
         return max(P.bounds[i], s0) < min(P.bounds[i + 1], s1);
     };
     float out[D / 32];
@@ -1188,13 +1181,13 @@ __device__ void merge_row(const TcParams &P, long long T, int wcn, int b, int h,
         }
     } else {
         for (int i = first; i <= last; ++i) {
-            if (!holds_b(i)) continue;
+            if (!holds(i)) continue;
             for (int w = 0; w < wcn; ++w)
                 mstar = fmaxf(mstar, A.part_ml[slot_row(P, seg, i, w, wcn, rr) * 2]);
         }
         if (mstar != -INFINITY) {
             for (int i = first; i <= last; ++i) {
-                if (!holds_b(i)) continue;
+                if (!holds(i)) continue;
                 for (int w = 0; w < wcn; ++w) {
                     const size_t row = slot_row(P, seg, i, w, wcn, rr);
                     const float ms = A.part_ml[row * 2];
@@ -1237,14 +1230,19 @@ __global__ void __launch_bounds__(128) attn_tc_combine_kernel(const __grid_const
     if (p == 0 && h == 0 && lane == 0) check_seq_len(A, b);
     const WarpSched ws = warp_sched(P);
     int S;
-    long long t0;
-    sched_request(P, ws, b, S, t0);
+    long long t0, c0;
+    sched_request(P, ws, b, S, t0, c0);
     const int rb = p / A.rb_rows;
     const int nt = seg_tiles(P, S);
-    const long long s0 = t0 + (long long)(h * A.n_rb + rb) * nt;
-    const long long s1 = s0 + nt;        // nt >= 1: every segment has block tiles
+    const int si = h * A.n_rb + rb;           // segment within the request
+    const long long s0 = t0 + (long long)si * nt;
+    const long long s1 = s0 + nt;             // nt >= 1: every segment has block tiles
+    // the CTAs holding its first and last tiles, from their cost positions
+    const long long x0 = c0 + (long long)si * (nt + P.seg_cost) + P.seg_cost;
+    const int first = cost_split_cta(ws.C, P.n_ctas, x0);
+    const int last = cost_split_cta(ws.C, P.n_ctas, x0 + nt - 1);
     const int seg = (b * A.Hkv + h) * A.n_rb + rb;
-    merge_row<D>(P, ws.T, wcn, b, h, seg, s0, s1, p, lane);
+    merge_row<D>(P, wcn, b, h, seg, s0, s1, first, last, p, lane);
 }
 
 // tcgen05 path: a unit wholly inside one CTA's range already holds its
@@ -1540,10 +1538,11 @@ spec_status_t launch_attn_tc(const AttnParams &A, cudaStream_t s) {
     // a unit start (epilogue, query block, row flags) costs the tcgen05
     // kernel about two steps in rows mode and one in merged mode (GB300,
     // per-CTA loop times fitted as a x steps + b x units: ConFu 1.47 us x
-    // steps + 2.77 us x units, SS 1.52 us x steps + 1.85 us x units); the
-    // mma.sync kernel's segments (decode-shaped: long prefixes, few rows)
-    // are split by tiles alone
-    P.seg_cost = use_umma ? (umma_plan(A).merged ? 1 : 2) : 0;
+    // steps + 2.77 us x units, SS 1.52 us x steps + 1.85 us x units); a
+    // segment of the mma.sync kernel (every warp's partial written, the
+    // query fragments loaded) about four tiles (la7b attention 122 -> 114 us
+    // against a plain tile split, flat from four to six)
+    P.seg_cost = use_umma ? (umma_plan(A).merged ? 1 : 2) : 4;
     P.seg_h = A.Hkv;
     P.seg_rb = A.n_rb;
     if (use_umma) {

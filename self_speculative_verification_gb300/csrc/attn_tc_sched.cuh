@@ -152,16 +152,19 @@ __device__ void sched_locate(const TcParams &P, const WarpSched &w, long long x,
     }
 }
 
-// Request b's prefix length and the tiles of the requests before it
-// (warp-collective).
+// Request b's prefix length and the tiles and cost of the requests before
+// it (warp-collective).
 __device__ void sched_request(const TcParams &P, const WarpSched &w, int b, int &S,
-                              long long &t0) {
+                              long long &t0, long long &c0) {
     const int per = ceil_div(P.a.B, 32), src = b / per;
     t0 = __shfl_sync(0xffffffffu, w.et, src);
+    c0 = __shfl_sync(0xffffffffu, w.ec, src);
     S = __shfl_sync(0xffffffffu, w.s_lo, src);
     const long long units = (long long)P.seg_h * P.seg_rb;
     for (int i = src * per; i < b; ++i) {      // more than 32 requests
-        t0 += (long long)seg_tiles(P, S) * units;
+        const long long nt = (long long)seg_tiles(P, S) * units;
+        t0 += nt;
+        c0 += nt + (long long)P.seg_cost * units;
         S = req_seq(P, i + 1);
     }
 }
@@ -181,11 +184,12 @@ __device__ long long sched_range_lo(const TcParams &P, const WarpSched &w, int i
     return t0 + seg * nt + (off > P.seg_cost ? off - P.seg_cost : 0);
 }
 
-// CTA whose range holds tile t (< T) when the split is by tiles alone
-// (seg_cost 0, range i = [T i / n, T (i + 1) / n)): the last i with
-// T i / n <= t.
-__device__ __forceinline__ int tile_split_cta(long long T, int n, long long t) {
-    const long long i = ((long long)n * (t + 1) + T - 1) / T - 1;
+// CTA whose range holds a tile, from the tile's last position x in the
+// cost space (C in total): CTA i's range starts at the tile that position
+// C i / n maps to, so it is the last i with C i / n <= x.  For tile j of a
+// segment whose costs start at cs, x = cs + seg_cost + j.
+__device__ __forceinline__ int cost_split_cta(long long C, int n, long long x) {
+    const long long i = ((long long)n * (x + 1) + C - 1) / C - 1;
     return (int)(i < 0 ? 0 : (i >= n ? n - 1 : i));
 }
 
