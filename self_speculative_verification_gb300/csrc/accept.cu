@@ -17,6 +17,7 @@
 #include "common.cuh"
 #include "logits.cuh"
 #include "ptx_sm103.cuh"
+#include "row_scan.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -24,35 +25,6 @@ namespace sv {
 namespace {
 
 constexpr int kReduceThreads = 256;
-
-struct Best {
-    float m;     // running max
-    int idx;     // lowest index attaining it
-    float s;     // sum of exp(z - m)
-};
-
-// inv_t: 1 / temperature (the sums are of exp(z / T)).
-__device__ __forceinline__ void best_push(Best &b, float z, int i, float inv_t) {
-    if (z > b.m) {
-        b.s = b.s * __expf((b.m - z) * inv_t) + 1.f;
-        b.m = z;
-        b.idx = i;
-    } else {
-        b.s += __expf((z - b.m) * inv_t);
-        if (z == b.m && i < b.idx) b.idx = i;
-    }
-}
-
-__device__ __forceinline__ Best best_merge(Best a, Best b, float inv_t) {
-    if (b.m > a.m || (b.m == a.m && b.idx < a.idx)) {
-        Best t = a;
-        a = b;
-        b = t;
-    }
-    // a has the larger max (or equal max with the lower index)
-    if (b.m != -INFINITY) a.s += b.s * __expf((b.m - a.m) * inv_t);
-    return a;
-}
 
 // One thread-block cluster per row: CTA `rank` of the cluster reduces slice
 // `rank` of the row, kUnroll 16-byte loads in flight per thread, one pass
@@ -62,70 +34,8 @@ __device__ __forceinline__ Best best_merge(Best a, Best b, float inv_t) {
 // increasing order, so an equal later value never wins a tie); then one
 // FFMA + one ex2 per element.  Rank 0 merges the CTAs' results through
 // distributed shared memory.
-// bf16 batches without a ragged end take packed arithmetic: the batch max
-// on bf16 pairs (exact: a max selects one of its inputs), the exponent
-// arguments and the sums on fp32 pairs, so per element about one ex2 and
-// three other instructions issue.
-constexpr int kUnroll = 4;
-
-struct Bf16Batch {
-    uint32_t w[kUnroll][4];     // kUnroll x 8 bf16, pairs in 32-bit words
-};
-
-__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
-// Running (max, index, sum) over one full batch of kUnroll 8-element
-// vectors; vector u starts at element (i0 + u * kStride) * 8.
-template <int kStride = kReduceThreads>
-__device__ __forceinline__ void push_bf16_batch(Best &best, const Bf16Batch &x, int i0, float c2) {
-    uint32_t m2 = x.w[0][0];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) m2 = bf16x2_max(m2, x.w[u][q]);
-    const float bm = fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xffff0000u));
-    if (bm > best.m) {
-        int bi = INT_MAX;
-#pragma unroll
-        for (int u = kUnroll - 1; u >= 0; --u)
-#pragma unroll
-            for (int j = 7; j >= 0; --j) {
-                const uint32_t wq = x.w[u][j >> 1];
-                const float v = __uint_as_float((j & 1) ? (wq & 0xffff0000u) : (wq << 16));
-                if (v == bm) bi = (i0 + u * kStride) * 8 + j;
-            }
-        best.s *= ex2((best.m - bm) * c2);
-        best.m = bm;
-        best.idx = bi;
-    }
-    const uint64_t c22 = pair(c2, c2);
-    const float nmb = -best.m * c2;
-    const uint64_t nmb2 = pair(nmb, nmb);
-    uint64_t acc[4] = {pair(0.f, 0.f), pair(0.f, 0.f), pair(0.f, 0.f), pair(0.f, 0.f)};
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint32_t wq = x.w[u][q];
-            float t0, t1;
-            unpair(fma2(pair(__uint_as_float(wq << 16), __uint_as_float(wq & 0xffff0000u)), c22,
-                        nmb2),
-                   t0, t1);
-            acc[q] = add2(acc[q], pair(ex2(t0), ex2(t1)));
-        }
-    float a0, a1, a2, a3, a4, a5, a6, a7;
-    unpair(acc[0], a0, a1);
-    unpair(acc[1], a2, a3);
-    unpair(acc[2], a4, a5);
-    unpair(acc[3], a6, a7);
-    best.s += ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7));
-}
-
-
+// bf16 batches without a ragged end take the packed arithmetic of
+// push_bf16_batch.
 template <typename T>
 __global__ void __launch_bounds__(kReduceThreads)
 vocab_reduce_kernel(const T *__restrict__ logits, int V, const int32_t *__restrict__ proposal,
@@ -157,7 +67,7 @@ vocab_reduce_kernel(const T *__restrict__ logits, int V, const int32_t *__restri
                     x.w[u][2] = v.z;
                     x.w[u][3] = v.w;
                 }
-                push_bf16_batch(best, x, i0, c2);
+                push_bf16_batch<kReduceThreads>(best, x, i0, c2);
             }
         }
         // the ragged last batch (all batches for fp32)
@@ -245,30 +155,16 @@ vocab_reduce_kernel(const T *__restrict__ logits, int V, const int32_t *__restri
 }
 
 // The same reduction for bf16 rows whose start is 16-byte aligned, with the
-// row slice streamed through shared memory: thread 0 issues bulk copies
-// (cp.async.bulk) of kBulkChunk-element chunks into a ring of kBulkStages
-// buffers ahead of the consumers, so about kBulkStages chunks per CTA are in
-// flight instead of one batch of loads per thread.  Every thread then reduces
-// its kUnroll 16-byte vectors of a chunk from shared memory with the packed
-// arithmetic of the kernel above.  CTAs are small (kBulkThreads threads,
-// kBulkStages x 8 KB of shared memory) so that many fit on an SM: the host
-// picks the CTAs per row so that every CTA is resident at once and the SMs'
-// shares of the bytes are even (bulk_cluster_size).  A copy that has not
-// landed within the bounded wait sets SPEC_DEV_TIMEOUT; the CTA then waits
-// for its other copies and writes nothing.
+// row slice streamed through shared memory (bulk_row_scan: thread 0 keeps
+// kBulkStages chunks of bulk copies in flight ahead of the reducing
+// threads).  CTAs are small (kBulkThreads threads, kBulkStages x 8 KB of
+// shared memory) so that many fit on an SM: the host picks the CTAs per row
+// so that every CTA is resident at once and the SMs' shares of the bytes are
+// even (bulk_cluster_size).  A copy that has not landed within the bounded
+// wait sets SPEC_DEV_TIMEOUT; the CTA then writes nothing.
 constexpr int kBulkThreads = 128;
-constexpr int kBulkChunk = kBulkThreads * kUnroll * 8;     // elements (8 KB of bf16)
 constexpr int kBulkStages = 3;
-constexpr int kBulkSmem = kBulkStages * kBulkChunk * 2;
-
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
-                                          uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
+constexpr int kBulkSmem = bulk_smem<kBulkThreads, kBulkStages>();
 
 __global__ void __launch_bounds__(kBulkThreads)
 vocab_reduce_bulk_kernel(const __nv_bfloat16 *__restrict__ logits, int V,
@@ -289,112 +185,9 @@ vocab_reduce_bulk_kernel(const __nv_bfloat16 *__restrict__ logits, int V,
     const int nv = V / 8;
     const int lo = (int)((long long)nv * rank / nc), hi = (int)((long long)nv * (rank + 1) / nc);
     const int n_el = (hi - lo) * 8;
-    const int n_chunks = (n_el + kBulkChunk - 1) / kBulkChunk;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kBulkStages; ++i) mbar_init(&full[i], 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
-    __syncthreads();
-    const uint64_t pol = policy_evict_first();
-    auto issue = [&](int ch) {        // thread 0: chunk ch into its stage
-        const int b = ch % kBulkStages;
-        const uint32_t bytes = (uint32_t)min(kBulkChunk, n_el - ch * kBulkChunk) * 2u;
-        mbar_arrive_expect_tx(&full[b], bytes);
-        bulk_load(stage + b * (kBulkChunk * 2), z + (size_t)lo * 8 + (size_t)ch * kBulkChunk, bytes,
-                  &full[b], pol);
-    };
-    if (threadIdx.x == 0)
-        for (int ch = 0; ch < n_chunks && ch < kBulkStages; ++ch) issue(ch);
-    int ch = 0;
-    bool failed = false;
-    for (; ch < n_chunks; ++ch) {
-        const int b = ch % kBulkStages;
-        const uint32_t parity = (uint32_t)((ch / kBulkStages) & 1);
-        // Thread 0 alone polls; the others sleep in the block barrier rather
-        // than spin (spinning threads took the issue slots of the reducing
-        // warps).  After the barrier every thread tests the completed phase
-        // once, which also gives each its own acquire of the copied bytes.
-        const bool got = threadIdx.x != 0 || mbar_wait(&full[b], parity, wait);
-        if (__syncthreads_or(!got)) {
-            failed = true;
-            break;
-        }
-        (void)mbar_test_wait(&full[b], parity);
-        const uint4 *sv = reinterpret_cast<const uint4 *>(stage + b * (kBulkChunk * 2));
-        const int i0 = lo + ch * (kBulkChunk / 8) + (int)threadIdx.x;   // vector index in the row
-        const int nvec = min(kBulkChunk, n_el - ch * kBulkChunk) / 8;
-        if ((int)threadIdx.x + (kUnroll - 1) * kBulkThreads < nvec) {
-            Bf16Batch x;
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const uint4 v = sv[threadIdx.x + u * kBulkThreads];
-                x.w[u][0] = v.x;
-                x.w[u][1] = v.y;
-                x.w[u][2] = v.z;
-                x.w[u][3] = v.w;
-            }
-            push_bf16_batch<kBulkThreads>(best, x, i0, c2);
-        } else if ((int)threadIdx.x < nvec) {
-            // a batch that runs past the end of the slice
-            float xs[kUnroll][8];
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int iv = (int)threadIdx.x + u * kBulkThreads;
-                if (iv < nvec) {
-                    const uint4 v = sv[iv];
-                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        xs[u][2 * j] = __uint_as_float(w[j] << 16);
-                        xs[u][2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) xs[u][j] = -INFINITY;
-                }
-            }
-            float bm = xs[0][0];
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) bm = fmaxf(bm, xs[u][j]);
-            if (bm > best.m) {
-                int bi = INT_MAX;
-#pragma unroll
-                for (int u = kUnroll - 1; u >= 0; --u)
-#pragma unroll
-                    for (int j = 7; j >= 0; --j)
-                        if (xs[u][j] == bm) bi = (i0 + u * kBulkThreads) * 8 + j;
-                best.s *= ex2((best.m - bm) * c2);
-                best.m = bm;
-                best.idx = bi;
-            }
-            const float mb = best.m * c2;
-            float acc[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) acc[j] += ex2(fmaf(xs[u][j], c2, -mb));
-#pragma unroll
-            for (int j = 1; j < 8; ++j) acc[0] += acc[j];
-            best.s += acc[0];
-        }
-        __syncthreads();                 // every thread is done with this stage
-        if (threadIdx.x == 0 && ch + kBulkStages < n_chunks) issue(ch + kBulkStages);
-    }
-    if (failed) {
-        if (threadIdx.x == 0) {
-            raise_status(status, SPEC_DEV_TIMEOUT);
-            // do not leave while copies into this CTA's shared memory are in
-            // flight
-            for (int c = ch; c < n_chunks && c < ch + kBulkStages; ++c)
-                if (!mbar_wait(&full[c % kBulkStages], (uint32_t)((c / kBulkStages) & 1))) break;
-        }
-        __syncthreads();
-    }
+    const bool failed = !bulk_row_scan<kBulkThreads, kBulkStages>(z + (size_t)lo * 8, n_el, lo, c2,
+                                                                   best, stage, full, wait);
+    if (failed && threadIdx.x == 0) raise_status(status, SPEC_DEV_TIMEOUT);
     if (rank == nc - 1)
         for (int i = nv * 8 + threadIdx.x; i < V; i += kBulkThreads)
             best_push(best, load_f(z + i), i, inv_t);
