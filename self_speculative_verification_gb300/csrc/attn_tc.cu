@@ -55,6 +55,14 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t 
                  : "r"(addr));
 }
 
+// The transpose of an 8x8 b16 matrix held as an mma fragment (each thread
+// row lane / 4, columns 2 (lane % 4) and + 1).
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
     asm volatile(
@@ -259,8 +267,9 @@ __device__ __forceinline__ void run_producer(const TcParams &P, const CUtensorMa
 }
 
 // D: head_dim; WR: 16-row warp groups per row block; NCW: consumer warps;
-// NS: pipeline stages; MINB: CTAs per SM the launch is sized for.
-template <int D, int WR, int NCW, int NS, int MINB>
+// NS: pipeline stages; MINB: CTAs per SM the launch is sized for; SWAP: row
+// blocks of 8 packed rows computed transposed (below).
+template <int D, int WR, int NCW, int NS, int MINB, int SWAP = 0>
 __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
 attn_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUtensorMap mk,
                const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mkb,
@@ -322,6 +331,229 @@ attn_tc_kernel(const __grid_constant__ TcParams P, const __grid_constant__ CUten
     const int g = lane >> 2, cq = lane & 3;
     const int c0 = wc * TW;                  // first token of this warp in a tile
     const uint32_t smem_base = smem_u32(smem);
+
+    if constexpr (SWAP != 0) {
+        // Row blocks of 8 packed rows, transposed: S^T = K Q^T with the keys
+        // as the MMA's M (16 per m16 tile) and the 8 rows as its N, so no row
+        // is padding; O^T = V^T P^T likewise (head dimensions as M).  Thread
+        // (g, cq) holds rows 2 cq and 2 cq + 1 of the block and keys g, g + 8
+        // of each m16 tile; a row's max and sum over keys combine across the
+        // eight lanes with its cq.  P (bf16) goes from the S^T accumulator
+        // layout to the PV B operand by an in-register 8x8 transpose.
+        static_assert(WR == 1 && D % 16 == 0, "transposed blocks: one 8-row group");
+        constexpr int MT = TW / 16;          // m16 key tiles per warp per tile
+        constexpr int DK = D / 16;           // k-steps of QK, m16 tiles of O^T
+        uint32_t qb[DK][2];                  // Q^T B fragments of row g
+        float oacc[DK][4];                   // O^T: d 16 dp + g (+ 8), rows 2 cq (+ 1)
+        float m[2], l[2];                    // rows 2 cq + i; l: this thread's keys only
+        bool rvalid[2], rsoft[2];
+        int rrow[2];
+        uint64_t vmask[2] = {0ull, 0ull};
+        int vmask_j = -1;
+        Cursor c;
+        cursor_init(P, ws, t_begin, c);
+        bool seg_open = false;
+        long long k = 0;
+        for (long long t = t_begin; t < t_end; ++t, ++k) {
+            if (!seg_open) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int p = c.rb * 8 + 2 * cq + i;
+                    rvalid[i] = false;
+                    rsoft[i] = false;
+                    rrow[i] = -1;
+                    if (p < A.M) {
+                        const int r = p / A.G;
+                        const uint8_t fl = A.row_flags[(size_t)c.b * A.R + r];
+                        rvalid[i] = (fl & SPEC_ROW_VALID) != 0;
+                        rsoft[i] = rvalid[i] && (fl & SPEC_ROW_SEES_SOFT) != 0;
+                        rrow[i] = r;
+                    }
+                }
+                {
+                    // Q^T fragments: row g of the block, head dimensions 16 ks +
+                    // 2 cq (+ 1) and + 8
+                    const int p = c.rb * 8 + g;
+                    const __nv_bfloat16 *qr = nullptr;
+                    if (p < A.M) {
+                        const int hq = c.h * A.G + p % A.G;
+                        qr = static_cast<const __nv_bfloat16 *>(A.q) +
+                             (((size_t)c.b * A.R + p / A.G) * A.Hq + hq) * D;
+                    }
+#pragma unroll
+                    for (int ks = 0; ks < DK; ++ks) {
+                        qb[ks][0] = qr ? *reinterpret_cast<const uint32_t *>(qr + 16 * ks + 2 * cq) : 0u;
+                        qb[ks][1] = qr ? *reinterpret_cast<const uint32_t *>(qr + 16 * ks + 8 + 2 * cq) : 0u;
+                    }
+                }
+#pragma unroll
+                for (int dp = 0; dp < DK; ++dp)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) oacc[dp][e] = 0.f;
+                m[0] = m[1] = -INFINITY;
+                l[0] = l[1] = 0.f;
+                vmask_j = -1;
+                seg_open = true;
+            }
+
+            const int s = (int)(k % NS);
+            const uint32_t ph = (uint32_t)((k / NS) & 1);
+            if (!mbar_wait_warp(&full[s], ph, P.wait)) {
+                raise_status(A.status, SPEC_DEV_TIMEOUT);
+                break;
+            }
+            const uint32_t kb = smem_base + s * STAGE;
+            const uint32_t vb = kb + KV_BYTES;
+            const TileInfo ti = tile_info(P, c);
+            const int rbl = (ti.kind == kPrefix && A.paged) ? P.page_log2 : 6;
+            if (ti.kind == kBlock && vmask_j != ti.j) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    uint64_t w = 0;
+                    if (rrow[i] >= 0 && rvalid[i]) {
+                        const uint32_t *vr = A.vis + ((size_t)c.b * A.R + rrow[i]) * A.W;
+                        const int w0 = 2 * ti.j;
+                        w = vr[w0];
+                        if (w0 + 1 < A.W) w |= (uint64_t)vr[w0 + 1] << 32;
+                    }
+                    vmask[i] = w;
+                }
+                vmask_j = ti.j;
+            }
+
+            // ---- S^T = K Q^T: m16 tiles of this warp's keys, two accumulator
+            // sets over alternating k-steps
+            float sacc[MT][4], sacc2[MT][4];
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sacc[mt][e] = sacc2[mt][e] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < DK; ++ks) {
+                const int chunk = (ks & 3) * 2 + (lane >> 4);
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    const int tok = c0 + mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                    uint32_t a[4];
+                    ldsm_x4(tile_addr<NH>(kb, tok, ks >> 2, chunk, rbl), a[0], a[1], a[2], a[3]);
+                    if (ks & 1) mma_bf16(sacc2[mt], a, qb[ks][0], qb[ks][1]);
+                    else mma_bf16(sacc[mt], a, qb[ks][0], qb[ks][1]);
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sacc[mt][e] += sacc2[mt][e];
+
+            // ---- mask, scale, online softmax; element e: key g + 8 (e >> 1)
+            // of its m16 tile, row 2 cq + (e & 1)
+            float tmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = e & 1;
+                    const int col = c0 + mt * 16 + g + 8 * (e >> 1);
+                    bool vis = col < ti.nvalid;
+                    if (ti.kind == kPrefix) vis = vis && rvalid[i];
+                    else if (ti.kind == kSoft) vis = vis && rsoft[i];
+                    else vis = vis && ((vmask[i] >> col) & 1ull);
+                    const float x = vis ? sacc[mt][e] * A.scale_log2 : -INFINITY;
+                    sacc[mt][e] = x;
+                    tmax[i] = fmaxf(tmax[i], x);
+                }
+            }
+            float alpha[2], muse[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1)
+                    tmax[i] = fmaxf(tmax[i], __shfl_xor_sync(0xffffffffu, tmax[i], o));
+                const float mn = fmaxf(m[i], tmax[i]);
+                muse[i] = mn == -INFINITY ? 0.f : mn;
+                alpha[i] = fast_exp2(m[i] - muse[i]);
+                m[i] = mn;
+            }
+            // P^T, as the PV B operand: per m16 key tile, the pair of rows of
+            // key g (and g + 8) transposed to keys 2 cq (+ 1, + 8, + 9) of row g
+            uint32_t pb[MT][2];
+            float rs[2] = {0.f, 0.f};
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                const float p0 = fast_exp2(sacc[mt][0] - muse[0]);
+                const float p1 = fast_exp2(sacc[mt][1] - muse[1]);
+                const float p2 = fast_exp2(sacc[mt][2] - muse[0]);
+                const float p3 = fast_exp2(sacc[mt][3] - muse[1]);
+                rs[0] += p0 + p2;
+                rs[1] += p1 + p3;
+                pb[mt][0] = movmatrix_t(pack_bf16(p0, p1));
+                pb[mt][1] = movmatrix_t(pack_bf16(p2, p3));
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) l[i] = l[i] * alpha[i] + rs[i];
+#pragma unroll
+            for (int dp = 0; dp < DK; ++dp) {
+                oacc[dp][0] *= alpha[0];
+                oacc[dp][1] *= alpha[1];
+                oacc[dp][2] *= alpha[0];
+                oacc[dp][3] *= alpha[1];
+            }
+
+            // ---- O^T += V^T P^T (A = V^T by transposing loads of V rows)
+            const bool ragged = ti.nvalid < kTile;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                const int k0 = c0 + mt * 16;
+                const int tok = k0 + ((lane >> 4) << 3) + (lane & 7);
+                uint32_t keep0 = 0xffffffffu, keep1 = 0xffffffffu;
+                if (ragged) {
+                    const int t0 = k0 + 2 * cq, t1 = k0 + 8 + 2 * cq;
+                    keep0 = (t0 < ti.nvalid ? 0x0000ffffu : 0u) | (t0 + 1 < ti.nvalid ? 0xffff0000u : 0u);
+                    keep1 = (t1 < ti.nvalid ? 0x0000ffffu : 0u) | (t1 + 1 < ti.nvalid ? 0xffff0000u : 0u);
+                }
+#pragma unroll
+                for (int dp = 0; dp < DK; ++dp) {
+                    const int dchunk = dp * 2 + ((lane >> 3) & 1);
+                    uint32_t a[4];
+                    ldsm_x4_t(tile_addr<NH>(vb, tok, dchunk >> 3, dchunk & 7, rbl), a[0], a[1], a[2],
+                              a[3]);
+                    a[0] &= keep0;
+                    a[1] &= keep0;
+                    a[2] &= keep1;
+                    a[3] &= keep1;
+                    mma_bf16(oacc[dp], a, pb[mt][0], pb[mt][1]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+
+            // ---- segment done (or range done): this warp's partial
+            const bool seg_end = (c.tile == c.n_tiles - 1) || (t == t_end - 1);
+            if (seg_end) {
+                const int seg = (c.b * A.Hkv + c.h) * A.n_rb + c.rb;
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    float lt = l[i];
+#pragma unroll
+                    for (int o = 4; o < 32; o <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, o);
+                    const size_t row = slot_row(P, seg, cta, wc, WC, 2 * cq + i);
+                    float *po = A.part_o + row * D;
+#pragma unroll
+                    for (int dp = 0; dp < DK; ++dp) {
+                        po[16 * dp + g] = oacc[dp][i];
+                        po[16 * dp + g + 8] = oacc[dp][2 + i];
+                    }
+                    if (g == 0) {
+                        A.part_ml[row * 2] = m[i];
+                        A.part_ml[row * 2 + 1] = lt;
+                    }
+                }
+                seg_open = false;
+            }
+            cursor_next(P, c);
+        }
+        return;
+    }
 
     uint32_t qf[D / 16][4];
     float oacc[ND][4];
@@ -1377,10 +1609,11 @@ bool make_map(CUtensorMap *map, const void *base, long long rows, int d, int box
 
 // Kernel shape chosen per problem shape.
 struct TcConfig {
-    int wr;     // 16-row warp groups per row block
+    int wr;     // 16-row warp groups per row block (1 for the transposed 8-row blocks)
     int ncw;    // consumer warps
     int ns;     // pipeline stages
     int minb;   // CTAs per SM
+    int swap;   // 8-row blocks computed transposed
 };
 
 TcConfig choose(const AttnParams &P) {
@@ -1390,9 +1623,11 @@ TcConfig choose(const AttnParams &P) {
     // One 16-row group at d = 128 takes two consumer warps, 32 keys of each
     // tile apiece (measured on the LLaMA-7B-shaped step: 141 -> 138 us; one
     // warp: 168 us; two warps with three CTAs per SM: 139 us).
-    if (wr == 1 && P.d == 128) return {1, 2, 3, 2};
-    if (wr <= 2) return {wr, 4, P.d == 128 ? 3 : 6, 2};
-    return {wr, 8, P.d == 128 ? 5 : 8, 1};
+    // Up to 8 rows (d = 128): 8-row blocks computed transposed, two warps.
+    if (P.rb_rows == 8) return {1, 2, 3, 2, 1};
+    if (wr == 1 && P.d == 128) return {1, 2, 3, 2, 0};
+    if (wr <= 2) return {wr, 4, P.d == 128 ? 3 : 6, 2, 0};
+    return {wr, 8, P.d == 128 ? 5 : 8, 1, 0};
 }
 
 size_t smem_bytes(int d, int ns) {
@@ -1400,13 +1635,13 @@ size_t smem_bytes(int d, int ns) {
     return (size_t)ns * stage + 2 * ns * sizeof(uint64_t) + 1024;
 }
 
-template <int D, int WR, int NCW, int NS, int MINB>
+template <int D, int WR, int NCW, int NS, int MINB, int SWAP = 0>
 spec_status_t launch_impl(const TcParams &P, const CUtensorMap *maps, cudaStream_t s) {
     const size_t smem = smem_bytes(D, NS);
-    if (set_smem_limit(reinterpret_cast<const void *>(attn_tc_kernel<D, WR, NCW, NS, MINB>),
+    if (set_smem_limit(reinterpret_cast<const void *>(attn_tc_kernel<D, WR, NCW, NS, MINB, SWAP>),
                        smem) != SPEC_OK)
         return SPEC_ERR_CUDA;
-    if (launch(attn_tc_kernel<D, WR, NCW, NS, MINB>, dim3(P.n_ctas), dim3((NCW + 1) * 32), smem, s,
+    if (launch(attn_tc_kernel<D, WR, NCW, NS, MINB, SWAP>, dim3(P.n_ctas), dim3((NCW + 1) * 32), smem, s,
                P, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5]) != SPEC_OK)
         return SPEC_ERR_CUDA;
     spec_status_t st = launch_status();
@@ -1490,6 +1725,7 @@ bool umma_selected(const AttnParams &P) { return P.d == 128 && P.M >= 64 && 128 
 
 int tc_rows_per_block(const AttnParams &P) {
     if (umma_selected(P)) return tcs::kRows;
+    if (P.M <= 8 && P.d == 128) return 8;     // transposed: the rows as the MMA's N
     if (P.M <= 16) return 16;
     if (P.M <= 32) return 32;
     return 64;
@@ -1525,7 +1761,7 @@ spec_status_t launch_attn_tc(const AttnParams &A, cudaStream_t s) {
     P.a = A;
     P.wait = wait_limit();
     const bool use_umma = umma_selected(A);
-    const TcConfig cfg = use_umma ? TcConfig{8, 4, 0, 1} : choose(A);
+    const TcConfig cfg = use_umma ? TcConfig{8, 4, 0, 1, 0} : choose(A);
     {
         // the bounds follow the partials (same sizes as tc_workspace_bytes)
         const size_t rows = tc_slot_rows(A, &P.n_ctas);
@@ -1592,6 +1828,7 @@ spec_status_t launch_attn_tc(const AttnParams &A, cudaStream_t s) {
     if (!ok) return SPEC_ERR_CUDA;
     if (use_umma) return launch_umma(P, maps, s);
     if (A.d == 128) {
+        if (cfg.swap) return launch_impl<128, 1, 2, 3, 2, 1>(P, maps, s);
         if (cfg.wr == 1) return launch_impl<128, 1, 2, 3, 2>(P, maps, s);
         if (cfg.wr == 2) return launch_impl<128, 2, 4, 3, 2>(P, maps, s);
         return launch_impl<128, 4, 8, 5, 1>(P, maps, s);
