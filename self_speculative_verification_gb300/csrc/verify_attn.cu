@@ -66,14 +66,26 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnParams P) {
     const int row0 = rb * kSimtRows;
 
     const T *q = static_cast<const T *>(P.q);
-    for (int i = tid; i < kSimtRows * D; i += blockDim.x) {
-        const int pr = i / D, k = i % D, p = row0 + pr;
-        float x = 0.f;
-        if (p < P.M) {
-            const int r = p / P.G, hq = h * P.G + p % P.G;
-            x = load_f(q + (((size_t)b * P.R + r) * P.Hq + hq) * D + k) * P.scale_log2;
+    {
+        // the block's queries: every load in flight before the stores
+        constexpr int kPerQ = kSimtRows * D / 128;
+        float xs[kPerQ];
+#pragma unroll
+        for (int it = 0; it < kPerQ; ++it) {
+            const int i = tid + it * 128;
+            const int pr = i / D, k = i % D, p = row0 + pr;
+            float x = 0.f;
+            if (p < P.M) {
+                const int r = p / P.G, hq = h * P.G + p % P.G;
+                x = load_f(q + (((size_t)b * P.R + r) * P.Hq + hq) * D + k) * P.scale_log2;
+            }
+            xs[it] = x;
         }
-        sq[pr][k] = x;
+#pragma unroll
+        for (int it = 0; it < kPerQ; ++it) {
+            const int i = tid + it * 128;
+            sq[i / D][i % D] = xs[it];
+        }
     }
     for (int i = tid; i < kSimtRows * P.W; i += blockDim.x) {
         const int pr = i / P.W, w = i % P.W, p = row0 + pr;
@@ -121,7 +133,13 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnParams P) {
             ncols = min(kSimtCols, P.R - base);
         }
         __syncthreads();   // previous tile fully consumed (and sq/svis ready)
-        for (int i = tid; i < kSimtCols * D; i += blockDim.x) {
+        // every load of the tile in flight before the first store (the
+        // per-element loop of loads and stores waited one round trip each)
+        constexpr int kPer = kSimtCols * D / 128;
+        float kxs[kPer], vxs[kPer];
+#pragma unroll
+        for (int it = 0; it < kPer; ++it) {
+            const int i = tid + it * 128;
             const int j = i / D, k = i % D;
             float kx = 0.f, vx = 0.f;
             if (j < ncols) {
@@ -145,8 +163,14 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnParams P) {
                     vx = load_f(vr + off);
                 }
             }
-            sk[j][k] = kx;
-            sv_[j][k] = vx;
+            kxs[it] = kx;
+            vxs[it] = vx;
+        }
+#pragma unroll
+        for (int it = 0; it < kPer; ++it) {
+            const int i = tid + it * 128;
+            sk[i / D][i % D] = kxs[it];
+            sv_[i / D][i % D] = vxs[it];
         }
         __syncthreads();
 

@@ -101,3 +101,15 @@ def test_odd_kv_heads(name, kw):
     wl = W.make_workload(name, 29, B=3, seq=("uniform", 150, 700), V=2000, **kw)
     gh.run_and_check(wl)
     gh.run_and_check(wl, split_tokens=64)
+
+
+@pytest.mark.parametrize("page_size", [16, 32, 64])
+def test_eight_row_blocks_on_paged_cache(page_size):
+    """Blocks of 8 packed rows (the LLaMA-7B Lookahead shape) run transposed
+    (the rows as the MMA's N): paged prefix tiles of every page size, ragged
+    tails, and 64-token splits so that most segments are merged from
+    several CTAs' partials."""
+    wl = W.make_workload("la7b", 30, B=3, seq=("uniform", 150, 900), V=3000, paged=True,
+                         page_size=page_size)
+    gh.run_and_check(wl)
+    gh.run_and_check(wl, split_tokens=64)
