@@ -113,3 +113,13 @@ def test_eight_row_blocks_on_paged_cache(page_size):
                          page_size=page_size)
     gh.run_and_check(wl)
     gh.run_and_check(wl, split_tokens=64)
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_eight_row_blocks_gqa(paged):
+    """Transposed 8-row blocks with GQA: 4 lookahead rows x 2 query heads
+    per KV head, bf16, head_dim 128, contiguous and paged caches."""
+    wl = W.make_workload("tiny_la", 31, dtype="bf16", d=128, B=3, seq=("uniform", 100, 500),
+                         V=3000, paged=paged)
+    gh.run_and_check(wl)
+    gh.run_and_check(wl, split_tokens=64)
