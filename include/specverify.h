@@ -42,8 +42,10 @@
  *     dtype/shape, a too-small workspace) are returned before anything is
  *     launched.  Errors only visible on the device (a bad parent pointer, a
  *     page id out of range, a full cache) set bits in a per-device status
- *     word and the kernel skips the offending work; nothing traps, nothing
- *     spins.  spec_get_status() reads and clears that word.
+ *     word and the kernel skips the offending work; nothing traps, and
+ *     every wait inside a kernel is bounded (spec_set_wait_limit; on expiry
+ *     SPEC_DEV_TIMEOUT is set and the kernel returns).  spec_get_status()
+ *     reads and clears that word.
  *   - The status word is shared by all calls on a device: with concurrent
  *     streams, an error bit cannot be attributed to one call.
  */
