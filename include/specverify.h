@@ -580,7 +580,8 @@ spec_status_t kv_commit(const spec_kv_desc *cache, int batch, int n_rows,
 /*
  * spec_set_wait_limit -- limit, in SM clock cycles, of the internal pipeline
  * waits of the kernels launched from now on (verify attention, prefill
- * attention), process-wide.  The pages have no counterpart: this is the
+ * attention, and the bulk row stream of the vocabulary reduction),
+ * process-wide.  The pages have no counterpart: this is the
  * library's guard against a hang.  A wait that runs out sets
  * SPEC_DEV_TIMEOUT; the kernel then stops issuing work, waits (with the
  * default limit) for its own copies and tensor-core operations, frees its

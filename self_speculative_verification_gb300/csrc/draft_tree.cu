@@ -276,33 +276,44 @@ __device__ __forceinline__ int clamp_nodes(const PruneParams &P, int b, bool rep
     return n;
 }
 
-// CTA (p, b): the children of node p keep their edge iff their token's
-// probability under p's early-exit logits reaches the threshold
-// (keep[c] = 1 / 0; the root's entry is left to the compaction).
+// Exclusive prefix sum over a kT-thread block of one count per thread
+// (every thread calls it); *s_total receives the sum.
+template <int kT>
+__device__ __forceinline__ int block_exclusive_scan(int cnt, int *s_wsum, int *s_total) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int w = lane < kT / 32 ? s_wsum[lane] : 0;
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += y;
+        }
+        if (lane < kT / 32) s_wsum[lane] = wi - w;
+        if (lane == kT / 32 - 1) *s_total = wi;
+    }
+    __syncthreads();
+    return s_wsum[warp] + incl - cnt;
+}
+
+// ln sum exp of one row of V logits (every thread calls it): a running
+// (max, sum) per thread over 16-byte vectors (kEdgeLoads loads in flight),
+// then the warp, then the block.  s_m / s_s: one slot per warp.
+constexpr int kEdgeLoads = 4;
 template <typename T>
-__global__ void __launch_bounds__(kThreads) prune_edge_kernel(PruneParams P) {
-    pdl_wait();
-    __shared__ int s_kids[kMaxPruneNodes];
-    __shared__ int s_nk;
-    __shared__ float s_m[kThreads / 32], s_s[kThreads / 32];
-    __shared__ float s_lse;
-    const int p = blockIdx.x, b = blockIdx.y;
-    const int n = clamp_nodes(P, b, p == 0 && threadIdx.x == 0);
-    if (p >= n) return;
-    if (threadIdx.x == 0) s_nk = 0;
-    __syncthreads();
-    const size_t nb = (size_t)b * P.N;
-    for (int c = p + 1 + threadIdx.x; c < n; c += kThreads)
-        if (P.parent[nb + c] == p) s_kids[atomicAdd(&s_nk, 1)] = c;
-    __syncthreads();
-    const int nk = s_nk;
-    if (nk == 0) return;
-    // ln sum exp of row p: running (max, sum) per thread, then the block
-    const T *z = static_cast<const T *>(P.early) + (nb + p) * P.V;
+__device__ float row_lse(const T *z, int V, float *s_m, float *s_s) {
     float m = -INFINITY, s = 0.f;
     const bool vec = (reinterpret_cast<uintptr_t>(z) & 15) == 0;
-    const int nv = vec ? P.V / 8 : 0;
-    constexpr int U = 4;
+    const int nv = vec ? V / 8 : 0;
+    constexpr int U = kEdgeLoads;
     for (int i0 = threadIdx.x; i0 < nv; i0 += U * kThreads) {
         float x[U][8];
 #pragma unroll
@@ -330,7 +341,7 @@ __global__ void __launch_bounds__(kThreads) prune_edge_kernel(PruneParams P) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) s += ex2(fmaf(x[u][e], kLog2e, -mb));
     }
-    for (int v = nv * 8 + threadIdx.x; v < P.V; v += kThreads) {
+    for (int v = nv * 8 + threadIdx.x; v < V; v += kThreads) {
         const float x = load_f(z + v);
         if (x > m) {
             s = s * ex2((m - x) * kLog2e) + 1.f;
@@ -339,7 +350,6 @@ __global__ void __launch_bounds__(kThreads) prune_edge_kernel(PruneParams P) {
             s += ex2((x - m) * kLog2e);
         }
     }
-    // merge (m, s) pairs: warp, then block
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -355,25 +365,97 @@ __global__ void __launch_bounds__(kThreads) prune_edge_kernel(PruneParams P) {
         s_s[warp] = s;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        float M = -INFINITY, S = 0.f;
-        for (int w = 0; w < kThreads / 32; ++w) {
-            const float nm = fmaxf(M, s_m[w]);
-            S = (M == -INFINITY ? 0.f : S * ex2((M - nm) * kLog2e)) +
-                (s_m[w] == -INFINITY ? 0.f : s_s[w] * ex2((s_m[w] - nm) * kLog2e));
-            M = nm;
-        }
-        s_lse = M + logf(S);
+    float M = -INFINITY, S = 0.f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+        const float nm = fmaxf(M, s_m[w]);
+        S = (M == -INFINITY ? 0.f : S * ex2((M - nm) * kLog2e)) +
+            (s_m[w] == -INFINITY ? 0.f : s_s[w] * ex2((s_m[w] - nm) * kLog2e));
+        M = nm;
+    }
+    __syncthreads();                     // s_m / s_s free for the next row
+    return M + logf(S);
+}
+
+// A request's tree takes ceil(N / kEdgeNodesPerPart) edge-test CTAs.
+constexpr int kEdgeNodesPerPart = 4;
+
+// The edge test of child c of node p: keep[c] = 1 iff its token's
+// probability under p's logits (z[token] given, lse the row's) reaches the
+// threshold.
+__device__ __forceinline__ void edge_keep(const PruneParams &P, size_t nb, int c, int x, float zx,
+                                          float lse) {
+    int keep = 0;
+    if (x < 0 || x >= P.V) raise_status(P.status, SPEC_DEV_BAD_INDEX);
+    else keep = __expf(zx - lse) >= P.threshold;
+    P.keep[nb + c] = keep;
+}
+
+// CTA (part, b): request b's inner nodes (those with a child), in index
+// order, every gridDim.x-th from the part-th; for each such node p, the LSE
+// of p's early-exit row, and each child keeps its edge iff its token's
+// probability under p's logits reaches the threshold (keep[c] = 1 / 0; the
+// root's entry is left to the compaction).  A child counts only when its
+// parent index precedes it (the compaction reports the others).  The
+// request's parents and tokens come in with one round of loads, and a
+// thread's first child's logit is loaded before the row, so that only the
+// row's loads remain in line.
+// (five CTAs per SM, 760 resident: 32 requests x 22 parts of 85-node trees
+// fit in one wave)
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 5) prune_edge_kernel(PruneParams P) {
+    pdl_wait();
+    constexpr int kPer = kMaxPruneNodes / kThreads;
+    __shared__ int s_par[kMaxPruneNodes], s_tok[kMaxPruneNodes], s_inner[kMaxPruneNodes];
+    __shared__ uint8_t s_has[kMaxPruneNodes];
+    __shared__ int s_wsum[kThreads / 32];
+    __shared__ int s_ni;
+    __shared__ float s_m[kThreads / 32], s_s[kThreads / 32];
+    const int part = blockIdx.x, b = blockIdx.y;
+    const int n = clamp_nodes(P, b, part == 0 && threadIdx.x == 0);
+    const size_t nb = (size_t)b * P.N;
+    for (int c = threadIdx.x; c < n; c += kThreads) {
+        s_par[c] = P.parent[nb + c];
+        s_tok[c] = P.tokens[nb + c];
+        s_has[c] = 0;
     }
     __syncthreads();
-    const float lse = s_lse;
-    for (int i = threadIdx.x; i < nk; i += kThreads) {
-        const int c = s_kids[i];
-        const int x = P.tokens[nb + c];
-        int ok = 0;
-        if (x < 0 || x >= P.V) raise_status(P.status, SPEC_DEV_BAD_INDEX);
-        else ok = __expf(load_f(z + x) - lse) >= P.threshold;
-        P.keep[nb + c] = ok;
+    for (int c = threadIdx.x; c < n; c += kThreads) {
+        const int a = s_par[c];
+        if (a >= 0 && a < c) s_has[a] = 1;
+    }
+    __syncthreads();
+    // the inner nodes numbered in index order (this thread: nodes
+    // t * kPer .. t * kPer + kPer - 1)
+    int cnt = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int c = threadIdx.x * kPer + i;
+        cnt += (c < n && s_has[c]) ? 1 : 0;
+    }
+    int idx = block_exclusive_scan<kThreads>(cnt, s_wsum, &s_ni);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int c = threadIdx.x * kPer + i;
+        if (c < n && s_has[c]) s_inner[idx++] = c;
+    }
+    __syncthreads();
+    const int ni = s_ni;
+    for (int i = part; i < ni; i += gridDim.x) {
+        const int p = s_inner[i];
+        const T *z = static_cast<const T *>(P.early) + (nb + p) * P.V;
+        // this thread's first candidate child and its token's logit
+        const int c0 = p + 1 + threadIdx.x;
+        const bool kid0 = c0 < n && s_par[c0] == p;
+        const int x0 = kid0 ? s_tok[c0] : -1;
+        const float z0 = (x0 >= 0 && x0 < P.V) ? load_f(z + x0) : 0.f;
+        const float lse = row_lse(z, P.V, s_m, s_s);
+        if (kid0) edge_keep(P, nb, c0, x0, z0, lse);
+        for (int c = c0 + kThreads; c < n; c += kThreads) {
+            if (s_par[c] != p) continue;
+            const int x = s_tok[c];
+            edge_keep(P, nb, c, x, (x >= 0 && x < P.V) ? load_f(z + x) : 0.f, lse);
+        }
     }
 }
 
@@ -390,7 +472,6 @@ __global__ void __launch_bounds__(kThreads) prune_compact_kernel(PruneParams P) 
     __shared__ int s_wsum[kThreads / 32];
     __shared__ int s_cnt;
     const int b = blockIdx.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = clamp_nodes(P, b, false);
     const size_t nb = (size_t)b * P.N;
     for (int c = threadIdx.x; c < n; c += kThreads) {
@@ -425,28 +506,7 @@ __global__ void __launch_bounds__(kThreads) prune_compact_kernel(PruneParams P) 
         cnt += alive;
     }
     if (bad) raise_status(P.status, SPEC_DEV_BAD_TREE);
-    // exclusive scan of the per-thread counts
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (lane == 31) s_wsum[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        int w = lane < kThreads / 32 ? s_wsum[lane] : 0;
-        int wi = w;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, wi, o);
-            if (lane >= o) wi += y;
-        }
-        if (lane < kThreads / 32) s_wsum[lane] = wi - w;
-        if (lane == kThreads / 32 - 1) s_cnt = wi;
-    }
-    __syncthreads();
-    int idx = s_wsum[warp] + incl - cnt;
+    int idx = block_exclusive_scan<kThreads>(cnt, s_wsum, &s_cnt);
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
         const int c = threadIdx.x * kPer + i;
@@ -566,7 +626,7 @@ extern "C" spec_status_t spec_prune_tree(const spec_prune_desc *d, const int32_t
     P.status = status_ptr();
     if (!P.status) return SPEC_ERR_CUDA;
     cudaStream_t s = as_stream(stream);
-    dim3 grid(d->max_nodes, d->batch);
+    dim3 grid(ceil_div(d->max_nodes, kEdgeNodesPerPart), d->batch);
     const spec_status_t ls =
         d->logit_dtype == SPEC_BF16
             ? launch(prune_edge_kernel<__nv_bfloat16>, grid, dim3(kThreads), 0, s, P)

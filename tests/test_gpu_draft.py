@@ -12,6 +12,7 @@ import gpu_helpers as gh
 import oracle
 from self_speculative_verification_gb300 import binding as bn
 from self_speculative_verification_gb300 import workloads as W
+from self_speculative_verification_gb300.workloads import round_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -131,6 +132,54 @@ def test_draft_then_prune(seed, B, V):
         assert np.all(t2[b, m:] == -1) and np.all(p2[b, m:] == -1)
         assert vp[b].tolist() == oracle.ss_block_vparent(rp, dw.gamma, R).tolist()
 
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("V", [777, 4096, 50272])
+def test_prune_irregular_trees(dtype, V):
+    """Trees that are not full: random recursive parents mixed with chains,
+    requests of 1, 2, 57 and 200 nodes, so that an edge-test CTA takes
+    several inner rows (the row stream's barriers carried from one row to
+    the next) and some rows take the plain-load path (odd V)."""
+    rng = np.random.Generator(np.random.PCG64(V * 2 + (dtype == "f32")))
+    sizes = [1, 2, 57, 200]
+    B, N, gamma, thr = len(sizes), max(sizes), 2, 0.05
+    R = N * (1 + gamma)
+    par = np.full((B, N), -1, np.int32)
+    tok = np.full((B, N), -1, np.int32)
+    early = rng.standard_normal((B, N, V), dtype=np.float32)
+    for b, n in enumerate(sizes):
+        for c in range(1, n):
+            par[b, c] = rng.integers(0, c) if rng.random() < 0.7 else c - 1
+        tok[b, :n] = rng.integers(0, V, size=n)
+        # most edges far above the threshold (their tokens' logit 12 against
+        # N(0, 1) elsewhere), the others far below it
+        for c in range(1, n):
+            if rng.random() < 0.85:
+                early[b, par[b, c], tok[b, c]] = 12.0
+    if dtype == "bf16":
+        early = round_bf16(early)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    keep = torch.full((B, N), 9, dtype=I32, device=DEV)
+    t2 = torch.full((B, N), 9, dtype=I32, device=DEV)
+    p2 = torch.full((B, N), 9, dtype=I32, device=DEV)
+    n2 = torch.zeros(B, dtype=I32, device=DEV)
+    vp = torch.full((B, R), 9, dtype=I32, device=DEV)
+    d = bn.PruneDesc(B, N, V, bn.SPEC_BF16 if dtype == "bf16" else bn.SPEC_F32, thr, gamma, R)
+    nn = torch.tensor(sizes, dtype=I32, device=DEV)
+    bn.spec_prune_tree(d, torch.from_numpy(tok).to(DEV), torch.from_numpy(par).to(DEV), nn,
+                       _logits(early, tdt), keep, t2, p2, n2, vp)
+    torch.cuda.synchronize()
+    assert bn.spec_get_status() == 0
+    keep, t2, p2, n2, vp = (x.cpu().numpy() for x in (keep, t2, p2, n2, vp))
+    for b, n in enumerate(sizes):
+        rt, rp, km = oracle.prune_tree(tok[b, :n], par[b, :n], early[b, :n].astype(np.float64), thr)
+        assert keep[b, :n].tolist() == km.tolist() and np.all(keep[b, n:] == -1)
+        m = len(rt)
+        assert n2[b] == m
+        assert t2[b, :m].tolist() == rt.tolist() and p2[b, :m].tolist() == rp.tolist()
+        assert np.all(t2[b, m:] == -1) and np.all(p2[b, m:] == -1)
+        assert vp[b].tolist() == oracle.ss_block_vparent(rp, gamma, R).tolist()
 
 def test_pruned_block_feeds_mask_build():
     """draft -> prune -> spec_mask_build gives the oracle's visibility."""
