@@ -33,6 +33,7 @@ def _snapshot(ds):
 @pytest.mark.parametrize("name,kw", [
     ("la7b", dict(B=3, seq=("uniform", 100, 700), V=4000)),
     ("long_paged", dict(B=3, seq=("uniform", 300, 1100), V=4000)),
+    ("ss", dict(B=3, seq=("uniform", 100, 500), V=5000)),
     ("ss_soft", dict(B=3, seq=("uniform", 100, 500), V=5000)),
     ("ss_rot", dict(B=3, seq=("uniform", 100, 500), V=5000)),
     ("confu", dict(B=2, seq=("uniform", 150, 600), V=5000)),
@@ -80,3 +81,42 @@ def test_prefill_graph_replay_matches_direct():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(o, o0) and torch.equal(lse, l0)
+
+
+def test_draft_and_prune_graph_replay_matches_direct():
+    """The draft tree and its pruning (two entry points, five launches)
+    captured together replay to the same trees as direct calls."""
+    gh.require_gpu()
+    dw = W.make_draft(5, B=4, V=5000)
+    dev = torch.device("cuda", 0)
+    B, N, g = dw.B, dw.N, dw.gamma
+    R = N * (1 + g)
+    i32 = torch.int32
+    stream_l = torch.from_numpy(dw.stream_logits).to(dev, torch.bfloat16)
+    early = torch.from_numpy(dw.early_logits).to(dev, torch.bfloat16)
+    root = torch.from_numpy(dw.root_token).to(dev)
+    tok, par, t2, p2, keep = (torch.zeros((B, N), dtype=i32, device=dev) for _ in range(5))
+    nn, n2 = torch.zeros(B, dtype=i32, device=dev), torch.zeros(B, dtype=i32, device=dev)
+    vp_full, vp = (torch.zeros((B, R), dtype=i32, device=dev) for _ in range(2))
+    ddesc = bn.DraftDesc(B, g, g, dw.k, dw.V, bn.SPEC_BF16, N, R)
+    pdesc = bn.PruneDesc(B, N, dw.V, bn.SPEC_BF16, dw.threshold, g, R)
+    outs = (tok, par, nn, vp_full, keep, t2, p2, n2, vp)
+
+    def calls():
+        bn.spec_draft_tree(ddesc, stream_l, None, root, tok, par, nn, vp_full)
+        bn.spec_prune_tree(pdesc, tok, par, nn, early, keep, t2, p2, n2, vp)
+
+    calls()
+    torch.cuda.synchronize()
+    assert bn.spec_get_status() == 0
+    want = [t.clone() for t in outs]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        calls()
+    for t in outs:
+        t.fill_(-7)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert bn.spec_get_status() == 0
+    for t, w in zip(outs, want):
+        assert torch.equal(t, w)

@@ -1,20 +1,23 @@
 """Bounded pipeline waits.  With the wait limit set to 0 cycles, any wait of
-the tensor-core kernels whose condition is not met at its first test gives
-up at once: the kernel must report SPEC_DEV_TIMEOUT, stop, drain its own
-copies and tensor-core operations, free its tensor memory and return, so the
-context stays usable.  The workloads are sized so that every CTA has more
+the tensor-core kernels (or of the vocabulary reduction's row stream) whose
+condition is not met at its first test gives up at once: the kernel must
+report SPEC_DEV_TIMEOUT, stop, drain its own copies and tensor-core
+operations, free its tensor memory and return, so the context stays usable.  The workloads are sized so that every CTA has more
 tiles than its stage ring holds (a producer waiting for a stage to be
 released cannot find it free at the first test).  After each case the
 default limit is restored and a full step on the same process must match the
 oracle."""
 
+import numpy as np
 import pytest
 import torch
 
 import gpu_helpers as gh
+import oracle
 from self_speculative_verification_gb300 import binding as bn
 from self_speculative_verification_gb300 import workloads as W
 from self_speculative_verification_gb300.device import DeviceStep
+from self_speculative_verification_gb300.workloads import round_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -74,3 +77,38 @@ def test_prefill_wait_runs_out_and_context_recovers():
     # (request, head) slices
     O, LSE = run_gpu(wl)
     check(wl, O, LSE, pairs=[(0, 0), (1, 5)])
+
+
+def test_vocab_stream_wait_runs_out_and_context_recovers():
+    """bf16 rows on 16-byte boundaries take the bulk row stream, whose chunk
+    waits are bounded by the same limit: at 0 the first chunk, tested right
+    after its copy was issued, has not landed."""
+    gh.require_gpu()
+    rows, V = 64, 128256
+    rng = np.random.Generator(np.random.PCG64(77))
+    z = round_bf16((rng.standard_normal((rows, V), dtype=np.float32) * 3).astype(np.float32))
+    prop = rng.integers(0, V, size=rows).astype(np.int32)
+    dev = torch.device("cuda", 0)
+    dz = torch.from_numpy(z).to(dev, torch.bfloat16)
+    dp = torch.from_numpy(prop).to(dev)
+    am = torch.empty(rows, dtype=torch.int32, device=dev)
+    lse = torch.empty(rows, dtype=torch.float32, device=dev)
+    zp = torch.empty(rows, dtype=torch.float32, device=dev)
+    assert bn.spec_get_status() == 0
+    bn.spec_set_wait_limit(0)
+    try:
+        bn.spec_vocab_reduce(dz, dp, am, lse, zp)
+        torch.cuda.synchronize()
+    finally:
+        bn.spec_set_wait_limit(-1)
+    status = bn.spec_get_status()
+    assert status & bn.SPEC_DEV_TIMEOUT, f"status {status:#x}"
+    # the default limit again: the same call matches the oracle
+    bn.spec_vocab_reduce(dz, dp, am, lse, zp)
+    torch.cuda.synchronize()
+    assert bn.spec_get_status() == 0
+    am_o, lse_o, zp_o = oracle.vocab_reduce(z, prop)
+    assert am.cpu().numpy().tolist() == am_o.tolist()
+    rel = np.abs(lse.cpu().numpy().astype(np.float64) - lse_o) / np.abs(lse_o)
+    assert rel.max() <= 1e-5
+    assert np.array_equal(zp.cpu().numpy().astype(np.float64), zp_o)
