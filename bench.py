@@ -491,6 +491,8 @@ def run_gpu(args):
             "verified_tokens_per_step": tokens,
             "accepted_rows_per_step": accepted_rows,
             "per_call_ms": {n: float(per[:, i].mean()) for i, (n, _) in enumerate(stages)},
+            "step_ms_spread": {"min": float(step_ms.min()), "median": float(np.median(step_ms)),
+                               "max": float(step_ms.max())},
             "step_includes": "seq_len/free_head restore (2 small device copies)",
             "step_algorithmic_bytes": step_algorithmic_bytes(wl, accepted_rows),
         },
