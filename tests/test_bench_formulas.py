@@ -1,7 +1,8 @@
 """The numerators of the bench's roofline figures, checked by counting on
 small cases instead of by the closed forms bench.py uses: visible
 (query, key) pairs of the LA prefill mask, inner nodes of the draft trees
-the oracle builds, and the page-table entries a paged prefix touches."""
+the oracle builds, the page-table entries a paged prefix touches, and the
+verify attention's bytes rebuilt from the arrays the oracle reads."""
 
 from types import SimpleNamespace
 
@@ -48,3 +49,34 @@ def test_paged_attention_bytes_count_touched_pages():
     base = bench.attn_algorithmic_bytes(wl)
     wl.paged = False
     assert base - bench.attn_algorithmic_bytes(wl) == touched * 4
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("confu", dict(B=2, seq=("uniform", 50, 200), V=64)),
+    ("long_paged", dict(B=2, seq=("uniform", 40, 200), V=64)),
+])
+def test_attention_bytes_count_the_arrays(name, kw):
+    """spec_verify_attn's algorithmic bytes rebuilt from the arrays the
+    oracle's attention reads: each request's prefix K and V (gathered from
+    the paged cache where there is one), the block and soft-prompt K/V, q
+    and an O of its size, LSE, and the integer inputs (lengths, the packed
+    visibility words of the oracle's mask, row flags, touched pages)."""
+    wl = W.make_workload(name, 4, **kw)
+    e = 2 if wl.dtype == "bf16" else 4
+    if wl.paged:
+        Kp, Vp = wl.paged_cache(fill=0.0)
+        ks = oracle.gather_paged(Kp, wl.page_table, wl.seq_len, wl.page_size)
+        vs = oracle.gather_paged(Vp, wl.page_table, wl.seq_len, wl.page_size)
+        prefix = sum(k.size + v.size for k, v in zip(ks, vs))
+        pages = sum(len({int(wl.page_table[b, t // wl.page_size])
+                         for t in range(int(wl.seq_len[b]))}) for b in range(wl.B))
+    else:
+        prefix = sum(sum(x.size for x in wl.prefix_kv(b)) for b in range(wl.B))
+        pages = 0
+    soft = (wl.soft_k.size + wl.soft_v.size) if wl.n_soft > 0 else 0
+    vis, _, _ = oracle.mask_build(wl.vparent, wl.soft_flags)
+    words = vis.shape[0] * vis.shape[1] * ((vis.shape[2] + 31) // 32)
+    ints = wl.seq_len.size * 4 + words * 4 + wl.B * wl.R + pages * 4
+    lse = wl.B * wl.Hq * wl.R * 4
+    want = (prefix + wl.kb.size + wl.vb.size + soft + 2 * wl.q.size) * e + lse + ints
+    assert bench.attn_algorithmic_bytes(wl) == want
