@@ -150,3 +150,84 @@ def test_wait_limit_setter_round_trips_without_gpu():
     finally:
         binding.spec_set_wait_limit(prev)
     assert lib is binding.load_library()
+
+
+def test_host_side_errors_of_the_other_entry_points_need_no_gpu():
+    """Descriptor and pointer checks of the draft, pruning, prefill, rotation,
+    gather, vocabulary and mask entry points return before any CUDA call
+    (the pointers below are never dereferenced on the host)."""
+    lib = binding.load_library()
+    BF, F32 = binding.SPEC_BF16, binding.SPEC_F32
+    P = ctypes.c_void_p(0x1000)          # a 16-byte aligned address
+    Pm = ctypes.c_void_p(0x1008)         # not 16-byte aligned
+    N = None
+
+    def draft(desc, ptrs=True, vp=None):
+        args = [P] * 6 if ptrs else [N] * 6
+        return lib.spec_draft_tree(ctypes.byref(desc) if desc is not None else None,
+                                   args[0], None, args[1], args[2], args[3], args[4], vp, None)
+
+    D = binding.DraftDesc
+    assert draft(None) == 1
+    assert draft(D(2, 3, 3, 9, 100, BF, 1000, 0)) == 2              # k above 8
+    assert draft(D(2, 3, 3, 4, 100, 7, 1000, 0)) == 2               # logit dtype
+    assert draft(D(2, 3, 3, 4, 100, BF, 84, 0)) == 4                # 85-node tree, 84 slots
+    assert draft(D(2, 3, 3, 4, 100, BF, 85, 339), vp=P) == 4        # block rows 340 > 339
+    assert draft(D(0, 3, 3, 4, 100, BF, 85, 0), ptrs=False) == 0    # empty batch
+    assert draft(D(2, 3, 3, 4, 100, BF, 85, 0), ptrs=False) == 1    # NULL buffers
+
+    def prune(desc, ptrs=True, vp=None):
+        args = [P] * 8 if ptrs else [N] * 8
+        return lib.spec_prune_tree(ctypes.byref(desc) if desc is not None else None,
+                                   *args, vp, None)
+
+    R = binding.PruneDesc
+    assert prune(None) == 1
+    assert prune(R(2, 85, 100, BF, float("nan"), 3, 340)) == 1      # NaN threshold
+    assert prune(R(2, 1025, 100, BF, 0.1, 3, 4100)) == 2            # more than 1024 nodes
+    assert prune(R(2, 85, 100, 7, 0.1, 3, 340)) == 2                # logit dtype
+    assert prune(R(2, 85, 100, BF, 0.1, 3, 339), vp=P) == 4         # block rows too few
+    assert prune(R(0, 85, 100, BF, 0.1, 3, 340), ptrs=False) == 0
+    assert prune(R(2, 85, 100, BF, 0.1, 3, 340), ptrs=False) == 1
+
+    def prefill(desc, q=P, k=P, v=P, o=P, lse=P):
+        return lib.spec_la_prefill_attn(ctypes.byref(desc) if desc is not None else None,
+                                        q, k, v, o, lse, None)
+
+    F = binding.PrefillDesc
+    assert prefill(None) == 1
+    assert prefill(F(1, 0, 4, 8, 8, 128, BF, 0.0)) == 1             # no original positions
+    assert prefill(F(1, 64, 4, 8, 3, 128, BF, 0.0)) == 1            # Hq % Hkv != 0
+    assert prefill(F(1, 64, 4, 8, 8, 64, BF, 0.0)) == 2             # head_dim 64
+    assert prefill(F(1, 64, 4, 8, 8, 128, F32, 0.0)) == 2           # fp32
+    assert prefill(F(0, 64, 4, 8, 8, 128, BF, 0.0), N, N, N, N, N) == 0
+    assert prefill(F(1, 64, 4, 8, 8, 128, BF, 0.0), N, N, N, N, N) == 1
+    assert prefill(F(1, 64, 4, 8, 8, 128, BF, 0.0), q=Pm) == 1      # q off 16 bytes
+
+    Rt = binding.RotateDesc
+    rot = lambda d, nn=P, vb=P: lib.spec_stream_rotate_values(ctypes.byref(d), nn, vb, None)
+    assert lib.spec_stream_rotate_values(None, P, P, None) == 1
+    assert rot(Rt(2, 16, 4, 12, BF, 3, 0.01)) == 2                  # head_dim not a multiple of 8
+    assert rot(Rt(2, 16, 4, 128, BF, 3, float("nan"))) == 1         # NaN angle
+    assert rot(Rt(2, 16, 4, 128, BF, 3, 0.01), vb=Pm) == 1          # block off 16 bytes
+    assert rot(Rt(0, 16, 4, 128, BF, 3, 0.01), N, N) == 0
+
+    g = lib.spec_future_gather
+    assert g(2, 8, 100, BF, P, P, 0, P, None) == 2                  # 200-byte rows
+    assert g(2, 8, 12, BF, P, P, 0, P, None) == 2                   # 24-byte rows
+    assert g(2, 8, 128, 7, P, P, 0, P, None) == 2                   # dtype
+    assert g(2, 8, 128, BF, P, P, -1, P, None) == 1                 # negative offset
+    assert g(0, 8, 128, BF, N, N, 0, N, None) == 0
+    assert g(2, 8, 128, BF, Pm, P, 0, P, None) == 1                 # O off 16 bytes
+
+    v = lib.spec_vocab_reduce
+    assert v(P, BF, 4, 0, N, P, P, N, None) == 1                    # empty vocabulary
+    assert v(P, 7, 4, 100, N, P, P, N, None) == 2                   # dtype
+    assert v(P, BF, 4, 100, P, P, P, N, None) == 1                  # proposal without zprop
+    assert v(N, BF, 0, 100, N, N, N, N, None) == 0
+
+    m = lib.spec_mask_build
+    assert m(P, N, 2, 0, P, P, None) == 1                           # no rows
+    assert m(P, N, 2, 257, P, P, None) == 2                         # above SPEC_MAX_ROWS
+    assert m(N, N, 0, 8, N, N, None) == 0
+    assert m(N, N, 2, 8, P, P, None) == 1                           # NULL parents
