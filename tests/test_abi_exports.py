@@ -231,3 +231,55 @@ def test_host_side_errors_of_the_other_entry_points_need_no_gpu():
     assert m(P, N, 2, 257, P, P, None) == 2                         # above SPEC_MAX_ROWS
     assert m(N, N, 0, 8, N, N, None) == 0
     assert m(N, N, 2, 8, P, P, None) == 1                           # NULL parents
+
+
+def test_host_side_errors_of_acceptance_and_commit_need_no_gpu():
+    """The same for spec_accept, spec_accept_soft and kv_commit."""
+    lib = binding.load_library()
+    BF = binding.SPEC_BF16
+    CH, TR = binding.SPEC_ACCEPT_THRESH_CHAIN, binding.SPEC_ACCEPT_GREEDY_TREE
+    P = ctypes.c_void_p(0x1000)
+    N = None
+
+    def acc(d, logits=P, tokens=P, parent=P, row_of=N, zprop=P):
+        return lib.spec_accept(ctypes.byref(d) if d is not None else None, logits, tokens,
+                               parent, row_of, P, P, P, zprop, P, P, P, P, None)
+
+    A = binding.AcceptDesc
+    assert acc(None) == 1
+    assert acc(A(5, 0.3, 2, 8, 100, BF, 8, 8)) == 1                 # unknown mode
+    assert acc(A(CH, 0.3, 2, 0, 100, BF, 8, 8)) == 1                # no judged rows
+    assert acc(A(CH, 0.0, 2, 8, 100, BF, 8, 8)) == 1                # tau not in (0, 1]
+    assert acc(A(CH, 0.3, 2, 8, 100, BF, 8, 8), row_of=P) == 1      # chains take no row map
+    assert acc(A(CH, 0.3, 2, 8, 100, BF, 6, 8)) == 1                # proposals != judged rows
+    assert acc(A(TR, 0.0, 2, 8, 100, BF, 300, 8)) == 2              # tree above 256 nodes
+    assert acc(A(TR, 0.0, 2, 8, 100, BF, 8, 8), parent=N) == 1      # tree without parents
+    assert acc(A(TR, 0.0, 2, 8, 0, BF, 8, 8)) == 1                  # empty vocabulary
+    assert acc(A(TR, 0.0, 2, 8, 100, 7, 8, 8)) == 2                 # logit dtype
+    assert acc(A(TR, 0.0, 0, 8, 100, BF, 8, 8), logits=N, tokens=N, parent=N) == 0
+
+    def soft(d, draft=P):
+        return lib.spec_accept_soft(ctypes.byref(d) if d is not None else None, P, draft, P, P,
+                                    N, P, P, P, P, P, P, P, P, P, P, None)
+
+    S = binding.SoftDesc
+    assert soft(None) == 1
+    assert soft(S(2, 8, 4, 100, BF, 8, 8, 0.0)) == 1                # temperature 0
+    assert soft(S(2, 8, 4, 100, BF, 8, 8, float("inf"))) == 1       # infinite temperature
+    assert soft(S(2, 8, 4, 100, 7, 8, 8, 1.0)) == 2                 # logit dtype
+    assert soft(S(2, 8, 4, (1 << 20) + 1, BF, 8, 8, 1.0)) == 2      # vocabulary above 2^20
+    assert soft(S(2, 8, 4, 100, BF, 300, 8, 1.0)) == 2              # tree above 256 nodes
+    assert soft(S(2, 8, 4, 100, BF, 8, 8, 1.0), draft=N) == 1       # draft rows without logits
+    assert soft(S(0, 8, 4, 100, BF, 8, 8, 1.0), draft=N) == 0
+
+    K = binding.KvDesc
+    com = lambda c, batch=2: lib.kv_commit(ctypes.byref(c) if c is not None else None, batch, 8,
+                                           P, P, 8, P, P, P, N, 0, N, None)
+    kv = lambda dt=BF, d=128, kind=binding.SPEC_KV_CONTIGUOUS, B=2: K(kind, dt, 4, d, P, P, B, 64,
+                                                                     0, 0, 0, N)
+    assert com(None) == 1
+    assert com(kv(dt=7)) == 2                                       # dtype
+    assert com(kv(d=12)) == 2                                       # 24-byte rows
+    assert com(kv(d=96, kind=binding.SPEC_KV_PAGED)) == 2           # paged head_dim not 64k
+    assert com(kv(B=1)) == 1                                        # cache holds fewer requests
+    assert com(kv(), batch=0) == 0
